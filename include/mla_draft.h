@@ -1,0 +1,199 @@
+/*
+ * mla_draft.h -- C ABI of the MLA (Multi-head Latent Attention) draft-layer
+ * forward for NVIDIA GB300 (sm_103a).
+ *
+ * What the layer computes (sources are web pages, cited by title/section):
+ *  - "MLA (Multi-Head Latent Attention)" blog, DeepseekV2MLAAttention.__init__
+ *    and MultiHeadLatentAttentionWrapper.forward: optional low-rank query
+ *    (fused_qkv_a_proj -> q_a_layernorm -> q_b_proj, or q_proj without
+ *    q_lora_rank), the shared compressed KV latent (kv_a_proj_with_mqa ->
+ *    kv_a_layernorm), partial RoPE on qk_rope_head_dim, kv_b_proj expansion,
+ *    o_proj.
+ *  - same blog, do_kv_cache_update / concat_and_cache_mla and
+ *    get_kv_cache_shape: the latent cache [num_pages, page_size,
+ *    kv_lora_rank + qk_rope_head_dim], one entry [kv_c_normed | k_pe] per
+ *    token, written by slot index.
+ *  - same blog, forward_impl (MQA branch) and forward_mqa: attention in the
+ *    latent space (q_nope @ W_UK, scores against [c | k_pe], W_UV up-proj).
+ *  - "Add config-selectable MLA draft attention" (SpecForge PR #758),
+ *    Summary/Structure: DFlash-family target-context injection, full/sliding
+ *    masks, zeroing of fully masked queries, optional output gate, NeoX or
+ *    interleaved rotation; dimension validation once at init.
+ *  - "extract GQA/MLA attention into reusable layers" (SpecForge PR #1026),
+ *    Modifications: masks by logical position; empty queries zeroed before
+ *    o_proj.
+ *
+ * Conventions for every entry point
+ *  - Pointers named "device" are CUDA device pointers (cudaMalloc / torch),
+ *    "host" pointers are CPU memory.  The library never allocates device
+ *    memory: weights, arena, cache, workspace and outputs belong to the
+ *    caller.  The library owns only the host-side handle.
+ *  - Weights use torch.nn.Linear layout W[out, in], row-major, contiguous, of
+ *    the config's dtype (bf16 or fp32).  Hidden states are row-major
+ *    [tokens, hidden_size] of the same dtype; so is the cache.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  append and
+ *    forward only enqueue work: no host synchronisation, no allocation.
+ *  - Errors: host-side validation returns a status and never aborts; the
+ *    message is available from mla_last_error().  Index errors found on the
+ *    device (slot, page or position out of range) skip the offending access
+ *    and set a bit in a device status word read by mla_get_device_status().
+ */
+#ifndef MLA_DRAFT_H
+#define MLA_DRAFT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t mla_status_t;
+enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, inconsistent dims    */
+  MLA_ERR_UNSUPPORTED = 2,   /* valid dims this build has no kernel for       */
+  MLA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed             */
+  MLA_ERR_DEVICE_CHECK = 4,  /* the device reported an index error            */
+  MLA_ERR_TIMEOUT = 5        /* a bounded device wait expired                 */
+};
+
+enum { MLA_BF16 = 0, MLA_FP32 = 1 };              /* mla_config_t.dtype */
+enum { MLA_ROPE_NEOX = 0, MLA_ROPE_INTERLEAVED = 1 }; /* mla_config_t.rope */
+
+/* Bits of the device status word (mla_get_device_status). */
+enum {
+  MLA_DEV_BAD_SLOT = 1,      /* slot_mapping entry outside the cache          */
+  MLA_DEV_BAD_POSITION = 2,  /* position < 0 or >= max_position               */
+  MLA_DEV_BAD_PAGE = 4,      /* block_table entry outside [0, num_pages)      */
+  MLA_DEV_TIMEOUT = 8,       /* a bounded mbarrier wait gave up               */
+  MLA_DEV_BAD_LENGTH = 16    /* kv_len < 0 or > max_pages * page_size         */
+};
+
+/* Layer configuration.  Structural dims follow the HF DeepSeek-V2/V3 fields;
+ * q_lora_rank == 0 selects the non-low-rank path (q_proj +
+ * kv_a_proj_with_mqa).  softmax_scale == 0 means 1/sqrt(qk_nope + qk_rope).
+ * max_position bounds the RoPE table built at init. */
+typedef struct {
+  int32_t hidden_size, num_heads, q_lora_rank, kv_lora_rank;
+  int32_t qk_nope_head_dim, qk_rope_head_dim, v_head_dim;
+  int32_t rope;              /* MLA_ROPE_NEOX | MLA_ROPE_INTERLEAVED          */
+  int32_t use_output_gate;   /* 0/1: o *= sigmoid(x @ gate_proj^T)            */
+  int32_t dtype;             /* MLA_BF16 | MLA_FP32                           */
+  int32_t page_size;         /* tokens per cache page                         */
+  int32_t max_position;      /* positions must lie in [0, max_position)       */
+  double rope_theta, rms_norm_eps, softmax_scale;
+} mla_config_t;
+
+/* Device pointers to the layer's parameters, read only inside mla_draft_init
+ * (not retained).  Unused fields are NULL. */
+typedef struct {
+  const void *fused_qkv_a_proj;    /* [q_lora_rank + kv_lora_rank + qk_rope, D]  (q_lora_rank > 0) */
+  const void *q_a_layernorm;       /* [q_lora_rank]                               (q_lora_rank > 0) */
+  const void *q_b_proj;            /* [H * (qk_nope + qk_rope), q_lora_rank]      (q_lora_rank > 0) */
+  const void *q_proj;              /* [H * (qk_nope + qk_rope), D]                (q_lora_rank == 0) */
+  const void *kv_a_proj_with_mqa;  /* [kv_lora_rank + qk_rope, D]                 (q_lora_rank == 0) */
+  const void *kv_a_layernorm;      /* [kv_lora_rank]                                                */
+  const void *kv_b_proj;           /* [H * (qk_nope + v_head), kv_lora_rank]                        */
+  const void *gate_proj;           /* [H * v_head, D]                             (use_output_gate) */
+  const void *o_proj;              /* [D, H * v_head]                                               */
+} mla_weights_t;
+
+/* Which keys each query block attends (device pointers).  Block b holds
+ * queries b*block_len .. (b+1)*block_len-1.  Its key j (logical position j)
+ * is the cache entry at page block_table[b*max_pages + j/page_size], row
+ * j%page_size.  Key j is visible to query i of block b iff
+ *   q_visible[i] != 0  &&  j < kv_len[b]  &&
+ *   (window[b] == 0 || positions[i] - j < window[b]).
+ * A query with no visible key produces an exact zero output row. */
+typedef struct {
+  int32_t num_blocks, block_len, max_pages, reserved;
+  const int32_t *block_table;  /* [num_blocks, max_pages]                      */
+  const int32_t *kv_len;       /* [num_blocks]                                 */
+  const int32_t *window;       /* [num_blocks]; NULL = every block full        */
+  const uint8_t *q_visible;    /* [num_blocks * block_len]; NULL = all visible */
+  int32_t *vis_stats;          /* optional output [num_blocks*block_len, 3]:
+                                  visible-key count, first and last visible
+                                  key (-1 when none), as the kernel's own mask
+                                  applied them; NULL = not written            */
+} mla_attn_desc_t;
+
+typedef struct mla_handle mla_handle_t;
+
+/* ---- geometry (host only; no GPU needed) --------------------------------
+ * MLA blog, MLAAttention.__init__ / get_kv_cache_shape: one cache entry is
+ * kv_lora_rank + qk_rope_head_dim wide (576 for DeepSeek dims), one KV head;
+ * MLAAttentionSpec.real_page_size_bytes: page bytes = page_size * 1 *
+ * entry * dtype size.  Return 0 for a NULL or inconsistent config. */
+int32_t mla_cache_entry_dim(const mla_config_t *cfg);
+size_t mla_cache_page_bytes(const mla_config_t *cfg);
+
+/* Bytes of the derived-weight arena mla_draft_init fills (0 = invalid cfg). */
+size_t mla_weight_arena_bytes(const mla_config_t *cfg);
+
+/* Validate `cfg` (returns MLA_ERR_INVALID_ARG / MLA_ERR_UNSUPPORTED with a
+ * message), re-lay the weights out into the caller's device `arena`
+ * (>= mla_weight_arena_bytes): W_UK / W_UV split out of kv_b_proj (MLA blog,
+ * forward_impl: W_UK_T and _v_up_proj), the A-projection rows ordered
+ * [kv | q | gate], a RoPE cos/sin table computed in fp64 on the host, and the
+ * device status word.  Synchronises `stream` before returning; `w` is not
+ * retained.  On success *out receives a handle owned by the caller (free with
+ * mla_draft_destroy).  One handle serves one stream at a time. */
+mla_status_t mla_draft_init(const mla_config_t *cfg, const mla_weights_t *w,
+                            void *arena, size_t arena_bytes, void *stream,
+                            mla_handle_t **out);
+
+/* Device scratch needed by one append of n tokens / one forward of
+ * num_tokens block tokens. */
+size_t mla_append_workspace_bytes(const mla_handle_t *h, int32_t n);
+size_t mla_forward_workspace_bytes(const mla_handle_t *h, int32_t num_tokens);
+
+/* Latent-cache append (target-context injection, PR #758; MLA blog,
+ * do_kv_cache_update): for each of the n tokens,
+ *   kv = hidden[t] @ W_kva^T            (W_kva = last kv_lora_rank+qk_rope rows
+ *                                         of fused_qkv_a_proj, or
+ *                                         kv_a_proj_with_mqa)
+ *   cache[slot_mapping[t]] = [RMSNorm(kv[:r]) * kv_a_layernorm |
+ *                             RoPE(kv[r:], positions[t])]
+ * hidden: device [n, hidden_size]; positions: device int32 [n];
+ * slot_mapping: device int64 [n], slot = page * page_size + row;
+ * cache: device [num_pages, page_size, entry].  n == 0 is a no-op. */
+mla_status_t mla_latent_cache_append(mla_handle_t *h, const void *hidden,
+                                     const int32_t *positions,
+                                     const int64_t *slot_mapping, int32_t n,
+                                     void *cache, int32_t num_pages,
+                                     void *workspace, size_t workspace_bytes,
+                                     void *stream);
+
+/* Draft-layer forward for desc->num_blocks blocks of desc->block_len tokens
+ * (MLA blog, wrapper forward + forward_impl MQA branch; PR #758 masks, gate):
+ *   q = rope(q_b_proj(RMSNorm(q_c)))  (or q_proj), absorbed with W_UK;
+ *   latent attention over the cache keys each block sees (mla_attn_desc_t);
+ *   o = W_UV * latent output, optionally * sigmoid(hidden @ gate_proj^T);
+ *   out = o @ o_proj^T.
+ * hidden: device [nb*T, hidden_size]; positions: device int32 [nb*T];
+ * block_slot_mapping: device int64 [nb*T] -- when non-NULL the block's own
+ * latents are written to the cache there before attending; when NULL they
+ * must already be in the cache (mla_latent_cache_append).  out: device
+ * [nb*T, hidden_size].  Fully masked query rows come out as exact +0. */
+mla_status_t mla_draft_forward(mla_handle_t *h, const void *hidden,
+                               const int32_t *positions,
+                               const int64_t *block_slot_mapping, void *cache,
+                               int32_t num_pages, const mla_attn_desc_t *desc,
+                               void *out, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
+/* Synchronise `stream`, read and clear the device status word.  Returns
+ * MLA_OK, MLA_ERR_TIMEOUT (MLA_DEV_TIMEOUT set) or MLA_ERR_DEVICE_CHECK; the
+ * raw bits go to *bits when non-NULL. */
+mla_status_t mla_get_device_status(mla_handle_t *h, void *stream, int32_t *bits);
+
+void mla_draft_destroy(mla_handle_t *h);
+const char *mla_status_string(mla_status_t s);
+/* Message of the last failing call on this thread ("" if none). */
+const char *mla_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_DRAFT_H */
