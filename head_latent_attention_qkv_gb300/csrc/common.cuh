@@ -1,0 +1,71 @@
+// Shared host/device definitions of the MLA draft-layer library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "../../include/mla_draft.h"
+
+namespace mla {
+
+// ---- error reporting (host) -------------------------------------------------
+void set_error(const std::string& msg);
+mla_status_t fail(mla_status_t s, const std::string& msg);
+mla_status_t cuda_fail(cudaError_t e, const char* what);
+
+#define MLA_CUDA_TRY(expr)                                  \
+  do {                                                      \
+    cudaError_t _e = (expr);                                \
+    if (_e != cudaSuccess) return ::mla::cuda_fail(_e, #expr); \
+  } while (0)
+
+// ---- element conversion (device) ------------------------------------------
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {
+  if (status) atomicOr(status, bits);
+}
+
+// ---- derived layout of one layer (host handle) ------------------------------
+struct Layout {
+  int D, H, rq, rkv, dn, dr, dv, L, dqk;
+  int qdim;        // width of the query block of the A projection: rq or H*dqk
+  int gdim;        // gate width (H*dv or 0)
+  int NA;          // rows of W_A: L + qdim + gdim, ordered [kv | q | gate]
+  size_t elt;      // bytes per element of the configured dtype
+  // byte offsets inside the arena
+  size_t off_WA, off_Wqb, off_gq, off_gkv, off_WUKT, off_WUV, off_Wo, off_rope, off_status, total;
+};
+
+bool make_layout(const mla_config_t& c, Layout* out);
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace mla
+
+struct mla_handle {
+  mla_config_t cfg;
+  mla::Layout lay;
+  int device;
+  int num_sms;
+  char* arena;
+  float scale;     // softmax scale
+  uint32_t* status;
+  const float2* rope;   // [max_position, dr/2] (cos, sin)
+  const float* gamma_q;
+  const float* gamma_kv;
+  const void* WA;
+  const void* Wqb;
+  const void* WUKT;     // [H, rkv, dn]
+  const void* WUV;      // [H, dv, rkv]
+  const void* Wo;
+};

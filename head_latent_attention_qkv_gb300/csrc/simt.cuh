@@ -1,0 +1,48 @@
+// SIMT (CUDA-core, fp32-accumulate) kernels of the MLA draft layer.
+//
+// These are the production path for the fp32 configuration (tensor-core
+// TF32 would not meet a 1e-4 relative tolerance) and the first, plain
+// implementation of every step for bf16.  T is the storage type of weights,
+// activations and the latent cache (float or __nv_bfloat16); every sum is
+// accumulated in fp32.
+#pragma once
+
+#include "common.cuh"
+
+namespace mla {
+namespace simt {
+
+// C[z][m][n] = sum_k A[z][m][k] * B[z][n][k]  (both operands K-contiguous, the
+// torch.nn.Linear product x @ W^T), optionally multiplied by sigmoid(G[z][m][n])
+// (G fp32).  Leading dims / batch strides are in elements.
+template <typename TA, typename TC>
+void gemm_nt(cudaStream_t st, int M, int N, int K, int batch,
+             const TA* A, long lda, long sA, const TA* B, long ldb, long sB,
+             TC* C, long ldc, long sC, const float* G, long ldg, long sG);
+
+// Latent entry of each of n tokens from its raw kv row (fp32, row stride ld):
+// cache[slot] = [RMSNorm(kv[:rkv]) * gamma | RoPE(kv[rkv:], pos)].
+template <typename T>
+void kv_finish(cudaStream_t st, const mla_handle* h, const float* kv, long ld, int n,
+               const int32_t* positions, const int64_t* slots, T* cache, long num_slots);
+
+// out[m][:] = RMSNorm(in[m][:n]) * gamma  (in fp32 with row stride ld).
+template <typename T>
+void rmsnorm_rows(cudaStream_t st, const float* in, long ld, int M, int n,
+                  const float* gamma, float eps, T* out);
+
+// q [M, H, dqk] fp32 (row stride ldq) -> q_nope [M, H, dn] and the rotated
+// rope part into Q_abs[m, h, rkv:rkv+dr].
+template <typename T>
+void q_rope_split(cudaStream_t st, const mla_handle* h, const float* q, long ldq, int M,
+                  const int32_t* positions, T* q_nope, T* q_abs);
+
+// Latent attention: O_lat[m, h, :rkv] = sum_j p_j c_j over the visible keys of
+// each query's block, scores scale * <Q_abs[m,h,:], entry_j>.
+template <typename T>
+void latent_attention(cudaStream_t st, const mla_handle* h, const T* q_abs,
+                      const T* cache, int num_pages, const mla_attn_desc_t& desc,
+                      const int32_t* positions, T* o_lat);
+
+}  // namespace simt
+}  // namespace mla

@@ -1,0 +1,157 @@
+// Row-wise SIMT kernels: latent finish (RMSNorm + RoPE + cache store),
+// query RMSNorm, query RoPE split (see simt.cuh).
+#include "simt.cuh"
+
+#include <math.h>
+
+namespace mla {
+namespace simt {
+
+namespace {
+
+constexpr int ROW_THREADS = 128;
+
+// Sum of v over the CTA (blockDim.x == ROW_THREADS); every thread gets it.
+__device__ float block_sum(float v) {
+  __shared__ float part[ROW_THREADS / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x / 32;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) part[w] = v;
+  __syncthreads();
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < ROW_THREADS / 32; ++i) s += part[i];
+  return s;
+}
+
+// Rotation pair k of a rope slice of width dr: element indices (ia, ib).
+__device__ __forceinline__ void rope_pair(int k, int dr, int interleaved, int* ia, int* ib) {
+  if (interleaved) { *ia = 2 * k; *ib = 2 * k + 1; }
+  else { *ia = k; *ib = k + dr / 2; }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(ROW_THREADS)
+kv_finish_kernel(const float* __restrict__ kv, long ld, const int32_t* __restrict__ positions,
+                 const int64_t* __restrict__ slots, T* __restrict__ cache, long num_slots,
+                 int rkv, int dr, float eps, const float* __restrict__ gamma,
+                 const float2* __restrict__ rope, int max_pos, int interleaved,
+                 uint32_t* status) {
+  const int t = blockIdx.x;
+  const float* row = kv + (long)t * ld;
+  const long slot = slots[t];
+  const int p = positions[t];
+  const bool bad_slot = slot < 0 || slot >= num_slots;
+  const bool bad_pos = p < 0 || p >= max_pos;
+  if (bad_slot || bad_pos) {
+    if (threadIdx.x == 0)
+      set_status(status, (bad_slot ? MLA_DEV_BAD_SLOT : 0) | (bad_pos ? MLA_DEV_BAD_POSITION : 0));
+    return;
+  }
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < rkv; i += ROW_THREADS) ss = fmaf(row[i], row[i], ss);
+  ss = block_sum(ss);
+  const float rstd = 1.f / sqrtf(ss / (float)rkv + eps);
+  T* dst = cache + slot * (long)(rkv + dr);
+  for (int i = threadIdx.x; i < rkv; i += ROW_THREADS) dst[i] = from_f32<T>(row[i] * rstd * gamma[i]);
+  const int half = dr / 2;
+  for (int k = threadIdx.x; k < half; k += ROW_THREADS) {
+    int ia, ib;
+    rope_pair(k, dr, interleaved, &ia, &ib);
+    const float2 cs = rope[(long)p * half + k];
+    const float a = row[rkv + ia], b = row[rkv + ib];
+    dst[rkv + ia] = from_f32<T>(a * cs.x - b * cs.y);
+    dst[rkv + ib] = from_f32<T>(b * cs.x + a * cs.y);
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(ROW_THREADS)
+rmsnorm_rows_kernel(const float* __restrict__ in, long ld, int n, const float* __restrict__ gamma,
+                    float eps, T* __restrict__ out) {
+  const float* row = in + (long)blockIdx.x * ld;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < n; i += ROW_THREADS) ss = fmaf(row[i], row[i], ss);
+  ss = block_sum(ss);
+  const float rstd = 1.f / sqrtf(ss / (float)n + eps);
+  T* o = out + (long)blockIdx.x * n;
+  for (int i = threadIdx.x; i < n; i += ROW_THREADS) o[i] = from_f32<T>(row[i] * rstd * gamma[i]);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(ROW_THREADS)
+q_rope_split_kernel(const float* __restrict__ q, long ldq, const int32_t* __restrict__ positions,
+                    int H, int dn, int dr, int rkv, const float2* __restrict__ rope, int max_pos,
+                    int interleaved, uint32_t* status, T* __restrict__ q_nope,
+                    T* __restrict__ q_abs) {
+  const int m = blockIdx.x;
+  const float* row = q + (long)m * ldq;
+  const int dqk = dn + dr, L = rkv + dr, half = dr / 2;
+  for (int i = threadIdx.x; i < H * dn; i += ROW_THREADS) {
+    const int h = i / dn, d = i % dn;
+    q_nope[(long)m * H * dn + i] = from_f32<T>(row[h * dqk + d]);
+  }
+  const int p = positions[m];
+  const bool bad = p < 0 || p >= max_pos;
+  if (bad && threadIdx.x == 0) set_status(status, MLA_DEV_BAD_POSITION);
+  for (int i = threadIdx.x; i < H * half; i += ROW_THREADS) {
+    const int h = i / half, k = i % half;
+    int ia, ib;
+    rope_pair(k, dr, interleaved, &ia, &ib);
+    T* dst = q_abs + ((long)m * H + h) * L + rkv;
+    if (bad) {
+      dst[ia] = from_f32<T>(0.f);
+      dst[ib] = from_f32<T>(0.f);
+      continue;
+    }
+    const float2 cs = rope[(long)p * half + k];
+    const float a = row[h * dqk + dn + ia], b = row[h * dqk + dn + ib];
+    dst[ia] = from_f32<T>(a * cs.x - b * cs.y);
+    dst[ib] = from_f32<T>(b * cs.x + a * cs.y);
+  }
+}
+
+}  // namespace
+
+template <typename T>
+void kv_finish(cudaStream_t st, const mla_handle* h, const float* kv, long ld, int n,
+               const int32_t* positions, const int64_t* slots, T* cache, long num_slots) {
+  if (n <= 0) return;
+  const Layout& l = h->lay;
+  kv_finish_kernel<T><<<n, ROW_THREADS, 0, st>>>(
+      kv, ld, positions, slots, cache, num_slots, l.rkv, l.dr, (float)h->cfg.rms_norm_eps,
+      h->gamma_kv, h->rope, h->cfg.max_position, h->cfg.rope == MLA_ROPE_INTERLEAVED, h->status);
+}
+
+template <typename T>
+void rmsnorm_rows(cudaStream_t st, const float* in, long ld, int M, int n, const float* gamma,
+                  float eps, T* out) {
+  if (M <= 0) return;
+  rmsnorm_rows_kernel<T><<<M, ROW_THREADS, 0, st>>>(in, ld, n, gamma, eps, out);
+}
+
+template <typename T>
+void q_rope_split(cudaStream_t st, const mla_handle* h, const float* q, long ldq, int M,
+                  const int32_t* positions, T* q_nope, T* q_abs) {
+  if (M <= 0) return;
+  const Layout& l = h->lay;
+  q_rope_split_kernel<T><<<M, ROW_THREADS, 0, st>>>(
+      q, ldq, positions, l.H, l.dn, l.dr, l.rkv, h->rope, h->cfg.max_position,
+      h->cfg.rope == MLA_ROPE_INTERLEAVED, h->status, q_nope, q_abs);
+}
+
+#define MLA_INST(T)                                                                          \
+  template void kv_finish<T>(cudaStream_t, const mla_handle*, const float*, long, int,      \
+                             const int32_t*, const int64_t*, T*, long);                     \
+  template void rmsnorm_rows<T>(cudaStream_t, const float*, long, int, int, const float*,   \
+                                float, T*);                                                 \
+  template void q_rope_split<T>(cudaStream_t, const mla_handle*, const float*, long, int,   \
+                                const int32_t*, T*, T*);
+MLA_INST(float)
+MLA_INST(__nv_bfloat16)
+#undef MLA_INST
+
+}  // namespace simt
+}  // namespace mla
