@@ -1,0 +1,321 @@
+// C ABI of the MLA draft-layer library: validation, derived-weight arena,
+// launch sequences (include/mla_draft.h documents every entry point).
+#include <math.h>
+#include <string.h>
+
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "simt.cuh"
+
+namespace mla {
+
+static thread_local std::string g_last_error;
+
+void set_error(const std::string& msg) { g_last_error = msg; }
+
+mla_status_t fail(mla_status_t s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+
+mla_status_t cuda_fail(cudaError_t e, const char* what) {
+  g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
+  return MLA_ERR_CUDA;
+}
+
+// Arena layout: W_A [NA, D] (rows [kv | q | gate]), W_qb [H*dqk, rq],
+// gamma_q fp32 [rq], gamma_kv fp32 [rkv], W_UK^T [H, rkv, dn],
+// W_UV [H, dv, rkv], W_o [D, H*dv], rope float2 [max_pos, dr/2], status.
+bool make_layout(const mla_config_t& c, Layout* out) {
+  Layout l;
+  l.D = c.hidden_size; l.H = c.num_heads; l.rq = c.q_lora_rank; l.rkv = c.kv_lora_rank;
+  l.dn = c.qk_nope_head_dim; l.dr = c.qk_rope_head_dim; l.dv = c.v_head_dim;
+  if (l.D <= 0 || l.H <= 0 || l.rq < 0 || l.rkv <= 0 || l.dn <= 0 || l.dr <= 0 || l.dv <= 0)
+    return false;
+  if (l.dr % 2 || c.page_size <= 0 || c.max_position <= 0) return false;
+  if (c.dtype != MLA_BF16 && c.dtype != MLA_FP32) return false;
+  if (c.rope != MLA_ROPE_NEOX && c.rope != MLA_ROPE_INTERLEAVED) return false;
+  l.L = l.rkv + l.dr;
+  l.dqk = l.dn + l.dr;
+  l.qdim = l.rq > 0 ? l.rq : l.H * l.dqk;
+  l.gdim = c.use_output_gate ? l.H * l.dv : 0;
+  l.NA = l.L + l.qdim + l.gdim;
+  l.elt = c.dtype == MLA_BF16 ? 2 : 4;
+  size_t o = 0;
+  l.off_WA = o;   o = align256(o + (size_t)l.NA * l.D * l.elt);
+  l.off_Wqb = o;  o = align256(o + (l.rq > 0 ? (size_t)l.H * l.dqk * l.rq * l.elt : 0));
+  l.off_gq = o;   o = align256(o + (size_t)l.rq * 4);
+  l.off_gkv = o;  o = align256(o + (size_t)l.rkv * 4);
+  l.off_WUKT = o; o = align256(o + (size_t)l.H * l.rkv * l.dn * l.elt);
+  l.off_WUV = o;  o = align256(o + (size_t)l.H * l.dv * l.rkv * l.elt);
+  l.off_Wo = o;   o = align256(o + (size_t)l.D * l.H * l.dv * l.elt);
+  l.off_rope = o; o = align256(o + (size_t)c.max_position * (l.dr / 2) * sizeof(float2));
+  l.off_status = o; o = align256(o + 256);
+  l.total = o;
+  *out = l;
+  return true;
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+const char* mla_status_string(mla_status_t s) {
+  switch (s) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MLA_ERR_CUDA: return "CUDA error";
+    case MLA_ERR_DEVICE_CHECK: return "device index check failed";
+    case MLA_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+const char* mla_last_error(void) { return g_last_error.c_str(); }
+
+int32_t mla_cache_entry_dim(const mla_config_t* cfg) {
+  Layout l;
+  if (!cfg || !make_layout(*cfg, &l)) return 0;
+  return l.L;
+}
+
+size_t mla_cache_page_bytes(const mla_config_t* cfg) {
+  Layout l;
+  if (!cfg || !make_layout(*cfg, &l)) return 0;
+  return (size_t)cfg->page_size * 1 /* one latent KV head */ * l.L * l.elt;
+}
+
+size_t mla_weight_arena_bytes(const mla_config_t* cfg) {
+  Layout l;
+  if (!cfg || !make_layout(*cfg, &l)) return 0;
+  return l.total;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Init: validation and re-layout of the weights into the arena
+// ---------------------------------------------------------------------------
+namespace mla {
+namespace {
+
+template <typename T>
+__global__ void to_f32_kernel(const T* __restrict__ in, float* __restrict__ out, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    out[i] = to_f32(in[i]);
+}
+
+// W_UK^T[h][c][i] = kv_b_proj[h*(dn+dv) + i][c]   (i < dn, c < rkv)
+template <typename T>
+__global__ void wuk_transpose_kernel(const T* __restrict__ kvb, T* __restrict__ out, int H,
+                                     int dn, int dv, int rkv) {
+  const long total = (long)H * rkv * dn;
+  for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < total;
+       idx += (long)gridDim.x * blockDim.x) {
+    const int i = idx % dn;
+    const int c = (idx / dn) % rkv;
+    const int h = idx / ((long)dn * rkv);
+    out[idx] = kvb[((long)h * (dn + dv) + i) * rkv + c];
+  }
+}
+
+mla_status_t validate(const mla_config_t& c, const mla_weights_t& w, Layout* l) {
+  if (!make_layout(c, l))
+    return fail(MLA_ERR_INVALID_ARG,
+                "config: dims must be positive (q_lora_rank >= 0), qk_rope_head_dim even, "
+                "page_size/max_position positive, dtype and rope valid");
+  if (!(c.rope_theta > 0) || !(c.rms_norm_eps >= 0) || !(c.softmax_scale >= 0))
+    return fail(MLA_ERR_INVALID_ARG, "config: rope_theta > 0, rms_norm_eps >= 0, softmax_scale >= 0");
+  if (c.q_lora_rank > 0) {
+    if (!w.fused_qkv_a_proj || !w.q_a_layernorm || !w.q_b_proj)
+      return fail(MLA_ERR_INVALID_ARG, "weights: q_lora_rank > 0 needs fused_qkv_a_proj, q_a_layernorm, q_b_proj");
+  } else if (!w.q_proj || !w.kv_a_proj_with_mqa) {
+    return fail(MLA_ERR_INVALID_ARG, "weights: q_lora_rank == 0 needs q_proj and kv_a_proj_with_mqa");
+  }
+  if (!w.kv_a_layernorm || !w.kv_b_proj || !w.o_proj)
+    return fail(MLA_ERR_INVALID_ARG, "weights: kv_a_layernorm, kv_b_proj and o_proj are required");
+  if (c.use_output_gate && !w.gate_proj)
+    return fail(MLA_ERR_INVALID_ARG, "weights: use_output_gate needs gate_proj");
+  if (l->rkv % 16 || l->rkv > 512)
+    return fail(MLA_ERR_UNSUPPORTED, "kv_lora_rank must be a multiple of 16 and at most 512");
+  if (l->L > 1024)
+    return fail(MLA_ERR_UNSUPPORTED, "kv_lora_rank + qk_rope_head_dim must be at most 1024");
+  return MLA_OK;
+}
+
+}  // namespace
+}  // namespace mla
+
+extern "C" mla_status_t mla_draft_init(const mla_config_t* cfg, const mla_weights_t* w,
+                                       void* arena, size_t arena_bytes, void* stream,
+                                       mla_handle_t** out) {
+  if (!cfg || !w || !arena || !out) return fail(MLA_ERR_INVALID_ARG, "init: null argument");
+  *out = nullptr;
+  Layout l;
+  mla_status_t s = validate(*cfg, *w, &l);
+  if (s != MLA_OK) return s;
+  if (arena_bytes < l.total)
+    return fail(MLA_ERR_INVALID_ARG, "init: arena smaller than mla_weight_arena_bytes()");
+  if ((uintptr_t)arena % 256)
+    return fail(MLA_ERR_INVALID_ARG, "init: arena must be 256-byte aligned");
+  cudaStream_t st = (cudaStream_t)stream;
+  auto* h = new mla_handle();
+  h->cfg = *cfg;
+  h->lay = l;
+  h->arena = (char*)arena;
+  {
+    cudaError_t e0 = cudaGetDevice(&h->device);
+    if (e0 == cudaSuccess)
+      e0 = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+    if (e0 != cudaSuccess) { delete h; return cuda_fail(e0, "init: device query"); }
+  }
+  h->scale = cfg->softmax_scale > 0 ? (float)cfg->softmax_scale : (float)(1.0 / sqrt((double)l.dqk));
+  char* a = h->arena;
+  h->WA = a + l.off_WA; h->Wqb = a + l.off_Wqb; h->WUKT = a + l.off_WUKT; h->WUV = a + l.off_WUV;
+  h->Wo = a + l.off_Wo; h->gamma_q = (float*)(a + l.off_gq); h->gamma_kv = (float*)(a + l.off_gkv);
+  h->rope = (float2*)(a + l.off_rope); h->status = (uint32_t*)(a + l.off_status);
+  const size_t e = l.elt, rowb = (size_t)l.D * e;
+  char* WA = a + l.off_WA;
+  const char* kv_src = cfg->q_lora_rank > 0 ? (const char*)w->fused_qkv_a_proj + (size_t)l.rq * rowb
+                                            : (const char*)w->kv_a_proj_with_mqa;
+  const char* q_src = cfg->q_lora_rank > 0 ? (const char*)w->fused_qkv_a_proj : (const char*)w->q_proj;
+  cudaError_t err = cudaSuccess;
+#define STEP(x) if (err == cudaSuccess) err = (x)
+  STEP(cudaMemcpyAsync(WA, kv_src, (size_t)l.L * rowb, cudaMemcpyDeviceToDevice, st));
+  STEP(cudaMemcpyAsync(WA + (size_t)l.L * rowb, q_src, (size_t)l.qdim * rowb, cudaMemcpyDeviceToDevice, st));
+  if (l.gdim)
+    STEP(cudaMemcpyAsync(WA + (size_t)(l.L + l.qdim) * rowb, w->gate_proj, (size_t)l.gdim * rowb,
+                         cudaMemcpyDeviceToDevice, st));
+  if (l.rq > 0)
+    STEP(cudaMemcpyAsync(a + l.off_Wqb, w->q_b_proj, (size_t)l.H * l.dqk * l.rq * e,
+                         cudaMemcpyDeviceToDevice, st));
+  // W_UV[h] = rows h*(dn+dv)+dn .. +dv of kv_b_proj
+  STEP(cudaMemcpy2DAsync(a + l.off_WUV, (size_t)l.dv * l.rkv * e,
+                         (const char*)w->kv_b_proj + (size_t)l.dn * l.rkv * e,
+                         (size_t)(l.dn + l.dv) * l.rkv * e, (size_t)l.dv * l.rkv * e, l.H,
+                         cudaMemcpyDeviceToDevice, st));
+  STEP(cudaMemcpyAsync(a + l.off_Wo, w->o_proj, (size_t)l.D * l.H * l.dv * e,
+                       cudaMemcpyDeviceToDevice, st));
+  STEP(cudaMemsetAsync(a + l.off_status, 0, 256, st));
+  if (err != cudaSuccess) { delete h; return cuda_fail(err, "init: weight copy"); }
+  if (cfg->dtype == MLA_BF16) {
+    auto bf = [](const void* p) { return (const __nv_bfloat16*)p; };
+    if (l.rq > 0) to_f32_kernel<<<8, 256, 0, st>>>(bf(w->q_a_layernorm), (float*)(a + l.off_gq), l.rq);
+    to_f32_kernel<<<8, 256, 0, st>>>(bf(w->kv_a_layernorm), (float*)(a + l.off_gkv), l.rkv);
+    wuk_transpose_kernel<<<1024, 256, 0, st>>>(bf(w->kv_b_proj), (__nv_bfloat16*)(a + l.off_WUKT),
+                                               l.H, l.dn, l.dv, l.rkv);
+  } else {
+    auto f = [](const void* p) { return (const float*)p; };
+    if (l.rq > 0) to_f32_kernel<<<8, 256, 0, st>>>(f(w->q_a_layernorm), (float*)(a + l.off_gq), l.rq);
+    to_f32_kernel<<<8, 256, 0, st>>>(f(w->kv_a_layernorm), (float*)(a + l.off_gkv), l.rkv);
+    wuk_transpose_kernel<<<1024, 256, 0, st>>>(f(w->kv_b_proj), (float*)(a + l.off_WUKT), l.H,
+                                               l.dn, l.dv, l.rkv);
+  }
+  // RoPE table: angle = pos * theta^(-2k/dr), cos/sin evaluated in double.
+  const int half = l.dr / 2;
+  std::vector<float2> tab((size_t)cfg->max_position * half);
+  for (int k = 0; k < half; ++k) {
+    const double inv = pow(cfg->rope_theta, -2.0 * k / l.dr);
+    for (int p = 0; p < cfg->max_position; ++p) {
+      const double ang = (double)p * inv;
+      tab[(size_t)p * half + k] = make_float2((float)cos(ang), (float)sin(ang));
+    }
+  }
+  STEP(cudaMemcpyAsync(a + l.off_rope, tab.data(), tab.size() * sizeof(float2),
+                       cudaMemcpyHostToDevice, st));
+  STEP(cudaGetLastError());
+  STEP(cudaStreamSynchronize(st));
+#undef STEP
+  if (err != cudaSuccess) { delete h; return cuda_fail(err, "init: relayout"); }
+  *out = h;
+  return MLA_OK;
+}
+
+extern "C" void mla_draft_destroy(mla_handle_t* h) { delete h; }
+
+// ---------------------------------------------------------------------------
+// Workspace
+// ---------------------------------------------------------------------------
+namespace mla {
+namespace {
+
+struct FwdWs {
+  size_t a_out, q_cn, q_raw, q_nope, q_abs, o_lat, o, total;
+};
+
+FwdWs forward_ws(const Layout& l, long M) {
+  FwdWs w;
+  size_t o = 0;
+  w.a_out = o;  o = align256(o + (size_t)M * l.NA * 4);
+  w.q_cn = o;   o = align256(o + (size_t)M * l.rq * l.elt);
+  w.q_raw = o;  o = align256(o + (l.rq > 0 ? (size_t)M * l.H * l.dqk * 4 : 0));
+  w.q_nope = o; o = align256(o + (size_t)M * l.H * l.dn * l.elt);
+  w.q_abs = o;  o = align256(o + (size_t)M * l.H * l.L * l.elt);
+  w.o_lat = o;  o = align256(o + (size_t)M * l.H * l.rkv * l.elt);
+  w.o = o;      o = align256(o + (size_t)M * l.H * l.dv * l.elt);
+  w.total = o;
+  return w;
+}
+
+size_t append_ws(const Layout& l, long n) { return align256((size_t)n * l.L * 4); }
+
+}  // namespace
+}  // namespace mla
+
+extern "C" size_t mla_append_workspace_bytes(const mla_handle_t* h, int32_t n) {
+  return (h && n >= 0) ? append_ws(h->lay, n) : 0;
+}
+
+extern "C" size_t mla_forward_workspace_bytes(const mla_handle_t* h, int32_t num_tokens) {
+  return (h && num_tokens >= 0) ? forward_ws(h->lay, num_tokens).total : 0;
+}
+
+// ---------------------------------------------------------------------------
+// Latent-cache append
+// ---------------------------------------------------------------------------
+namespace mla {
+namespace {
+
+template <typename T>
+void append_impl(mla_handle_t* h, const void* hidden, const int32_t* positions,
+                 const int64_t* slots, int n, void* cache, long num_slots, float* kv_ws,
+                 cudaStream_t st) {
+  const Layout& l = h->lay;
+  // kv = hidden @ W_kva^T : W_kva = first L rows of W_A
+  simt::gemm_nt<T, float>(st, n, l.L, l.D, 1, (const T*)hidden, l.D, 0, (const T*)h->WA, l.D, 0,
+                          kv_ws, l.L, 0, nullptr, 0, 0);
+  simt::kv_finish<T>(st, h, kv_ws, l.L, n, positions, slots, (T*)cache, num_slots);
+}
+
+}  // namespace
+}  // namespace mla
+
+extern "C" mla_status_t mla_latent_cache_append(mla_handle_t* h, const void* hidden,
+                                                const int32_t* positions,
+                                                const int64_t* slot_mapping, int32_t n,
+                                                void* cache, int32_t num_pages, void* workspace,
+                                                size_t workspace_bytes, void* stream) {
+  if (!h) return fail(MLA_ERR_INVALID_ARG, "append: null handle");
+  if (n < 0) return fail(MLA_ERR_INVALID_ARG, "append: n < 0");
+  if (n == 0) return MLA_OK;
+  if (!hidden || !positions || !slot_mapping || !cache || !workspace)
+    return fail(MLA_ERR_INVALID_ARG, "append: null pointer");
+  if (num_pages <= 0) return fail(MLA_ERR_INVALID_ARG, "append: num_pages <= 0");
+  if (workspace_bytes < append_ws(h->lay, n))
+    return fail(MLA_ERR_INVALID_ARG, "append: workspace smaller than mla_append_workspace_bytes()");
+  cudaStream_t st = (cudaStream_t)stream;
+  const long num_slots = (long)num_pages * h->cfg.page_size;
+  if (h->cfg.dtype == MLA_BF16)
+    append_impl<__nv_bfloat16>(h, hidden, positions, slot_mapping, n, cache, num_slots,
+                               (float*)workspace, st);
+  else
+    append_impl<float>(h, hidden, positions, slot_mapping, n, cache, num_slots,
+                       (float*)workspace, st);
+  MLA_CUDA_TRY(cudaGetLastError());
+  return MLA_OK;
+}
