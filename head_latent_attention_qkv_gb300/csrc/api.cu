@@ -319,3 +319,105 @@ extern "C" mla_status_t mla_latent_cache_append(mla_handle_t* h, const void* hid
   MLA_CUDA_TRY(cudaGetLastError());
   return MLA_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Forward
+// ---------------------------------------------------------------------------
+namespace mla {
+namespace {
+
+template <typename T>
+void forward_impl(mla_handle_t* h, const void* hidden, const int32_t* pos, const int64_t* bslots,
+                  void* cache, int num_pages, const mla_attn_desc_t& d, void* out, char* ws,
+                  cudaStream_t st) {
+  const Layout& l = h->lay;
+  const int M = d.num_blocks * d.block_len;
+  const FwdWs w = forward_ws(l, M);
+  float* a_out = (float*)(ws + w.a_out);
+  const T* x = (const T*)hidden;
+  const T* WA = (const T*)h->WA;
+  // A projection; the kv rows only when the block writes its own latents
+  const int r0 = bslots ? 0 : l.L;
+  simt::gemm_nt<T, float>(st, M, l.NA - r0, l.D, 1, x, l.D, 0, WA + (long)r0 * l.D, l.D, 0,
+                          a_out + r0, l.NA, 0, nullptr, 0, 0);
+  if (bslots)
+    simt::kv_finish<T>(st, h, a_out, l.NA, M, pos, bslots, (T*)cache,
+                       (long)num_pages * h->cfg.page_size);
+  const float* q_raw;
+  long ldq;
+  if (l.rq > 0) {
+    T* q_cn = (T*)(ws + w.q_cn);
+    simt::rmsnorm_rows<T>(st, a_out + l.L, l.NA, M, l.rq, h->gamma_q, (float)h->cfg.rms_norm_eps, q_cn);
+    float* qr = (float*)(ws + w.q_raw);
+    simt::gemm_nt<T, float>(st, M, l.H * l.dqk, l.rq, 1, q_cn, l.rq, 0, (const T*)h->Wqb, l.rq, 0,
+                            qr, l.H * l.dqk, 0, nullptr, 0, 0);
+    q_raw = qr;
+    ldq = l.H * l.dqk;
+  } else {
+    q_raw = a_out + l.L;
+    ldq = l.NA;
+  }
+  T* q_nope = (T*)(ws + w.q_nope);
+  T* q_abs = (T*)(ws + w.q_abs);
+  simt::q_rope_split<T>(st, h, q_raw, ldq, M, pos, q_nope, q_abs);
+  // q_lat[h] = q_nope[h] @ W_UK[h]  ->  Q_abs[:, h, :rkv]
+  simt::gemm_nt<T, T>(st, M, l.rkv, l.dn, l.H, q_nope, (long)l.H * l.dn, l.dn,
+                      (const T*)h->WUKT, l.dn, (long)l.rkv * l.dn, q_abs, (long)l.H * l.L, l.L,
+                      nullptr, 0, 0);
+  T* o_lat = (T*)(ws + w.o_lat);
+  simt::latent_attention<T>(st, h, q_abs, (const T*)cache, num_pages, d, pos, o_lat);
+  // o[h] = o_lat[h] @ W_UV[h]^T (* sigmoid(gate))
+  T* o = (T*)(ws + w.o);
+  const float* gate = l.gdim ? a_out + l.L + l.qdim : nullptr;
+  simt::gemm_nt<T, T>(st, M, l.dv, l.rkv, l.H, o_lat, (long)l.H * l.rkv, l.rkv, (const T*)h->WUV,
+                      l.rkv, (long)l.dv * l.rkv, o, (long)l.H * l.dv, l.dv, gate, l.NA, l.dv);
+  simt::gemm_nt<T, T>(st, M, l.D, l.H * l.dv, 1, o, (long)l.H * l.dv, 0, (const T*)h->Wo,
+                      (long)l.H * l.dv, 0, (T*)out, l.D, 0, nullptr, 0, 0);
+}
+
+}  // namespace
+}  // namespace mla
+
+extern "C" mla_status_t mla_draft_forward(mla_handle_t* h, const void* hidden,
+                                          const int32_t* positions,
+                                          const int64_t* block_slot_mapping, void* cache,
+                                          int32_t num_pages, const mla_attn_desc_t* desc,
+                                          void* out, void* workspace, size_t workspace_bytes,
+                                          void* stream) {
+  if (!h || !desc) return fail(MLA_ERR_INVALID_ARG, "forward: null handle or descriptor");
+  const mla_attn_desc_t& d = *desc;
+  if (d.num_blocks < 0 || d.block_len <= 0 || d.max_pages <= 0)
+    return fail(MLA_ERR_INVALID_ARG, "forward: num_blocks >= 0, block_len > 0, max_pages > 0");
+  if (d.num_blocks == 0) return MLA_OK;
+  if ((long)d.num_blocks * d.block_len > 0x7fffffffL)
+    return fail(MLA_ERR_INVALID_ARG, "forward: too many tokens");
+  if (!hidden || !positions || !cache || !out || !workspace || !d.block_table || !d.kv_len)
+    return fail(MLA_ERR_INVALID_ARG, "forward: null pointer");
+  if (num_pages <= 0) return fail(MLA_ERR_INVALID_ARG, "forward: num_pages <= 0");
+  const int M = d.num_blocks * d.block_len;
+  if (workspace_bytes < forward_ws(h->lay, M).total)
+    return fail(MLA_ERR_INVALID_ARG, "forward: workspace smaller than mla_forward_workspace_bytes()");
+  if ((uintptr_t)workspace % 256) return fail(MLA_ERR_INVALID_ARG, "forward: workspace must be 256-byte aligned");
+  cudaStream_t st = (cudaStream_t)stream;
+  if (h->cfg.dtype == MLA_BF16)
+    forward_impl<__nv_bfloat16>(h, hidden, positions, block_slot_mapping, cache, num_pages, d, out,
+                                (char*)workspace, st);
+  else
+    forward_impl<float>(h, hidden, positions, block_slot_mapping, cache, num_pages, d, out,
+                        (char*)workspace, st);
+  MLA_CUDA_TRY(cudaGetLastError());
+  return MLA_OK;
+}
+
+extern "C" mla_status_t mla_get_device_status(mla_handle_t* h, void* stream, int32_t* bits) {
+  if (!h) return fail(MLA_ERR_INVALID_ARG, "status: null handle");
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t v = 0;
+  MLA_CUDA_TRY(cudaStreamSynchronize(st));
+  MLA_CUDA_TRY(cudaMemcpy(&v, h->status, sizeof(v), cudaMemcpyDeviceToHost));
+  MLA_CUDA_TRY(cudaMemset(h->status, 0, sizeof(v)));
+  if (bits) *bits = (int32_t)v;
+  if (v & MLA_DEV_TIMEOUT) return fail(MLA_ERR_TIMEOUT, "device: a bounded wait expired");
+  if (v) return fail(MLA_ERR_DEVICE_CHECK, "device: index check failed (bits " + std::to_string(v) + ")");
+  return MLA_OK;
+}
