@@ -1,0 +1,87 @@
+"""Drive a synthetic workload through the CUDA library (device side).
+
+Uploads the seeded inputs of ``workloads.Workload`` to the GPU, then runs the
+call sequence: prefilled cache entries are copied in, context tokens are
+appended with ``mla_latent_cache_append``, and every step appends its tokens
+(if any) and calls ``mla_draft_forward``.  Only data movement happens here;
+all of the layer's arithmetic runs in the library.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import api
+
+
+def to_dev(a, dtype=None, device="cuda"):
+    if a is None:
+        return None
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.to(device)
+
+
+class DeviceWorkload:
+    """Device copies of a workload's inputs, ready for repeated runs."""
+
+    def __init__(self, wl, device="cuda", cache_fill=float("nan")):
+        self.wl, self.device = wl, device
+        dt = api.torch_dtype(wl.dims)
+        self.dtype = dt
+        self.weights = {k: to_dev(v, dt, device) for k, v in wl.weights.items() if v is not None}
+        self.handle = api.mla_draft_init(wl.dims, self.weights, wl.page_size, device)
+        self.cache = torch.full(wl.cache_shape, cache_fill, dtype=dt, device=device)
+        self.cache_fill = cache_fill
+        self.ctx = None
+        if wl.ctx_hidden is not None:
+            self.ctx = (to_dev(wl.ctx_hidden, dt, device), to_dev(wl.ctx_positions, None, device),
+                        to_dev(wl.ctx_slots, None, device))
+        self.prefill = None
+        if wl.prefill_slots is not None:
+            self.prefill = (to_dev(wl.prefill_slots, None, device),
+                            to_dev(wl.prefill_values, dt, device))
+        self.steps = []
+        for s in wl.steps:
+            d = dict(
+                append=None if s.append_hidden is None else (
+                    to_dev(s.append_hidden, dt, device), to_dev(s.append_positions, None, device),
+                    to_dev(s.append_slots, None, device)),
+                hidden=to_dev(s.block_hidden, dt, device),
+                positions=to_dev(s.block_positions, None, device),
+                slots=to_dev(s.block_slots, None, device),
+                block_table=to_dev(s.block_table, None, device),
+                kv_len=to_dev(s.kv_len, None, device),
+                window=to_dev(s.window, None, device),
+                q_visible=to_dev(s.q_visible, None, device),
+                vis_stats=torch.full((len(s.block_positions), 3), -7, dtype=torch.int32, device=device),
+            )
+            d["desc"] = api.make_desc(d["block_table"], d["kv_len"], d["window"], d["q_visible"],
+                                      wl.block_len, d["vis_stats"])
+            d["out"] = torch.empty(len(s.block_positions), wl.dims.hidden_size, dtype=dt, device=device)
+            self.steps.append(d)
+
+    def reset_cache(self):
+        self.cache.fill_(self.cache_fill)
+        if self.prefill is not None:
+            flat = self.cache.view(-1, self.wl.dims.cache_dim)
+            flat[self.prefill[0]] = self.prefill[1]
+
+    def append_context(self):
+        if self.ctx is not None:
+            api.mla_latent_cache_append(self.handle, *self.ctx, self.cache)
+
+    def run_step(self, k):
+        s = self.steps[k]
+        if s["append"] is not None:
+            api.mla_latent_cache_append(self.handle, *s["append"], self.cache)
+        api.mla_draft_forward(self.handle, s["hidden"], s["positions"], s["slots"], self.cache,
+                              s["desc"], out=s["out"])
+        return s["out"]
+
+    def run_all(self):
+        """Fresh cache, context append, every step.  Returns the step outputs."""
+        self.reset_cache()
+        self.append_context()
+        return [self.run_step(k).clone() for k in range(len(self.steps))]
