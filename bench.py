@@ -1,0 +1,310 @@
+"""Benchmark of the MLA draft-layer hot path on GB300.
+
+One step = the whole path over one batch of the Qwen3-4B-sized block-prefill
+workload (8 sequences x (2048 context tokens + one 16-token draft block),
+bf16): latent-cache append of the 16384 context tokens, then the draft-layer
+forward of the 128 block tokens.  Inputs are seeded synthetic data resident
+in HBM; L2 (126 MB) is flushed by writing a 256 MB buffer between timed steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun as independent replicas (the forward shards by
+sequence with no exchange step): each rank owns a full workload, rank 0
+prints one JSON line with the max time over ranks and the summed tokens.
+``--impl reference`` times the fp64 CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "qwen3_4b_prefill"
+METRIC = "MLA draft-layer tokens/s (block query tokens; TFLOP/s and %bf16 peak alongside)"
+
+
+def algorithmic_flops(wl):
+    """Absorbed latent path: per block token 2D(r_q+L) [+2D*H*dv gate] +
+    2 r_q H dqk + 2 H dn r_kv + 2 H r_kv dv + 2 H dv D, per visible key
+    H (2L + 2 r_kv); per appended context token 2 D L."""
+    d = wl.dims
+    H, D, L = d.num_heads, d.hidden_size, d.cache_dim
+    qdim = d.q_lora_rank if d.q_lora_rank else H * d.qk_head_dim
+    per_tok = 2 * D * (qdim + L) + (2 * D * H * d.v_head_dim if d.use_output_gate else 0)
+    if d.q_lora_rank:
+        per_tok += 2 * d.q_lora_rank * H * d.qk_head_dim
+    per_tok += 2 * H * d.qk_nope_head_dim * d.kv_lora_rank + 2 * H * d.kv_lora_rank * d.v_head_dim
+    per_tok += 2 * H * d.v_head_dim * D
+    step = wl.steps[0]
+    T = wl.block_len
+    keys = 0
+    for b in range(len(step.kv_len)):      # visible keys per query: [lo, kv_len)
+        r = slice(b * T, (b + 1) * T)
+        n, w = int(step.kv_len[b]), int(step.window[b])
+        p = step.block_positions[r].astype(np.int64)
+        lo = np.maximum(0, p - w + 1) if w > 0 else np.zeros_like(p)
+        keys += int(((n - lo) * step.q_visible[r]).sum())
+    n_ctx = 0 if wl.ctx_hidden is None else len(wl.ctx_hidden)
+    append = 2 * D * L * n_ctx
+    return dict(total=per_tok * len(step.block_positions) + H * (2 * L + 2 * d.kv_lora_rank) * keys + append,
+                append=append, block_tokens=len(step.block_positions), ctx_tokens=n_ctx)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.samples, self.index, self.stop = [], index, threading.Event()
+
+    def _run(self):
+        while not self.stop.is_set():
+            try:
+                out = subprocess.run(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                      "--format=csv,noheader,nounits"], capture_output=True,
+                                     text=True, timeout=5).stdout.strip()
+                if out:
+                    self.samples.append([x.strip() for x in out.split(",")])
+            except Exception:
+                pass
+            time.sleep(0.2)
+
+    def __enter__(self):
+        self.t = threading.Thread(target=self._run, daemon=True)
+        self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        self.stop.set()
+        self.t.join(timeout=10)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4)
+                          if len(s) > 2 + i and s[2 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.samples)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def run_ours(args, rank, world):
+    import torch
+    from head_latent_attention_qkv_gb300 import api, workloads
+    from head_latent_attention_qkv_gb300.runner import DeviceWorkload
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    wl = workloads.make_workload(WORKLOAD)
+    fl = algorithmic_flops(wl)
+    dev = DeviceWorkload(wl)
+    step = dev.steps[0]
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def append():
+        dev.append_context()
+
+    def forward():
+        dev.run_step(0)
+
+    dev.reset_cache()
+    n0 = api._lib.lib.mla_kernel_launches(dev.handle.h)
+    append()
+    forward()
+    launches = int(api._lib.lib.mla_kernel_launches(dev.handle.h) - n0)
+    for _ in range(args.warmup):
+        append()
+        forward()
+    graphs = None
+    if not args.no_graph:
+        graphs = []
+        for fn in (append, forward):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            graphs.append(g)
+        for _ in range(2):
+            graphs[0].replay()
+            graphs[1].replay()
+    run_a = graphs[0].replay if graphs else append
+    run_f = graphs[1].replay if graphs else forward
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        for k in range(args.steps):
+            flush.fill_(k & 0xFF)                      # evict L2 between steps (untimed)
+            ev[k][0].record(stream)
+            run_a()
+            ev[k][1].record(stream)
+            run_f()
+            ev[k][2].record(stream)
+        torch.cuda.synchronize()
+    t_step = [e[0].elapsed_time(e[2]) for e in ev]
+    t_app = [e[0].elapsed_time(e[1]) for e in ev]
+    ms = sum(t_step) / len(t_step)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    assert api.mla_get_device_status(dev.handle) == 0, "device status word set"
+    e2e = measure_e2e(args, dev, wl, torch)
+    return dict(ms=ms, ms_append=sum(t_app) / len(t_app), flops=fl, clocks=clocks.summary(),
+                e2e=e2e, graphs=graphs is not None, launches=launches)
+
+
+def measure_e2e(args, dev, wl, torch):
+    """Same step through the C ABI with host buffers: pinned host -> device
+    copies of the step's inputs, append + forward, device -> host of the
+    output, all inside the timed region."""
+    from head_latent_attention_qkv_gb300 import api
+    s = dev.steps[0]
+    host = {n: t.cpu().pin_memory() for n, t in (("ctx_h", dev.ctx[0]), ("ctx_p", dev.ctx[1]),
+                                                  ("ctx_s", dev.ctx[2]), ("h", s["hidden"]),
+                                                  ("p", s["positions"]), ("s", s["slots"]))}
+    out_host = torch.empty(s["out"].shape, dtype=s["out"].dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    dst = {"ctx_h": dev.ctx[0], "ctx_p": dev.ctx[1], "ctx_s": dev.ctx[2], "h": s["hidden"],
+           "p": s["positions"], "s": s["slots"]}
+    times = []
+    for k in range(args.warmup + args.steps):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for n, t in host.items():
+            dst[n].copy_(t, non_blocking=True)
+        api.mla_latent_cache_append(dev.handle, dev.ctx[0], dev.ctx[1], dev.ctx[2], dev.cache)
+        api.mla_draft_forward(dev.handle, s["hidden"], s["positions"], s["slots"], dev.cache,
+                              s["desc"], out=s["out"])
+        out_host.copy_(s["out"], non_blocking=True)
+        torch.cuda.synchronize()
+        if k >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    return sum(times) / len(times), h2d, d2h
+
+
+def cpu_baseline(budget_s=15.0):
+    """The fp64 oracle as it stands, on a bounded sample of the same workload:
+    whole blocks (context latents of the block's sequence + the block's
+    forward), as many as fit in ``budget_s``.  Returns block tokens/s."""
+    from head_latent_attention_qkv_gb300 import workloads
+    from oracle.keys import OracleRun
+    wl = workloads.make_workload(WORKLOAD)
+    step = wl.steps[0]
+    run = OracleRun(wl)
+    t0 = time.perf_counter()
+    done = 0
+    for b in range(len(step.kv_len)):
+        rows = np.nonzero(wl.ctx_seq == step.block_seq[b])[0]
+        run.append(wl.ctx_hidden, wl.ctx_positions, wl.ctx_slots, rows)
+        run.forward_blocks(step, [b])
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0))
+    return dict(value=done * wl.block_len / dt, unit="tokens/s", cores=cores, kind="oracle",
+                sample=f"{done} of {len(step.kv_len)} blocks (each: {len(rows)} context-token "
+                       f"appends + one 16-token block forward), fp64 numpy, {dt:.1f} s")
+
+
+def base_line(args, world):
+    return {"metric": METRIC, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "data": "synthetic (seeded N(0,1) hidden, N(0,0.02) weights)",
+            "config": {"workload": WORKLOAD, "model": "Qwen3-4B-sized MLA draft layer",
+                       "global_batch": 8 * world, "seq_len": 2048 + 16, "block_len": 16,
+                       "parallelism": f"replicas x{world}", "l2": "flushed (256 MB write) between steps"}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        # the reference arm is the fp64 CPU oracle; rank 0 alone runs it
+        if rank != 0:
+            return
+        per = []
+        for _ in range(args.steps):
+            per.append(cpu_baseline(budget_s=max(2.0, 60.0 / max(args.steps, 1))))
+        v = statistics.median(p["value"] for p in per)
+        line = base_line(args, 1)
+        line.update({"impl": "reference", "value": v, "ms_per_step": 8 * 16 / v * 1e3,
+                     "dtype": "f64", "cpu_baseline": dict(per[-1], value=v),
+                     "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                             "d2h_bytes_per_step": 0}})
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    r = run_ours(args, rank, world)
+    if rank != 0:
+        torch.distributed.destroy_process_group() if world > 1 else None
+        return
+    hbm, bf16, bf16_sus, src = measured_peaks()
+    fl = r["flops"]
+    value = world * fl["block_tokens"] / (r["ms"] * 1e-3)
+    tflops = fl["total"] / (r["ms"] * 1e-3) / 1e12
+    t_app = r["ms_append"] * 1e-3
+    ach = fl["append"] / t_app / 1e12
+    line = base_line(args, world)
+    e2e_s, h2d, d2h = r["e2e"]
+    line.update({
+        "value": value, "ms_per_step": r["ms"], "dtype": "bf16",
+        "tflops": tflops, "pct_bf16_peak": 100 * tflops / bf16,
+        "context_tokens_per_s": world * fl["ctx_tokens"] / (r["ms"] * 1e-3),
+        "roofline": {"kernel": "latent-cache append (context GEMM N=576 + norm/RoPE/cache store)",
+                     "bound": "tensor", "achieved": ach, "peak": bf16, "unit": "TFLOP/s",
+                     "frac": ach / bf16, "traffic": None,
+                     "peak_source": f"{src} bf16 burst"},
+        "e2e": {"value": world * fl["block_tokens"] / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": r["launches"] * args.steps,
+        "cuda_graphs": r["graphs"],
+        "clocks": r["clocks"],
+    })
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -65,6 +65,7 @@ def _load():
         "mla_draft_forward": (I32, [P, P, P, P, P, I32, C.POINTER(mla_attn_desc_t), P, P, SZ, P]),
         "mla_get_device_status": (I32, [P, P, C.POINTER(I32)]),
         "mla_draft_destroy": (None, [P]),
+        "mla_kernel_launches": (C.c_ulonglong, [P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)

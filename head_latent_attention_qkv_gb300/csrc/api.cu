@@ -290,6 +290,7 @@ void append_impl(mla_handle_t* h, const void* hidden, const int32_t* positions,
   simt::gemm_nt<T, float>(st, n, l.L, l.D, 1, (const T*)hidden, l.D, 0, (const T*)h->WA, l.D, 0,
                           kv_ws, l.L, 0, nullptr, 0, 0);
   simt::kv_finish<T>(st, h, kv_ws, l.L, n, positions, slots, (T*)cache, num_slots);
+  h->launches += 2;
 }
 
 }  // namespace
@@ -373,6 +374,8 @@ void forward_impl(mla_handle_t* h, const void* hidden, const int32_t* pos, const
                       l.rkv, (long)l.dv * l.rkv, o, (long)l.H * l.dv, l.dv, gate, l.NA, l.dv);
   simt::gemm_nt<T, T>(st, M, l.D, l.H * l.dv, 1, o, (long)l.H * l.dv, 0, (const T*)h->Wo,
                       (long)l.H * l.dv, 0, (T*)out, l.D, 0, nullptr, 0, 0);
+  // A proj, [kv finish], [q norm, q_b], rope split, W_UK, attention, W_UV, o_proj
+  h->launches += 6 + (bslots ? 1 : 0) + (l.rq > 0 ? 2 : 0);
 }
 
 }  // namespace
@@ -421,3 +424,5 @@ extern "C" mla_status_t mla_get_device_status(mla_handle_t* h, void* stream, int
   if (v) return fail(MLA_ERR_DEVICE_CHECK, "device: index check failed (bits " + std::to_string(v) + ")");
   return MLA_OK;
 }
+
+extern "C" unsigned long long mla_kernel_launches(const mla_handle_t* h) { return h ? h->launches : 0; }

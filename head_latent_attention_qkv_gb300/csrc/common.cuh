@@ -68,4 +68,5 @@ struct mla_handle {
   const void* WUKT;     // [H, rkv, dn]
   const void* WUV;      // [H, dv, rkv]
   const void* Wo;
+  unsigned long long launches;  // kernels enqueued through this handle
 };

@@ -188,6 +188,10 @@ mla_status_t mla_draft_forward(mla_handle_t *h, const void *hidden,
  * raw bits go to *bits when non-NULL. */
 mla_status_t mla_get_device_status(mla_handle_t *h, void *stream, int32_t *bits);
 
+/* Number of CUDA kernels this handle has enqueued so far (host counter;
+ * launches replayed from a captured CUDA graph are not counted). */
+unsigned long long mla_kernel_launches(const mla_handle_t *h);
+
 void mla_draft_destroy(mla_handle_t *h);
 const char *mla_status_string(mla_status_t s);
 /* Message of the last failing call on this thread ("" if none). */

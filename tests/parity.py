@@ -1,0 +1,77 @@
+"""GPU-vs-oracle comparison helpers for the parity tests.
+
+Tolerances (from the layer's contract): outputs max|gpu - ref| <= 2e-2 * rms
+and mean|gpu - ref| <= 2e-3 * rms for bf16 (rms over rows that are not fully
+masked), 1e-4 for both in the fp32 configuration.  Exact checks: fully
+masked rows are bitwise +0.0; the per-row visible-key count, first and last
+visible key reported by the kernel equal the oracle's visibility; the cache
+slots written are exactly the slots the calls name (every other slot keeps
+its NaN sentinel); written latents are within tolerance of the oracle's.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from head_latent_attention_qkv_gb300 import api
+from head_latent_attention_qkv_gb300.runner import DeviceWorkload
+from oracle.keys import run_workload
+
+
+def tolerances(dims):
+    return (1e-4, 1e-4) if dims.dtype == "fp32" else (2e-2, 2e-3)
+
+
+def compare(got, ref, dims, what, valid_rows=None):
+    tmax, tmean = tolerances(dims)
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    sel = slice(None) if valid_rows is None else valid_rows
+    rms = np.sqrt(np.mean(ref[sel] ** 2))
+    assert np.all(np.isfinite(got[sel])), f"{what}: non-finite values"
+    err = np.abs(got[sel] - ref[sel])
+    emax, emean = err.max() / rms, err.mean() / rms
+    assert emax <= tmax and emean <= tmean, f"{what}: max {emax:.3e} mean {emean:.3e} (rms {rms:.3e})"
+    return emax, emean
+
+
+def vis_expected(run, step, b):
+    vis = run.block_visibility(step, b)
+    cnt = vis.sum(axis=1)
+    first = np.where(cnt > 0, vis.argmax(axis=1), -1)
+    last = np.where(cnt > 0, vis.shape[1] - 1 - vis[:, ::-1].argmax(axis=1), -1)
+    return np.stack([cnt, first, last], axis=1)
+
+
+def check_workload(wl, blocks_per_step=None, check_cache=True):
+    dev = DeviceWorkload(wl)
+    outs_gpu = dev.run_all()
+    torch.cuda.synchronize()
+    assert api.mla_get_device_status(dev.handle) == 0
+    run, outs_ref = run_workload(wl, blocks_per_step)
+    T = wl.block_len
+    report = []
+    for k, step in enumerate(wl.steps):
+        blocks = sorted(outs_ref[k])
+        got = outs_gpu[k].float().cpu().numpy().reshape(-1, T, wl.dims.hidden_size)[blocks]
+        ref = np.stack([outs_ref[k][b] for b in blocks])
+        qv = step.q_visible.reshape(-1, T)[blocks].astype(bool)
+        report.append(compare(got, ref, wl.dims, f"{wl.name} step {k} out", qv))
+        assert np.all(got[~qv] == 0) and not np.signbit(got[~qv]).any(), "masked rows not +0"
+        vs = dev.steps[k]["vis_stats"].cpu().numpy().reshape(-1, T, 3)
+        for b in blocks:
+            np.testing.assert_array_equal(vs[b], vis_expected(run, step, b),
+                                          err_msg=f"{wl.name} step {k} block {b} visibility")
+    if check_cache:
+        cache = dev.cache.float().cpu().numpy().reshape(-1, wl.dims.cache_dim)
+        named = np.zeros(len(cache), dtype=bool)
+        for s in (wl.ctx_slots, wl.prefill_slots, *[x.block_slots for x in wl.steps],
+                  *[x.append_slots for x in wl.steps]):
+            if s is not None:
+                named[s] = True
+        assert np.all(np.isnan(cache[~named])), "a slot outside the slot mappings was written"
+        assert np.all(np.isfinite(cache[named])), "a named slot was not written"
+        report.append(compare(cache[run.written], run.cache[run.written], wl.dims,
+                              f"{wl.name} cache"))
+    dev.handle.close()
+    return report
