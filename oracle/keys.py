@@ -38,7 +38,8 @@ class OracleRun:
         rows = np.asarray(rows)
         if rows.size == 0:
             return np.zeros((0, self.d.cache_dim))
-        ent = mla.latent_cache_entries(self.d, self.wl.weights, hidden[rows], positions[rows])
+        ent = mla.store_in_cache_dtype(
+            self.d, mla.latent_cache_entries(self.d, self.wl.weights, hidden[rows], positions[rows]))
         self.cache[slots[rows]] = ent
         self.written[slots[rows]] = True
         return ent

@@ -130,6 +130,22 @@ def latent_cache_entries(d, w, hidden, positions):
     return np.concatenate([c, k_pe], axis=1)
 
 
+def store_in_cache_dtype(d, entries):
+    """The value a cache slot holds: the entry rounded to the cache's dtype.
+
+    MLA blog, ``do_kv_cache_update`` / ``concat_and_cache_mla(...,
+    kv_cache_dtype=...)`` and ``get_kv_cache_spec`` (``dtype=kv_cache_dtype``):
+    the latent cache is a typed tensor, so attention reads back the stored
+    values.  For a bf16 cache each fp64 entry is rounded to the nearest bf16
+    (ties to even); an fp32 cache keeps fp64 here (the fp32 rounding is far
+    below that configuration's tolerance)."""
+    e = _f64(entries)
+    if getattr(d, "dtype", "fp32") != "bf16":
+        return e
+    m, ex = np.frexp(e)                      # e = m * 2^ex, 0.5 <= |m| < 1
+    return np.ldexp(np.rint(m * 256.0), ex - 8)  # 8 significant bits, ties to even
+
+
 def project_queries(d, w, x, positions):
     """Rotated queries ``[N, H, qk_nope + qk_rope]`` (nope first, rope last).
 
