@@ -110,9 +110,29 @@ __global__ void to_f32_kernel(const T* __restrict__ in, float* __restrict__ out,
     out[i] = to_f32(in[i]);
 }
 
+template <typename TI, typename TO>
+__global__ void convert_kernel(const TI* __restrict__ in, TO* __restrict__ out, long n) {
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x)
+    out[i] = from_f32<TO>(to_f32(in[i]));
+}
+
+// W_UV[h][v][c] = kv_b_proj[h*(dn+dv) + dn + v][c]   (v < dv, c < rkv)
+template <typename TI, typename TO>
+__global__ void wuv_gather_kernel(const TI* __restrict__ kvb, TO* __restrict__ out, int H, int dn,
+                                  int dv, int rkv) {
+  const long total = (long)H * dv * rkv;
+  for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < total;
+       idx += (long)gridDim.x * blockDim.x) {
+    const int c = idx % rkv;
+    const int v = (idx / rkv) % dv;
+    const int h = idx / ((long)rkv * dv);
+    out[idx] = from_f32<TO>(to_f32(kvb[((long)h * (dn + dv) + dn + v) * rkv + c]));
+  }
+}
+
 // W_UK^T[h][c][i] = kv_b_proj[h*(dn+dv) + i][c]   (i < dn, c < rkv)
-template <typename T>
-__global__ void wuk_transpose_kernel(const T* __restrict__ kvb, T* __restrict__ out, int H,
+template <typename TI, typename TO>
+__global__ void wuk_transpose_kernel(const TI* __restrict__ kvb, TO* __restrict__ out, int H,
                                      int dn, int dv, int rkv) {
   const long total = (long)H * rkv * dn;
   for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < total;
@@ -120,8 +140,28 @@ __global__ void wuk_transpose_kernel(const T* __restrict__ kvb, T* __restrict__ 
     const int i = idx % dn;
     const int c = (idx / dn) % rkv;
     const int h = idx / ((long)dn * rkv);
-    out[idx] = kvb[((long)h * (dn + dv) + i) * rkv + c];
+    out[idx] = from_f32<TO>(to_f32(kvb[((long)h * (dn + dv) + i) * rkv + c]));
   }
+}
+
+// Derived weights that meet the intermediate activations (W_qb, W_UK^T, W_UV,
+// W_o) are stored in the intermediate type TO (fp16 for bf16 layers, an
+// exact conversion for weights of normal magnitude).
+template <typename TI, typename TO>
+void relayout_weights(const Layout& l, const mla_weights_t& w, char* a, cudaStream_t st) {
+  const int G = 1024, B = 256;
+  if (l.rq > 0) {
+    convert_kernel<TI, TO><<<G, B, 0, st>>>((const TI*)w.q_b_proj, (TO*)(a + l.off_Wqb),
+                                            (long)l.H * l.dqk * l.rq);
+    convert_kernel<TI, float><<<8, B, 0, st>>>((const TI*)w.q_a_layernorm, (float*)(a + l.off_gq), l.rq);
+  }
+  convert_kernel<TI, float><<<8, B, 0, st>>>((const TI*)w.kv_a_layernorm, (float*)(a + l.off_gkv), l.rkv);
+  wuk_transpose_kernel<TI, TO><<<G, B, 0, st>>>((const TI*)w.kv_b_proj, (TO*)(a + l.off_WUKT), l.H,
+                                                 l.dn, l.dv, l.rkv);
+  wuv_gather_kernel<TI, TO><<<G, B, 0, st>>>((const TI*)w.kv_b_proj, (TO*)(a + l.off_WUV), l.H,
+                                              l.dn, l.dv, l.rkv);
+  convert_kernel<TI, TO><<<G, B, 0, st>>>((const TI*)w.o_proj, (TO*)(a + l.off_Wo),
+                                          (long)l.D * l.H * l.dv);
 }
 
 mla_status_t validate(const mla_config_t& c, const mla_weights_t& w, Layout* l) {
@@ -191,31 +231,12 @@ extern "C" mla_status_t mla_draft_init(const mla_config_t* cfg, const mla_weight
   if (l.gdim)
     STEP(cudaMemcpyAsync(WA + (size_t)(l.L + l.qdim) * rowb, w->gate_proj, (size_t)l.gdim * rowb,
                          cudaMemcpyDeviceToDevice, st));
-  if (l.rq > 0)
-    STEP(cudaMemcpyAsync(a + l.off_Wqb, w->q_b_proj, (size_t)l.H * l.dqk * l.rq * e,
-                         cudaMemcpyDeviceToDevice, st));
-  // W_UV[h] = rows h*(dn+dv)+dn .. +dv of kv_b_proj
-  STEP(cudaMemcpy2DAsync(a + l.off_WUV, (size_t)l.dv * l.rkv * e,
-                         (const char*)w->kv_b_proj + (size_t)l.dn * l.rkv * e,
-                         (size_t)(l.dn + l.dv) * l.rkv * e, (size_t)l.dv * l.rkv * e, l.H,
-                         cudaMemcpyDeviceToDevice, st));
-  STEP(cudaMemcpyAsync(a + l.off_Wo, w->o_proj, (size_t)l.D * l.H * l.dv * e,
-                       cudaMemcpyDeviceToDevice, st));
   STEP(cudaMemsetAsync(a + l.off_status, 0, 256, st));
   if (err != cudaSuccess) { delete h; return cuda_fail(err, "init: weight copy"); }
-  if (cfg->dtype == MLA_BF16) {
-    auto bf = [](const void* p) { return (const __nv_bfloat16*)p; };
-    if (l.rq > 0) to_f32_kernel<<<8, 256, 0, st>>>(bf(w->q_a_layernorm), (float*)(a + l.off_gq), l.rq);
-    to_f32_kernel<<<8, 256, 0, st>>>(bf(w->kv_a_layernorm), (float*)(a + l.off_gkv), l.rkv);
-    wuk_transpose_kernel<<<1024, 256, 0, st>>>(bf(w->kv_b_proj), (__nv_bfloat16*)(a + l.off_WUKT),
-                                               l.H, l.dn, l.dv, l.rkv);
-  } else {
-    auto f = [](const void* p) { return (const float*)p; };
-    if (l.rq > 0) to_f32_kernel<<<8, 256, 0, st>>>(f(w->q_a_layernorm), (float*)(a + l.off_gq), l.rq);
-    to_f32_kernel<<<8, 256, 0, st>>>(f(w->kv_a_layernorm), (float*)(a + l.off_gkv), l.rkv);
-    wuk_transpose_kernel<<<1024, 256, 0, st>>>(f(w->kv_b_proj), (float*)(a + l.off_WUKT), l.H,
-                                               l.dn, l.dv, l.rkv);
-  }
+  if (cfg->dtype == MLA_BF16)
+    relayout_weights<__nv_bfloat16, __half>(l, *w, a, st);
+  else
+    relayout_weights<float, float>(l, *w, a, st);
   // RoPE table: angle = pos * theta^(-2k/dr), cos/sin evaluated in double.
   const int half = l.dr / 2;
   std::vector<float2> tab((size_t)cfg->max_position * half);
@@ -327,7 +348,7 @@ extern "C" mla_status_t mla_latent_cache_append(mla_handle_t* h, const void* hid
 namespace mla {
 namespace {
 
-template <typename T>
+template <typename TX, typename TI>
 void forward_impl(mla_handle_t* h, const void* hidden, const int32_t* pos, const int64_t* bslots,
                   void* cache, int num_pages, const mla_attn_desc_t& d, void* out, char* ws,
                   cudaStream_t st) {
@@ -335,22 +356,22 @@ void forward_impl(mla_handle_t* h, const void* hidden, const int32_t* pos, const
   const int M = d.num_blocks * d.block_len;
   const FwdWs w = forward_ws(l, M);
   float* a_out = (float*)(ws + w.a_out);
-  const T* x = (const T*)hidden;
-  const T* WA = (const T*)h->WA;
+  const TX* x = (const TX*)hidden;
+  const TX* WA = (const TX*)h->WA;
   // A projection; the kv rows only when the block writes its own latents
   const int r0 = bslots ? 0 : l.L;
-  simt::gemm_nt<T, float>(st, M, l.NA - r0, l.D, 1, x, l.D, 0, WA + (long)r0 * l.D, l.D, 0,
+  simt::gemm_nt<TX, float>(st, M, l.NA - r0, l.D, 1, x, l.D, 0, WA + (long)r0 * l.D, l.D, 0,
                           a_out + r0, l.NA, 0, nullptr, 0, 0);
   if (bslots)
-    simt::kv_finish<T>(st, h, a_out, l.NA, M, pos, bslots, (T*)cache,
+    simt::kv_finish<TX>(st, h, a_out, l.NA, M, pos, bslots, (TX*)cache,
                        (long)num_pages * h->cfg.page_size);
   const float* q_raw;
   long ldq;
   if (l.rq > 0) {
-    T* q_cn = (T*)(ws + w.q_cn);
-    simt::rmsnorm_rows<T>(st, a_out + l.L, l.NA, M, l.rq, h->gamma_q, (float)h->cfg.rms_norm_eps, q_cn);
+    TI* q_cn = (TI*)(ws + w.q_cn);
+    simt::rmsnorm_rows<TI>(st, a_out + l.L, l.NA, M, l.rq, h->gamma_q, (float)h->cfg.rms_norm_eps, q_cn);
     float* qr = (float*)(ws + w.q_raw);
-    simt::gemm_nt<T, float>(st, M, l.H * l.dqk, l.rq, 1, q_cn, l.rq, 0, (const T*)h->Wqb, l.rq, 0,
+    simt::gemm_nt<TI, float>(st, M, l.H * l.dqk, l.rq, 1, q_cn, l.rq, 0, (const TI*)h->Wqb, l.rq, 0,
                             qr, l.H * l.dqk, 0, nullptr, 0, 0);
     q_raw = qr;
     ldq = l.H * l.dqk;
@@ -358,22 +379,22 @@ void forward_impl(mla_handle_t* h, const void* hidden, const int32_t* pos, const
     q_raw = a_out + l.L;
     ldq = l.NA;
   }
-  T* q_nope = (T*)(ws + w.q_nope);
-  T* q_abs = (T*)(ws + w.q_abs);
-  simt::q_rope_split<T>(st, h, q_raw, ldq, M, pos, q_nope, q_abs);
+  TI* q_nope = (TI*)(ws + w.q_nope);
+  TI* q_abs = (TI*)(ws + w.q_abs);
+  simt::q_rope_split<TI>(st, h, q_raw, ldq, M, pos, q_nope, q_abs);
   // q_lat[h] = q_nope[h] @ W_UK[h]  ->  Q_abs[:, h, :rkv]
-  simt::gemm_nt<T, T>(st, M, l.rkv, l.dn, l.H, q_nope, (long)l.H * l.dn, l.dn,
-                      (const T*)h->WUKT, l.dn, (long)l.rkv * l.dn, q_abs, (long)l.H * l.L, l.L,
+  simt::gemm_nt<TI, TI>(st, M, l.rkv, l.dn, l.H, q_nope, (long)l.H * l.dn, l.dn,
+                      (const TI*)h->WUKT, l.dn, (long)l.rkv * l.dn, q_abs, (long)l.H * l.L, l.L,
                       nullptr, 0, 0);
-  T* o_lat = (T*)(ws + w.o_lat);
-  simt::latent_attention<T>(st, h, q_abs, (const T*)cache, num_pages, d, pos, o_lat);
+  TI* o_lat = (TI*)(ws + w.o_lat);
+  simt::latent_attention<TI, TX>(st, h, q_abs, (const TX*)cache, num_pages, d, pos, o_lat);
   // o[h] = o_lat[h] @ W_UV[h]^T (* sigmoid(gate))
-  T* o = (T*)(ws + w.o);
+  TI* o = (TI*)(ws + w.o);
   const float* gate = l.gdim ? a_out + l.L + l.qdim : nullptr;
-  simt::gemm_nt<T, T>(st, M, l.dv, l.rkv, l.H, o_lat, (long)l.H * l.rkv, l.rkv, (const T*)h->WUV,
+  simt::gemm_nt<TI, TI>(st, M, l.dv, l.rkv, l.H, o_lat, (long)l.H * l.rkv, l.rkv, (const TI*)h->WUV,
                       l.rkv, (long)l.dv * l.rkv, o, (long)l.H * l.dv, l.dv, gate, l.NA, l.dv);
-  simt::gemm_nt<T, T>(st, M, l.D, l.H * l.dv, 1, o, (long)l.H * l.dv, 0, (const T*)h->Wo,
-                      (long)l.H * l.dv, 0, (T*)out, l.D, 0, nullptr, 0, 0);
+  simt::gemm_nt<TI, TX>(st, M, l.D, l.H * l.dv, 1, o, (long)l.H * l.dv, 0, (const TI*)h->Wo,
+                      (long)l.H * l.dv, 0, (TX*)out, l.D, 0, nullptr, 0, 0);
   // A proj, [kv finish], [q norm, q_b], rope split, W_UK, attention, W_UV, o_proj
   h->launches += 6 + (bslots ? 1 : 0) + (l.rq > 0 ? 2 : 0);
 }
@@ -403,10 +424,10 @@ extern "C" mla_status_t mla_draft_forward(mla_handle_t* h, const void* hidden,
   if ((uintptr_t)workspace % 256) return fail(MLA_ERR_INVALID_ARG, "forward: workspace must be 256-byte aligned");
   cudaStream_t st = (cudaStream_t)stream;
   if (h->cfg.dtype == MLA_BF16)
-    forward_impl<__nv_bfloat16>(h, hidden, positions, block_slot_mapping, cache, num_pages, d, out,
+    forward_impl<__nv_bfloat16, __half>(h, hidden, positions, block_slot_mapping, cache, num_pages, d, out,
                                 (char*)workspace, st);
   else
-    forward_impl<float>(h, hidden, positions, block_slot_mapping, cache, num_pages, d, out,
+    forward_impl<float, float>(h, hidden, positions, block_slot_mapping, cache, num_pages, d, out,
                         (char*)workspace, st);
   MLA_CUDA_TRY(cudaGetLastError());
   return MLA_OK;

@@ -78,18 +78,15 @@ void gemm_nt(cudaStream_t st, int M, int N, int K, int batch, const TA* A, long 
                                                       sC, G, ldg, sG);
 }
 
-template void gemm_nt<float, float>(cudaStream_t, int, int, int, int, const float*, long, long,
-                                    const float*, long, long, float*, long, long, const float*,
-                                    long, long);
-template void gemm_nt<__nv_bfloat16, float>(cudaStream_t, int, int, int, int,
-                                            const __nv_bfloat16*, long, long,
-                                            const __nv_bfloat16*, long, long, float*, long, long,
-                                            const float*, long, long);
-template void gemm_nt<__nv_bfloat16, __nv_bfloat16>(cudaStream_t, int, int, int, int,
-                                                    const __nv_bfloat16*, long, long,
-                                                    const __nv_bfloat16*, long, long,
-                                                    __nv_bfloat16*, long, long, const float*,
-                                                    long, long);
+#define MLA_GEMM_INST(TA, TC)                                                              \
+  template void gemm_nt<TA, TC>(cudaStream_t, int, int, int, int, const TA*, long, long,   \
+                                const TA*, long, long, TC*, long, long, const float*, long, long);
+MLA_GEMM_INST(float, float)
+MLA_GEMM_INST(__nv_bfloat16, float)
+MLA_GEMM_INST(__half, float)
+MLA_GEMM_INST(__half, __half)
+MLA_GEMM_INST(__half, __nv_bfloat16)
+#undef MLA_GEMM_INST
 
 }  // namespace simt
 }  // namespace mla

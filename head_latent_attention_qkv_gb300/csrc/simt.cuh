@@ -2,9 +2,12 @@
 //
 // These are the production path for the fp32 configuration (tensor-core
 // TF32 would not meet a 1e-4 relative tolerance) and the first, plain
-// implementation of every step for bf16.  T is the storage type of weights,
-// activations and the latent cache (float or __nv_bfloat16); every sum is
-// accumulated in fp32.
+// implementation of every step for bf16.  Storage types: fp32 throughout for
+// the fp32 configuration; for bf16 layers the hidden states, A-projection
+// weights and latent cache are bf16 while the intermediate activations
+// (normed q_c, q_nope, Q_abs, O_lat, o) and the weights they meet are fp16,
+// whose 3 extra mantissa bits keep the rounding of these tensor-core operands
+// well inside the output tolerance.  Every sum is accumulated in fp32.
 #pragma once
 
 #include "common.cuh"
@@ -39,10 +42,10 @@ void q_rope_split(cudaStream_t st, const mla_handle* h, const float* q, long ldq
 
 // Latent attention: O_lat[m, h, :rkv] = sum_j p_j c_j over the visible keys of
 // each query's block, scores scale * <Q_abs[m,h,:], entry_j>.
-template <typename T>
-void latent_attention(cudaStream_t st, const mla_handle* h, const T* q_abs,
-                      const T* cache, int num_pages, const mla_attn_desc_t& desc,
-                      const int32_t* positions, T* o_lat);
+template <typename TQ, typename TC>
+void latent_attention(cudaStream_t st, const mla_handle* h, const TQ* q_abs,
+                      const TC* cache, int num_pages, const mla_attn_desc_t& desc,
+                      const int32_t* positions, TQ* o_lat);
 
 }  // namespace simt
 }  // namespace mla

@@ -34,14 +34,14 @@ __device__ __forceinline__ int hsumi16(int v) {
   return v;
 }
 
-template <typename T>
+template <typename TQ, typename TC>
 __global__ void __launch_bounds__(A_THREADS)
-latent_attn_kernel(const T* __restrict__ q_abs, const T* __restrict__ cache, int num_pages,
+latent_attn_kernel(const TQ* __restrict__ q_abs, const TC* __restrict__ cache, int num_pages,
                    int page_size, const int32_t* __restrict__ block_table, int max_pages,
                    const int32_t* __restrict__ kv_len, const int32_t* __restrict__ window,
                    const uint8_t* __restrict__ q_visible, const int32_t* __restrict__ positions,
                    int Tb, int H, int rkv, int L, float scale, uint32_t* status,
-                   int32_t* vis_stats, T* __restrict__ o_lat) {
+                   int32_t* vis_stats, TQ* __restrict__ o_lat) {
   extern __shared__ float sm[];
   float* Qs = sm;                      // [QT][L]
   float* Ks = Qs + QT * L;             // [KT][L + 1]
@@ -129,10 +129,10 @@ latent_attn_kernel(const T* __restrict__ q_abs, const T* __restrict__ cache, int
   }
   if (row_ok) {
     const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
-    T* dst = o_lat + (m * H + h) * rkv;
+    TQ* dst = o_lat + (m * H + h) * rkv;
 #pragma unroll
     for (int i = 0; i < MAX_OUT; ++i)
-      if (i < nout) dst[c0 + 16 * i] = from_f32<T>(lrow > 0.f ? o[i] * inv : 0.f);
+      if (i < nout) dst[c0 + 16 * i] = from_f32<TQ>(lrow > 0.f ? o[i] * inv : 0.f);
   }
   const int tot = hsumi16(cnt), hi = hmaxi16(last), lo = -hmaxi16(-first);
   if (vis_stats && h == 0 && row_ok && c0 == 0) {
@@ -144,34 +144,33 @@ latent_attn_kernel(const T* __restrict__ q_abs, const T* __restrict__ cache, int
 
 }  // namespace
 
-template <typename T>
-void latent_attention(cudaStream_t st, const mla_handle* h, const T* q_abs, const T* cache,
+template <typename TQ, typename TC>
+void latent_attention(cudaStream_t st, const mla_handle* h, const TQ* q_abs, const TC* cache,
                       int num_pages, const mla_attn_desc_t& desc, const int32_t* positions,
-                      T* o_lat) {
+                      TQ* o_lat) {
   const Layout& l = h->lay;
   if (desc.num_blocks <= 0 || desc.block_len <= 0) return;
   const size_t smem = sizeof(float) * (QT * l.L + KT * (l.L + 1) + QT * KT);
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(latent_attn_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(latent_attn_kernel<TQ, TC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          227 * 1024);
     configured = true;
   }
   dim3 grid(desc.num_blocks, l.H, (desc.block_len + QT - 1) / QT);
-  latent_attn_kernel<T><<<grid, A_THREADS, smem, st>>>(
+  latent_attn_kernel<TQ, TC><<<grid, A_THREADS, smem, st>>>(
       q_abs, cache, num_pages, h->cfg.page_size, desc.block_table, desc.max_pages, desc.kv_len,
       desc.window, desc.q_visible, positions, desc.block_len, l.H, l.rkv, l.L, h->scale,
       h->status, desc.vis_stats, o_lat);
 }
 
-size_t latent_attention_smem(int L) { return sizeof(float) * (QT * L + KT * (L + 1) + QT * KT); }
-
-template void latent_attention<float>(cudaStream_t, const mla_handle*, const float*, const float*,
-                                      int, const mla_attn_desc_t&, const int32_t*, float*);
-template void latent_attention<__nv_bfloat16>(cudaStream_t, const mla_handle*,
-                                              const __nv_bfloat16*, const __nv_bfloat16*, int,
-                                              const mla_attn_desc_t&, const int32_t*,
-                                              __nv_bfloat16*);
+template void latent_attention<float, float>(cudaStream_t, const mla_handle*, const float*,
+                                             const float*, int, const mla_attn_desc_t&,
+                                             const int32_t*, float*);
+template void latent_attention<__half, __nv_bfloat16>(cudaStream_t, const mla_handle*,
+                                                      const __half*, const __nv_bfloat16*, int,
+                                                      const mla_attn_desc_t&, const int32_t*,
+                                                      __half*);
 
 }  // namespace simt
 }  // namespace mla

@@ -151,6 +151,7 @@ void q_rope_split(cudaStream_t st, const mla_handle* h, const float* q, long ldq
                                 const int32_t*, T*, T*);
 MLA_INST(float)
 MLA_INST(__nv_bfloat16)
+MLA_INST(__half)
 #undef MLA_INST
 
 }  // namespace simt
