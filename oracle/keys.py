@@ -38,7 +38,7 @@ class OracleRun:
         rows = np.asarray(rows)
         if rows.size == 0:
             return np.zeros((0, self.d.cache_dim))
-        ent = mla.store_in_cache_dtype(
+        ent = mla.round_to_dtype(
             self.d, mla.latent_cache_entries(self.d, self.wl.weights, hidden[rows], positions[rows]))
         self.cache[slots[rows]] = ent
         self.written[slots[rows]] = True
@@ -94,10 +94,11 @@ class OracleRun:
             x = step.block_hidden[rows]
             if not segs:
                 o = np.zeros((T, d.num_heads, d.v_head_dim))
-                out[b] = mla.output_projection(d, w, x, o)
+                out[b] = mla.round_to_dtype(d, mla.output_projection(d, w, x, o))
                 continue
             v = vis[:, np.concatenate(cols)]
-            out[b] = mla.block_forward(d, w, x, step.block_positions[rows], segs, v)
+            out[b] = mla.round_to_dtype(
+                d, mla.block_forward(d, w, x, step.block_positions[rows], segs, v))
         return out
 
 

@@ -130,19 +130,20 @@ def latent_cache_entries(d, w, hidden, positions):
     return np.concatenate([c, k_pe], axis=1)
 
 
-def store_in_cache_dtype(d, entries):
-    """The value a cache slot holds: the entry rounded to the cache's dtype.
+def round_to_dtype(d, x):
+    """The value a typed tensor of the layer's dtype holds for fp64 ``x``.
 
-    MLA blog, ``do_kv_cache_update`` / ``concat_and_cache_mla(...,
-    kv_cache_dtype=...)`` and ``get_kv_cache_spec`` (``dtype=kv_cache_dtype``):
-    the latent cache is a typed tensor, so attention reads back the stored
-    values.  For a bf16 cache each fp64 entry is rounded to the nearest bf16
-    (ties to even); an fp32 cache keeps fp64 here (the fp32 rounding is far
-    below that configuration's tolerance)."""
-    e = _f64(entries)
+    The method stores two tensors in the model dtype: the latent cache (MLA
+    blog, ``do_kv_cache_update`` passes ``kv_cache_dtype`` to
+    ``concat_and_cache_mla``; ``get_kv_cache_spec`` types the cache with it)
+    and the attention output (``MLAAttention.forward`` allocates it with
+    ``dtype=q.dtype``).  For bf16 layers each value is rounded to the nearest
+    bf16 (8 significant bits, ties to even); fp32 layers keep fp64 here, their
+    rounding being far below that configuration's tolerance."""
+    x = _f64(x)
     if getattr(d, "dtype", "fp32") != "bf16":
-        return e
-    m, ex = np.frexp(e)                      # e = m * 2^ex, 0.5 <= |m| < 1
+        return x
+    m, ex = np.frexp(x)                          # x = m * 2^ex, 0.5 <= |m| < 1
     return np.ldexp(np.rint(m * 256.0), ex - 8)  # 8 significant bits, ties to even
 
 

@@ -245,12 +245,12 @@ def test_cached_two_block_decode_equals_one_shot():
     assert rel_err(out_one[:T], out1) < 1e-13
 
 
-def test_cache_storage_rounds_to_nearest_bf16_ties_to_even():
+def test_typed_storage_rounds_to_nearest_bf16_ties_to_even():
     """bf16 keeps 8 significant bits: 1 + 2^-8 is a tie between 1 and
     1 + 2^-7 (goes to the even 1), 1 + 3*2^-8 is a tie between 1 + 2^-7 and
     1 + 2^-6 (goes to the even 1 + 2^-6); representable values stay."""
     from head_latent_attention_qkv_gb300.workloads import QWEN3_4B_MLA, TINY_FP32_MLA
     x = np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 1.5, 3.0 + 2 ** -7, 1 + 2 ** -9])
     want = np.array([1.0, 1 + 2 ** -6, -1.0, 1.5, 3.0, 1.0])
-    np.testing.assert_array_equal(mla.store_in_cache_dtype(QWEN3_4B_MLA, x), want)
-    np.testing.assert_array_equal(mla.store_in_cache_dtype(TINY_FP32_MLA, x), x)
+    np.testing.assert_array_equal(mla.round_to_dtype(QWEN3_4B_MLA, x), want)
+    np.testing.assert_array_equal(mla.round_to_dtype(TINY_FP32_MLA, x), x)
