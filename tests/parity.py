@@ -2,7 +2,10 @@
 
 Tolerances (from the layer's contract): outputs max|gpu - ref| <= 2e-2 * rms
 and mean|gpu - ref| <= 2e-3 * rms for bf16 (rms over rows that are not fully
-masked), 1e-4 for both in the fp32 configuration.  Exact checks: fully
+masked), 1e-4 for both in the fp32 configuration.  For bf16 tensors the
+per-element bound is max(2e-2 * rms, one bf16 ulp of the reference value):
+the oracle, like the method, holds the output and the cache in bf16, and one
+ulp is the format's resolution.  Exact checks: fully
 masked rows are bitwise +0.0; the per-row visible-key count, first and last
 visible key reported by the kernel equal the oracle's visibility; the cache
 slots written are exactly the slots the calls name (every other slot keeps
@@ -31,8 +34,24 @@ def compare(got, ref, dims, what, valid_rows=None):
     assert np.all(np.isfinite(got[sel])), f"{what}: non-finite values"
     err = np.abs(got[sel] - ref[sel])
     emax, emean = err.max() / rms, err.mean() / rms
-    assert emax <= tmax and emean <= tmean, f"{what}: max {emax:.3e} mean {emean:.3e} (rms {rms:.3e})"
+    bound = np.full(err.shape, tmax * rms)
+    if dims.dtype == "bf16":
+        # resolution floor of a bf16 tensor: both sides hold bf16 values, so a
+        # difference far below tolerance still shows as one ulp where it
+        # straddles a rounding boundary; 1 ulp of an element above ~2.6*rms
+        # exceeds 2e-2*rms
+        bound = np.maximum(bound, bf16_ulp(ref[sel]))
+    over = err > bound
+    assert not over.any() and emean <= tmean, (
+        f"{what}: max {emax:.3e} mean {emean:.3e} (rms {rms:.3e}), "
+        f"{int(over.sum())} elements beyond max(tol*rms, 1 ulp)")
     return emax, emean
+
+
+def bf16_ulp(x):
+    """Spacing of bf16 values (8 significant bits) at |x|."""
+    ax = np.maximum(np.abs(np.asarray(x, np.float64)), np.finfo(np.float32).tiny)
+    return np.ldexp(1.0, np.frexp(ax)[1] - 8)
 
 
 def vis_expected(run, step, b):
