@@ -66,6 +66,8 @@ def _load():
         "mla_get_device_status": (I32, [P, P, C.POINTER(I32)]),
         "mla_draft_destroy": (None, [P]),
         "mla_kernel_launches": (C.c_ulonglong, [P]),
+        "mla_latent_cache_append_noalloc": (I32, [P, P, P, P, I32, P, I32, P]),
+        "mla_append_noalloc_max_tokens": (C.c_int64, [P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)

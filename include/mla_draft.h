@@ -183,6 +183,30 @@ mla_status_t mla_draft_forward(mla_handle_t *h, const void *hidden,
                                void *out, void *workspace,
                                size_t workspace_bytes, void *stream);
 
+/* Allocation-free latent-cache append.  The pages have no counterpart: this
+ * is a library convenience for callers that cannot allocate device memory
+ * where they append (host callbacks, allocator hooks, runtimes with a memory
+ * pool fixed in advance, embedders that only hand over tensors they own).
+ * Same result as mla_latent_cache_append, same arguments minus the
+ * workspace: the fp32 staging of the projection lives in a fixed 4 MiB
+ * device array inside the library, held by every GPU that loads it until
+ * the process exits.  Limits and rules:
+ *  - n * (kv_lora_rank + qk_rope_head_dim) must fit 2^20 floats
+ *    (mla_append_noalloc_max_tokens(h) tokens, 1820 at entry width 576);
+ *    larger n returns MLA_ERR_INVALID_ARG with a message, nothing launched;
+ *  - the handle's device must be current; the first call on each device
+ *    looks up the array's device address (cudaGetSymbolAddress), so make
+ *    that first call before any stream capture;
+ *  - every call shares the one array per device: calls whose work overlaps
+ *    on the GPU (other streams, other handles, other threads) race on it and
+ *    must be ordered by the caller.  Nothing in it needs to start at zero.
+ * Calls no cudaMalloc/cudaFree and no allocating library routine. */
+mla_status_t mla_latent_cache_append_noalloc(mla_handle_t *h, const void *hidden,
+                                             const int32_t *positions,
+                                             const int64_t *slot_mapping, int32_t n,
+                                             void *cache, int32_t num_pages, void *stream);
+int64_t mla_append_noalloc_max_tokens(const mla_handle_t *h);
+
 /* Synchronise `stream`, read and clear the device status word.  Returns
  * MLA_OK, MLA_ERR_TIMEOUT (MLA_DEV_TIMEOUT set) or MLA_ERR_DEVICE_CHECK; the
  * raw bits go to *bits when non-NULL. */
