@@ -4,9 +4,11 @@
 #include <string.h>
 
 #include <string>
+#include <type_traits>
 #include <vector>
 
 #include "common.cuh"
+#include "gemm_tc.cuh"
 #include "simt.cuh"
 
 namespace mla {
@@ -297,21 +299,49 @@ extern "C" size_t mla_forward_workspace_bytes(const mla_handle_t* h, int32_t num
 }
 
 // ---------------------------------------------------------------------------
+// Projections: tcgen05 GEMM for 16-bit operands, SIMT for the fp32 layer
+// ---------------------------------------------------------------------------
+namespace mla {
+namespace {
+
+template <typename TA, typename TC>
+mla_status_t proj(mla_handle_t* h, cudaStream_t st, int M, int N, int K, int batch, const TA* A,
+                  long lda, long sA, const TA* B, long ldb, long sB, TC* C, long ldc, long sC,
+                  const float* G = nullptr, long ldg = 0, long sG = 0) {
+  h->launches += (M > 0 && N > 0 && batch > 0);
+  if constexpr (std::is_same<TA, float>::value) {
+    simt::gemm_nt<TA, TC>(st, M, N, K, batch, A, lda, sA, B, ldb, sB, C, ldc, sC, G, ldg, sG);
+    return MLA_OK;
+  } else {
+    tc::Out o = std::is_same<TC, float>::value ? tc::Out::F32
+                : std::is_same<TC, __half>::value ? tc::Out::F16 : tc::Out::BF16;
+    tc::GemmArgs a{M, N, K, batch, std::is_same<TA, __half>::value, A, lda, sA, B, ldb, sB,
+                   C, ldc, sC, o, G, ldg, sG};
+    return tc::gemm(st, a, h->status);
+  }
+}
+
+}  // namespace
+}  // namespace mla
+
+// ---------------------------------------------------------------------------
 // Latent-cache append
 // ---------------------------------------------------------------------------
 namespace mla {
 namespace {
 
 template <typename T>
-void append_impl(mla_handle_t* h, const void* hidden, const int32_t* positions,
+mla_status_t append_impl(mla_handle_t* h, const void* hidden, const int32_t* positions,
                  const int64_t* slots, int n, void* cache, long num_slots, float* kv_ws,
                  cudaStream_t st) {
   const Layout& l = h->lay;
   // kv = hidden @ W_kva^T : W_kva = first L rows of W_A
-  simt::gemm_nt<T, float>(st, n, l.L, l.D, 1, (const T*)hidden, l.D, 0, (const T*)h->WA, l.D, 0,
-                          kv_ws, l.L, 0, nullptr, 0, 0);
+  mla_status_t s = proj<T, float>(h, st, n, l.L, l.D, 1, (const T*)hidden, l.D, 0,
+                                  (const T*)h->WA, l.D, 0, kv_ws, l.L, 0);
+  if (s != MLA_OK) return s;
   simt::kv_finish<T>(st, h, kv_ws, l.L, n, positions, slots, (T*)cache, num_slots);
-  h->launches += 2;
+  h->launches += 1;
+  return MLA_OK;
 }
 
 }  // namespace
@@ -332,12 +362,13 @@ extern "C" mla_status_t mla_latent_cache_append(mla_handle_t* h, const void* hid
     return fail(MLA_ERR_INVALID_ARG, "append: workspace smaller than mla_append_workspace_bytes()");
   cudaStream_t st = (cudaStream_t)stream;
   const long num_slots = (long)num_pages * h->cfg.page_size;
-  if (h->cfg.dtype == MLA_BF16)
-    append_impl<__nv_bfloat16>(h, hidden, positions, slot_mapping, n, cache, num_slots,
+  const mla_status_t s =
+      h->cfg.dtype == MLA_BF16
+          ? append_impl<__nv_bfloat16>(h, hidden, positions, slot_mapping, n, cache, num_slots,
+                                       (float*)workspace, st)
+          : append_impl<float>(h, hidden, positions, slot_mapping, n, cache, num_slots,
                                (float*)workspace, st);
-  else
-    append_impl<float>(h, hidden, positions, slot_mapping, n, cache, num_slots,
-                       (float*)workspace, st);
+  if (s != MLA_OK) return s;
   MLA_CUDA_TRY(cudaGetLastError());
   return MLA_OK;
 }
@@ -349,7 +380,7 @@ namespace mla {
 namespace {
 
 template <typename TX, typename TI>
-void forward_impl(mla_handle_t* h, const void* hidden, const int32_t* pos, const int64_t* bslots,
+mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* pos, const int64_t* bslots,
                   void* cache, int num_pages, const mla_attn_desc_t& d, void* out, char* ws,
                   cudaStream_t st) {
   const Layout& l = h->lay;
@@ -360,8 +391,9 @@ void forward_impl(mla_handle_t* h, const void* hidden, const int32_t* pos, const
   const TX* WA = (const TX*)h->WA;
   // A projection; the kv rows only when the block writes its own latents
   const int r0 = bslots ? 0 : l.L;
-  simt::gemm_nt<TX, float>(st, M, l.NA - r0, l.D, 1, x, l.D, 0, WA + (long)r0 * l.D, l.D, 0,
-                          a_out + r0, l.NA, 0, nullptr, 0, 0);
+  mla_status_t s = proj<TX, float>(h, st, M, l.NA - r0, l.D, 1, x, l.D, 0,
+                                   WA + (long)r0 * l.D, l.D, 0, a_out + r0, l.NA, 0);
+  if (s != MLA_OK) return s;
   if (bslots)
     simt::kv_finish<TX>(st, h, a_out, l.NA, M, pos, bslots, (TX*)cache,
                        (long)num_pages * h->cfg.page_size);
@@ -371,8 +403,9 @@ void forward_impl(mla_handle_t* h, const void* hidden, const int32_t* pos, const
     TI* q_cn = (TI*)(ws + w.q_cn);
     simt::rmsnorm_rows<TI>(st, a_out + l.L, l.NA, M, l.rq, h->gamma_q, (float)h->cfg.rms_norm_eps, q_cn);
     float* qr = (float*)(ws + w.q_raw);
-    simt::gemm_nt<TI, float>(st, M, l.H * l.dqk, l.rq, 1, q_cn, l.rq, 0, (const TI*)h->Wqb, l.rq, 0,
-                            qr, l.H * l.dqk, 0, nullptr, 0, 0);
+    s = proj<TI, float>(h, st, M, l.H * l.dqk, l.rq, 1, q_cn, l.rq, 0, (const TI*)h->Wqb, l.rq,
+                        0, qr, l.H * l.dqk, 0);
+    if (s != MLA_OK) return s;
     q_raw = qr;
     ldq = l.H * l.dqk;
   } else {
@@ -383,20 +416,24 @@ void forward_impl(mla_handle_t* h, const void* hidden, const int32_t* pos, const
   TI* q_abs = (TI*)(ws + w.q_abs);
   simt::q_rope_split<TI>(st, h, q_raw, ldq, M, pos, q_nope, q_abs);
   // q_lat[h] = q_nope[h] @ W_UK[h]  ->  Q_abs[:, h, :rkv]
-  simt::gemm_nt<TI, TI>(st, M, l.rkv, l.dn, l.H, q_nope, (long)l.H * l.dn, l.dn,
-                      (const TI*)h->WUKT, l.dn, (long)l.rkv * l.dn, q_abs, (long)l.H * l.L, l.L,
-                      nullptr, 0, 0);
+  s = proj<TI, TI>(h, st, M, l.rkv, l.dn, l.H, q_nope, (long)l.H * l.dn, l.dn,
+                   (const TI*)h->WUKT, l.dn, (long)l.rkv * l.dn, q_abs, (long)l.H * l.L, l.L);
+  if (s != MLA_OK) return s;
   TI* o_lat = (TI*)(ws + w.o_lat);
   simt::latent_attention<TI, TX>(st, h, q_abs, (const TX*)cache, num_pages, d, pos, o_lat);
   // o[h] = o_lat[h] @ W_UV[h]^T (* sigmoid(gate))
   TI* o = (TI*)(ws + w.o);
   const float* gate = l.gdim ? a_out + l.L + l.qdim : nullptr;
-  simt::gemm_nt<TI, TI>(st, M, l.dv, l.rkv, l.H, o_lat, (long)l.H * l.rkv, l.rkv, (const TI*)h->WUV,
-                      l.rkv, (long)l.dv * l.rkv, o, (long)l.H * l.dv, l.dv, gate, l.NA, l.dv);
-  simt::gemm_nt<TI, TX>(st, M, l.D, l.H * l.dv, 1, o, (long)l.H * l.dv, 0, (const TI*)h->Wo,
-                      (long)l.H * l.dv, 0, (TX*)out, l.D, 0, nullptr, 0, 0);
-  // A proj, [kv finish], [q norm, q_b], rope split, W_UK, attention, W_UV, o_proj
-  h->launches += 6 + (bslots ? 1 : 0) + (l.rq > 0 ? 2 : 0);
+  s = proj<TI, TI>(h, st, M, l.dv, l.rkv, l.H, o_lat, (long)l.H * l.rkv, l.rkv,
+                   (const TI*)h->WUV, l.rkv, (long)l.dv * l.rkv, o, (long)l.H * l.dv, l.dv, gate,
+                   l.NA, l.dv);
+  if (s != MLA_OK) return s;
+  s = proj<TI, TX>(h, st, M, l.D, l.H * l.dv, 1, o, (long)l.H * l.dv, 0, (const TI*)h->Wo,
+                   (long)l.H * l.dv, 0, (TX*)out, l.D, 0);
+  if (s != MLA_OK) return s;
+  // non-GEMM kernels: [kv finish], [q norm], rope split, attention
+  h->launches += 2 + (bslots ? 1 : 0) + (l.rq > 0 ? 1 : 0);
+  return MLA_OK;
 }
 
 }  // namespace
@@ -423,12 +460,13 @@ extern "C" mla_status_t mla_draft_forward(mla_handle_t* h, const void* hidden,
     return fail(MLA_ERR_INVALID_ARG, "forward: workspace smaller than mla_forward_workspace_bytes()");
   if ((uintptr_t)workspace % 256) return fail(MLA_ERR_INVALID_ARG, "forward: workspace must be 256-byte aligned");
   cudaStream_t st = (cudaStream_t)stream;
-  if (h->cfg.dtype == MLA_BF16)
-    forward_impl<__nv_bfloat16, __half>(h, hidden, positions, block_slot_mapping, cache, num_pages, d, out,
-                                (char*)workspace, st);
-  else
-    forward_impl<float, float>(h, hidden, positions, block_slot_mapping, cache, num_pages, d, out,
-                        (char*)workspace, st);
+  const mla_status_t s =
+      h->cfg.dtype == MLA_BF16
+          ? forward_impl<__nv_bfloat16, __half>(h, hidden, positions, block_slot_mapping, cache,
+                                                num_pages, d, out, (char*)workspace, st)
+          : forward_impl<float, float>(h, hidden, positions, block_slot_mapping, cache,
+                                       num_pages, d, out, (char*)workspace, st);
+  if (s != MLA_OK) return s;
   MLA_CUDA_TRY(cudaGetLastError());
   return MLA_OK;
 }

@@ -1,0 +1,26 @@
+// tcgen05 GEMM launcher (see gemm_tc.cu).
+#pragma once
+
+#include "common.cuh"
+
+namespace mla {
+namespace tc {
+
+enum class Out { F32, F16, BF16 };
+
+struct GemmArgs {
+  int M, N, K, batch;
+  bool fp16;                 // operand type: fp16 (true) or bf16 (false)
+  const void* A; long lda, sA;   // [batch][M][K] (elements; lda, sA strides)
+  const void* B; long ldb, sB;   // [batch][N][K]
+  void* C; long ldc, sC; Out out;
+  const float* G; long ldg, sG;  // optional sigmoid gate, same indexing as C
+};
+
+// Enqueue C = A B^T (* sigmoid(G)) on `st`.  Returns MLA_ERR_UNSUPPORTED for
+// shapes the kernel does not take (K or leading dims not multiples of 8,
+// unaligned pointers) and MLA_ERR_CUDA if the tensor maps cannot be built.
+mla_status_t gemm(cudaStream_t st, const GemmArgs& a, uint32_t* status);
+
+}  // namespace tc
+}  // namespace mla
