@@ -8,6 +8,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "attn_tc.cuh"
 #include "gemm_tc.cuh"
 #include "simt.cuh"
 
@@ -413,14 +414,20 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
     ldq = l.NA;
   }
   TI* q_nope = (TI*)(ws + w.q_nope);
-  TI* q_abs = (TI*)(ws + w.q_abs);
-  simt::q_rope_split<TI>(st, h, q_raw, ldq, M, pos, q_nope, q_abs);
+  // Q_abs shares the cache's type: the two meet in the attention contraction
+  TX* q_abs = (TX*)(ws + w.q_abs);
+  simt::q_rope_split<TI, TX>(st, h, q_raw, ldq, M, pos, q_nope, q_abs);
   // q_lat[h] = q_nope[h] @ W_UK[h]  ->  Q_abs[:, h, :rkv]
-  s = proj<TI, TI>(h, st, M, l.rkv, l.dn, l.H, q_nope, (long)l.H * l.dn, l.dn,
+  s = proj<TI, TX>(h, st, M, l.rkv, l.dn, l.H, q_nope, (long)l.H * l.dn, l.dn,
                    (const TI*)h->WUKT, l.dn, (long)l.rkv * l.dn, q_abs, (long)l.H * l.L, l.L);
   if (s != MLA_OK) return s;
   TI* o_lat = (TI*)(ws + w.o_lat);
-  simt::latent_attention<TI, TX>(st, h, q_abs, (const TX*)cache, num_pages, d, pos, o_lat);
+  if constexpr (std::is_same<TX, float>::value) {
+    simt::latent_attention<TI, TX>(st, h, q_abs, (const TX*)cache, num_pages, d, pos, o_lat);
+  } else {
+    s = tc::latent_attention(st, h, q_abs, (const TX*)cache, num_pages, d, pos, o_lat);
+    if (s != MLA_OK) return s;
+  }
   // o[h] = o_lat[h] @ W_UV[h]^T (* sigmoid(gate))
   TI* o = (TI*)(ws + w.o);
   const float* gate = l.gdim ? a_out + l.L + l.qdim : nullptr;

@@ -269,3 +269,12 @@ mla_status_t gemm(cudaStream_t st, const GemmArgs& a, uint32_t* status) {
 
 }  // namespace tc
 }  // namespace mla
+
+namespace mla {
+namespace tc {
+bool make_tmap_2d(CUtensorMap* m, bool fp16, const void* base, long rows, long cols, long ld,
+                  int box_rows) {
+  return make_map(m, fp16, base, rows, cols, ld, 0, 1, box_rows);
+}
+}  // namespace tc
+}  // namespace mla

@@ -1,6 +1,8 @@
 // tcgen05 GEMM launcher (see gemm_tc.cu).
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace mla {
@@ -22,5 +24,14 @@ struct GemmArgs {
 // unaligned pointers) and MLA_ERR_CUDA if the tensor maps cannot be built.
 mla_status_t gemm(cudaStream_t st, const GemmArgs& a, uint32_t* status);
 
+}  // namespace tc
+}  // namespace mla
+
+namespace mla {
+namespace tc {
+// 2D tensor map of a row-major 16-bit matrix [rows, cols] (row stride ld
+// elements), box = 64 columns x box_rows rows, 128-byte swizzle.
+bool make_tmap_2d(CUtensorMap* m, bool fp16, const void* base, long rows, long cols, long ld,
+                  int box_rows);
 }  // namespace tc
 }  // namespace mla

@@ -36,9 +36,9 @@ void rmsnorm_rows(cudaStream_t st, const float* in, long ld, int M, int n,
 
 // q [M, H, dqk] fp32 (row stride ldq) -> q_nope [M, H, dn] and the rotated
 // rope part into Q_abs[m, h, rkv:rkv+dr].
-template <typename T>
+template <typename TN, typename TQ>
 void q_rope_split(cudaStream_t st, const mla_handle* h, const float* q, long ldq, int M,
-                  const int32_t* positions, T* q_nope, T* q_abs);
+                  const int32_t* positions, TN* q_nope, TQ* q_abs);
 
 // Latent attention: O_lat[m, h, :rkv] = sum_j p_j c_j over the visible keys of
 // each query's block, scores scale * <Q_abs[m,h,:], entry_j>.

@@ -167,10 +167,5 @@ void latent_attention(cudaStream_t st, const mla_handle* h, const TQ* q_abs, con
 template void latent_attention<float, float>(cudaStream_t, const mla_handle*, const float*,
                                              const float*, int, const mla_attn_desc_t&,
                                              const int32_t*, float*);
-template void latent_attention<__half, __nv_bfloat16>(cudaStream_t, const mla_handle*,
-                                                      const __half*, const __nv_bfloat16*, int,
-                                                      const mla_attn_desc_t&, const int32_t*,
-                                                      __half*);
-
 }  // namespace simt
 }  // namespace mla

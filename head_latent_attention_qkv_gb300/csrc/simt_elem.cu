@@ -80,18 +80,18 @@ rmsnorm_rows_kernel(const float* __restrict__ in, long ld, int n, const float* _
   for (int i = threadIdx.x; i < n; i += ROW_THREADS) o[i] = from_f32<T>(row[i] * rstd * gamma[i]);
 }
 
-template <typename T>
+template <typename TN, typename TQ>
 __global__ void __launch_bounds__(ROW_THREADS)
 q_rope_split_kernel(const float* __restrict__ q, long ldq, const int32_t* __restrict__ positions,
                     int H, int dn, int dr, int rkv, const float2* __restrict__ rope, int max_pos,
-                    int interleaved, uint32_t* status, T* __restrict__ q_nope,
-                    T* __restrict__ q_abs) {
+                    int interleaved, uint32_t* status, TN* __restrict__ q_nope,
+                    TQ* __restrict__ q_abs) {
   const int m = blockIdx.x;
   const float* row = q + (long)m * ldq;
   const int dqk = dn + dr, L = rkv + dr, half = dr / 2;
   for (int i = threadIdx.x; i < H * dn; i += ROW_THREADS) {
     const int h = i / dn, d = i % dn;
-    q_nope[(long)m * H * dn + i] = from_f32<T>(row[h * dqk + d]);
+    q_nope[(long)m * H * dn + i] = from_f32<TN>(row[h * dqk + d]);
   }
   const int p = positions[m];
   const bool bad = p < 0 || p >= max_pos;
@@ -100,16 +100,16 @@ q_rope_split_kernel(const float* __restrict__ q, long ldq, const int32_t* __rest
     const int h = i / half, k = i % half;
     int ia, ib;
     rope_pair(k, dr, interleaved, &ia, &ib);
-    T* dst = q_abs + ((long)m * H + h) * L + rkv;
+    TQ* dst = q_abs + ((long)m * H + h) * L + rkv;
     if (bad) {
-      dst[ia] = from_f32<T>(0.f);
-      dst[ib] = from_f32<T>(0.f);
+      dst[ia] = from_f32<TQ>(0.f);
+      dst[ib] = from_f32<TQ>(0.f);
       continue;
     }
     const float2 cs = rope[(long)p * half + k];
     const float a = row[h * dqk + dn + ia], b = row[h * dqk + dn + ib];
-    dst[ia] = from_f32<T>(a * cs.x - b * cs.y);
-    dst[ib] = from_f32<T>(b * cs.x + a * cs.y);
+    dst[ia] = from_f32<TQ>(a * cs.x - b * cs.y);
+    dst[ib] = from_f32<TQ>(b * cs.x + a * cs.y);
   }
 }
 
@@ -132,12 +132,12 @@ void rmsnorm_rows(cudaStream_t st, const float* in, long ld, int M, int n, const
   rmsnorm_rows_kernel<T><<<M, ROW_THREADS, 0, st>>>(in, ld, n, gamma, eps, out);
 }
 
-template <typename T>
+template <typename TN, typename TQ>
 void q_rope_split(cudaStream_t st, const mla_handle* h, const float* q, long ldq, int M,
-                  const int32_t* positions, T* q_nope, T* q_abs) {
+                  const int32_t* positions, TN* q_nope, TQ* q_abs) {
   if (M <= 0) return;
   const Layout& l = h->lay;
-  q_rope_split_kernel<T><<<M, ROW_THREADS, 0, st>>>(
+  q_rope_split_kernel<TN, TQ><<<M, ROW_THREADS, 0, st>>>(
       q, ldq, positions, l.H, l.dn, l.dr, l.rkv, h->rope, h->cfg.max_position,
       h->cfg.rope == MLA_ROPE_INTERLEAVED, h->status, q_nope, q_abs);
 }
@@ -146,13 +146,16 @@ void q_rope_split(cudaStream_t st, const mla_handle* h, const float* q, long ldq
   template void kv_finish<T>(cudaStream_t, const mla_handle*, const float*, long, int,      \
                              const int32_t*, const int64_t*, T*, long);                     \
   template void rmsnorm_rows<T>(cudaStream_t, const float*, long, int, int, const float*,   \
-                                float, T*);                                                 \
-  template void q_rope_split<T>(cudaStream_t, const mla_handle*, const float*, long, int,   \
-                                const int32_t*, T*, T*);
+                                float, T*);
 MLA_INST(float)
 MLA_INST(__nv_bfloat16)
 MLA_INST(__half)
 #undef MLA_INST
+template void q_rope_split<float, float>(cudaStream_t, const mla_handle*, const float*, long, int,
+                                         const int32_t*, float*, float*);
+template void q_rope_split<__half, __nv_bfloat16>(cudaStream_t, const mla_handle*, const float*,
+                                                  long, int, const int32_t*, __half*,
+                                                  __nv_bfloat16*);
 
 }  // namespace simt
 }  // namespace mla
