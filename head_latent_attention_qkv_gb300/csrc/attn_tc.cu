@@ -262,8 +262,8 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
       prefetch_tmap(&P.tmKV);
       mbar_arrive_expect_tx(&B->q_full, nch * Q_CH_BYTES);
       for (int i = 0; i < nch; ++i)
-        tma_load_2d(smem + OFF_Q + i * Q_CH_BYTES, &P.tmQ, &B->q_full, dim_chunk(rank, i) * DCH,
-                    (int)row0);
+        tma_load_3d(smem + OFF_Q + i * Q_CH_BYTES, &P.tmQ, &B->q_full, dim_chunk(rank, i) * DCH,
+                    (int)row0, 0);
       const int R = P.seg_rows, past_end = P.num_pages * P.page_size;
       int issued = 0;
       for (int t = 0; t < nt; ++t) {
@@ -281,8 +281,8 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
             else set_status(P.status, MLA_DEV_BAD_PAGE);
           }
           for (int i = 0; i < nch; ++i)
-            tma_load_2d(stage + i * KV_CH_BYTES + seg * R * 128, &P.tmKV, &B->kv_full[s],
-                        dim_chunk(rank, i) * DCH, y);
+            tma_load_3d(stage + i * KV_CH_BYTES + seg * R * 128, &P.tmKV, &B->kv_full[s],
+                        dim_chunk(rank, i) * DCH, y, 0);
         }
         issued = t + 1;
       }

@@ -29,8 +29,9 @@ mla_status_t gemm(cudaStream_t st, const GemmArgs& a, uint32_t* status);
 
 namespace mla {
 namespace tc {
-// 2D tensor map of a row-major 16-bit matrix [rows, cols] (row stride ld
-// elements), box = 64 columns x box_rows rows, 128-byte swizzle.
+// Tensor map of a row-major 16-bit matrix [rows, cols] (row stride ld
+// elements), box = 64 columns x box_rows rows, 128-byte swizzle.  The map has
+// rank 3 (a unit batch dimension): load it with 3-D TMA, z = 0.
 bool make_tmap_2d(CUtensorMap* m, bool fp16, const void* base, long rows, long cols, long ld,
                   int box_rows);
 }  // namespace tc
