@@ -232,15 +232,21 @@ mla_status_t launch_bn(cudaStream_t st, const GemmArgs& a, uint32_t* status, int
   }
 }
 
+// Tile width: among the widths that give at least one tile per SM, the one
+// with the least padded work (ties: the wider tile, fewer A re-reads); if none
+// fills the GPU, the narrowest.
 int pick_bn(int M, int N, int batch, int num_sms) {
   const int mt = (M + BM - 1) / BM;
   const int cands[4] = {256, 192, 128, 64};
+  int best = 0;
+  long best_pad = 0;
   for (int bn : cands) {
-    if (bn == 192 && N % 192) continue;
-    if (bn > 64 && bn >= 2 * N) continue;
-    if ((long)mt * ((N + bn - 1) / bn) * batch >= num_sms) return bn;
+    const long nt = (N + bn - 1) / bn;
+    if ((long)mt * nt * batch < num_sms) continue;
+    const long pad = nt * bn - N;
+    if (!best || pad < best_pad) { best = bn; best_pad = pad; }
   }
-  return 64;
+  return best ? best : 64;
 }
 
 }  // namespace
