@@ -43,11 +43,11 @@ constexpr int OFF_P = OFF_KV + 2 * KV_STAGE_BYTES;
 constexpr int OFF_X = OFF_P + QROWS * KT * 2;
 constexpr int OFF_BAR = OFF_X + QROWS * KT * 4;
 constexpr int SMEM_BYTES = 1024 + OFF_BAR + 256;
-constexpr uint32_t TMEM_COLS = 512, TM_O = 0, TM_S = 256;
+constexpr uint32_t TMEM_COLS = 512, TM_O = 0, TM_S = 256;   // S double-buffered: 256, 320
 constexpr float RESCALE_LOG2 = 8.f;               // lazy rescale threshold (factor 256)
 
 struct Bars {
-  uint64_t q_full, kv_full[2], kv_empty[2], s_full, s_free, p_full, o_done, x_full, x_empty;
+  uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, o_done, x_full, x_empty;
   uint32_t tmem_slot;
   int abort;
 };
@@ -100,12 +100,13 @@ __device__ __forceinline__ void softmax_and_store(const AttnParams& P, Bars* B, 
   for (int t = 0; t < nt; ++t) {
     const int j0 = j_lo + t * KT;
     float s[KT];
-    wait_local(B, &B->s_full, t & 1, P.status);
+    const uint32_t sbuf = tmem + TM_S + 64 * (t & 1) + lane_base;
+    wait_local(B, &B->s_full[t & 1], (t >> 1) & 1, P.status);
     tc_fence_after();
-    tmem_ld32(tmem + TM_S + lane_base, s);
-    tmem_ld32(tmem + TM_S + lane_base + 32, s + 32);
+    tmem_ld32(sbuf, s);
+    tmem_ld32(sbuf + 32, s + 32);
     tc_fence_before();
-    mbar_arrive(&B->s_free);
+    mbar_arrive(&B->s_free[t & 1]);
     // exchange the partial scores with the peer CTA
     wait_local(B, &B->x_empty, (t & 1) ^ 1, P.status);
 #pragma unroll
@@ -222,8 +223,10 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
       mbar_init(&B->kv_full[s], 1);
       mbar_init(&B->kv_empty[s], 1);
     }
-    mbar_init(&B->s_full, 1);
-    mbar_init(&B->s_free, QROWS);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&B->s_full[s], 1);
+      mbar_init(&B->s_free[s], QROWS);
+    }
     mbar_init(&B->p_full, QROWS);
     mbar_init(&B->o_done, 1);
     mbar_init(&B->x_full, QROWS);
@@ -297,10 +300,11 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
       const uint32_t idesc_qk = idesc_f16(QROWS, KT, false);
       const uint32_t idesc_pv = idesc_f16_bmn(QROWS, 256, false);
       const bool have_q = wait_local(B, &B->q_full, 0, P.status);
-      for (int t = 0; t < nt && have_q; ++t) {
+      // S(t) = Q K(t)^T into score buffer t % 2 (its (t/2)-th use)
+      auto issue_qk = [&](int t) -> bool {
         const int s = t & 1;
-        if (!wait_local(B, &B->kv_full[s], (t >> 1) & 1, P.status)) break;
-        if (!wait_local(B, &B->s_free, (t & 1) ^ 1, P.status)) break;
+        if (!wait_local(B, &B->kv_full[s], (t >> 1) & 1, P.status)) return false;
+        if (!wait_local(B, &B->s_free[s], ((t >> 1) & 1) ^ 1, P.status)) return false;
         tc_fence_after();
         const uint8_t* stage = smem + OFF_KV + s * KV_STAGE_BYTES;
         for (int i = 0; i < nch; ++i) {
@@ -308,11 +312,18 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
           const uint64_t db = smem_desc_sw128(stage + i * KV_CH_BYTES);
 #pragma unroll
           for (int k = 0; k < DCH / 16; ++k)
-            mma_f16(tmem + TM_S, da + 2 * k, db + 2 * k, idesc_qk, (i | k) != 0);
+            mma_f16(tmem + TM_S + 64 * s, da + 2 * k, db + 2 * k, idesc_qk, (i | k) != 0);
         }
-        mma_commit(&B->s_full);
+        mma_commit(&B->s_full[s]);
+        return true;
+      };
+      bool ok = have_q && (nt == 0 || issue_qk(0));
+      for (int t = 0; t < nt && ok; ++t) {
+        // the next tile's scores overlap this tile's softmax
+        if (t + 1 < nt && !issue_qk(t + 1)) break;
         if (!wait_local(B, &B->p_full, t & 1, P.status)) break;
         tc_fence_after();
+        const uint8_t* stage = smem + OFF_KV + (t & 1) * KV_STAGE_BYTES;
         const uint64_t dp = smem_desc_sw128(smem + OFF_P);
         const uint64_t dv = smem_desc_sw128_mn(stage, KV_CH_BYTES);
 #pragma unroll
@@ -320,7 +331,7 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
           mma_f16(tmem + TM_O, dp + 2 * k, dv + (uint64_t)(16 * 128 / 16) * k, idesc_pv,
                   (t | k) != 0);
         mma_commit(&B->o_done);
-        mma_commit(&B->kv_empty[s]);
+        mma_commit(&B->kv_empty[t & 1]);
       }
     }
   } else {
