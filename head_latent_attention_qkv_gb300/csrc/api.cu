@@ -269,10 +269,11 @@ namespace mla {
 namespace {
 
 struct FwdWs {
-  size_t a_out, q_cn, q_raw, q_nope, q_abs, o_lat, o, total;
+  size_t a_out, q_cn, q_raw, q_nope, q_abs, o_lat, o, part, total;
 };
 
-FwdWs forward_ws(const Layout& l, long M) {
+FwdWs forward_ws(const mla_handle* h, long M) {
+  const Layout& l = h->lay;
   FwdWs w;
   size_t o = 0;
   w.a_out = o;  o = align256(o + (size_t)M * l.NA * 4);
@@ -282,6 +283,8 @@ FwdWs forward_ws(const Layout& l, long M) {
   w.q_abs = o;  o = align256(o + (size_t)M * l.H * l.L * l.elt);
   w.o_lat = o;  o = align256(o + (size_t)M * l.H * l.rkv * l.elt);
   w.o = o;      o = align256(o + (size_t)M * l.H * l.dv * l.elt);
+  // split-KV partial outputs of the tensor-core attention (bf16 layers)
+  w.part = o;   o = align256(o + (h->cfg.dtype == MLA_BF16 ? tc::attn_split_floats(h, M) * 4 : 0));
   w.total = o;
   return w;
 }
@@ -296,7 +299,7 @@ extern "C" size_t mla_append_workspace_bytes(const mla_handle_t* h, int32_t n) {
 }
 
 extern "C" size_t mla_forward_workspace_bytes(const mla_handle_t* h, int32_t num_tokens) {
-  return (h && num_tokens >= 0) ? forward_ws(h->lay, num_tokens).total : 0;
+  return (h && num_tokens >= 0) ? forward_ws(h, num_tokens).total : 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -386,7 +389,7 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
                   cudaStream_t st) {
   const Layout& l = h->lay;
   const int M = d.num_blocks * d.block_len;
-  const FwdWs w = forward_ws(l, M);
+  const FwdWs w = forward_ws(h, M);
   float* a_out = (float*)(ws + w.a_out);
   const TX* x = (const TX*)hidden;
   const TX* WA = (const TX*)h->WA;
@@ -425,8 +428,11 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
   if constexpr (std::is_same<TX, float>::value) {
     simt::latent_attention<TI, TX>(st, h, q_abs, (const TX*)cache, num_pages, d, pos, o_lat);
   } else {
-    s = tc::latent_attention(st, h, q_abs, (const TX*)cache, num_pages, d, pos, o_lat);
+    s = tc::latent_attention(st, h, q_abs, (const TX*)cache, num_pages, d, pos, o_lat,
+                             (float*)(ws + w.part));
     if (s != MLA_OK) return s;
+    const int sp = tc::attn_splits(h, M);
+    h->launches += (sp > 1) + (sp > 1 && d.vis_stats);   // merge, visibility-stat init
   }
   // o[h] = o_lat[h] @ W_UV[h]^T (* sigmoid(gate))
   TI* o = (TI*)(ws + w.o);
@@ -463,7 +469,7 @@ extern "C" mla_status_t mla_draft_forward(mla_handle_t* h, const void* hidden,
     return fail(MLA_ERR_INVALID_ARG, "forward: null pointer");
   if (num_pages <= 0) return fail(MLA_ERR_INVALID_ARG, "forward: num_pages <= 0");
   const int M = d.num_blocks * d.block_len;
-  if (workspace_bytes < forward_ws(h->lay, M).total)
+  if (workspace_bytes < forward_ws(h, M).total)
     return fail(MLA_ERR_INVALID_ARG, "forward: workspace smaller than mla_forward_workspace_bytes()");
   if ((uintptr_t)workspace % 256) return fail(MLA_ERR_INVALID_ARG, "forward: workspace must be 256-byte aligned");
   cudaStream_t st = (cudaStream_t)stream;

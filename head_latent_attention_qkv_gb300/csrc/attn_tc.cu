@@ -184,25 +184,49 @@ __device__ __forceinline__ void softmax_and_store(const AttnParams& P, Bars* B, 
   if (nt > 0) wait_local(B, &B->o_done, (nt - 1) & 1, P.status);
   tc_fence_after();
   const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-  __half* dst = P.o_lat + (row0 + r) * 512 + rank * 256;
+  const bool any = nt > 0 && lsum > 0.f;
+  if (P.splits == 1) {
+    __half* dst = P.o_lat + (row0 + r) * 512 + rank * 256;
 #pragma unroll 1
-  for (int c = 0; c < 256; c += 32) {
-    float o[32];
-    if (nt > 0) tmem_ld32(tmem + TM_O + lane_base + c, o);
+    for (int c = 0; c < 256; c += 32) {
+      float o[32];
+      if (nt > 0) tmem_ld32(tmem + TM_O + lane_base + c, o);
 #pragma unroll
-    for (int i = 0; i < 32; i += 8) {
-      __half2 h2[4];
+      for (int i = 0; i < 32; i += 8) {
+        __half2 h2[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        h2[u] = nt > 0 && lsum > 0.f ? __floats2half2_rn(o[i + 2 * u] * inv, o[i + 2 * u + 1] * inv)
-                                     : __floats2half2_rn(0.f, 0.f);
-      *reinterpret_cast<uint4*>(dst + c + i) = *reinterpret_cast<uint4*>(h2);
+        for (int u = 0; u < 4; ++u)
+          h2[u] = any ? __floats2half2_rn(o[i + 2 * u] * inv, o[i + 2 * u + 1] * inv)
+                      : __floats2half2_rn(0.f, 0.f);
+        *reinterpret_cast<uint4*>(dst + c + i) = *reinterpret_cast<uint4*>(h2);
+      }
     }
+  } else {
+    // normalised partial output and its log2-sum-exp, merged by merge_splits()
+    const long prow = (long)blockIdx.y * P.rows + row0 + r;
+    float* dst = P.o_part + prow * 512 + rank * 256;
+#pragma unroll 1
+    for (int c = 0; c < 256; c += 32) {
+      float o[32];
+      if (nt > 0) tmem_ld32(tmem + TM_O + lane_base + c, o);
+#pragma unroll
+      for (int i = 0; i < 32; i += 4)
+        *reinterpret_cast<float4*>(dst + c + i) =
+            any ? make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv)
+                : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (rank == 0) P.lse_part[prow] = any ? mrun + log2f(lsum) : -INFINITY;
   }
   if (P.vis_stats && rank == 0 && head == 0) {
-    P.vis_stats[m * 3 + 0] = cnt;
-    P.vis_stats[m * 3 + 1] = cnt ? first : -1;
-    P.vis_stats[m * 3 + 2] = cnt ? last : -1;
+    if (P.splits == 1) {
+      P.vis_stats[m * 3 + 0] = cnt;
+      P.vis_stats[m * 3 + 1] = cnt ? first : -1;
+      P.vis_stats[m * 3 + 2] = cnt ? last : -1;
+    } else if (cnt) {
+      atomicAdd(&P.vis_stats[m * 3 + 0], cnt);
+      atomicMin(&P.vis_stats[m * 3 + 1], first);
+      atomicMax(&P.vis_stats[m * 3 + 2], last);
+    }
   }
 }
 
@@ -256,7 +280,13 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
     for (int t = t_first; t <= t_last; ++t) pmin = min(pmin, P.positions[(long)b * P.T + t]);
     j_lo = max(0, pmin - W + 1) / KT * KT;
   }
-  const int nt = kvl > j_lo ? (kvl - j_lo + KT - 1) / KT : 0;
+  int nt = kvl > j_lo ? (kvl - j_lo + KT - 1) / KT : 0;
+  {  // this split's share of the tiles
+    const int tb = (int)((long)blockIdx.y * nt / P.splits);
+    const int te = (int)((long)(blockIdx.y + 1) * nt / P.splits);
+    j_lo += tb * KT;
+    nt = te - tb;
+  }
 
   if (warp == 4) {
     if (lane == 0) {
@@ -269,20 +299,34 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
                     (int)row0, 0);
       const int R = P.seg_rows, past_end = P.num_pages * P.page_size;
       int issued = 0;
+      // cache row of key j (beyond the cache when j is past kv_len or its page
+      // is invalid: TMA then fills zeros)
+      auto cache_row = [&](int j, bool report) {
+        if (j >= kvl) return past_end;
+        const int pg = P.block_table[(long)b * P.max_pages + j / P.page_size];
+        if (pg >= 0 && pg < P.num_pages) return pg * P.page_size + j % P.page_size;
+        if (report) set_status(P.status, MLA_DEV_BAD_PAGE);
+        return past_end;
+      };
+      auto prefetch_tile = [&](int t) {
+        if (t >= nt) return;
+        for (int seg = 0; seg < KT / R; ++seg) {
+          const int y = cache_row(j_lo + t * KT + seg * R, false);
+          if (y == past_end) continue;
+          for (int i = 0; i < nch; ++i) tma_prefetch_3d(&P.tmKV, dim_chunk(rank, i) * DCH, y, 0);
+        }
+      };
+      prefetch_tile(0);
+      prefetch_tile(1);
       for (int t = 0; t < nt; ++t) {
         const int s = t & 1;
+        prefetch_tile(t + 2);
         if (!wait_local(B, &B->kv_empty[s], ((t >> 1) & 1) ^ 1, P.status)) break;
         const int j0 = j_lo + t * KT;
         uint8_t* stage = smem + OFF_KV + s * KV_STAGE_BYTES;
         mbar_arrive_expect_tx(&B->kv_full[s], nch * KV_CH_BYTES);
         for (int seg = 0; seg < KT / R; ++seg) {
-          const int j = j0 + seg * R;
-          int y = past_end;                       // beyond the cache: TMA fills zeros
-          if (j < kvl) {
-            const int pg = P.block_table[(long)b * P.max_pages + j / P.page_size];
-            if (pg >= 0 && pg < P.num_pages) y = pg * P.page_size + j % P.page_size;
-            else set_status(P.status, MLA_DEV_BAD_PAGE);
-          }
+          const int y = cache_row(j0 + seg * R, true);
           for (int i = 0; i < nch; ++i)
             tma_load_3d(stage + i * KV_CH_BYTES + seg * R * 128, &P.tmKV, &B->kv_full[s],
                         dim_chunk(rank, i) * DCH, y, 0);
@@ -358,7 +402,8 @@ namespace tc {
 
 mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_bfloat16* q_abs,
                               const __nv_bfloat16* cache, int num_pages,
-                              const mla_attn_desc_t& d, const int32_t* positions, __half* o_lat) {
+                              const mla_attn_desc_t& d, const int32_t* positions, __half* o_lat,
+                              float* part) {
   const Layout& l = h->lay;
   const int ps = h->cfg.page_size;
   if (l.rkv != 512 || l.dr != 64)
@@ -368,6 +413,8 @@ mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_b
   if (ps % 16 || (ps < KT && KT % ps) || (ps > KT && ps % KT))
     return fail(MLA_ERR_UNSUPPORTED, "tcgen05 attention: page_size must be 16, 32 or a multiple of 64");
   if (d.num_blocks <= 0) return MLA_OK;
+  const long tokens = (long)d.num_blocks * d.block_len;
+  const int splits = attn_splits(h, tokens);
   AttnParams P;
   const long rows = (long)d.num_blocks * d.block_len * l.H;
   if (!make_tmap_2d(&P.tmQ, false, q_abs, rows, l.L, l.L, QROWS) ||
@@ -389,13 +436,18 @@ mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_b
   P.H = l.H;
   P.tiles_per_block = d.block_len * l.H / QROWS;
   P.scale_log2 = h->scale * 1.4426950408889634f;
+  P.splits = splits;
+  P.rows = rows;
+  P.o_part = part;
+  P.lse_part = part + (size_t)splits * rows * 512;
+  if (splits > 1 && d.vis_stats) init_vis_stats(st, d.vis_stats, tokens);
   static std::once_flag once;
   std::call_once(once, [] {
     cudaFuncSetAttribute(latent_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          SMEM_BYTES);
   });
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * d.num_blocks * P.tiles_per_block, 1, 1);
+  cfg.gridDim = dim3(2 * d.num_blocks * P.tiles_per_block, splits, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = st;
@@ -408,7 +460,21 @@ mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_b
   cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, latent_attn_tc_kernel, P);
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 attention launch");
+  if (splits > 1) merge_splits(st, P.o_part, P.lse_part, splits, rows, o_lat, d.vis_stats, l.H);
   return MLA_OK;
+}
+
+// Enough splits that the (block, 128-row) units fill every SM once, at most 8.
+int attn_splits(const mla_handle* h, long tokens) {
+  const long units = tokens * h->lay.H / QROWS;
+  if (units <= 0) return 1;
+  const long s = (h->num_sms + 2 * units - 1) / (2 * units);
+  return (int)(s < 1 ? 1 : s > 8 ? 8 : s);
+}
+
+size_t attn_split_floats(const mla_handle* h, long tokens) {
+  const int s = attn_splits(h, tokens);
+  return s > 1 ? (size_t)s * tokens * h->lay.H * (512 + 1) : 0;
 }
 
 }  // namespace tc
