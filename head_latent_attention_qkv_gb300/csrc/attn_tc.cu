@@ -78,6 +78,19 @@ __device__ __forceinline__ bool wait_peer(Bars* B, uint64_t* bar, uint32_t parit
   return false;
 }
 
+// 2^x by the hardware approximation (relative error ~2^-22, far below the
+// bf16 rounding P gets); 2^-inf = 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Named barrier of the 128 softmax threads (barrier 0 is __syncthreads).
+__device__ __forceinline__ void softmax_bar_sync() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
 // Warps 0-3: thread r owns accumulator row r (TMEM lane r) of the tile.
 __device__ __forceinline__ void softmax_and_store(const AttnParams& P, Bars* B, uint8_t* smem,
                                                   uint32_t tmem, uint32_t rank, uint32_t peer,
@@ -90,6 +103,10 @@ __device__ __forceinline__ void softmax_and_store(const AttnParams& P, Bars* B, 
   const long m = (long)b * P.T + tok;
   const int p = P.positions[m];
   const bool qv = P.q_visible ? P.q_visible[m] != 0 : true;
+  // the keys this query sees form one interval [vlo, vhi): j < kv_len and, for
+  // a sliding window, p - j < W; a fully masked query sees none
+  const int vlo = W > 0 ? max(0, p - W + 1) : 0;
+  const int vhi = qv ? kvl : 0;
   float* xrow = (float*)(smem + OFF_X) + r * KT;
   const uint32_t peer_xrow = mapa(smem_u32(xrow), peer);
   const uint32_t peer_xfull = mapa(smem_u32(&B->x_full), peer);
@@ -103,15 +120,20 @@ __device__ __forceinline__ void softmax_and_store(const AttnParams& P, Bars* B, 
     const uint32_t sbuf = tmem + TM_S + 64 * (t & 1) + lane_base;
     wait_local(B, &B->s_full[t & 1], (t >> 1) & 1, P.status);
     tc_fence_after();
+    // exchange the partial scores with the peer CTA (its buffer is free once
+    // it has read the previous tile)
     tmem_ld32(sbuf, s);
+    wait_local(B, &B->x_empty, (t & 1) ^ 1, P.status);
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) st_cluster_v4(peer_xrow + 4 * i, s[i], s[i + 1], s[i + 2], s[i + 3]);
     tmem_ld32(sbuf + 32, s + 32);
     tc_fence_before();
     mbar_arrive(&B->s_free[t & 1]);
-    // exchange the partial scores with the peer CTA
-    wait_local(B, &B->x_empty, (t & 1) ^ 1, P.status);
 #pragma unroll
-    for (int i = 0; i < KT; i += 4) st_cluster_v4(peer_xrow + 4 * i, s[i], s[i + 1], s[i + 2], s[i + 3]);
-    mbar_arrive_remote(peer_xfull);
+    for (int i = 32; i < KT; i += 4) st_cluster_v4(peer_xrow + 4 * i, s[i], s[i + 1], s[i + 2], s[i + 3]);
+    // all 128 rows stored, then one cluster-scope release carries them to the peer
+    softmax_bar_sync();
+    if (r == 0) mbar_arrive_remote(peer_xfull);
     wait_peer(B, &B->x_full, t & 1, P.status);
 #pragma unroll
     for (int i = 0; i < KT; i += 4) {
@@ -120,29 +142,32 @@ __device__ __forceinline__ void softmax_and_store(const AttnParams& P, Bars* B, 
 #pragma unroll
       for (int u = 0; u < 4; ++u) s[i + u] = rank == 0 ? s[i + u] + xs[u] : xs[u] + s[i + u];
     }
-    mbar_arrive_remote(peer_xempty);
+    softmax_bar_sync();
+    if (r == 0) mbar_arrive_remote(peer_xempty);   // every row read: the peer may write again
     // mask by logical position, scale into the exp2 domain
-    float tmax = -INFINITY;
+    const int lo = max(vlo - j0, 0), hi = min(vhi - j0, KT);   // visible columns [lo, hi)
+    if (hi > lo) {
+      cnt += hi - lo;
+      if (first < 0) first = j0 + lo;
+      last = j0 + hi - 1;
+    }
+    float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
     for (int i = 0; i < KT; ++i) {
-      const int j = j0 + i;
-      const bool vis = qv && j < kvl && (W == 0 || p - j < W);
-      s[i] = vis ? s[i] * P.scale_log2 : -INFINITY;
-      if (vis) {
-        ++cnt;
-        if (first < 0) first = j;
-        last = j;
-      }
-      tmax = fmaxf(tmax, s[i]);
+      s[i] = (i >= lo && i < hi) ? s[i] * P.scale_log2 : -INFINITY;
+      mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
     }
+    const float tmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
     const bool grow = tmax > mrun + RESCALE_LOG2;
     const float m_new = grow ? tmax : mrun;
-    float psum = 0.f;
+    const float mref = m_new == -INFINITY ? 0.f : m_new;      // all masked so far: P = 0
+    float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < KT; ++i) {
-      s[i] = s[i] == -INFINITY ? 0.f : exp2f(s[i] - m_new);
-      psum += s[i];
+      s[i] = fast_exp2(s[i] - mref);
+      ps4[i & 3] += s[i];
     }
+    const float psum = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
     // the previous P.V has finished: P may be overwritten and O rescaled
     if (t > 0) wait_local(B, &B->o_done, (t - 1) & 1, P.status);
     tc_fence_after();
@@ -253,8 +278,8 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
     }
     mbar_init(&B->p_full, QROWS);
     mbar_init(&B->o_done, 1);
-    mbar_init(&B->x_full, QROWS);
-    mbar_init(&B->x_empty, QROWS);
+    mbar_init(&B->x_full, 1);      // one arrival per tile from the peer
+    mbar_init(&B->x_empty, 1);
     B->abort = 0;
     fence_mbar_init();
   }
