@@ -14,6 +14,7 @@
 #include "gemm_tc.cuh"
 
 #include <mutex>
+#include <type_traits>
 
 #include "tc_ptx.cuh"
 
@@ -62,7 +63,8 @@ template <int BN, int STAGES, typename TC>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                int M, int N, int K, TC* __restrict__ C, long ldc, long sC,
-               const float* __restrict__ G, long ldg, long sG, uint32_t idesc, uint32_t* status) {
+               const float* __restrict__ G, long ldg, long sG, uint32_t idesc, int splitk,
+               uint32_t* status) {
   using S = Smem<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -72,8 +74,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   uint32_t* tmem_slot = (uint32_t*)(accum + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM, z = blockIdx.z;
-  const int nk = (K + BK - 1) / BK;
+  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
+  const int z = blockIdx.z / splitk, ks = blockIdx.z % splitk;
+  const int nk_all = (K + BK - 1) / BK;
+  const int kb0 = (int)((long)ks * nk_all / splitk);          // this split's K blocks
+  const int nk = (int)((long)(ks + 1) * nk_all / splitk) - kb0;
   constexpr uint32_t TMEM_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
 
   if (threadIdx.x == 0) {
@@ -103,8 +108,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint8_t* a = smem + s * S::STAGE_BYTES;
       uint8_t* b = a + S::A_BYTES;
       mbar_arrive_expect_tx(&full[s], S::STAGE_BYTES);
-      tma_load_3d(a, &tmA, &full[s], kb * BK, m0, z);
-      tma_load_3d(b, &tmB, &full[s], kb * BK, n0, z);
+      tma_load_3d(a, &tmA, &full[s], (kb0 + kb) * BK, m0, z);
+      tma_load_3d(b, &tmB, &full[s], (kb0 + kb) * BK, n0, z);
     }
     // drain: the last loads of every slot have landed before the CTA can exit
     for (int kb = max(0, nk - STAGES); kb < nk; ++kb)
@@ -127,7 +132,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
   __syncwarp();
   // epilogue: every warp reads its 32 accumulator lanes
-  const bool have = mbar_wait(accum, 0, status);
+  const bool have = nk > 0 && mbar_wait(accum, 0, status);
   tc_fence_after();
   const int row = m0 + warp * 32 + lane;
   const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
@@ -144,6 +149,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (n + i < N) v[i] = v[i] / (1.f + expf(-g[i]));
     }
     TC* dst = C + z * sC + (long)row * ldc + n;
+    if constexpr (std::is_same<TC, float>::value) {
+      if (splitk > 1) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (n + i < N) atomicAdd(dst + i, v[i]);
+        continue;
+      }
+    }
     if (n + 32 <= N) {
       store32<TC>(dst, v);
     } else {
@@ -216,9 +229,14 @@ mla_status_t launch(cudaStream_t st, const GemmArgs& a, uint32_t* status) {
   std::call_once(once, [&] {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
   });
-  dim3 grid((a.N + BN - 1) / BN, (a.M + BM - 1) / BM, a.batch);
+  if (a.splitk > 1) {
+    const cudaError_t e = cudaMemset2DAsync(a.C, a.ldc * sizeof(float), 0, a.N * sizeof(float),
+                                            (size_t)a.M, st);
+    if (e != cudaSuccess) return cuda_fail(e, "tcgen05 gemm: zeroing the split-K output");
+  }
+  dim3 grid((a.N + BN - 1) / BN, (a.M + BM - 1) / BM, a.batch * a.splitk);
   kern<<<grid, THREADS, S::BYTES, st>>>(ta, tb, a.M, a.N, a.K, (TC*)a.C, a.ldc, a.sC, a.G, a.ldg,
-                                         a.sG, idesc_f16(BM, BN, a.fp16), status);
+                                         a.sG, idesc_f16(BM, BN, a.fp16), a.splitk, status);
   return MLA_OK;
 }
 
@@ -251,6 +269,21 @@ int pick_bn(int M, int N, int batch, int num_sms) {
 
 }  // namespace
 
+int auto_splitk(int M, int N, int K, int batch) {
+  static int num_sms = 0;
+  if (!num_sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+  }
+  const long tiles = (long)((M + BM - 1) / BM) * ((N + 63) / 64) * batch;
+  const int kblocks = (K + BK - 1) / BK;
+  if (batch != 1 || tiles >= num_sms || kblocks < 16) return 1;
+  int s = (int)((num_sms + tiles - 1) / tiles);
+  s = s < kblocks / 8 ? s : kblocks / 8;        // keep >= 8 K blocks per split
+  return s < 1 ? 1 : s;
+}
+
 mla_status_t gemm(cudaStream_t st, const GemmArgs& a, uint32_t* status) {
   if (a.M <= 0 || a.N <= 0 || a.batch <= 0) return MLA_OK;
   const bool ok = a.K % 8 == 0 && a.lda % 8 == 0 && a.ldb % 8 == 0 && a.sA % 8 == 0 &&
@@ -259,6 +292,8 @@ mla_status_t gemm(cudaStream_t st, const GemmArgs& a, uint32_t* status) {
                   (uintptr_t)a.C % 16 == 0;
   if (!ok) return fail(MLA_ERR_UNSUPPORTED, "tcgen05 gemm: K/leading dims must be multiples of 8 "
                                              "and pointers 16-byte aligned");
+  if (a.splitk < 1 || (a.splitk > 1 && (a.out != Out::F32 || a.G || a.batch != 1)))
+    return fail(MLA_ERR_INVALID_ARG, "tcgen05 gemm: split-K needs an fp32 output, no gate, batch 1");
   static int num_sms = 0;
   if (!num_sms) {
     int dev = 0;

@@ -17,9 +17,16 @@ struct GemmArgs {
   const void* B; long ldb, sB;   // [batch][N][K]
   void* C; long ldc, sC; Out out;
   const float* G; long ldg, sG;  // optional sigmoid gate, same indexing as C
+  int splitk = 1;                // >1: K split across CTAs, fp32 C accumulated atomically
 };
 
-// Enqueue C = A B^T (* sigmoid(G)) on `st`.  Returns MLA_ERR_UNSUPPORTED for
+// Split-K factor that lets a small-M GEMM fill the GPU (1 = none).  Only
+// meaningful for fp32 outputs without a gate.
+int auto_splitk(int M, int N, int K, int batch);
+
+// Enqueue C = A B^T (* sigmoid(G)) on `st`.  With splitk > 1 the fp32 C
+// region is zeroed first (cudaMemset2DAsync) and every split adds into it.  With splitk > 1 the fp32 C
+// region is zeroed first (cudaMemset2DAsync) and every split adds into it.  Returns MLA_ERR_UNSUPPORTED for
 // shapes the kernel does not take (K or leading dims not multiples of 8,
 // unaligned pointers) and MLA_ERR_CUDA if the tensor maps cannot be built.
 mla_status_t gemm(cudaStream_t st, const GemmArgs& a, uint32_t* status);
