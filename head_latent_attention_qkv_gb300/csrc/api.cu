@@ -8,6 +8,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "append_tc.cuh"
 #include "attn_tc.cuh"
 #include "gemm_tc.cuh"
 #include "simt.cuh"
@@ -296,13 +297,17 @@ FwdWs forward_ws(const mla_handle* h, long M) {
   return w;
 }
 
-size_t append_ws(const Layout& l, long n) { return align256((size_t)n * l.L * 4); }
+// The bf16 append runs as one fused kernel; only the fp32 layer stages the
+// projection in a workspace.
+size_t append_ws(const mla_handle* h, long n) {
+  return h->cfg.dtype == MLA_BF16 ? 0 : align256((size_t)n * h->lay.L * 4);
+}
 
 }  // namespace
 }  // namespace mla
 
 extern "C" size_t mla_append_workspace_bytes(const mla_handle_t* h, int32_t n) {
-  return (h && n >= 0) ? append_ws(h->lay, n) : 0;
+  return (h && n >= 0) ? append_ws(h, n) : 0;
 }
 
 extern "C" size_t mla_forward_workspace_bytes(const mla_handle_t* h, int32_t num_tokens) {
@@ -348,12 +353,17 @@ mla_status_t append_impl(mla_handle_t* h, const void* hidden, const int32_t* pos
                  cudaStream_t st) {
   const Layout& l = h->lay;
   // kv = hidden @ W_kva^T : W_kva = first L rows of W_A
-  mla_status_t s = proj<T, float>(h, st, n, l.L, l.D, 1, (const T*)hidden, l.D, 0,
-                                  (const T*)h->WA, l.D, 0, kv_ws, l.L, 0);
-  if (s != MLA_OK) return s;
-  simt::kv_finish<T>(st, h, kv_ws, l.L, n, positions, slots, (T*)cache, num_slots);
-  h->launches += 1;
-  return MLA_OK;
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    h->launches += 1;
+    return tc::kv_append(st, h, (const T*)hidden, n, positions, slots, (T*)cache, num_slots);
+  } else {
+    mla_status_t s = proj<T, float>(h, st, n, l.L, l.D, 1, (const T*)hidden, l.D, 0,
+                                    (const T*)h->WA, l.D, 0, kv_ws, l.L, 0);
+    if (s != MLA_OK) return s;
+    simt::kv_finish<T>(st, h, kv_ws, l.L, n, positions, slots, (T*)cache, num_slots);
+    h->launches += 1;
+    return MLA_OK;
+  }
 }
 
 }  // namespace
@@ -367,10 +377,10 @@ extern "C" mla_status_t mla_latent_cache_append(mla_handle_t* h, const void* hid
   if (!h) return fail(MLA_ERR_INVALID_ARG, "append: null handle");
   if (n < 0) return fail(MLA_ERR_INVALID_ARG, "append: n < 0");
   if (n == 0) return MLA_OK;
-  if (!hidden || !positions || !slot_mapping || !cache || !workspace)
+  if (!hidden || !positions || !slot_mapping || !cache || (!workspace && append_ws(h, n)))
     return fail(MLA_ERR_INVALID_ARG, "append: null pointer");
   if (num_pages <= 0) return fail(MLA_ERR_INVALID_ARG, "append: num_pages <= 0");
-  if (workspace_bytes < append_ws(h->lay, n))
+  if (workspace_bytes < append_ws(h, n))
     return fail(MLA_ERR_INVALID_ARG, "append: workspace smaller than mla_append_workspace_bytes()");
   cudaStream_t st = (cudaStream_t)stream;
   const long num_slots = (long)num_pages * h->cfg.page_size;
@@ -401,14 +411,22 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
   float* a_out = (float*)(ws + w.a_out);
   const TX* x = (const TX*)hidden;
   const TX* WA = (const TX*)h->WA;
-  // A projection; the kv rows only when the block writes its own latents
-  const int r0 = bslots ? 0 : l.L;
+  // A projection; the block's own latents only when it writes them (bf16: the
+  // fused append kernel, fp32: the projection rows then the finish kernel)
+  constexpr bool kBf16 = std::is_same<TX, __nv_bfloat16>::value;
+  const long num_slots = (long)num_pages * h->cfg.page_size;
+  const int r0 = (bslots && !kBf16) ? 0 : l.L;
   mla_status_t s = proj<TX, float>(h, st, M, l.NA - r0, l.D, 1, x, l.D, 0,
                                    WA + (long)r0 * l.D, l.D, 0, a_out + r0, l.NA, 0);
   if (s != MLA_OK) return s;
-  if (bslots)
-    simt::kv_finish<TX>(st, h, a_out, l.NA, M, pos, bslots, (TX*)cache,
-                       (long)num_pages * h->cfg.page_size);
+  if (bslots) {
+    if constexpr (kBf16) {
+      s = tc::kv_append(st, h, x, M, pos, bslots, (TX*)cache, num_slots);
+      if (s != MLA_OK) return s;
+    } else {
+      simt::kv_finish<TX>(st, h, a_out, l.NA, M, pos, bslots, (TX*)cache, num_slots);
+    }
+  }
   const float* q_raw;
   long ldq;
   if (l.rq > 0) {
