@@ -36,7 +36,8 @@ METRIC = "MLA draft-layer tokens/s (block query tokens; TFLOP/s and %bf16 peak a
 def algorithmic_flops(wl):
     """Absorbed latent path: per block token 2D(r_q+L) [+2D*H*dv gate] +
     2 r_q H dqk + 2 H dn r_kv + 2 H r_kv dv + 2 H dv D, per visible key
-    H (2L + 2 r_kv); per appended context token 2 D L."""
+    H (2L + 2 r_kv); per appended token 2 D L.  Also the cache bytes the
+    attention reads (1152 B per key a block can see, once per block)."""
     d = wl.dims
     H, D, L = d.num_heads, d.hidden_size, d.cache_dim
     qdim = d.q_lora_rank if d.q_lora_rank else H * d.qk_head_dim
@@ -45,19 +46,26 @@ def algorithmic_flops(wl):
         per_tok += 2 * d.q_lora_rank * H * d.qk_head_dim
     per_tok += 2 * H * d.qk_nope_head_dim * d.kv_lora_rank + 2 * H * d.kv_lora_rank * d.v_head_dim
     per_tok += 2 * H * d.v_head_dim * D
-    step = wl.steps[0]
     T = wl.block_len
-    keys = 0
-    for b in range(len(step.kv_len)):      # visible keys per query: [lo, kv_len)
-        r = slice(b * T, (b + 1) * T)
-        n, w = int(step.kv_len[b]), int(step.window[b])
-        p = step.block_positions[r].astype(np.int64)
-        lo = np.maximum(0, p - w + 1) if w > 0 else np.zeros_like(p)
-        keys += int(((n - lo) * step.q_visible[r]).sum())
-    n_ctx = 0 if wl.ctx_hidden is None else len(wl.ctx_hidden)
-    append = 2 * D * L * n_ctx
-    return dict(total=per_tok * len(step.block_positions) + H * (2 * L + 2 * d.kv_lora_rank) * keys + append,
-                append=append, block_tokens=len(step.block_positions), ctx_tokens=n_ctx)
+    total = block_tokens = cache_bytes = 0
+    appended = 0 if wl.ctx_hidden is None else len(wl.ctx_hidden)
+    for step in wl.steps:
+        keys = 0
+        for b in range(len(step.kv_len)):      # visible keys per query: [lo, kv_len)
+            r = slice(b * T, (b + 1) * T)
+            n, w = int(step.kv_len[b]), int(step.window[b])
+            p = step.block_positions[r].astype(np.int64)
+            lo = np.maximum(0, p - w + 1) if w > 0 else np.zeros_like(p)
+            keys += int(((n - lo) * step.q_visible[r]).sum())
+            cache_bytes += (n - int(lo.min())) * L * 2
+        total += per_tok * len(step.block_positions) + H * (2 * L + 2 * d.kv_lora_rank) * keys
+        block_tokens += len(step.block_positions)
+        if step.append_hidden is not None:
+            appended += len(step.append_hidden)
+    append = 2 * D * L * (0 if wl.ctx_hidden is None else len(wl.ctx_hidden))
+    total += 2 * D * L * (appended - (0 if wl.ctx_hidden is None else len(wl.ctx_hidden))) + append
+    return dict(total=total, append=append, block_tokens=block_tokens, ctx_tokens=appended,
+                cache_bytes=cache_bytes)
 
 
 class ClockSampler:
@@ -117,10 +125,9 @@ def run_ours(args, rank, world):
     from head_latent_attention_qkv_gb300.runner import DeviceWorkload
 
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
-    wl = workloads.make_workload(WORKLOAD)
+    wl = workloads.make_workload(args.workload)
     fl = algorithmic_flops(wl)
     dev = DeviceWorkload(wl)
-    step = dev.steps[0]
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
 
@@ -128,9 +135,11 @@ def run_ours(args, rank, world):
         dev.append_context()
 
     def forward():
-        dev.run_step(0)
+        for k in range(len(dev.steps)):
+            dev.run_step(k)
 
     dev.reset_cache()
+    torch.cuda.synchronize()
     n0 = api._lib.lib.mla_kernel_launches(dev.handle.h)
     append()
     forward()
@@ -142,14 +151,18 @@ def run_ours(args, rank, world):
     if not args.no_graph:
         graphs = []
         for fn in (append, forward):
+            if fn is append and dev.ctx is None:
+                graphs.append(None)
+                continue
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 fn()
             graphs.append(g)
         for _ in range(2):
-            graphs[0].replay()
-            graphs[1].replay()
-    run_a = graphs[0].replay if graphs else append
+            for g in graphs:
+                if g is not None:
+                    g.replay()
+    run_a = (graphs[0].replay if graphs[0] is not None else (lambda: None)) if graphs else append
     run_f = graphs[1].replay if graphs else forward
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     if world > 1:
@@ -179,48 +192,55 @@ def run_ours(args, rank, world):
 
 def measure_e2e(args, dev, wl, torch):
     """Same step through the C ABI with host buffers: pinned host -> device
-    copies of the step's inputs, append + forward, device -> host of the
-    output, all inside the timed region."""
-    from head_latent_attention_qkv_gb300 import api
-    s = dev.steps[0]
-    host = {n: t.cpu().pin_memory() for n, t in (("ctx_h", dev.ctx[0]), ("ctx_p", dev.ctx[1]),
-                                                  ("ctx_s", dev.ctx[2]), ("h", s["hidden"]),
-                                                  ("p", s["positions"]), ("s", s["slots"]))}
-    out_host = torch.empty(s["out"].shape, dtype=s["out"].dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_host.numel() * out_host.element_size()
-    dst = {"ctx_h": dev.ctx[0], "ctx_p": dev.ctx[1], "ctx_s": dev.ctx[2], "h": s["hidden"],
-           "p": s["positions"], "s": s["slots"]}
+    copies of the step's inputs, the appends and forwards, device -> host of
+    the outputs, all inside the timed region."""
+    pairs = []
+    if dev.ctx is not None:
+        pairs += list(dev.ctx)
+    for s in dev.steps:
+        if s["append"] is not None:
+            pairs += list(s["append"])
+        pairs += [s["hidden"], s["positions"]] + ([s["slots"]] if s["slots"] is not None else [])
+    host = [(t.cpu().pin_memory(), t) for t in pairs]
+    outs = [(torch.empty(s["out"].shape, dtype=s["out"].dtype).pin_memory(), s["out"]) for s in dev.steps]
+    h2d = sum(h.numel() * h.element_size() for h, _ in host)
+    d2h = sum(h.numel() * h.element_size() for h, _ in outs)
     times = []
     for k in range(args.warmup + args.steps):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for n, t in host.items():
-            dst[n].copy_(t, non_blocking=True)
-        api.mla_latent_cache_append(dev.handle, dev.ctx[0], dev.ctx[1], dev.ctx[2], dev.cache)
-        api.mla_draft_forward(dev.handle, s["hidden"], s["positions"], s["slots"], dev.cache,
-                              s["desc"], out=s["out"])
-        out_host.copy_(s["out"], non_blocking=True)
+        for h, d in host:
+            d.copy_(h, non_blocking=True)
+        dev.append_context()
+        for j in range(len(dev.steps)):
+            dev.run_step(j)
+        for h, d in outs:
+            h.copy_(d, non_blocking=True)
         torch.cuda.synchronize()
         if k >= args.warmup:
             times.append(time.perf_counter() - t0)
     return sum(times) / len(times), h2d, d2h
 
 
-def cpu_baseline(budget_s=15.0):
+def cpu_baseline(workload=WORKLOAD, budget_s=15.0):
     """The fp64 oracle as it stands, on a bounded sample of the same workload:
     whole blocks (context latents of the block's sequence + the block's
     forward), as many as fit in ``budget_s``.  Returns block tokens/s."""
     from head_latent_attention_qkv_gb300 import workloads
     from oracle.keys import OracleRun
-    wl = workloads.make_workload(WORKLOAD)
+    wl = workloads.make_workload(workload)
     step = wl.steps[0]
     run = OracleRun(wl)
     t0 = time.perf_counter()
     done = 0
+    rows = []
     for b in range(len(step.kv_len)):
-        rows = np.nonzero(wl.ctx_seq == step.block_seq[b])[0]
-        run.append(wl.ctx_hidden, wl.ctx_positions, wl.ctx_slots, rows)
+        if wl.ctx_hidden is not None:
+            rows = np.nonzero(wl.ctx_seq == step.block_seq[b])[0]
+            run.append(wl.ctx_hidden, wl.ctx_positions, wl.ctx_slots, rows)
+        if step.append_hidden is not None:
+            r = np.arange(b * wl.block_len, (b + 1) * wl.block_len)
+            run.append(step.append_hidden, step.append_positions, step.append_slots, r)
         run.forward_blocks(step, [b])
         done += 1
         if time.perf_counter() - t0 > budget_s:
@@ -233,12 +253,18 @@ def cpu_baseline(budget_s=15.0):
 
 
 def base_line(args, world):
+    from head_latent_attention_qkv_gb300 import workloads
+    desc = {"tiny_fp32": "1 x (64 context + 8-token block), fp32",
+            "qwen3_4b_prefill": "8 x (2048 context + 16-token block), full mask",
+            "qwen3_4b_sliding_gate": "16 x (8192 context + 16), sliding 512, gate, masked rows",
+            "qwen3_4b_cached_decode": "64 seqs, cache pre-filled, 2 consecutive 16-token blocks",
+            "deepseek_v3_block_parallel": "4 x 1024 proposals of 16 over a 4096 context, gate"}
     return {"metric": METRIC, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "data": "synthetic (seeded N(0,1) hidden, N(0,0.02) weights)",
-            "config": {"workload": WORKLOAD, "model": "Qwen3-4B-sized MLA draft layer",
-                       "global_batch": 8 * world, "seq_len": 2048 + 16, "block_len": 16,
-                       "parallelism": f"replicas x{world}", "l2": "flushed (256 MB write) between steps"}}
+            "config": {"workload": args.workload, "shape": desc.get(args.workload, ""),
+                       "parallelism": f"replicas x{world}",
+                       "l2": "flushed (256 MB write) between steps"}}
 
 
 def main():
@@ -249,6 +275,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -260,10 +287,10 @@ def main():
             return
         per = []
         for _ in range(args.steps):
-            per.append(cpu_baseline(budget_s=max(2.0, 60.0 / max(args.steps, 1))))
+            per.append(cpu_baseline(args.workload, budget_s=max(2.0, 60.0 / max(args.steps, 1))))
         v = statistics.median(p["value"] for p in per)
         line = base_line(args, 1)
-        line.update({"impl": "reference", "value": v, "ms_per_step": 8 * 16 / v * 1e3,
+        line.update({"impl": "reference", "value": v, "ms_per_step": None,
                      "dtype": "f64", "cpu_baseline": dict(per[-1], value=v),
                      "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                              "d2h_bytes_per_step": 0}})
@@ -282,14 +309,19 @@ def main():
     value = world * fl["block_tokens"] / (r["ms"] * 1e-3)
     tflops = fl["total"] / (r["ms"] * 1e-3) / 1e12
     t_app = r["ms_append"] * 1e-3
-    ach = fl["append"] / t_app / 1e12
+    if fl["append"]:
+        ach, rl_kernel = fl["append"] / t_app / 1e12, "latent-cache append (tcgen05 GEMM N=576 + RMSNorm/RoPE/slot scatter)"
+    else:   # no context append in this workload: the whole step against the tensor peak
+        ach, rl_kernel = fl["total"] / (r["ms"] * 1e-3) / 1e12, "whole step (appends + forwards)"
     line = base_line(args, world)
     e2e_s, h2d, d2h = r["e2e"]
     line.update({
         "value": value, "ms_per_step": r["ms"], "dtype": "bf16",
         "tflops": tflops, "pct_bf16_peak": 100 * tflops / bf16,
         "context_tokens_per_s": world * fl["ctx_tokens"] / (r["ms"] * 1e-3),
-        "roofline": {"kernel": "latent-cache append (context GEMM N=576 + norm/RoPE/cache store)",
+        "cache_read_gbs": fl["cache_bytes"] / (r["ms"] * 1e-3) / 1e9,
+        "pct_hbm_cache_read": 100 * fl["cache_bytes"] / (r["ms"] * 1e-3) / 1e9 / hbm,
+        "roofline": {"kernel": rl_kernel,
                      "bound": "tensor", "achieved": ach, "peak": bf16, "unit": "TFLOP/s",
                      "frac": ach / bf16, "traffic": None,
                      "peak_source": f"{src} bf16 burst"},
@@ -300,7 +332,7 @@ def main():
         "clocks": r["clocks"],
     })
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline()
+        line["cpu_baseline"] = cpu_baseline(args.workload)
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
