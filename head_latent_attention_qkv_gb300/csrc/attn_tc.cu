@@ -6,21 +6,27 @@
 // Work unit: one query block and 128 consecutive rows of Q_abs (rows are
 // (token, head) pairs, token-major), handled by a cluster of two CTAs.  The
 // 128 x 512 fp32 output accumulator does not fit one SM's tensor memory next
-// to a score tile, so CTA r keeps value columns [256r, 256r+256) in TMEM
-// (256 columns) plus a 128 x 64 score tile (64 columns).  The score reduction
-// over the 576 latent dims is split between the pair: CTA 0 owns dims
-// 0..255 and the rope dims 512..575, CTA 1 owns dims 256..511, which are also
-// exactly the value dims each needs, so every cache byte is loaded once per
-// pair.  Per 64-key tile:
-//   MMA warp : S_r = Q_r K_r^T over its own dims (tcgen05, TMEM)
-//   softmax  : read S_r, send it to the peer through DSMEM, add the peer's
-//              partial (same order in both CTAs, so both see identical
-//              scores), mask by logical position, online softmax in fp32
-//              (exp2 domain, rescale of the TMEM accumulator only when the
-//              running max grows by more than 2^8), write P (bf16) to smem
-//   MMA warp : O_r += P V_r (V read MN-major straight from the staged tile)
-// Warps 0-3 (thread = accumulator row / TMEM lane) run the softmax and the
-// epilogue, warp 4 streams Q and KV tiles with TMA, warp 5 issues MMAs.
+// to the score tiles, so CTA r keeps value columns [256r, 256r+256) in TMEM.
+// The score reduction over the 576 latent dims is split between the pair:
+// CTA 0 owns dims 0..255 and the rope dims 512..575, CTA 1 owns dims
+// 256..511, which are also exactly the value dims each needs, so every cache
+// byte is loaded once per pair.  Per 64-key tile t:
+//   MMA warp      : S_r(t) = Q_r K_r(t)^T over its own dims into score buffer
+//                   t % 2 (issued while the softmax still works on tile t-1)
+//   exchange warps: as soon as S_r(t) lands, send it to the peer with
+//                   asynchronous DSMEM stores that count their bytes on the
+//                   peer's barrier (double-buffered, so the send overlaps the
+//                   softmax of the previous tile)
+//   softmax warps : add own and peer partial (same order in both CTAs, so
+//                   both see identical scores), mask by logical position,
+//                   online softmax in fp32 (exp2 domain; the TMEM accumulator
+//                   is rescaled only when the running max grows by more than
+//                   2^8), write P (bf16) into tensor memory, buffer t % 2
+//   MMA warp      : O_r += P(t) V_r(t), P read from tensor memory, V read
+//                   MN-major straight from the staged KV tile
+// Warps 0-3 run the softmax and the epilogue (thread = accumulator row = TMEM
+// lane), warps 4-7 the score exchange (same lanes), warp 8 streams Q and KV
+// tiles with TMA, warp 9 owns TMEM and issues the MMAs.
 #include "attn_tc.cuh"
 
 #include <mutex>
@@ -32,22 +38,25 @@ namespace tc {
 namespace {
 
 constexpr int QROWS = 128, KT = 64, DCH = 64;    // query rows, keys per tile, dims per chunk
-constexpr int THREADS = 192;
+constexpr int THREADS = 320;
 constexpr int MAX_CH = 5;                         // dim chunks held by CTA 0 (4 latent + rope)
 constexpr int Q_CH_BYTES = QROWS * DCH * 2;       // 16 KiB
 constexpr int KV_CH_BYTES = KT * DCH * 2;         // 8 KiB
 constexpr int KV_STAGE_BYTES = MAX_CH * KV_CH_BYTES;
+constexpr int X_BYTES = QROWS * KT * 4;           // one tile of peer partial scores
 constexpr int OFF_Q = 0;
 constexpr int OFF_KV = OFF_Q + MAX_CH * Q_CH_BYTES;
-constexpr int OFF_P = OFF_KV + 2 * KV_STAGE_BYTES;
-constexpr int OFF_X = OFF_P + QROWS * KT * 2;
-constexpr int OFF_BAR = OFF_X + QROWS * KT * 4;
+constexpr int OFF_X = OFF_KV + 2 * KV_STAGE_BYTES;
+constexpr int OFF_BAR = OFF_X + 2 * X_BYTES;
 constexpr int SMEM_BYTES = 1024 + OFF_BAR + 256;
-constexpr uint32_t TMEM_COLS = 512, TM_O = 0, TM_S = 256;   // S double-buffered: 256, 320
+// TMEM columns: O at 0..255, scores at 256 + 64 b, P (bf16 pairs) at 384 + 32 b
+constexpr uint32_t TMEM_COLS = 512, TM_O = 0, TM_S = 256, TM_P = 384;
 constexpr float RESCALE_LOG2 = 8.f;               // lazy rescale threshold (factor 256)
 
 struct Bars {
-  uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, o_done, x_full, x_empty;
+  uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, o_done[2];
+  uint64_t x_full[2];    // peer's partial scores landed (expect-tx, 1 local arrival)
+  uint64_t x_empty[2];   // peer has read the partial scores sent to it (4 warp arrivals)
   uint32_t tmem_slot;
   int abort;
 };
@@ -55,14 +64,6 @@ struct Bars {
 __device__ __forceinline__ int dim_chunk(int rank, int i) {
   return rank == 0 ? (i < 4 ? i : 8) : 4 + i;    // global 64-dim chunk of local chunk i
 }
-
-}  // namespace
-}  // namespace tc
-}  // namespace mla
-
-namespace mla {
-namespace tc {
-namespace {
 
 // Bounded waits that give up at once after any earlier timeout of this CTA.
 __device__ __forceinline__ bool wait_local(Bars* B, uint64_t* bar, uint32_t parity, uint32_t* st) {
@@ -86,9 +87,32 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// Named barrier of the 128 softmax threads (barrier 0 is __syncthreads).
-__device__ __forceinline__ void softmax_bar_sync() {
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+// Warps 4-7: forward this CTA's partial scores of every tile to the peer.
+__device__ __forceinline__ void exchange_scores(const AttnParams& P, Bars* B, uint8_t* smem,
+                                                uint32_t tmem, uint32_t peer, int nt) {
+  const int r = threadIdx.x - QROWS;                  // row / TMEM lane
+  const uint32_t lane_base = (uint32_t)((r / 32) * 32) << 16;
+  const uint32_t peer_x = mapa(smem_u32((float*)(smem + OFF_X) + r * KT), peer);
+  const uint32_t peer_full[2] = {mapa(smem_u32(&B->x_full[0]), peer), mapa(smem_u32(&B->x_full[1]), peer)};
+  for (int t = 0; t < nt; ++t) {
+    const int buf = t & 1;
+    const uint32_t ph = (t >> 1) & 1;
+    if (!wait_local(B, &B->s_full[buf], ph, P.status)) break;
+    tc_fence_after();
+    float s[KT];
+    tmem_ld32(tmem + TM_S + 64 * buf + lane_base, s);
+    tmem_ld32(tmem + TM_S + 64 * buf + lane_base + 32, s + 32);
+    tc_fence_before();
+    mbar_arrive(&B->s_free[buf]);
+    // the peer has read what was sent into this buffer two tiles ago
+    if (!wait_peer(B, &B->x_empty[buf], ph ^ 1, P.status)) break;
+    // 16-byte chunk c of a row sits at chunk c ^ (row % 8): the eight rows a
+    // quarter-warp touches at once fall in distinct banks
+#pragma unroll
+    for (int c = 0; c < KT / 4; ++c)
+      st_async_v4(peer_x + buf * X_BYTES + 16 * (c ^ (r & 7)), s[4 * c], s[4 * c + 1], s[4 * c + 2],
+                  s[4 * c + 3], peer_full[buf]);
+  }
 }
 
 // Warps 0-3: thread r owns accumulator row r (TMEM lane r) of the tile.
@@ -96,7 +120,7 @@ __device__ __forceinline__ void softmax_and_store(const AttnParams& P, Bars* B, 
                                                   uint32_t tmem, uint32_t rank, uint32_t peer,
                                                   int b, int qt, long row0, int kvl, int W,
                                                   int j_lo, int nt) {
-  const int r = threadIdx.x;
+  const int r = threadIdx.x, lane = r % 32;
   const uint32_t lane_base = (uint32_t)((r / 32) * 32) << 16;
   const int row_in_block = qt * QROWS + r;
   const int tok = row_in_block / P.H, head = row_in_block % P.H;
@@ -107,43 +131,34 @@ __device__ __forceinline__ void softmax_and_store(const AttnParams& P, Bars* B, 
   // a sliding window, p - j < W; a fully masked query sees none
   const int vlo = W > 0 ? max(0, p - W + 1) : 0;
   const int vhi = qv ? kvl : 0;
-  float* xrow = (float*)(smem + OFF_X) + r * KT;
-  const uint32_t peer_xrow = mapa(smem_u32(xrow), peer);
-  const uint32_t peer_xfull = mapa(smem_u32(&B->x_full), peer);
-  const uint32_t peer_xempty = mapa(smem_u32(&B->x_empty), peer);
-  uint8_t* prow = smem + OFF_P + r * 128;
+  const float* xrow = (const float*)(smem + OFF_X) + r * KT;
+  const uint32_t peer_empty[2] = {mapa(smem_u32(&B->x_empty[0]), peer), mapa(smem_u32(&B->x_empty[1]), peer)};
   float mrun = -INFINITY, lsum = 0.f;
   int cnt = 0, first = -1, last = -1;
   for (int t = 0; t < nt; ++t) {
+    const int buf = t & 1;
+    const uint32_t ph = (t >> 1) & 1;
     const int j0 = j_lo + t * KT;
     float s[KT];
-    const uint32_t sbuf = tmem + TM_S + 64 * (t & 1) + lane_base;
-    wait_local(B, &B->s_full[t & 1], (t >> 1) & 1, P.status);
+    wait_local(B, &B->s_full[buf], ph, P.status);
     tc_fence_after();
-    // exchange the partial scores with the peer CTA (its buffer is free once
-    // it has read the previous tile)
-    tmem_ld32(sbuf, s);
-    wait_local(B, &B->x_empty, (t & 1) ^ 1, P.status);
+    tmem_ld32(tmem + TM_S + 64 * buf + lane_base, s);
+    tmem_ld32(tmem + TM_S + 64 * buf + lane_base + 32, s + 32);
+    wait_peer(B, &B->x_full[buf], ph, P.status);
+    // arm this buffer for tile t + 2 before the peer can be told it is free
+    if (r == 0 && t + 2 < nt) mbar_arrive_expect_tx(&B->x_full[buf], X_BYTES);
+    const float* x = xrow + buf * (X_BYTES / 4);
 #pragma unroll
-    for (int i = 0; i < 32; i += 4) st_cluster_v4(peer_xrow + 4 * i, s[i], s[i + 1], s[i + 2], s[i + 3]);
-    tmem_ld32(sbuf + 32, s + 32);
-    tc_fence_before();
-    mbar_arrive(&B->s_free[t & 1]);
+    for (int c = 0; c < KT / 4; ++c) {
+      const float4 v = *reinterpret_cast<const float4*>(x + 4 * (c ^ (r & 7)));
+      const float xs[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int i = 32; i < KT; i += 4) st_cluster_v4(peer_xrow + 4 * i, s[i], s[i + 1], s[i + 2], s[i + 3]);
-    // all 128 rows stored, then one cluster-scope release carries them to the peer
-    softmax_bar_sync();
-    if (r == 0) mbar_arrive_remote(peer_xfull);
-    wait_peer(B, &B->x_full, t & 1, P.status);
-#pragma unroll
-    for (int i = 0; i < KT; i += 4) {
-      const float4 x = *reinterpret_cast<const float4*>(xrow + i);
-      const float xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-      for (int u = 0; u < 4; ++u) s[i + u] = rank == 0 ? s[i + u] + xs[u] : xs[u] + s[i + u];
+      for (int u = 0; u < 4; ++u) s[4 * c + u] = rank == 0 ? s[4 * c + u] + xs[u] : xs[u] + s[4 * c + u];
     }
-    softmax_bar_sync();
-    if (r == 0) mbar_arrive_remote(peer_xempty);   // every row read: the peer may write again
+    tc_fence_before();
+    mbar_arrive(&B->s_free[buf]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive_remote(peer_empty[buf]);   // this warp's rows are read
     // mask by logical position, scale into the exp2 domain
     const int lo = max(vlo - j0, 0), hi = min(vhi - j0, KT);   // visible columns [lo, hi)
     if (hi > lo) {
@@ -168,11 +183,11 @@ __device__ __forceinline__ void softmax_and_store(const AttnParams& P, Bars* B, 
       ps4[i & 3] += s[i];
     }
     const float psum = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
-    // the previous P.V has finished: P may be overwritten and O rescaled
-    if (t > 0) wait_local(B, &B->o_done, (t - 1) & 1, P.status);
-    tc_fence_after();
     const float alpha = (grow && mrun != -INFINITY) ? exp2f(mrun - m_new) : 1.f;
     if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      // every earlier P.V has finished before O is rescaled
+      wait_local(B, &B->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, P.status);
+      tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < 256; c += 32) {
         float o[32];
@@ -184,29 +199,35 @@ __device__ __forceinline__ void softmax_and_store(const AttnParams& P, Bars* B, 
     }
     lsum = lsum * alpha + psum;
     mrun = m_new;
+    // P buffer `buf` was last read by P.V of tile t - 2
+    if (t >= 2) {
+      wait_local(B, &B->o_done[buf], ph ^ 1, P.status);
+      tc_fence_after();
+    }
     // value rows of keys past kv_len may hold anything: zero them (last tile)
-    if (j0 + KT > kvl) {
-      uint8_t* stage = smem + OFF_KV + (t & 1) * KV_STAGE_BYTES;
+    const bool tail = j0 + KT > kvl;
+    if (tail) {
+      uint8_t* stage = smem + OFF_KV + buf * KV_STAGE_BYTES;
       const int z0 = max(0, kvl - j0), pieces = (KT - z0) * 4 * 8;
       for (int idx = r; idx < pieces; idx += QROWS) {
         const int key = z0 + idx / 32, ch = (idx % 32) / 8, q = idx % 8;
         *reinterpret_cast<uint4*>(stage + ch * KV_CH_BYTES + key * 128 + q * 16) = make_uint4(0, 0, 0, 0);
       }
+      fence_proxy_async_smem();
     }
-    // P row in bf16, 128-byte-swizzled K-major layout (16-byte chunk q of row r at q ^ (r % 8))
+    // P row in bf16 pairs: key 2c in the low half of column c
+    float pw[KT / 2];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      __nv_bfloat162 h2[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) h2[u] = __floats2bfloat162_rn(s[8 * q + 2 * u], s[8 * q + 2 * u + 1]);
-      *reinterpret_cast<uint4*>(prow + ((q ^ (r & 7)) * 16)) = *reinterpret_cast<uint4*>(h2);
+    for (int c = 0; c < KT / 2; ++c) {
+      __nv_bfloat162 h2 = __floats2bfloat162_rn(s[2 * c], s[2 * c + 1]);
+      pw[c] = *reinterpret_cast<float*>(&h2);
     }
-    fence_proxy_async_smem();
+    tmem_st32(tmem + TM_P + 32 * buf + lane_base, pw);
     tc_fence_before();
     mbar_arrive(&B->p_full);
   }
   // epilogue: O_r / l -> fp16 latent output columns [256 rank, 256 rank + 256)
-  if (nt > 0) wait_local(B, &B->o_done, (nt - 1) & 1, P.status);
+  if (nt > 0) wait_local(B, &B->o_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, P.status);
   tc_fence_after();
   const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
   const bool any = nt > 0 && lsum > 0.f;
@@ -266,30 +287,6 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
   const int b = unit / P.tiles_per_block, qt = unit % P.tiles_per_block;
   const long row0 = ((long)b * P.tiles_per_block + qt) * QROWS;   // first Q_abs row of the tile
 
-  if (tid == 0) {
-    mbar_init(&B->q_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&B->kv_full[s], 1);
-      mbar_init(&B->kv_empty[s], 1);
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&B->s_full[s], 1);
-      mbar_init(&B->s_free[s], QROWS);
-    }
-    mbar_init(&B->p_full, QROWS);
-    mbar_init(&B->o_done, 1);
-    mbar_init(&B->x_full, 1);      // one arrival per tile from the peer
-    mbar_init(&B->x_empty, 1);
-    B->abort = 0;
-    fence_mbar_init();
-  }
-  if (warp == 5) tmem_alloc(&B->tmem_slot, TMEM_COLS);
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync_all();          // the peer's barriers exist before anyone signals them
-  tc_fence_after();
-  const uint32_t tmem = B->tmem_slot;
-
   // key range of this tile: [j_lo, kvl) in 64-key tiles (identical in both CTAs)
   int kvl = P.kv_len[b];
   const int cap = P.max_pages * P.page_size;
@@ -313,7 +310,31 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
     nt = te - tb;
   }
 
-  if (warp == 4) {
+  if (tid == 0) {
+    mbar_init(&B->q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&B->kv_full[s], 1);
+      mbar_init(&B->kv_empty[s], 1);
+      mbar_init(&B->s_full[s], 1);
+      mbar_init(&B->s_free[s], 2 * QROWS);    // softmax and exchange threads
+      mbar_init(&B->o_done[s], 1);
+      mbar_init(&B->x_full[s], 1);
+      mbar_init(&B->x_empty[s], QROWS / 32);  // one arrival per peer softmax warp
+    }
+    mbar_init(&B->p_full, QROWS);
+    B->abort = 0;
+    fence_mbar_init();
+    // the first two score tiles from the peer are expected before it can send
+    for (int s = 0; s < 2 && s < nt; ++s) mbar_arrive_expect_tx(&B->x_full[s], X_BYTES);
+  }
+  if (warp == 9) tmem_alloc(&B->tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();          // the peer's barriers exist before anyone signals them
+  tc_fence_after();
+  const uint32_t tmem = B->tmem_slot;
+
+  if (warp == 8) {
     if (lane == 0) {
       // ---- TMA producer ----
       prefetch_tmap(&P.tmQ);
@@ -322,48 +343,55 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
       for (int i = 0; i < nch; ++i)
         tma_load_3d(smem + OFF_Q + i * Q_CH_BYTES, &P.tmQ, &B->q_full, dim_chunk(rank, i) * DCH,
                     (int)row0, 0);
-      const int R = P.seg_rows, past_end = P.num_pages * P.page_size;
-      int issued = 0;
+      const int R = P.seg_rows, nseg = KT / R, past_end = P.num_pages * P.page_size;
       // cache row of key j (beyond the cache when j is past kv_len or its page
       // is invalid: TMA then fills zeros)
-      auto cache_row = [&](int j, bool report) {
+      auto cache_row = [&](int j) {
         if (j >= kvl) return past_end;
         const int pg = P.block_table[(long)b * P.max_pages + j / P.page_size];
         if (pg >= 0 && pg < P.num_pages) return pg * P.page_size + j % P.page_size;
-        if (report) set_status(P.status, MLA_DEV_BAD_PAGE);
+        set_status(P.status, MLA_DEV_BAD_PAGE);
         return past_end;
       };
-      auto prefetch_tile = [&](int t) {
-        if (t >= nt) return;
-        for (int seg = 0; seg < KT / R; ++seg) {
-          const int y = cache_row(j_lo + t * KT + seg * R, false);
-          if (y == past_end) continue;
-          for (int i = 0; i < nch; ++i) tma_prefetch_3d(&P.tmKV, dim_chunk(rank, i) * DCH, y, 0);
+      // cache rows of tile t's segments (at most 4: page_size >= 16), looked
+      // up and pulled into L2 two tiles ahead of the tile's load
+      auto lookup = [&](int t, int* y) {
+#pragma unroll
+        for (int seg = 0; seg < 4; ++seg) {
+          y[seg] = past_end;
+          if (t < nt && seg < nseg) {
+            y[seg] = cache_row(j_lo + t * KT + seg * R);
+            if (y[seg] != past_end)
+              for (int i = 0; i < nch; ++i) tma_prefetch_3d(&P.tmKV, dim_chunk(rank, i) * DCH, y[seg], 0);
+          }
         }
       };
-      prefetch_tile(0);
-      prefetch_tile(1);
+      int cur[4], nxt[4];
+      lookup(0, cur);
+      lookup(1, nxt);
+      int issued = 0;
       for (int t = 0; t < nt; ++t) {
         const int s = t & 1;
-        prefetch_tile(t + 2);
         if (!wait_local(B, &B->kv_empty[s], ((t >> 1) & 1) ^ 1, P.status)) break;
-        const int j0 = j_lo + t * KT;
         uint8_t* stage = smem + OFF_KV + s * KV_STAGE_BYTES;
         mbar_arrive_expect_tx(&B->kv_full[s], nch * KV_CH_BYTES);
-        for (int seg = 0; seg < KT / R; ++seg) {
-          const int y = cache_row(j0 + seg * R, true);
-          for (int i = 0; i < nch; ++i)
-            tma_load_3d(stage + i * KV_CH_BYTES + seg * R * 128, &P.tmKV, &B->kv_full[s],
-                        dim_chunk(rank, i) * DCH, y, 0);
-        }
+#pragma unroll
+        for (int seg = 0; seg < 4; ++seg)
+          if (seg < nseg)
+            for (int i = 0; i < nch; ++i)
+              tma_load_3d(stage + i * KV_CH_BYTES + seg * R * 128, &P.tmKV, &B->kv_full[s],
+                          dim_chunk(rank, i) * DCH, cur[seg], 0);
         issued = t + 1;
+#pragma unroll
+        for (int seg = 0; seg < 4; ++seg) cur[seg] = nxt[seg];
+        lookup(t + 2, nxt);
       }
       // every issued copy has landed before the CTA may exit
       mbar_wait(&B->q_full, 0, P.status);
       for (int t = max(0, issued - 2); t < issued; ++t)
         mbar_wait(&B->kv_full[t & 1], (t >> 1) & 1, P.status);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     if (lane == 0) {
       // ---- MMA issuer ----
       const uint32_t idesc_qk = idesc_f16(QROWS, KT, false);
@@ -388,21 +416,22 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
       };
       bool ok = have_q && (nt == 0 || issue_qk(0));
       for (int t = 0; t < nt && ok; ++t) {
-        // the next tile's scores overlap this tile's softmax
+        // the next tile's scores overlap this tile's exchange and softmax
         if (t + 1 < nt && !issue_qk(t + 1)) break;
         if (!wait_local(B, &B->p_full, t & 1, P.status)) break;
         tc_fence_after();
         const uint8_t* stage = smem + OFF_KV + (t & 1) * KV_STAGE_BYTES;
-        const uint64_t dp = smem_desc_sw128(smem + OFF_P);
         const uint64_t dv = smem_desc_sw128_mn(stage, KV_CH_BYTES);
 #pragma unroll
-        for (int k = 0; k < KT / 16; ++k)   // 16 keys per MMA: 32 B along P rows, 16 V rows
-          mma_f16(tmem + TM_O, dp + 2 * k, dv + (uint64_t)(16 * 128 / 16) * k, idesc_pv,
-                  (t | k) != 0);
-        mma_commit(&B->o_done);
+        for (int k = 0; k < KT / 16; ++k)   // 16 keys per MMA: 8 P columns, 16 V rows
+          mma_f16_ts(tmem + TM_O, tmem + TM_P + 32 * (t & 1) + 8 * k,
+                     dv + (uint64_t)(16 * 128 / 16) * k, idesc_pv, (t | k) != 0);
+        mma_commit(&B->o_done[t & 1]);
         mma_commit(&B->kv_empty[t & 1]);
       }
     }
+  } else if (warp >= 4) {
+    exchange_scores(P, B, smem, tmem, peer, nt);
   } else {
     softmax_and_store(P, B, smem, tmem, rank, peer, b, qt, row0, kvl, W, j_lo, nt);
   }
@@ -410,7 +439,7 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();          // no CTA leaves while its peer may still signal it
-  if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
+  if (warp == 9) tmem_dealloc(tmem, TMEM_COLS);
 }
 
 }  // namespace
@@ -466,11 +495,6 @@ mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_b
   P.o_part = part;
   P.lse_part = part + (size_t)splits * rows * 512;
   if (splits > 1 && d.vis_stats) init_vis_stats(st, d.vis_stats, tokens);
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaFuncSetAttribute(latent_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         SMEM_BYTES);
-  });
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * d.num_blocks * P.tiles_per_block, splits, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
@@ -489,11 +513,43 @@ mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_b
   return MLA_OK;
 }
 
-// Enough splits that the (block, 128-row) units fill every SM once, at most 8.
+// Clusters of the attention kernel resident on the GPU at once (queried once;
+// also sets the kernel's shared-memory limit, so it runs before any launch).
+static int attn_clusters_per_wave(const mla_handle* h) {
+  static std::once_flag once;
+  static int clusters = 0;
+  std::call_once(once, [h] {
+    cudaFuncSetAttribute(latent_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         SMEM_BYTES);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, latent_attn_tc_kernel, &cfg) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      n = h->num_sms / 2;
+    }
+    clusters = n;
+  });
+  return clusters;
+}
+
+// When the (block, 128-row) units leave part of the GPU idle, split each
+// unit's key range so that the clusters fill one wave (at most 8 parts); a
+// split that would add a partial wave only lengthens the kernel.
 int attn_splits(const mla_handle* h, long tokens) {
   const long units = tokens * h->lay.H / QROWS;
-  if (units <= 0) return 1;
-  const long s = (h->num_sms + 2 * units - 1) / (2 * units);
+  const long wave = attn_clusters_per_wave(h);
+  if (units <= 0 || units >= wave) return 1;
+  const long s = wave / units;
   return (int)(s < 1 ? 1 : s > 8 ? 8 : s);
 }
 

@@ -261,3 +261,30 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
 
 }  // namespace tc
 }  // namespace mla
+
+// ---- asynchronous DSMEM stores, MMA with A in tensor memory -------------------
+namespace mla {
+namespace tc {
+
+// 16-byte store into a peer CTA's shared memory whose completion is counted
+// (16 transaction bytes) on the peer's barrier `remote_bar`: the receiver
+// waits on that barrier with an expected byte count, no release fence needed.
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float a, float b, float c, float d,
+                                            uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+      ::"r"(remote_addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar) : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]: A (M x K, 16-bit, two K elements per 32-bit
+// column, row i in lane i) read from tensor memory.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+}  // namespace tc
+}  // namespace mla
