@@ -157,9 +157,7 @@ __device__ __forceinline__ void softmax_and_store(const AttnParams& P, Bars* B, 
     }
     tc_fence_before();
     mbar_arrive(&B->s_free[buf]);
-    __syncwarp();
-    if (lane == 0) mbar_arrive_remote(peer_empty[buf]);   // this warp's rows are read
-    // mask by logical position, scale into the exp2 domain
+    // mask by logical position (a warp whose rows all see the whole tile skips it)
     const int lo = max(vlo - j0, 0), hi = min(vhi - j0, KT);   // visible columns [lo, hi)
     if (hi > lo) {
       cnt += hi - lo;
@@ -167,19 +165,25 @@ __device__ __forceinline__ void softmax_and_store(const AttnParams& P, Bars* B, 
       last = j0 + hi - 1;
     }
     float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    if (__all_sync(0xffffffffu, lo == 0 && hi == KT)) {
 #pragma unroll
-    for (int i = 0; i < KT; ++i) {
-      s[i] = (i >= lo && i < hi) ? s[i] * P.scale_log2 : -INFINITY;
-      mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
+      for (int i = 0; i < KT; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < KT; ++i) {
+        s[i] = (i >= lo && i < hi) ? s[i] : -INFINITY;
+        mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
+      }
     }
-    const float tmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+    // into the exp2 domain: the scale is positive, so it commutes with the max
+    const float tmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * P.scale_log2;
     const bool grow = tmax > mrun + RESCALE_LOG2;
     const float m_new = grow ? tmax : mrun;
     const float mref = m_new == -INFINITY ? 0.f : m_new;      // all masked so far: P = 0
     float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < KT; ++i) {
-      s[i] = fast_exp2(s[i] - mref);
+      s[i] = fast_exp2(fmaf(s[i], P.scale_log2, -mref));
       ps4[i & 3] += s[i];
     }
     const float psum = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
@@ -225,6 +229,10 @@ __device__ __forceinline__ void softmax_and_store(const AttnParams& P, Bars* B, 
     tmem_st32(tmem + TM_P + 32 * buf + lane_base, pw);
     tc_fence_before();
     mbar_arrive(&B->p_full);
+    // this warp's reads of the exchange buffer are complete: the peer may
+    // overwrite it (release orders those reads before the arrival)
+    __syncwarp();
+    if (lane == 0) mbar_arrive_remote(peer_empty[buf]);
   }
   // epilogue: O_r / l -> fp16 latent output columns [256 rank, 256 rank + 256)
   if (nt > 0) wait_local(B, &B->o_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, P.status);
