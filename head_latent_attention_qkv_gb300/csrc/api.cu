@@ -411,18 +411,24 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
   float* a_out = (float*)(ws + w.a_out);
   const TX* x = (const TX*)hidden;
   const TX* WA = (const TX*)h->WA;
-  // A projection; the block's own latents only when it writes them (bf16: the
-  // fused append kernel, fp32: the projection rows then the finish kernel)
+  // A projection; the block's own latents only when it writes them.  Enough
+  // tokens to fill the GPU with the fused append kernel (3 CTAs per 128 rows):
+  // that kernel; fewer tokens (or fp32): the latent rows join the projection
+  // (split-K spreads it over the SMs) and the finish kernel normalises,
+  // rotates and stores them.
   constexpr bool kBf16 = std::is_same<TX, __nv_bfloat16>::value;
   const long num_slots = (long)num_pages * h->cfg.page_size;
-  const int r0 = (bslots && !kBf16) ? 0 : l.L;
+  const bool fused_kv = kBf16 && bslots && 3L * ((M + 127) / 128) >= h->num_sms;
+  const int r0 = (bslots && !fused_kv) ? 0 : l.L;
   mla_status_t s = proj<TX, float>(h, st, M, l.NA - r0, l.D, 1, x, l.D, 0,
                                    WA + (long)r0 * l.D, l.D, 0, a_out + r0, l.NA, 0);
   if (s != MLA_OK) return s;
   if (bslots) {
-    if constexpr (kBf16) {
-      s = tc::kv_append(st, h, x, M, pos, bslots, (TX*)cache, num_slots);
-      if (s != MLA_OK) return s;
+    if (fused_kv) {
+      if constexpr (kBf16) {
+        s = tc::kv_append(st, h, x, M, pos, bslots, (TX*)cache, num_slots);
+        if (s != MLA_OK) return s;
+      }
     } else {
       simt::kv_finish<TX>(st, h, a_out, l.NA, M, pos, bslots, (TX*)cache, num_slots);
     }

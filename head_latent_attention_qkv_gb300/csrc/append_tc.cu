@@ -22,7 +22,7 @@ namespace mla {
 namespace tc {
 namespace {
 
-constexpr int BM = 128, BN = 192, BK = 64, THREADS = 128, STAGES = 4, CL = 3;
+constexpr int BM = 128, BN = 192, BK = 64, THREADS = 128, STAGES = 5, CL = 3;
 constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int OFF_BAR = STAGES * STAGE_BYTES;
 constexpr int SMEM_BYTES = 1024 + OFF_BAR + 1024;
@@ -77,6 +77,15 @@ __global__ void __launch_bounds__(THREADS, 1) kv_append_tc_kernel(const __grid_c
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
+    // hidden rows (CTA 0, which multicasts them) and weight rows are pulled
+    // into L2 2*STAGES k-blocks ahead of their load
+    auto prefetch = [&](int kb) {
+      if (kb < nk) {
+        if (rank == 0) tma_prefetch_3d(&P.tmA, kb * BK, m0, 0);
+        tma_prefetch_3d(&P.tmB, kb * BK, n0, 0);
+      }
+    };
+    for (int kb = STAGES; kb < 2 * STAGES; ++kb) prefetch(kb);
     bool ok = true;
     for (int kb = 0; kb < nk && ok; ++kb) {
       const int s = kb % STAGES;
@@ -86,6 +95,7 @@ __global__ void __launch_bounds__(THREADS, 1) kv_append_tc_kernel(const __grid_c
       mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
       if (rank == 0) tma_load_3d_mc(a, &P.tmA, &full[s], kb * BK, m0, 0, (1u << CL) - 1);
       tma_load_3d(a + A_BYTES, &P.tmB, &full[s], kb * BK, n0, 0);
+      prefetch(kb + 2 * STAGES);
     }
     for (int kb = max(0, nk - STAGES); kb < nk; ++kb)
       mbar_wait(&full[kb % STAGES], (kb / STAGES) & 1, P.status);

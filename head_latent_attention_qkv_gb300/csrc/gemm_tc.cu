@@ -98,7 +98,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    // producer: TMA ring
+    // producer: TMA ring; tiles are pulled into L2 2*STAGES k-blocks ahead
+    auto prefetch = [&](int kb) {
+      if (kb < nk) {
+        tma_prefetch_3d(&tmA, (kb0 + kb) * BK, m0, z);
+        tma_prefetch_3d(&tmB, (kb0 + kb) * BK, n0, z);
+      }
+    };
+    for (int kb = STAGES; kb < 2 * STAGES; ++kb) prefetch(kb);
     bool ok = true;
     for (int kb = 0; kb < nk && ok; ++kb) {
       const int s = kb % STAGES;
@@ -110,6 +117,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       mbar_arrive_expect_tx(&full[s], S::STAGE_BYTES);
       tma_load_3d(a, &tmA, &full[s], (kb0 + kb) * BK, m0, z);
       tma_load_3d(b, &tmB, &full[s], (kb0 + kb) * BK, n0, z);
+      prefetch(kb + 2 * STAGES);
     }
     // drain: the last loads of every slot have landed before the CTA can exit
     for (int kb = max(0, nk - STAGES); kb < nk; ++kb)

@@ -80,34 +80,36 @@ rmsnorm_rows_kernel(const float* __restrict__ in, long ld, int n, const float* _
   for (int i = threadIdx.x; i < n; i += ROW_THREADS) o[i] = from_f32<T>(row[i] * rstd * gamma[i]);
 }
 
+// One warp per (token, head): lanes copy q_nope and rotate the rope pairs
+// (consecutive lanes touch consecutive elements).
 template <typename TN, typename TQ>
 __global__ void __launch_bounds__(ROW_THREADS)
 q_rope_split_kernel(const float* __restrict__ q, long ldq, const int32_t* __restrict__ positions,
-                    int H, int dn, int dr, int rkv, const float2* __restrict__ rope, int max_pos,
-                    int interleaved, uint32_t* status, TN* __restrict__ q_nope,
+                    int M, int H, int dn, int dr, int rkv, const float2* __restrict__ rope,
+                    int max_pos, int interleaved, uint32_t* status, TN* __restrict__ q_nope,
                     TQ* __restrict__ q_abs) {
-  const int m = blockIdx.x;
-  const float* row = q + (long)m * ldq;
+  const long w = (blockIdx.x * (long)ROW_THREADS + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  if (w >= (long)M * H) return;
+  const int m = (int)(w / H), h = (int)(w % H);
   const int dqk = dn + dr, L = rkv + dr, half = dr / 2;
-  for (int i = threadIdx.x; i < H * dn; i += ROW_THREADS) {
-    const int h = i / dn, d = i % dn;
-    q_nope[(long)m * H * dn + i] = from_f32<TN>(row[h * dqk + d]);
-  }
+  const float* src = q + (long)m * ldq + (long)h * dqk;
+  TN* nope = q_nope + w * dn;
+  for (int d = lane; d < dn; d += 32) nope[d] = from_f32<TN>(src[d]);
   const int p = positions[m];
   const bool bad = p < 0 || p >= max_pos;
-  if (bad && threadIdx.x == 0) set_status(status, MLA_DEV_BAD_POSITION);
-  for (int i = threadIdx.x; i < H * half; i += ROW_THREADS) {
-    const int h = i / half, k = i % half;
+  if (bad && h == 0 && lane == 0) set_status(status, MLA_DEV_BAD_POSITION);
+  TQ* dst = q_abs + w * L + rkv;
+  for (int k = lane; k < half; k += 32) {
     int ia, ib;
     rope_pair(k, dr, interleaved, &ia, &ib);
-    TQ* dst = q_abs + ((long)m * H + h) * L + rkv;
     if (bad) {
       dst[ia] = from_f32<TQ>(0.f);
       dst[ib] = from_f32<TQ>(0.f);
       continue;
     }
     const float2 cs = rope[(long)p * half + k];
-    const float a = row[h * dqk + dn + ia], b = row[h * dqk + dn + ib];
+    const float a = src[dn + ia], b = src[dn + ib];
     dst[ia] = from_f32<TQ>(a * cs.x - b * cs.y);
     dst[ib] = from_f32<TQ>(b * cs.x + a * cs.y);
   }
@@ -159,8 +161,9 @@ void q_rope_split(cudaStream_t st, const mla_handle* h, const float* q, long ldq
                   const int32_t* positions, TN* q_nope, TQ* q_abs) {
   if (M <= 0) return;
   const Layout& l = h->lay;
-  q_rope_split_kernel<TN, TQ><<<M, ROW_THREADS, 0, st>>>(
-      q, ldq, positions, l.H, l.dn, l.dr, l.rkv, h->rope, h->cfg.max_position,
+  const long warps = (long)M * l.H, per_block = ROW_THREADS / 32;
+  q_rope_split_kernel<TN, TQ><<<(unsigned)((warps + per_block - 1) / per_block), ROW_THREADS, 0, st>>>(
+      q, ldq, positions, M, l.H, l.dn, l.dr, l.rkv, h->rope, h->cfg.max_position,
       h->cfg.rope == MLA_ROPE_INTERLEAVED, h->status, q_nope, q_abs);
 }
 
