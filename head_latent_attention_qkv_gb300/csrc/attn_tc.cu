@@ -4,29 +4,38 @@
 // 512-wide latent value space).
 //
 // Work unit: one query block and 128 consecutive rows of Q_abs (rows are
-// (token, head) pairs, token-major), handled by a cluster of two CTAs.  The
-// 128 x 512 fp32 output accumulator does not fit one SM's tensor memory next
-// to the score tiles, so CTA r keeps value columns [256r, 256r+256) in TMEM.
-// The score reduction over the 576 latent dims is split between the pair:
-// CTA 0 owns dims 0..255 and the rope dims 512..575, CTA 1 owns dims
-// 256..511, which are also exactly the value dims each needs, so every cache
-// byte is loaded once per pair.  Per 64-key tile t:
-//   MMA warp      : S_r(t) = Q_r K_r(t)^T over its own dims into score buffer
-//                   t % 2 (issued while the softmax still works on tile t-1)
-//   exchange warps: as soon as S_r(t) lands, send it to the peer with
-//                   asynchronous DSMEM stores that count their bytes on the
-//                   peer's barrier (double-buffered, so the send overlaps the
-//                   softmax of the previous tile)
-//   softmax warps : add own and peer partial (same order in both CTAs, so
-//                   both see identical scores), mask by logical position,
-//                   online softmax in fp32 (exp2 domain; the TMEM accumulator
-//                   is rescaled only when the running max grows by more than
-//                   2^8), write P (bf16) into tensor memory, buffer t % 2
-//   MMA warp      : O_r += P(t) V_r(t), P read from tensor memory, V read
-//                   MN-major straight from the staged KV tile
-// Warps 0-3 run the softmax and the epilogue (thread = accumulator row = TMEM
-// lane), warps 4-7 the score exchange (same lanes), warp 8 streams Q and KV
-// tiles with TMA, warp 9 owns TMEM and issues the MMAs.
+// (token, head) pairs, token-major), handled by a cluster of two CTAs, one per
+// half of the 512 latent value dims.  A 128 x 512 fp32 accumulator would fill
+// all of an SM's tensor memory, so each CTA keeps O for its 256 value dims and
+// computes the full 576-wide scores itself (QK^T is repeated by the two
+// halves; nothing is exchanged but the cache tiles both read).  Keys go in
+// tiles of 128 (one MMA costs about the same for any N up to 128, so narrower
+// score tiles waste the tensor pipe).
+//
+// Tensor memory (512 columns): O at 0..255, S (fp32, 128 keys) at 256..383,
+// P (bf16 pairs) at 384..447, Q_abs dims 0..127 (bf16 pairs, the A operand of
+// the first two score chunks) at 448..511.
+// Shared memory: Q_abs dims 128..575 (seven 64-dim chunks, one TMA copy), a
+// V buffer (this CTA's four value chunks of one tile, MN-major operand of
+// P V, one TMA copy) and a 3-slot ring of 64-dim key chunks (nine per tile).
+// A TMA copy costs about the same SM time whatever its size, so copies are as
+// large as the layout allows: the two CTAs of a cluster take turns loading
+// the key chunks and multicast each one to both, and a tile whose 128 cache
+// rows are contiguous (adjacent pages) comes in one copy per chunk.
+//
+// Tensor-pipe order: S(0), S(1), PV(0), S(2), PV(1), ...  The softmax reads
+// S(t) into registers and releases it at once, so S(t+1) runs while the
+// softmax works on tile t; V(t) is loaded while S(t+1) runs.
+//   MMA warp     : S(t) = Q K(t)^T (36 MMAs, N = 128); O += P(t) V(t) (8 MMAs,
+//                  N = 256, P read from tensor memory)
+//   softmax warps: thread r owns row r (TMEM lane r): mask by logical
+//                  position (one visible interval per row), online softmax in
+//                  fp32 in the exp2 domain (O rescaled in tensor memory only
+//                  when the running max grows by more than 2^8), P -> bf16
+//   TMA warp     : page rows of the key range (once), Q, key chunks, values
+// The key range of a unit may be split across clusters (grid y) when units
+// alone do not fill the GPU; splits write normalised partial outputs and
+// their log2-sum-exp, merged by merge_splits().
 #include "attn_tc.cuh"
 
 #include <mutex>
@@ -37,42 +46,48 @@ namespace mla {
 namespace tc {
 namespace {
 
-constexpr int QROWS = 128, KT = 64, DCH = 64;    // query rows, keys per tile, dims per chunk
-constexpr int THREADS = 320;
-constexpr int MAX_CH = 5;                         // dim chunks held by CTA 0 (4 latent + rope)
-constexpr int Q_CH_BYTES = QROWS * DCH * 2;       // 16 KiB
-constexpr int KV_CH_BYTES = KT * DCH * 2;         // 8 KiB
-constexpr int KV_STAGE_BYTES = MAX_CH * KV_CH_BYTES;
-constexpr int X_BYTES = QROWS * KT * 4;           // one tile of peer partial scores
+constexpr int QROWS = 128, KT = 128, DCH = 64, NCH = 9;  // rows, keys per tile, dims per chunk
+constexpr int NQT = 2;                                    // Q chunks held in tensor memory
+constexpr int NQS = NCH - NQT;                            // Q chunks held in shared memory
+constexpr int KSLOTS = 3;                                 // key-chunk ring
+constexpr int THREADS = 192;                              // softmax x4, TMA, MMA
+constexpr int Q_CH_BYTES = QROWS * DCH * 2;               // 16 KiB
+constexpr int KV_CH_BYTES = KT * DCH * 2;                 // 16 KiB
 constexpr int OFF_Q = 0;
-constexpr int OFF_KV = OFF_Q + MAX_CH * Q_CH_BYTES;
-constexpr int OFF_X = OFF_KV + 2 * KV_STAGE_BYTES;
-constexpr int OFF_BAR = OFF_X + 2 * X_BYTES;
-constexpr int SMEM_BYTES = 1024 + OFF_BAR + 256;
-// TMEM columns: O at 0..255, scores at 256 + 64 b, P (bf16 pairs) at 384 + 32 b
-constexpr uint32_t TMEM_COLS = 512, TM_O = 0, TM_S = 256, TM_P = 384;
-constexpr float RESCALE_LOG2 = 8.f;               // lazy rescale threshold (factor 256)
+constexpr int OFF_V = OFF_Q + NQS * Q_CH_BYTES;
+constexpr int OFF_K = OFF_V + 4 * KV_CH_BYTES;
+constexpr int OFF_BAR = OFF_K + KSLOTS * KV_CH_BYTES;
+constexpr int OFF_PG = OFF_BAR + 256;                     // cache row of each page of the key range
+constexpr int MAX_PG = 176;                               // pages held there (else looked up per load)
+constexpr int SMEM_BYTES = 1024 + OFF_PG + MAX_PG * 4;
+constexpr uint32_t TMEM_COLS = 512, TM_O = 0, TM_S = 256, TM_P = 384, TM_Q = 448;
+constexpr float RESCALE_LOG2 = 8.f;                       // lazy rescale threshold (factor 256)
 
 struct Bars {
-  uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, o_done[2];
-  uint64_t x_full[2];    // peer's partial scores landed (expect-tx, 1 local arrival)
-  uint64_t x_empty[2];   // peer has read the partial scores sent to it (4 warp arrivals)
+  uint64_t q_full;                    // Q chunks in shared memory (TMA)
+  uint64_t q_tmem;                    // Q chunks in tensor memory (128 arrivals)
+  uint64_t k_full[KSLOTS];            // key chunk landed (own arm + multicast bytes)
+  uint64_t k_empty[KSLOTS];           // both CTAs' MMAs done with the slot (2 commits)
+  uint64_t v_full;                    // V(t) landed (phase t)
+  uint64_t s_full, s_free;            // S(t) written / read into registers (phase t)
+  uint64_t p_full;                    // P(t) written (phase t)
+  uint64_t o_done;                    // P(t) V(t) complete (phase t)
+  uint64_t drain;                     // every MMA of the CTA complete
   uint32_t tmem_slot;
   int abort;
 };
+static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(SMEM_BYTES <= 232448, "shared memory");
 
-__device__ __forceinline__ int dim_chunk(int rank, int i) {
-  return rank == 0 ? (i < 4 ? i : 8) : 4 + i;    // global 64-dim chunk of local chunk i
-}
-
-// Bounded waits that give up at once after any earlier timeout of this CTA.
-__device__ __forceinline__ bool wait_local(Bars* B, uint64_t* bar, uint32_t parity, uint32_t* st) {
+// Bounded wait that gives up at once after any earlier timeout of this CTA.
+__device__ __forceinline__ bool wait_bar(Bars* B, uint64_t* bar, uint32_t parity, uint32_t* st) {
   if (*(volatile int*)&B->abort) return false;
   if (mbar_wait(bar, parity, st)) return true;
   B->abort = 1;
   return false;
 }
-__device__ __forceinline__ bool wait_peer(Bars* B, uint64_t* bar, uint32_t parity, uint32_t* st) {
+// The same on a barrier that the peer CTA also signals (acquire at cluster scope).
+__device__ __forceinline__ bool wait_bar_cl(Bars* B, uint64_t* bar, uint32_t parity, uint32_t* st) {
   if (*(volatile int*)&B->abort) return false;
   if (mbar_wait_cluster(bar, parity, st)) return true;
   B->abort = 1;
@@ -87,40 +102,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// Warps 4-7: forward this CTA's partial scores of every tile to the peer.
-__device__ __forceinline__ void exchange_scores(const AttnParams& P, Bars* B, uint8_t* smem,
-                                                uint32_t tmem, uint32_t peer, int nt) {
-  const int r = threadIdx.x - QROWS;                  // row / TMEM lane
-  const uint32_t lane_base = (uint32_t)((r / 32) * 32) << 16;
-  const uint32_t peer_x = mapa(smem_u32((float*)(smem + OFF_X) + r * KT), peer);
-  const uint32_t peer_full[2] = {mapa(smem_u32(&B->x_full[0]), peer), mapa(smem_u32(&B->x_full[1]), peer)};
-  for (int t = 0; t < nt; ++t) {
-    const int buf = t & 1;
-    const uint32_t ph = (t >> 1) & 1;
-    if (!wait_local(B, &B->s_full[buf], ph, P.status)) break;
-    tc_fence_after();
-    float s[KT];
-    tmem_ld32(tmem + TM_S + 64 * buf + lane_base, s);
-    tmem_ld32(tmem + TM_S + 64 * buf + lane_base + 32, s + 32);
-    tc_fence_before();
-    mbar_arrive(&B->s_free[buf]);
-    // the peer has read what was sent into this buffer two tiles ago
-    if (!wait_peer(B, &B->x_empty[buf], ph ^ 1, P.status)) break;
-    // 16-byte chunk c of a row sits at chunk c ^ (row % 8): the eight rows a
-    // quarter-warp touches at once fall in distinct banks
-#pragma unroll
-    for (int c = 0; c < KT / 4; ++c)
-      st_async_v4(peer_x + buf * X_BYTES + 16 * (c ^ (r & 7)), s[4 * c], s[4 * c + 1], s[4 * c + 2],
-                  s[4 * c + 3], peer_full[buf]);
-  }
-}
-
-// Warps 0-3: thread r owns accumulator row r (TMEM lane r) of the tile.
+// Warps 0-3: thread r owns accumulator row r (TMEM lane r) of the unit.
 __device__ __forceinline__ void softmax_and_store(const AttnParams& P, Bars* B, uint8_t* smem,
-                                                  uint32_t tmem, uint32_t rank, uint32_t peer,
-                                                  int b, int qt, long row0, int kvl, int W,
-                                                  int j_lo, int nt) {
-  const int r = threadIdx.x, lane = r % 32;
+                                                  uint32_t tmem, int half, int b, int qt,
+                                                  long row0, int kvl, int W, int j_lo, int nt) {
+  const int r = threadIdx.x;
   const uint32_t lane_base = (uint32_t)((r / 32) * 32) << 16;
   const int row_in_block = qt * QROWS + r;
   const int tok = row_in_block / P.H, head = row_in_block % P.H;
@@ -131,32 +117,34 @@ __device__ __forceinline__ void softmax_and_store(const AttnParams& P, Bars* B, 
   // a sliding window, p - j < W; a fully masked query sees none
   const int vlo = W > 0 ? max(0, p - W + 1) : 0;
   const int vhi = qv ? kvl : 0;
-  const float* xrow = (const float*)(smem + OFF_X) + r * KT;
-  const uint32_t peer_empty[2] = {mapa(smem_u32(&B->x_empty[0]), peer), mapa(smem_u32(&B->x_empty[1]), peer)};
   float mrun = -INFINITY, lsum = 0.f;
   int cnt = 0, first = -1, last = -1;
-  for (int t = 0; t < nt; ++t) {
-    const int buf = t & 1;
-    const uint32_t ph = (t >> 1) & 1;
-    const int j0 = j_lo + t * KT;
-    float s[KT];
-    wait_local(B, &B->s_full[buf], ph, P.status);
-    tc_fence_after();
-    tmem_ld32(tmem + TM_S + 64 * buf + lane_base, s);
-    tmem_ld32(tmem + TM_S + 64 * buf + lane_base + 32, s + 32);
-    wait_peer(B, &B->x_full[buf], ph, P.status);
-    // arm this buffer for tile t + 2 before the peer can be told it is free
-    if (r == 0 && t + 2 < nt) mbar_arrive_expect_tx(&B->x_full[buf], X_BYTES);
-    const float* x = xrow + buf * (X_BYTES / 4);
+  if (nt > 0) {
+    // Q_abs dims 0..127 of this row -> tensor memory (bf16 pairs, low half = even dim)
+    const uint4* src = reinterpret_cast<const uint4*>(P.q_abs + (row0 + r) * 576);
+#pragma unroll 1
+    for (int c = 0; c < NQT; ++c) {
+      uint32_t w[32];
 #pragma unroll
-    for (int c = 0; c < KT / 4; ++c) {
-      const float4 v = *reinterpret_cast<const float4*>(x + 4 * (c ^ (r & 7)));
-      const float xs[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int u = 0; u < 4; ++u) s[4 * c + u] = rank == 0 ? s[4 * c + u] + xs[u] : xs[u] + s[4 * c + u];
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = __ldg(src + c * 8 + i);
+        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+      }
+      tmem_st32_u(tmem + TM_Q + 32 * c + lane_base, w);
     }
     tc_fence_before();
-    mbar_arrive(&B->s_free[buf]);
+    mbar_arrive(&B->q_tmem);
+  }
+  for (int t = 0; t < nt; ++t) {
+    const uint32_t ph = t & 1;
+    const int j0 = j_lo + t * KT;
+    float s[KT];
+    wait_bar(B, &B->s_full, ph, P.status);
+    tc_fence_after();
+#pragma unroll
+    for (int c = 0; c < KT; c += 32) tmem_ld32(tmem + TM_S + c + lane_base, s + c);
+    tc_fence_before();
+    mbar_arrive(&B->s_free);
     // mask by logical position (a warp whose rows all see the whole tile skips it)
     const int lo = max(vlo - j0, 0), hi = min(vhi - j0, KT);   // visible columns [lo, hi)
     if (hi > lo) {
@@ -188,59 +176,56 @@ __device__ __forceinline__ void softmax_and_store(const AttnParams& P, Bars* B, 
     }
     const float psum = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
     const float alpha = (grow && mrun != -INFINITY) ? exp2f(mrun - m_new) : 1.f;
-    if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-      // every earlier P.V has finished before O is rescaled
-      wait_local(B, &B->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, P.status);
+    // P(t-1) V(t-1) has finished: P may be overwritten and O rescaled
+    if (t > 0) {
+      wait_bar(B, &B->o_done, ph ^ 1, P.status);
       tc_fence_after();
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-      for (int c = 0; c < 256; c += 32) {
-        float o[32];
-        tmem_ld32(tmem + TM_O + lane_base + c, o);
+        for (int c = 0; c < 256; c += 32) {
+          float o[32];
+          tmem_ld32(tmem + TM_O + lane_base + c, o);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-        tmem_st32(tmem + TM_O + lane_base + c, o);
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(tmem + TM_O + lane_base + c, o);
+        }
       }
     }
     lsum = lsum * alpha + psum;
     mrun = m_new;
-    // P buffer `buf` was last read by P.V of tile t - 2
-    if (t >= 2) {
-      wait_local(B, &B->o_done[buf], ph ^ 1, P.status);
-      tc_fence_after();
-    }
-    // value rows of keys past kv_len may hold anything: zero them (last tile)
-    const bool tail = j0 + KT > kvl;
-    if (tail) {
-      uint8_t* stage = smem + OFF_KV + buf * KV_STAGE_BYTES;
+    // value rows of keys past kv_len may hold anything: once V(t) has landed,
+    // zero those rows (last tile only)
+    if (j0 + KT > kvl) {
+      wait_bar(B, &B->v_full, ph, P.status);
+      uint8_t* vbase = smem + OFF_V;
       const int z0 = max(0, kvl - j0), pieces = (KT - z0) * 4 * 8;
       for (int idx = r; idx < pieces; idx += QROWS) {
         const int key = z0 + idx / 32, ch = (idx % 32) / 8, q = idx % 8;
-        *reinterpret_cast<uint4*>(stage + ch * KV_CH_BYTES + key * 128 + q * 16) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(vbase + ch * KV_CH_BYTES + key * 128 + q * 16) = make_uint4(0, 0, 0, 0);
       }
       fence_proxy_async_smem();
     }
     // P row in bf16 pairs: key 2c in the low half of column c
-    float pw[KT / 2];
 #pragma unroll
-    for (int c = 0; c < KT / 2; ++c) {
-      __nv_bfloat162 h2 = __floats2bfloat162_rn(s[2 * c], s[2 * c + 1]);
-      pw[c] = *reinterpret_cast<float*>(&h2);
+    for (int c = 0; c < KT / 2; c += 32) {
+      uint32_t pw[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(s[2 * (c + i)], s[2 * (c + i) + 1]);
+        pw[i] = *reinterpret_cast<uint32_t*>(&h2);
+      }
+      tmem_st32_u(tmem + TM_P + c + lane_base, pw);
     }
-    tmem_st32(tmem + TM_P + 32 * buf + lane_base, pw);
     tc_fence_before();
     mbar_arrive(&B->p_full);
-    // this warp's reads of the exchange buffer are complete: the peer may
-    // overwrite it (release orders those reads before the arrival)
-    __syncwarp();
-    if (lane == 0) mbar_arrive_remote(peer_empty[buf]);
   }
-  // epilogue: O_r / l -> fp16 latent output columns [256 rank, 256 rank + 256)
-  if (nt > 0) wait_local(B, &B->o_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, P.status);
+  // epilogue: O / l -> latent output columns [256 half, 256 half + 256)
+  if (nt > 0) wait_bar(B, &B->o_done, (nt - 1) & 1, P.status);
   tc_fence_after();
   const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
   const bool any = nt > 0 && lsum > 0.f;
   if (P.splits == 1) {
-    __half* dst = P.o_lat + (row0 + r) * 512 + rank * 256;
+    __half* dst = P.o_lat + (row0 + r) * 512 + half * 256;
 #pragma unroll 1
     for (int c = 0; c < 256; c += 32) {
       float o[32];
@@ -258,7 +243,7 @@ __device__ __forceinline__ void softmax_and_store(const AttnParams& P, Bars* B, 
   } else {
     // normalised partial output and its log2-sum-exp, merged by merge_splits()
     const long prow = (long)blockIdx.y * P.rows + row0 + r;
-    float* dst = P.o_part + prow * 512 + rank * 256;
+    float* dst = P.o_part + prow * 512 + half * 256;
 #pragma unroll 1
     for (int c = 0; c < 256; c += 32) {
       float o[32];
@@ -269,9 +254,9 @@ __device__ __forceinline__ void softmax_and_store(const AttnParams& P, Bars* B, 
             any ? make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv)
                 : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (rank == 0) P.lse_part[prow] = any ? mrun + log2f(lsum) : -INFINITY;
+    if (half == 0) P.lse_part[prow] = any ? mrun + log2f(lsum) : -INFINITY;
   }
-  if (P.vis_stats && rank == 0 && head == 0) {
+  if (P.vis_stats && half == 0 && head == 0) {
     if (P.splits == 1) {
       P.vis_stats[m * 3 + 0] = cnt;
       P.vis_stats[m * 3 + 1] = cnt ? first : -1;
@@ -289,17 +274,16 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   Bars* B = (Bars*)(smem + OFF_BAR);
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
-  const int nch = rank == 0 ? 5 : 4;
-  const int unit = blockIdx.x / 2;
+  const int half = (int)cluster_ctarank();             // == blockIdx.x & 1
+  const int unit = blockIdx.x >> 1;
   const int b = unit / P.tiles_per_block, qt = unit % P.tiles_per_block;
-  const long row0 = ((long)b * P.tiles_per_block + qt) * QROWS;   // first Q_abs row of the tile
+  const long row0 = ((long)b * P.tiles_per_block + qt) * QROWS;   // first Q_abs row of the unit
 
-  // key range of this tile: [j_lo, kvl) in 64-key tiles (identical in both CTAs)
+  // key range of this unit: [j_lo, kvl) in 128-key tiles (identical in both halves)
   int kvl = P.kv_len[b];
   const int cap = P.max_pages * P.page_size;
   if (kvl < 0 || kvl > cap) {
-    if (tid == 0 && rank == 0) set_status(P.status, MLA_DEV_BAD_LENGTH);
+    if (tid == 0 && half == 0) set_status(P.status, MLA_DEV_BAD_LENGTH);
     kvl = max(0, min(kvl, cap));
   }
   const int W = P.window ? P.window[b] : 0;
@@ -320,134 +304,184 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
 
   if (tid == 0) {
     mbar_init(&B->q_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&B->kv_full[s], 1);
-      mbar_init(&B->kv_empty[s], 1);
-      mbar_init(&B->s_full[s], 1);
-      mbar_init(&B->s_free[s], 2 * QROWS);    // softmax and exchange threads
-      mbar_init(&B->o_done[s], 1);
-      mbar_init(&B->x_full[s], 1);
-      mbar_init(&B->x_empty[s], QROWS / 32);  // one arrival per peer softmax warp
+    mbar_init(&B->q_tmem, QROWS);
+    for (int s = 0; s < KSLOTS; ++s) {
+      mbar_init(&B->k_full[s], 1);
+      mbar_init(&B->k_empty[s], 2);
     }
+    mbar_init(&B->v_full, 1);
+    mbar_init(&B->s_full, 1);
+    mbar_init(&B->s_free, QROWS);
     mbar_init(&B->p_full, QROWS);
+    mbar_init(&B->o_done, 1);
+    mbar_init(&B->drain, 1);
     B->abort = 0;
     fence_mbar_init();
-    // the first two score tiles from the peer are expected before it can send
-    for (int s = 0; s < 2 && s < nt; ++s) mbar_arrive_expect_tx(&B->x_full[s], X_BYTES);
   }
-  if (warp == 9) tmem_alloc(&B->tmem_slot, TMEM_COLS);
+  if (warp == 5) tmem_alloc(&B->tmem_slot, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();          // the peer's barriers exist before anyone signals them
+  cluster_sync_all();          // the peer's barriers exist before anyone multicasts to them
   tc_fence_after();
   const uint32_t tmem = B->tmem_slot;
 
-  if (warp == 8) {
-    if (lane == 0) {
+  if (warp == 4) {
+    // the cache row of every page this CTA reads, looked up once by the warp
+    // (past_end for a page the table marks invalid: TMA then reads zeros)
+    const int ps = P.page_size, past_end = P.num_pages * ps;
+    const int p0 = j_lo / ps;
+    const int npg = nt > 0 ? (min(kvl, j_lo + nt * KT) - 1) / ps - p0 + 1 : 0;
+    int* pg_row = (int*)(smem + OFF_PG);
+    const bool table = npg <= MAX_PG;
+    if (table) {
+      for (int i = lane; i < npg; i += 32) {
+        const int pg = P.block_table[(long)b * P.max_pages + p0 + i];
+        const bool okp = pg >= 0 && pg < P.num_pages;
+        if (!okp) set_status(P.status, MLA_DEV_BAD_PAGE);
+        pg_row[i] = okp ? pg * ps : past_end;
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && nt > 0) {
       // ---- TMA producer ----
       prefetch_tmap(&P.tmQ);
-      prefetch_tmap(&P.tmKV);
-      mbar_arrive_expect_tx(&B->q_full, nch * Q_CH_BYTES);
-      for (int i = 0; i < nch; ++i)
-        tma_load_3d(smem + OFF_Q + i * Q_CH_BYTES, &P.tmQ, &B->q_full, dim_chunk(rank, i) * DCH,
-                    (int)row0, 0);
-      const int R = P.seg_rows, nseg = KT / R, past_end = P.num_pages * P.page_size;
+      prefetch_tmap(&P.tmK);
+      prefetch_tmap(&P.tmKs);
+      prefetch_tmap(&P.tmV);
+      mbar_arrive_expect_tx(&B->q_full, NQS * Q_CH_BYTES);
+      tma_load_3d(smem + OFF_Q, &P.tmQ, &B->q_full, 0, (int)row0, NQT);
+      const int R = P.seg_rows, nseg = KT / R;
       // cache row of key j (beyond the cache when j is past kv_len or its page
       // is invalid: TMA then fills zeros)
       auto cache_row = [&](int j) {
         if (j >= kvl) return past_end;
-        const int pg = P.block_table[(long)b * P.max_pages + j / P.page_size];
-        if (pg >= 0 && pg < P.num_pages) return pg * P.page_size + j % P.page_size;
-        set_status(P.status, MLA_DEV_BAD_PAGE);
-        return past_end;
-      };
-      // cache rows of tile t's segments (at most 4: page_size >= 16), looked
-      // up and pulled into L2 two tiles ahead of the tile's load
-      auto lookup = [&](int t, int* y) {
-#pragma unroll
-        for (int seg = 0; seg < 4; ++seg) {
-          y[seg] = past_end;
-          if (t < nt && seg < nseg) {
-            y[seg] = cache_row(j_lo + t * KT + seg * R);
-            if (y[seg] != past_end)
-              for (int i = 0; i < nch; ++i) tma_prefetch_3d(&P.tmKV, dim_chunk(rank, i) * DCH, y[seg], 0);
-          }
+        int base;
+        if (table) {
+          base = pg_row[j / ps - p0];
+        } else {
+          const int pg = P.block_table[(long)b * P.max_pages + j / ps];
+          base = pg >= 0 && pg < P.num_pages ? pg * ps : past_end;
+          if (base == past_end) set_status(P.status, MLA_DEV_BAD_PAGE);
         }
+        return base == past_end ? past_end : base + j % ps;
       };
-      int cur[4], nxt[4];
-      lookup(0, cur);
-      lookup(1, nxt);
-      int issued = 0;
-      for (int t = 0; t < nt; ++t) {
-        const int s = t & 1;
-        if (!wait_local(B, &B->kv_empty[s], ((t >> 1) & 1) ^ 1, P.status)) break;
-        uint8_t* stage = smem + OFF_KV + s * KV_STAGE_BYTES;
-        mbar_arrive_expect_tx(&B->kv_full[s], nch * KV_CH_BYTES);
-#pragma unroll
-        for (int seg = 0; seg < 4; ++seg)
-          if (seg < nseg)
-            for (int i = 0; i < nch; ++i)
-              tma_load_3d(stage + i * KV_CH_BYTES + seg * R * 128, &P.tmKV, &B->kv_full[s],
-                          dim_chunk(rank, i) * DCH, cur[seg], 0);
-        issued = t + 1;
-#pragma unroll
-        for (int seg = 0; seg < 4; ++seg) cur[seg] = nxt[seg];
-        lookup(t + 2, nxt);
+      // rows of tile t: one run of KT contiguous cache rows (first row
+      // returned) or -1 when its segments must be copied one by one; rows past
+      // kv_len inside the run are read but masked (scores) and zeroed (values)
+      auto tile_run = [&](int t) {
+        const int j0 = j_lo + t * KT;
+        const int y0 = cache_row(j0);
+        if (y0 == past_end || y0 + KT > past_end) return -1;
+        for (int seg = 1; seg < nseg; ++seg) {
+          const int j = j0 + seg * R;
+          if (j < kvl && cache_row(j) != y0 + seg * R) return -1;
+        }
+        return y0;
+      };
+      const uint16_t both = 3;
+      bool ok = true;
+      int g = 0;             // key chunks issued so far (ring position)
+      // V(tv): this CTA's four value chunks, once P(tv - 1) V(tv - 1) has freed the buffer
+      auto load_v = [&](int tv) -> bool {
+        if (tv >= 1 && !wait_bar(B, &B->o_done, (tv - 1) & 1, P.status)) return false;
+        mbar_arrive_expect_tx(&B->v_full, 4 * KV_CH_BYTES);
+        const int y0 = tile_run(tv);
+        if (y0 >= 0) {
+          tma_load_3d(smem + OFF_V, &P.tmV, &B->v_full, 0, y0, 4 * half);
+        } else {
+          for (int i = 0; i < 4; ++i)
+            for (int seg = 0; seg < nseg; ++seg)
+              tma_load_3d(smem + OFF_V + i * KV_CH_BYTES + seg * R * 128, &P.tmKs, &B->v_full,
+                          (4 * half + i) * DCH, cache_row(j_lo + tv * KT + seg * R), 0);
+        }
+        return true;
+      };
+      for (int t = 0; t <= nt && ok; ++t) {
+        const int y0 = t < nt ? tile_run(t) : -1;
+        for (int c = 0; c < NCH && t < nt && ok; ++c) {
+          // V(t - 1) goes after the first ring-full of tile t's key chunks
+          if (c == KSLOTS && t >= 1) ok = load_v(t - 1);
+          if (!ok) break;
+          const int sl = g % KSLOTS;
+          // both CTAs are done with the slot's previous chunk
+          if (!wait_bar_cl(B, &B->k_empty[sl], ((g / KSLOTS) & 1) ^ 1, P.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&B->k_full[sl], KV_CH_BYTES);
+          if ((g & 1) == half) {   // the CTAs take turns; each copy lands in both
+            uint8_t* dst = smem + OFF_K + sl * KV_CH_BYTES;
+            if (y0 >= 0) {
+              tma_load_3d_mc(dst, &P.tmK, &B->k_full[sl], c * DCH, y0, 0, both);
+            } else {
+              for (int seg = 0; seg < nseg; ++seg)
+                tma_load_3d_mc(dst + seg * R * 128, &P.tmKs, &B->k_full[sl], c * DCH,
+                               cache_row(j_lo + t * KT + seg * R), 0, both);
+            }
+          }
+          ++g;
+        }
+        if (t == nt && ok) ok = load_v(nt - 1);
       }
-      // every issued copy has landed before the CTA may exit
+      // every copy into this CTA has landed before it may exit (the peer's
+      // multicast copies included: k_full counts them)
       mbar_wait(&B->q_full, 0, P.status);
-      for (int t = max(0, issued - 2); t < issued; ++t)
-        mbar_wait(&B->kv_full[t & 1], (t >> 1) & 1, P.status);
+      for (int i = max(0, g - KSLOTS); i < g; ++i) mbar_wait(&B->k_full[i % KSLOTS], (i / KSLOTS) & 1, P.status);
+      mbar_wait(&B->v_full, (nt - 1) & 1, P.status);
     }
-  } else if (warp == 9) {
-    if (lane == 0) {
+  } else if (warp == 5) {
+    if (lane == 0 && nt > 0) {
       // ---- MMA issuer ----
       const uint32_t idesc_qk = idesc_f16(QROWS, KT, false);
       const uint32_t idesc_pv = idesc_f16_bmn(QROWS, 256, false);
-      const bool have_q = wait_local(B, &B->q_full, 0, P.status);
-      // S(t) = Q K(t)^T into score buffer t % 2 (its (t/2)-th use)
+      const bool have_q = wait_bar(B, &B->q_full, 0, P.status) && wait_bar(B, &B->q_tmem, 0, P.status);
+      int g = 0;
+      // S(t) = Q K(t)^T, chunk by chunk from the ring
       auto issue_qk = [&](int t) -> bool {
-        const int s = t & 1;
-        if (!wait_local(B, &B->kv_full[s], (t >> 1) & 1, P.status)) return false;
-        if (!wait_local(B, &B->s_free[s], ((t >> 1) & 1) ^ 1, P.status)) return false;
-        tc_fence_after();
-        const uint8_t* stage = smem + OFF_KV + s * KV_STAGE_BYTES;
-        for (int i = 0; i < nch; ++i) {
-          const uint64_t da = smem_desc_sw128(smem + OFF_Q + i * Q_CH_BYTES);
-          const uint64_t db = smem_desc_sw128(stage + i * KV_CH_BYTES);
+        if (t >= 1 && !wait_bar(B, &B->s_free, (t - 1) & 1, P.status)) return false;
+        for (int c = 0; c < NCH; ++c, ++g) {
+          const int sl = g % KSLOTS;
+          if (!wait_bar_cl(B, &B->k_full[sl], (g / KSLOTS) & 1, P.status)) return false;
+          tc_fence_after();
+          const uint64_t db = smem_desc_sw128(smem + OFF_K + sl * KV_CH_BYTES);
+          if (c < NQT) {
 #pragma unroll
-          for (int k = 0; k < DCH / 16; ++k)
-            mma_f16(tmem + TM_S + 64 * s, da + 2 * k, db + 2 * k, idesc_qk, (i | k) != 0);
+            for (int k = 0; k < DCH / 16; ++k)
+              mma_f16_ts(tmem + TM_S, tmem + TM_Q + 32 * c + 8 * k, db + 2 * k, idesc_qk, (c | k) != 0);
+          } else {
+            const uint64_t da = smem_desc_sw128(smem + OFF_Q + (c - NQT) * Q_CH_BYTES);
+#pragma unroll
+            for (int k = 0; k < DCH / 16; ++k) mma_f16(tmem + TM_S, da + 2 * k, db + 2 * k, idesc_qk, 1);
+          }
+          mma_commit_mc(&B->k_empty[sl], 3);   // this slot is free in both CTAs' eyes
         }
-        mma_commit(&B->s_full[s]);
+        mma_commit(&B->s_full);
         return true;
       };
-      bool ok = have_q && (nt == 0 || issue_qk(0));
+      bool ok = have_q && issue_qk(0);
       for (int t = 0; t < nt && ok; ++t) {
-        // the next tile's scores overlap this tile's exchange and softmax
+        // the next tile's scores overlap this tile's softmax
         if (t + 1 < nt && !issue_qk(t + 1)) break;
-        if (!wait_local(B, &B->p_full, t & 1, P.status)) break;
+        if (!wait_bar(B, &B->p_full, t & 1, P.status)) break;
+        if (!wait_bar(B, &B->v_full, t & 1, P.status)) break;
         tc_fence_after();
-        const uint8_t* stage = smem + OFF_KV + (t & 1) * KV_STAGE_BYTES;
-        const uint64_t dv = smem_desc_sw128_mn(stage, KV_CH_BYTES);
+        const uint64_t dv = smem_desc_sw128_mn(smem + OFF_V, KV_CH_BYTES);
 #pragma unroll
         for (int k = 0; k < KT / 16; ++k)   // 16 keys per MMA: 8 P columns, 16 V rows
-          mma_f16_ts(tmem + TM_O, tmem + TM_P + 32 * (t & 1) + 8 * k,
-                     dv + (uint64_t)(16 * 128 / 16) * k, idesc_pv, (t | k) != 0);
-        mma_commit(&B->o_done[t & 1]);
-        mma_commit(&B->kv_empty[t & 1]);
+          mma_f16_ts(tmem + TM_O, tmem + TM_P + 8 * k, dv + (uint64_t)(16 * 128 / 16) * k, idesc_pv,
+                     (t | k) != 0);
+        mma_commit(&B->o_done);
       }
+      // no MMA of this CTA may still run when its tensor memory is freed
+      mma_commit(&B->drain);
+      mbar_wait(&B->drain, 0, P.status);
     }
-  } else if (warp >= 4) {
-    exchange_scores(P, B, smem, tmem, peer, nt);
   } else {
-    softmax_and_store(P, B, smem, tmem, rank, peer, b, qt, row0, kvl, W, j_lo, nt);
+    softmax_and_store(P, B, smem, tmem, half, b, qt, row0, kvl, W, j_lo, nt);
   }
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();          // no CTA leaves while its peer may still signal it
-  if (warp == 9) tmem_dealloc(tmem, TMEM_COLS);
+  cluster_sync_all();          // no CTA leaves while its peer may still multicast or commit to it
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
 }
 
 }  // namespace
@@ -473,15 +507,19 @@ mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_b
   if ((d.block_len * l.H) % QROWS)
     return fail(MLA_ERR_UNSUPPORTED, "tcgen05 attention: block_len * num_heads must be a multiple of 128");
   if (ps % 16 || (ps < KT && KT % ps) || (ps > KT && ps % KT))
-    return fail(MLA_ERR_UNSUPPORTED, "tcgen05 attention: page_size must be 16, 32 or a multiple of 64");
+    return fail(MLA_ERR_UNSUPPORTED, "tcgen05 attention: page_size must be 16, 32, 64 or a multiple of 128");
   if (d.num_blocks <= 0) return MLA_OK;
   const long tokens = (long)d.num_blocks * d.block_len;
   const int splits = attn_splits(h, tokens);
   AttnParams P;
   const long rows = (long)d.num_blocks * d.block_len * l.H;
-  if (!make_tmap_2d(&P.tmQ, false, q_abs, rows, l.L, l.L, QROWS) ||
-      !make_tmap_2d(&P.tmKV, false, cache, (long)num_pages * ps, l.L, l.L, ps < KT ? ps : KT))
+  const long slots = (long)num_pages * ps;
+  if (!make_tmap_chunked(&P.tmQ, false, q_abs, rows, l.L, l.L, QROWS, NQS) ||
+      !make_tmap_2d(&P.tmK, false, cache, slots, l.L, l.L, KT) ||
+      !make_tmap_2d(&P.tmKs, false, cache, slots, l.L, l.L, ps < KT ? ps : KT) ||
+      !make_tmap_chunked(&P.tmV, false, cache, slots, l.L, l.L, KT, 4))
     return fail(MLA_ERR_CUDA, "tcgen05 attention: cuTensorMapEncodeTiled failed");
+  P.q_abs = q_abs;
   P.block_table = d.block_table;
   P.kv_len = d.kv_len;
   P.window = d.window;
@@ -503,6 +541,10 @@ mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_b
   P.o_part = part;
   P.lse_part = part + (size_t)splits * rows * 512;
   if (splits > 1 && d.vis_stats) init_vis_stats(st, d.vis_stats, tokens);
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(latent_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  });
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * d.num_blocks * P.tiles_per_block, splits, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
@@ -521,43 +563,15 @@ mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_b
   return MLA_OK;
 }
 
-// Clusters of the attention kernel resident on the GPU at once (queried once;
-// also sets the kernel's shared-memory limit, so it runs before any launch).
-static int attn_clusters_per_wave(const mla_handle* h) {
-  static std::once_flag once;
-  static int clusters = 0;
-  std::call_once(once, [h] {
-    cudaFuncSetAttribute(latent_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         SMEM_BYTES);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, latent_attn_tc_kernel, &cfg) != cudaSuccess || n <= 0) {
-      (void)cudaGetLastError();
-      n = h->num_sms / 2;
-    }
-    clusters = n;
-  });
-  return clusters;
-}
-
-// When the (block, 128-row) units leave part of the GPU idle, split each
-// unit's key range so that the clusters fill one wave (at most 8 parts); a
-// split that would add a partial wave only lengthens the kernel.
+// When the (block, 128-row, value-half) CTAs leave part of the GPU idle
+// (one CTA per SM), split each unit's key range so that the CTAs fill one
+// wave (at most 8 parts); a split that would add a partial wave only
+// lengthens the kernel.
 int attn_splits(const mla_handle* h, long tokens) {
-  const long units = tokens * h->lay.H / QROWS;
-  const long wave = attn_clusters_per_wave(h);
-  if (units <= 0 || units >= wave) return 1;
-  const long s = wave / units;
+  const long ctas = 2 * (tokens * h->lay.H / QROWS);
+  const long wave = h->num_sms;
+  if (ctas <= 0 || ctas >= wave) return 1;
+  const long s = wave / ctas;
   return (int)(s < 1 ? 1 : s > 8 ? 8 : s);
 }
 

@@ -9,8 +9,11 @@ namespace mla {
 namespace tc {
 
 struct AttnParams {
-  CUtensorMap tmQ;    // Q_abs bf16 [rows, 576], box 64 x 128
-  CUtensorMap tmKV;   // latent cache bf16 [num_pages * page_size, 576], box 64 x seg_rows
+  CUtensorMap tmQ;    // Q_abs bf16 [rows, 576], chunked view, box 128 rows x 7 chunks
+  CUtensorMap tmK;    // latent cache bf16 [num_pages * page_size, 576], box 64 x 128 rows
+  CUtensorMap tmKs;   // the same, box 64 x seg_rows (one page or 128 rows)
+  CUtensorMap tmV;    // the cache, chunked view, box 128 rows x 4 chunks
+  const __nv_bfloat16* q_abs;   // the same Q_abs (dims 0..127 go to tensor memory)
   const int32_t* block_table;
   const int32_t* kv_len;
   const int32_t* window;
@@ -28,8 +31,8 @@ struct AttnParams {
 };
 
 // Supported: kv_lora_rank 512, qk_rope 64, block_len * num_heads a multiple
-// of 128, page_size a multiple of 16 (or of 64).  Returns
-// MLA_ERR_UNSUPPORTED otherwise.
+// of 128, page_size 16, 32, 64 or a multiple of 128.  Returns MLA_ERR_UNSUPPORTED
+// otherwise.
 // The key range of every (block, 128-row) unit is split in `splits` parts
 // when units alone do not fill the GPU; `part` (attn_split_floats() floats)
 // holds the partial outputs merged by log-sum-exp.

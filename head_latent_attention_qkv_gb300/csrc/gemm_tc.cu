@@ -327,3 +327,26 @@ bool make_tmap_2d(CUtensorMap* m, bool fp16, const void* base, long rows, long c
 }
 }  // namespace tc
 }  // namespace mla
+
+namespace mla {
+namespace tc {
+// Chunked view of a row-major 16-bit matrix [rows, cols] (row stride ld
+// elements, cols a multiple of 64): dims {64, rows, cols / 64}, so that one
+// box {64, box_rows, box_chunks} lands in shared memory as box_chunks
+// consecutive [box_rows x 128 B] blocks, each 128-byte swizzled -- several
+// 64-column K-major operand tiles in one TMA copy.
+bool make_tmap_chunked(CUtensorMap* m, bool fp16, const void* base, long rows, long cols, long ld,
+                       int box_rows, int box_chunks) {
+  EncodeFn enc = encode_fn();
+  if (!enc || cols % 64) return false;
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(cols / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_chunks};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+             const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace tc
+}  // namespace mla

@@ -41,5 +41,11 @@ namespace tc {
 // rank 3 (a unit batch dimension): load it with 3-D TMA, z = 0.
 bool make_tmap_2d(CUtensorMap* m, bool fp16, const void* base, long rows, long cols, long ld,
                   int box_rows);
+// The same matrix viewed as {64, rows, cols / 64}: a box {64, box_rows,
+// box_chunks} brings box_chunks 64-column tiles ([box_rows x 128 B] each,
+// 128-byte swizzled, consecutive in shared memory) in one copy.  Load it
+// with 3-D TMA at coordinates (0, row, first chunk).
+bool make_tmap_chunked(CUtensorMap* m, bool fp16, const void* base, long rows, long cols, long ld,
+                       int box_rows, int box_chunks);
 }  // namespace tc
 }  // namespace mla

@@ -370,26 +370,26 @@ def make_workload(name: str, scale: str = "full") -> Workload:
         if small:
             return prefill_workload(name, d, 1, [200, 77, 131], 16, page_size=64,
                                     description="3 x (ragged context + 16-token block), full mask")
-        return prefill_workload(name, d, 1, [2048] * 8, 16, page_size=64,
+        return prefill_workload(name, d, 1, [2048] * 8, 16, page_size=128,
                                 description="8 x (2048 context + 16-token block), full mask")
     if name == "qwen3_4b_sliding_gate":
         d = QWEN3_4B_MLA.replace(use_output_gate=True, rope_style="neox")
         masked = lambda s: range(4) if s % 4 == 0 else ()
         if small:
-            return prefill_workload(name, d, 2, [700, 300, 97, 1000, 513], 16, page_size=64,
+            return prefill_workload(name, d, 2, [700, 300, 97, 1000, 513], 16, page_size=128,
                                     window=512, masked_rows=masked,
                                     description="5 x (ragged context + 16), sliding 512, gate")
-        return prefill_workload(name, d, 2, [8192] * 16, 16, page_size=64, window=512,
+        return prefill_workload(name, d, 2, [8192] * 16, 16, page_size=128, window=512,
                                 masked_rows=masked,
                                 description="16 x (8192 context + 16), sliding 512, gate")
     if name == "qwen3_4b_cached_decode":
         d = QWEN3_4B_MLA
         if small:
             return cached_decode_workload(name, d, 3, batch=5, prefill_len=512, len_lo=100,
-                                          len_hi=512, block_len=16, num_blocks=2, page_size=64,
+                                          len_hi=512, block_len=16, num_blocks=2, page_size=32,
                                           description="5 seqs, prefilled 512, 2 cached blocks")
         return cached_decode_workload(name, d, 3, batch=64, prefill_len=4096, len_lo=1024,
-                                      len_hi=4096, block_len=16, num_blocks=2, page_size=64,
+                                      len_hi=4096, block_len=16, num_blocks=2, page_size=128,
                                       description="64 seqs, prefilled 4096, L~U[1024,4096], 2 blocks")
     if name == "deepseek_v3_block_parallel":
         d = DEEPSEEK_V3_MLA
@@ -398,6 +398,6 @@ def make_workload(name: str, scale: str = "full") -> Workload:
                                            block_len=16, page_size=64, windows=(0, 100),
                                            description="2 seqs x 3 proposals over 192 context")
         return block_parallel_workload(name, d, 4, batch=4, ctx_len=4096, blocks_per_seq=1024,
-                                       block_len=16, page_size=64, windows=(0, 1024),
+                                       block_len=16, page_size=128, windows=(0, 1024),
                                        description="4 x 1024 proposals of 16 over 4096 context")
     raise KeyError(name)
