@@ -270,14 +270,8 @@ namespace mla {
 namespace {
 
 struct FwdWs {
-  size_t a_out, q_cn, q_raw, q_nope, q_abs, o_lat, o, part, o_acc, total;
+  size_t a_out, q_cn, q_raw, q_nope, q_abs, o_lat, o, part, total;
 };
-
-// o_proj of few tokens runs split-K into an fp32 buffer, then converts.
-bool oproj_split(const mla_handle* h, long M) {
-  return h->cfg.dtype == MLA_BF16 &&
-         tc::auto_splitk((int)M, h->lay.D, h->lay.H * h->lay.dv, 1) > 1;
-}
 
 FwdWs forward_ws(const mla_handle* h, long M) {
   const Layout& l = h->lay;
@@ -292,7 +286,6 @@ FwdWs forward_ws(const mla_handle* h, long M) {
   w.o = o;      o = align256(o + (size_t)M * l.H * l.dv * l.elt);
   // split-KV partial outputs of the tensor-core attention (bf16 layers)
   w.part = o;   o = align256(o + (h->cfg.dtype == MLA_BF16 ? tc::attn_split_floats(h, M) * 4 : 0));
-  w.o_acc = o;  o = align256(o + (oproj_split(h, M) ? (size_t)M * l.D * 4 : 0));
   w.total = o;
   return w;
 }
@@ -333,7 +326,6 @@ mla_status_t proj(mla_handle_t* h, cudaStream_t st, int M, int N, int K, int bat
                 : std::is_same<TC, __half>::value ? tc::Out::F16 : tc::Out::BF16;
     tc::GemmArgs a{M, N, K, batch, std::is_same<TA, __half>::value, A, lda, sA, B, ldb, sB,
                    C, ldc, sC, o, G, ldg, sG};
-    if (o == tc::Out::F32 && !G && batch == 1) a.splitk = tc::auto_splitk(M, N, K, batch);
     return tc::gemm(st, a, h->status);
   }
 }
@@ -473,18 +465,9 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
                    (const TI*)h->WUV, l.rkv, (long)l.dv * l.rkv, o, (long)l.H * l.dv, l.dv, gate,
                    l.NA, l.dv);
   if (s != MLA_OK) return s;
-  if (oproj_split(h, M)) {
-    float* acc = (float*)(ws + w.o_acc);
-    s = proj<TI, float>(h, st, M, l.D, l.H * l.dv, 1, o, (long)l.H * l.dv, 0, (const TI*)h->Wo,
-                        (long)l.H * l.dv, 0, acc, l.D, 0);
-    if (s != MLA_OK) return s;
-    simt::f32_to<TX>(st, acc, (TX*)out, (long)M * l.D);
-    h->launches += 1;
-  } else {
-    s = proj<TI, TX>(h, st, M, l.D, l.H * l.dv, 1, o, (long)l.H * l.dv, 0, (const TI*)h->Wo,
-                     (long)l.H * l.dv, 0, (TX*)out, l.D, 0);
-    if (s != MLA_OK) return s;
-  }
+  s = proj<TI, TX>(h, st, M, l.D, l.H * l.dv, 1, o, (long)l.H * l.dv, 0, (const TI*)h->Wo,
+                   (long)l.H * l.dv, 0, (TX*)out, l.D, 0);
+  if (s != MLA_OK) return s;
   // non-GEMM kernels: [kv finish], [q norm], rope split, attention
   h->launches += 2 + (bslots ? 1 : 0) + (l.rq > 0 ? 1 : 0);
   return MLA_OK;

@@ -4,13 +4,22 @@
 // epilogue that optionally multiplies by sigmoid(G) before storing fp32,
 // fp16 or bf16.
 //
-// One CTA computes a 128 x BN tile.  Warp 0 (one lane) streams 64-wide K
-// slices of A and B through a STAGES-deep shared-memory ring with TMA
-// (128-byte swizzle); warp 1 (one lane) issues tcgen05.mma (M=128, N=BN,
-// K=16) into a TMEM accumulator and releases each ring slot with
-// tcgen05.commit; warp 2 owns the TMEM allocation; after the last commit all
-// four warps read the accumulator back (warp w owns TMEM lanes / tile rows
-// 32w..32w+31) and store.
+// One CTA computes a 128 x BN tile.  Warp 0 (one lane) streams A and B
+// through a shared-memory ring with TMA; one stage holds KBS consecutive
+// 64-wide K slices of each operand and arrives in a single copy per operand
+// (a chunked 4-D view of the matrix: a TMA copy costs about the same SM time
+// whatever its size, so few large copies keep the tensor pipe fed).  Warp 1
+// (one lane) issues tcgen05.mma (M=128, N=BN, K=16) into a TMEM accumulator
+// and frees each stage with tcgen05.commit; warp 2 owns the TMEM allocation.
+//
+// Split-K (small M): the K range is divided among the `splitk` CTAs of a
+// cluster along z.  Every CTA writes its fp32 partial tile to its own shared
+// memory; CTA j of the cluster then adds the partials of rows
+// [128 j / splitk, 128 (j+1) / splitk) from all of them through distributed
+// shared memory, always in rank order (deterministic), applies the epilogue
+// and stores.  Without split-K the CTA stages its own tile the same way.  The
+// store is done row by row by whole warps, so each row leaves as a coalesced
+// write.
 #include "gemm_tc.cuh"
 
 #include <mutex>
@@ -24,61 +33,94 @@ namespace {
 
 constexpr int BM = 128, BK = 64, THREADS = 128;
 
-template <int BN, int STAGES>
+// k-blocks per stage and stages by tile width: about 192 KB of ring
+template <int BN> struct Cfg;
+template <> struct Cfg<64> { static constexpr int KBS = 4, STAGES = 2; };
+template <> struct Cfg<128> { static constexpr int KBS = 2, STAGES = 3; };
+template <> struct Cfg<256> { static constexpr int KBS = 2, STAGES = 2; };
+
+template <int BN>
 struct Smem {
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int KBS = Cfg<BN>::KBS, STAGES = Cfg<BN>::STAGES;
+  static constexpr int A_BYTES = KBS * BM * BK * 2;
+  static constexpr int B_BYTES = KBS * BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256;
+  static constexpr int RING = STAGES * STAGE_BYTES;
+  static constexpr int PITCH = BN * 4 + 16;            // fp32 partial tile row (bank-conflict free)
+  static constexpr int BYTES = 1024 /*align slack*/ + RING + 256;
+  static_assert(BM * PITCH <= RING, "partial tile fits in the ring");
+  static_assert(BYTES <= 232448, "shared memory");
 };
 
-template <typename TC>
-__device__ __forceinline__ void store32(TC* dst, const float* v);
-template <>
-__device__ __forceinline__ void store32<float>(float* dst, const float* v) {
-#pragma unroll
-  for (int i = 0; i < 32; i += 4)
-    *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-}
-template <typename T16>
-__device__ __forceinline__ void store32_16(T16* dst, const float* v) {
-#pragma unroll
-  for (int i = 0; i < 32; i += 8) {
-    uint4 u;
-    T16 h[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) h[j] = from_f32<T16>(v[i + j]);
-    memcpy(&u, h, 16);
-    *reinterpret_cast<uint4*>(dst + i) = u;
-  }
-}
-template <>
-__device__ __forceinline__ void store32<__half>(__half* dst, const float* v) { store32_16(dst, v); }
-template <>
-__device__ __forceinline__ void store32<__nv_bfloat16>(__nv_bfloat16* dst, const float* v) {
-  store32_16(dst, v);
+// 4-D TMA tile load (coordinates innermost first).
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];"
+      ::"r"(smem_u32(dst)), "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+      : "memory");
 }
 
-template <int BN, int STAGES, typename TC>
+// Loads of the partial tiles after the cluster barrier (volatile: they stay
+// after it); the callers issue all of a row's loads before using any, so
+// they are in flight together.
+__device__ __forceinline__ float4 ld_peer_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float4 ld_own_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+
+template <typename TC> __device__ __forceinline__ void store4(TC* dst, float a, float b, float c, float d);
+template <>
+__device__ __forceinline__ void store4<float>(float* dst, float a, float b, float c, float d) {
+  *reinterpret_cast<float4*>(dst) = make_float4(a, b, c, d);
+}
+template <typename T16>
+__device__ __forceinline__ void store4_16(T16* dst, float a, float b, float c, float d) {
+  T16 h[4] = {from_f32<T16>(a), from_f32<T16>(b), from_f32<T16>(c), from_f32<T16>(d)};
+  uint2 u;
+  memcpy(&u, h, 8);
+  *reinterpret_cast<uint2*>(dst) = u;
+}
+template <>
+__device__ __forceinline__ void store4<__half>(__half* dst, float a, float b, float c, float d) {
+  store4_16(dst, a, b, c, d);
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float a, float b, float c, float d) {
+  store4_16(dst, a, b, c, d);
+}
+
+template <int BN, typename TC>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                int M, int N, int K, TC* __restrict__ C, long ldc, long sC,
                const float* __restrict__ G, long ldg, long sG, uint32_t idesc, int splitk,
                uint32_t* status) {
-  using S = Smem<BN, STAGES>;
+  using S = Smem<BN>;
+  constexpr int KBS = S::KBS, STAGES = S::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t* full = (uint64_t*)(smem + STAGES * S::STAGE_BYTES);
+  uint64_t* full = (uint64_t*)(smem + S::RING);
   uint64_t* empty = full + STAGES;
   uint64_t* accum = empty + STAGES;
   uint32_t* tmem_slot = (uint32_t*)(accum + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
-  const int z = blockIdx.z / splitk, ks = blockIdx.z % splitk;
-  const int nk_all = (K + BK - 1) / BK;
-  const int kb0 = (int)((long)ks * nk_all / splitk);          // this split's K blocks
-  const int nk = (int)((long)(ks + 1) * nk_all / splitk) - kb0;
+  const int z = blockIdx.z / splitk, ks = blockIdx.z % splitk;     // ks == cluster rank
+  const int nk = (K + BK - 1) / BK;
+  const int ng_all = (nk + KBS - 1) / KBS;                          // stages of the whole K
+  const int g0 = (int)((long)ks * ng_all / splitk);                 // this split's stages
+  const int ng = (int)((long)(ks + 1) * ng_all / splitk) - g0;
   constexpr uint32_t TMEM_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
 
   if (threadIdx.x == 0) {
@@ -98,82 +140,109 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    // producer: TMA ring; tiles are pulled into L2 2*STAGES k-blocks ahead
-    auto prefetch = [&](int kb) {
-      if (kb < nk) {
-        tma_prefetch_3d(&tmA, (kb0 + kb) * BK, m0, z);
-        tma_prefetch_3d(&tmB, (kb0 + kb) * BK, n0, z);
-      }
-    };
-    for (int kb = STAGES; kb < 2 * STAGES; ++kb) prefetch(kb);
+    // producer: one copy per operand per stage (KBS k-blocks)
     bool ok = true;
-    for (int kb = 0; kb < nk && ok; ++kb) {
-      const int s = kb % STAGES;
-      const uint32_t ph = (kb / STAGES) & 1;
-      ok = mbar_wait(&empty[s], ph ^ 1, status);
+    for (int g = 0; g < ng && ok; ++g) {
+      const int s = g % STAGES;
+      ok = mbar_wait(&empty[s], ((g / STAGES) & 1) ^ 1, status);
       if (!ok) break;
       uint8_t* a = smem + s * S::STAGE_BYTES;
-      uint8_t* b = a + S::A_BYTES;
       mbar_arrive_expect_tx(&full[s], S::STAGE_BYTES);
-      tma_load_3d(a, &tmA, &full[s], (kb0 + kb) * BK, m0, z);
-      tma_load_3d(b, &tmB, &full[s], (kb0 + kb) * BK, n0, z);
-      prefetch(kb + 2 * STAGES);
+      tma_load_4d(a, &tmA, &full[s], 0, m0, (g0 + g) * KBS, z);
+      tma_load_4d(a + S::A_BYTES, &tmB, &full[s], 0, n0, (g0 + g) * KBS, z);
     }
     // drain: the last loads of every slot have landed before the CTA can exit
-    for (int kb = max(0, nk - STAGES); kb < nk; ++kb)
-      mbar_wait(&full[kb % STAGES], (kb / STAGES) & 1, status);
+    for (int g = max(0, ng - STAGES); g < ng; ++g)
+      mbar_wait(&full[g % STAGES], (g / STAGES) & 1, status);
   } else if (warp == 1 && lane == 0) {
-    // MMA issuer
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % STAGES;
-      if (!mbar_wait(&full[s], (kb / STAGES) & 1, status)) break;
+    // MMA issuer (k-blocks past K were filled with zeros by TMA and are skipped)
+    for (int g = 0; g < ng; ++g) {
+      const int s = g % STAGES;
+      if (!mbar_wait(&full[s], (g / STAGES) & 1, status)) break;
       tc_fence_after();
       const uint8_t* a = smem + s * S::STAGE_BYTES;
       const uint8_t* b = a + S::A_BYTES;
-      const uint64_t da = smem_desc_sw128(a), db = smem_desc_sw128(b);
 #pragma unroll
-      for (int k = 0; k < BK / 16; ++k)  // advance 16 elements = 32 bytes = 2 descriptor units
-        mma_f16(tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+      for (int i = 0; i < KBS; ++i) {
+        if ((g0 + g) * KBS + i >= nk) break;
+        const uint64_t da = smem_desc_sw128(a + i * BM * BK * 2), db = smem_desc_sw128(b + i * BN * BK * 2);
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)  // advance 16 elements = 32 bytes = 2 descriptor units
+          mma_f16(tmem, da + 2 * k, db + 2 * k, idesc, (g | i | k) != 0);
+      }
       mma_commit(&empty[s]);
     }
     mma_commit(accum);
   }
   __syncwarp();
-  // epilogue: every warp reads its 32 accumulator lanes
-  const bool have = nk > 0 && mbar_wait(accum, 0, status);
+
+  // ---- epilogue: accumulator -> fp32 partial tile in shared memory (the
+  // ring is free once the accumulator is complete) ----
+  const bool have = ng > 0 && mbar_wait(accum, 0, status);
   tc_fence_after();
-  const int row = m0 + warp * 32 + lane;
-  const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+  {
+    const int r = warp * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    float* prow = (float*)(smem + r * S::PITCH);
 #pragma unroll 1
-  for (int c = 0; c < BN; c += 32) {
-    float v[32];
-    tmem_ld32(lane_addr + c, v);
-    const int n = n0 + c;
-    if (!have || row >= M || n >= N) continue;
-    if (G) {
-      const float* g = G + z * sG + (long)row * ldg + n;
+    for (int c = 0; c < BN; c += 32) {
+      float v[32];
+      if (have) {
+        tmem_ld32(lane_addr + c, v);
+      } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (n + i < N) v[i] = v[i] / (1.f + expf(-g[i]));
-    }
-    TC* dst = C + z * sC + (long)row * ldc + n;
-    if constexpr (std::is_same<TC, float>::value) {
-      if (splitk > 1) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (n + i < N) atomicAdd(dst + i, v[i]);
-        continue;
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
       }
-    }
-    if (n + 32 <= N) {
-      store32<TC>(dst, v);
-    } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (n + i < N) dst[i] = from_f32<TC>(v[i]);
+      for (int i = 0; i < 32; i += 4)
+        *reinterpret_cast<float4*>(prow + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
     }
   }
   tc_fence_before();
+  __syncthreads();
+  if (splitk > 1) cluster_sync_all();      // every partial of the cluster is in place
+  // ---- sum the partials of this CTA's rows (rank order), epilogue, store:
+  // lane l of a warp holds columns 4l .. 4l+3 of every 128-column group ----
+  const int r_lo = ks * BM / splitk, r_hi = (ks + 1) * BM / splitk;
+  for (int r = r_lo + warp; r < r_hi; r += THREADS / 32) {
+    const int row = m0 + r;
+#pragma unroll 1
+    for (int cg = 0; cg < BN; cg += 128) {
+      const int col = cg + 4 * lane;
+      if (col >= BN) break;
+      const uint32_t off = smem_u32(smem + r * S::PITCH + col * 4);
+      float4 v;
+      if (splitk > 1) {
+        // all partials first (independent loads in flight), then the sum in rank order
+        float4 t[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q < splitk) t[q] = ld_peer_v4(mapa(off, (uint32_t)q));
+        v = t[0];
+#pragma unroll
+        for (int q = 1; q < 8; ++q)
+          if (q < splitk) { v.x += t[q].x; v.y += t[q].y; v.z += t[q].z; v.w += t[q].w; }
+      } else {
+        v = ld_own_v4(off);
+      }
+      const int n = n0 + col;
+      if (row >= M || n >= N) continue;
+      float o[4] = {v.x, v.y, v.z, v.w};
+      if (G) {
+        const float* g = G + z * sG + (long)row * ldg + n;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (n + i < N) o[i] = o[i] / (1.f + expf(-g[i]));
+      }
+      TC* dst = C + z * sC + (long)row * ldc + n;
+      if (n + 4 <= N) {
+        store4<TC>(dst, o[0], o[1], o[2], o[3]);
+      } else {
+        for (int i = 0; i < 4 && n + i < N; ++i) dst[i] = from_f32<TC>(o[i]);
+      }
+    }
+  }
+  if (splitk > 1) cluster_sync_all();      // no CTA leaves while a peer may still read its partial
   __syncthreads();
   if (warp == 2) tmem_dealloc(tmem, TMEM_COLS);
 }
@@ -208,145 +277,136 @@ EncodeFn encode_fn() {
   return fn;
 }
 
-// [batch][rows][K] 16-bit matrix, K contiguous; box = 64 (K) x box_rows.
-bool make_map(CUtensorMap* m, bool fp16, const void* base, long rows, long K, long ld,
-              long sbatch, int batch, int box_rows) {
+bool encode(CUtensorMap* m, bool fp16, const void* base, int rank, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box) {
   EncodeFn enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)batch};
-  cuuint64_t strides[2] = {(cuuint64_t)ld * 2,
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+             (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [batch][rows][K] 16-bit matrix (K contiguous, row stride ld, batch stride
+// sbatch elements) viewed as {64, rows, K/64, batch}: a box {64, box_rows,
+// kbs, 1} is kbs consecutive 64-wide K slices of box_rows rows.
+bool make_operand_map(CUtensorMap* m, bool fp16, const void* base, long rows, long K, long ld,
+                      long sbatch, int batch, int box_rows, int kbs) {
+  cuuint64_t dims[4] = {64, (cuuint64_t)rows, (cuuint64_t)(K / 64), (cuuint64_t)batch};
+  cuuint64_t strides[3] = {(cuuint64_t)ld * 2, 128,
                            (cuuint64_t)(batch > 1 ? sbatch : ld * rows) * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-             const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  cuuint32_t box[4] = {64, (cuuint32_t)box_rows, (cuuint32_t)kbs, 1};
+  return encode(m, fp16, base, 4, dims, strides, box);
 }
 
 template <int BN, typename TC>
-mla_status_t launch(cudaStream_t st, const GemmArgs& a, uint32_t* status) {
-  constexpr int STAGES = 4;
-  using S = Smem<BN, STAGES>;
+mla_status_t launch(cudaStream_t st, const GemmArgs& a, int splitk, uint32_t* status) {
+  using S = Smem<BN>;
   CUtensorMap ta, tb;
-  if (!make_map(&ta, a.fp16, a.A, a.M, a.K, a.lda, a.sA, a.batch, BM) ||
-      !make_map(&tb, a.fp16, a.B, a.N, a.K, a.ldb, a.sB, a.batch, BN))
+  if (!make_operand_map(&ta, a.fp16, a.A, a.M, a.K, a.lda, a.sA, a.batch, BM, S::KBS) ||
+      !make_operand_map(&tb, a.fp16, a.B, a.N, a.K, a.ldb, a.sB, a.batch, BN, S::KBS))
     return fail(MLA_ERR_CUDA, "tcgen05 gemm: cuTensorMapEncodeTiled failed");
-  auto kern = gemm_tc_kernel<BN, STAGES, TC>;
+  auto kern = gemm_tc_kernel<BN, TC>;
   static std::once_flag once;
   std::call_once(once, [&] {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
   });
-  if (a.splitk > 1) {
-    const cudaError_t e = cudaMemset2DAsync(a.C, a.ldc * sizeof(float), 0, a.N * sizeof(float),
-                                            (size_t)a.M, st);
-    if (e != cudaSuccess) return cuda_fail(e, "tcgen05 gemm: zeroing the split-K output");
-  }
-  dim3 grid((a.N + BN - 1) / BN, (a.M + BM - 1) / BM, a.batch * a.splitk);
-  kern<<<grid, THREADS, S::BYTES, st>>>(ta, tb, a.M, a.N, a.K, (TC*)a.C, a.ldc, a.sC, a.G, a.ldg,
-                                         a.sG, idesc_f16(BM, BN, a.fp16), a.splitk, status);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.N + BN - 1) / BN, (a.M + BM - 1) / BM, a.batch * splitk);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = S::BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = splitk;
+  cfg.attrs = attr;
+  cfg.numAttrs = splitk > 1 ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, a.M, a.N, a.K, (TC*)a.C, a.ldc, a.sC,
+                                           a.G, a.ldg, a.sG, idesc_f16(BM, BN, a.fp16), splitk, status);
+  if (e != cudaSuccess) return cuda_fail(e, "tcgen05 gemm launch");
   return MLA_OK;
 }
 
 template <typename TC>
-mla_status_t launch_bn(cudaStream_t st, const GemmArgs& a, uint32_t* status, int bn) {
+mla_status_t launch_bn(cudaStream_t st, const GemmArgs& a, int bn, int splitk, uint32_t* status) {
   switch (bn) {
-    case 64: return launch<64, TC>(st, a, status);
-    case 128: return launch<128, TC>(st, a, status);
-    case 192: return launch<192, TC>(st, a, status);
-    default: return launch<256, TC>(st, a, status);
+    case 64: return launch<64, TC>(st, a, splitk, status);
+    case 128: return launch<128, TC>(st, a, splitk, status);
+    default: return launch<256, TC>(st, a, splitk, status);
   }
 }
 
-// Tile width: among the widths that give at least one tile per SM, the one
-// with the least padded work (ties: the wider tile, fewer A re-reads); if none
-// fills the GPU, the narrowest.
-int pick_bn(int M, int N, int batch, int num_sms) {
-  const int mt = (M + BM - 1) / BM;
-  const int cands[4] = {256, 192, 128, 64};
-  int best = 0;
-  long best_pad = 0;
-  for (int bn : cands) {
-    const long nt = (N + bn - 1) / bn;
-    if ((long)mt * nt * batch < num_sms) continue;
-    const long pad = nt * bn - N;
-    if (!best || pad < best_pad) { best = bn; best_pad = pad; }
+int num_sms_current() {
+  static int num_sms = 0;
+  if (!num_sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
   }
-  return best ? best : 64;
+  return num_sms;
 }
 
 }  // namespace
 
-int auto_splitk(int M, int N, int K, int batch) {
-  static int num_sms = 0;
-  if (!num_sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+void plan_gemm(int M, int N, int K, int batch, int* bn_out, int* split_out) {
+  const long sms = num_sms_current();
+  const int nk = (K + BK - 1) / BK;
+  const int bns[3] = {256, 128, 64};
+  double best = 1e30;
+  int best_bn = 64, best_s = 1;
+  for (int bn : bns) {
+    const double mma = bn == 256 ? 170.0 : 108.0;
+    const int kbs = bn == 64 ? 4 : 2;
+    const long tiles = (long)((N + bn - 1) / bn) * ((M + BM - 1) / BM) * batch;
+    for (int s = 1; s <= (batch == 1 ? 8 : 1); ++s) {
+      if (s > 1 && tiles * s > sms) break;
+      if (s > 1 && (nk + kbs - 1) / kbs < s) break;      // at least one stage per split
+      const long waves = (tiles * s + sms - 1) / sms;
+      const double per_cta = ((nk + s - 1) / s) * 4.0 * mma + 3000.0 + 400.0 * s;
+      const double t = waves * per_cta;
+      if (t < best * 0.98) { best = t; best_bn = bn; best_s = s; }
+    }
   }
-  const long tiles = (long)((M + BM - 1) / BM) * ((N + 63) / 64) * batch;
-  const int kblocks = (K + BK - 1) / BK;
-  if (batch != 1 || tiles >= num_sms || kblocks < 16) return 1;
-  int s = (int)((num_sms + tiles - 1) / tiles);
-  s = s < kblocks / 8 ? s : kblocks / 8;        // keep >= 8 K blocks per split
-  return s < 1 ? 1 : s;
+  *bn_out = best_bn;
+  *split_out = best_s;
 }
 
 mla_status_t gemm(cudaStream_t st, const GemmArgs& a, uint32_t* status) {
   if (a.M <= 0 || a.N <= 0 || a.batch <= 0) return MLA_OK;
-  const bool ok = a.K % 8 == 0 && a.lda % 8 == 0 && a.ldb % 8 == 0 && a.sA % 8 == 0 &&
-                  a.sB % 8 == 0 && a.ldc % 8 == 0 && a.sC % 8 == 0 &&
+  const bool ok = a.K % 64 == 0 && a.lda % 8 == 0 && a.ldb % 8 == 0 && a.sA % 8 == 0 &&
+                  a.sB % 8 == 0 && a.ldc % 4 == 0 && a.sC % 4 == 0 &&
                   (uintptr_t)a.A % 16 == 0 && (uintptr_t)a.B % 16 == 0 &&
                   (uintptr_t)a.C % 16 == 0;
-  if (!ok) return fail(MLA_ERR_UNSUPPORTED, "tcgen05 gemm: K/leading dims must be multiples of 8 "
-                                             "and pointers 16-byte aligned");
-  if (a.splitk < 1 || (a.splitk > 1 && (a.out != Out::F32 || a.G || a.batch != 1)))
-    return fail(MLA_ERR_INVALID_ARG, "tcgen05 gemm: split-K needs an fp32 output, no gate, batch 1");
-  static int num_sms = 0;
-  if (!num_sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-  }
-  const int bn = pick_bn(a.M, a.N, a.batch, num_sms);
+  if (!ok) return fail(MLA_ERR_UNSUPPORTED, "tcgen05 gemm: K must be a multiple of 64, leading dims "
+                                             "multiples of 8 and pointers 16-byte aligned");
+  int bn = 64, splitk = 1;
+  plan_gemm(a.M, a.N, a.K, a.batch, &bn, &splitk);
   switch (a.out) {
-    case Out::F32: return launch_bn<float>(st, a, status, bn);
-    case Out::F16: return launch_bn<__half>(st, a, status, bn);
-    default: return launch_bn<__nv_bfloat16>(st, a, status, bn);
+    case Out::F32: return launch_bn<float>(st, a, bn, splitk, status);
+    case Out::F16: return launch_bn<__half>(st, a, bn, splitk, status);
+    default: return launch_bn<__nv_bfloat16>(st, a, bn, splitk, status);
   }
 }
 
-}  // namespace tc
-}  // namespace mla
-
-namespace mla {
-namespace tc {
 bool make_tmap_2d(CUtensorMap* m, bool fp16, const void* base, long rows, long cols, long ld,
                   int box_rows) {
-  return make_map(m, fp16, base, rows, cols, ld, 0, 1, box_rows);
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, 1};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)ld * rows * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  return encode(m, fp16, base, 3, dims, strides, box);
 }
-}  // namespace tc
-}  // namespace mla
 
-namespace mla {
-namespace tc {
-// Chunked view of a row-major 16-bit matrix [rows, cols] (row stride ld
-// elements, cols a multiple of 64): dims {64, rows, cols / 64}, so that one
-// box {64, box_rows, box_chunks} lands in shared memory as box_chunks
-// consecutive [box_rows x 128 B] blocks, each 128-byte swizzled -- several
-// 64-column K-major operand tiles in one TMA copy.
 bool make_tmap_chunked(CUtensorMap* m, bool fp16, const void* base, long rows, long cols, long ld,
                        int box_rows, int box_chunks) {
-  EncodeFn enc = encode_fn();
-  if (!enc || cols % 64) return false;
+  if (cols % 64) return false;
   cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(cols / 64)};
   cuuint64_t strides[2] = {(cuuint64_t)ld * 2, 128};
   cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_chunks};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-             const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode(m, fp16, base, 3, dims, strides, box);
 }
+
 }  // namespace tc
 }  // namespace mla

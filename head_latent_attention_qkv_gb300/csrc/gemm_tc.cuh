@@ -17,18 +17,19 @@ struct GemmArgs {
   const void* B; long ldb, sB;   // [batch][N][K]
   void* C; long ldc, sC; Out out;
   const float* G; long ldg, sG;  // optional sigmoid gate, same indexing as C
-  int splitk = 1;                // >1: K split across CTAs, fp32 C accumulated atomically
 };
 
-// Split-K factor that lets a small-M GEMM fill the GPU (1 = none).  Only
-// meaningful for fp32 outputs without a gate.
-int auto_splitk(int M, int N, int K, int batch);
+// Tile width (64, 128 or 256 columns) and split-K factor (CTAs of a cluster
+// along K, 1 = none) the launcher uses for this shape.
+void plan_gemm(int M, int N, int K, int batch, int* bn, int* splitk);
 
-// Enqueue C = A B^T (* sigmoid(G)) on `st`.  With splitk > 1 the fp32 C
-// region is zeroed first (cudaMemset2DAsync) and every split adds into it.  With splitk > 1 the fp32 C
-// region is zeroed first (cudaMemset2DAsync) and every split adds into it.  Returns MLA_ERR_UNSUPPORTED for
-// shapes the kernel does not take (K or leading dims not multiples of 8,
-// unaligned pointers) and MLA_ERR_CUDA if the tensor maps cannot be built.
+// Enqueue C = A B^T (* sigmoid(G)) on `st`.  When the output tiles alone do
+// not fill the GPU (and batch == 1) K is split over a cluster of CTAs whose
+// fp32 partials are added in shared memory, in a fixed order, before the
+// epilogue: no atomics, no zeroing, any output type.  Returns
+// MLA_ERR_UNSUPPORTED for shapes the kernel does not take (K not a multiple
+// of 64, leading dims not multiples of 8, unaligned pointers) and
+// MLA_ERR_CUDA if the tensor maps cannot be built or the launch fails.
 mla_status_t gemm(cudaStream_t st, const GemmArgs& a, uint32_t* status);
 
 }  // namespace tc
