@@ -314,9 +314,9 @@ namespace mla {
 namespace {
 
 template <typename TA, typename TC>
-mla_status_t proj(mla_handle_t* h, cudaStream_t st, int M, int N, int K, int batch, const TA* A,
-                  long lda, long sA, const TA* B, long ldb, long sB, TC* C, long ldc, long sC,
-                  const float* G = nullptr, long ldg = 0, long sG = 0) {
+mla_status_t proj(mla_handle_t* h, cudaStream_t st, bool pdl, int M, int N, int K, int batch,
+                  const TA* A, long lda, long sA, const TA* B, long ldb, long sB, TC* C, long ldc,
+                  long sC, const float* G = nullptr, long ldg = 0, long sG = 0) {
   h->launches += (M > 0 && N > 0 && batch > 0);
   if constexpr (std::is_same<TA, float>::value) {
     simt::gemm_nt<TA, TC>(st, M, N, K, batch, A, lda, sA, B, ldb, sB, C, ldc, sC, G, ldg, sG);
@@ -325,7 +325,7 @@ mla_status_t proj(mla_handle_t* h, cudaStream_t st, int M, int N, int K, int bat
     tc::Out o = std::is_same<TC, float>::value ? tc::Out::F32
                 : std::is_same<TC, __half>::value ? tc::Out::F16 : tc::Out::BF16;
     tc::GemmArgs a{M, N, K, batch, std::is_same<TA, __half>::value, A, lda, sA, B, ldb, sB,
-                   C, ldc, sC, o, G, ldg, sG};
+                   C, ldc, sC, o, G, ldg, sG, pdl};
     return tc::gemm(st, a, h->status);
   }
 }
@@ -349,7 +349,7 @@ mla_status_t append_impl(mla_handle_t* h, const void* hidden, const int32_t* pos
     h->launches += 1;
     return tc::kv_append(st, h, (const T*)hidden, n, positions, slots, (T*)cache, num_slots);
   } else {
-    mla_status_t s = proj<T, float>(h, st, n, l.L, l.D, 1, (const T*)hidden, l.D, 0,
+    mla_status_t s = proj<T, float>(h, st, false, n, l.L, l.D, 1, (const T*)hidden, l.D, 0,
                                     (const T*)h->WA, l.D, 0, kv_ws, l.L, 0);
     if (s != MLA_OK) return s;
     simt::kv_finish<T>(st, h, kv_ws, l.L, n, positions, slots, (T*)cache, num_slots);
@@ -412,26 +412,31 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
   const long num_slots = (long)num_pages * h->cfg.page_size;
   const bool fused_kv = kBf16 && bslots && 3L * ((M + 127) / 128) >= h->num_sms;
   const int r0 = (bslots && !fused_kv) ? 0 : l.L;
-  mla_status_t s = proj<TX, float>(h, st, M, l.NA - r0, l.D, 1, x, l.D, 0,
+  // the first kernel of the call waits for everything before it; the others
+  // may start early (programmatic dependent launch, bf16 layers) and wait for
+  // their predecessor on the device
+  constexpr bool pdl = kBf16;
+  mla_status_t s = proj<TX, float>(h, st, false, M, l.NA - r0, l.D, 1, x, l.D, 0,
                                    WA + (long)r0 * l.D, l.D, 0, a_out + r0, l.NA, 0);
   if (s != MLA_OK) return s;
   if (bslots) {
     if (fused_kv) {
       if constexpr (kBf16) {
-        s = tc::kv_append(st, h, x, M, pos, bslots, (TX*)cache, num_slots);
+        s = tc::kv_append(st, h, x, M, pos, bslots, (TX*)cache, num_slots, pdl);
         if (s != MLA_OK) return s;
       }
     } else {
-      simt::kv_finish<TX>(st, h, a_out, l.NA, M, pos, bslots, (TX*)cache, num_slots);
+      simt::kv_finish<TX>(st, h, a_out, l.NA, M, pos, bslots, (TX*)cache, num_slots, pdl);
     }
   }
   const float* q_raw;
   long ldq;
   if (l.rq > 0) {
     TI* q_cn = (TI*)(ws + w.q_cn);
-    simt::rmsnorm_rows<TI>(st, a_out + l.L, l.NA, M, l.rq, h->gamma_q, (float)h->cfg.rms_norm_eps, q_cn);
+    simt::rmsnorm_rows<TI>(st, a_out + l.L, l.NA, M, l.rq, h->gamma_q, (float)h->cfg.rms_norm_eps, q_cn,
+                           pdl);
     float* qr = (float*)(ws + w.q_raw);
-    s = proj<TI, float>(h, st, M, l.H * l.dqk, l.rq, 1, q_cn, l.rq, 0, (const TI*)h->Wqb, l.rq,
+    s = proj<TI, float>(h, st, pdl, M, l.H * l.dqk, l.rq, 1, q_cn, l.rq, 0, (const TI*)h->Wqb, l.rq,
                         0, qr, l.H * l.dqk, 0);
     if (s != MLA_OK) return s;
     q_raw = qr;
@@ -443,9 +448,9 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
   TI* q_nope = (TI*)(ws + w.q_nope);
   // Q_abs shares the cache's type: the two meet in the attention contraction
   TX* q_abs = (TX*)(ws + w.q_abs);
-  simt::q_rope_split<TI, TX>(st, h, q_raw, ldq, M, pos, q_nope, q_abs);
+  simt::q_rope_split<TI, TX>(st, h, q_raw, ldq, M, pos, q_nope, q_abs, pdl);
   // q_lat[h] = q_nope[h] @ W_UK[h]  ->  Q_abs[:, h, :rkv]
-  s = proj<TI, TX>(h, st, M, l.rkv, l.dn, l.H, q_nope, (long)l.H * l.dn, l.dn,
+  s = proj<TI, TX>(h, st, pdl, M, l.rkv, l.dn, l.H, q_nope, (long)l.H * l.dn, l.dn,
                    (const TI*)h->WUKT, l.dn, (long)l.rkv * l.dn, q_abs, (long)l.H * l.L, l.L);
   if (s != MLA_OK) return s;
   TI* o_lat = (TI*)(ws + w.o_lat);
@@ -453,7 +458,7 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
     simt::latent_attention<TI, TX>(st, h, q_abs, (const TX*)cache, num_pages, d, pos, o_lat);
   } else {
     s = tc::latent_attention(st, h, q_abs, (const TX*)cache, num_pages, d, pos, o_lat,
-                             (float*)(ws + w.part));
+                             (float*)(ws + w.part), pdl);
     if (s != MLA_OK) return s;
     const int sp = tc::attn_splits(h, M);
     h->launches += (sp > 1) + (sp > 1 && d.vis_stats);   // merge, visibility-stat init
@@ -461,11 +466,11 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
   // o[h] = o_lat[h] @ W_UV[h]^T (* sigmoid(gate))
   TI* o = (TI*)(ws + w.o);
   const float* gate = l.gdim ? a_out + l.L + l.qdim : nullptr;
-  s = proj<TI, TI>(h, st, M, l.dv, l.rkv, l.H, o_lat, (long)l.H * l.rkv, l.rkv,
+  s = proj<TI, TI>(h, st, pdl, M, l.dv, l.rkv, l.H, o_lat, (long)l.H * l.rkv, l.rkv,
                    (const TI*)h->WUV, l.rkv, (long)l.dv * l.rkv, o, (long)l.H * l.dv, l.dv, gate,
                    l.NA, l.dv);
   if (s != MLA_OK) return s;
-  s = proj<TI, TX>(h, st, M, l.D, l.H * l.dv, 1, o, (long)l.H * l.dv, 0, (const TI*)h->Wo,
+  s = proj<TI, TX>(h, st, pdl, M, l.D, l.H * l.dv, 1, o, (long)l.H * l.dv, 0, (const TI*)h->Wo,
                    (long)l.H * l.dv, 0, (TX*)out, l.D, 0);
   if (s != MLA_OK) return s;
   // non-GEMM kernels: [kv finish], [q norm], rope split, attention

@@ -89,6 +89,8 @@ __global__ void __launch_bounds__(THREADS, 1) kv_append_tc_kernel(const __grid_c
   cluster_sync_all();             // peers' barriers exist before any multicast lands
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) pdl_trigger();
+  pdl_wait();
 
   if (warp == 0 && lane == 0) {
     // the hidden rows of a k-block are pulled into L2 2*STAGES k-blocks ahead
@@ -232,7 +234,7 @@ __global__ void __launch_bounds__(THREADS, 1) kv_append_tc_kernel(const __grid_c
 
 mla_status_t kv_append(cudaStream_t st, const mla_handle* h, const __nv_bfloat16* hidden, int M,
                        const int32_t* positions, const int64_t* slots, __nv_bfloat16* cache,
-                       long num_slots) {
+                       long num_slots, bool pdl) {
   const Layout& l = h->lay;
   if (l.rkv != 512 || l.dr != 64)
     return fail(MLA_ERR_UNSUPPORTED, "tcgen05 append: needs kv_lora_rank 512, qk_rope_head_dim 64");
@@ -258,19 +260,9 @@ mla_status_t kv_append(cudaStream_t st, const mla_handle* h, const __nv_bfloat16
   std::call_once(once, [] {
     cudaFuncSetAttribute(kv_append_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   });
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(CL, CR * ((M + CR * BM - 1) / (CR * BM)), 1);
-  cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL;
-  attr[0].val.clusterDim.y = CR;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kv_append_tc_kernel, P);
+  Launch L(dim3(CL, CR * ((M + CR * BM - 1) / (CR * BM)), 1), dim3(THREADS), SMEM_BYTES, st, pdl,
+           dim3(CL, CR, 1));
+  const cudaError_t e = cudaLaunchKernelEx(&L.cfg, kv_append_tc_kernel, P);
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 append launch");
   return MLA_OK;
 }

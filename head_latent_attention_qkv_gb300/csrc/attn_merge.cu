@@ -18,6 +18,8 @@ constexpr int DV = 512;  // latent value width
 __global__ void __launch_bounds__(256)
 merge_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part, int splits,
              long rows, __half* __restrict__ o_lat, int32_t* vis_stats, int H) {
+  pdl_trigger();
+  pdl_wait();
   const long row = blockIdx.x * 8L + threadIdx.x / 32;   // one warp per row
   const int lane = threadIdx.x % 32;
   if (row >= rows) return;
@@ -52,6 +54,8 @@ merge_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_par
 }
 
 __global__ void vis_init_kernel(int32_t* vis_stats, long tokens) {
+  pdl_trigger();
+  pdl_wait();
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < tokens; i += (long)gridDim.x * blockDim.x) {
     vis_stats[i * 3 + 0] = 0;
     vis_stats[i * 3 + 1] = 0x7fffffff;
@@ -62,14 +66,15 @@ __global__ void vis_init_kernel(int32_t* vis_stats, long tokens) {
 }  // namespace
 
 void merge_splits(cudaStream_t st, const float* o_part, const float* lse_part, int splits,
-                  long rows, __half* o_lat, int32_t* vis_stats, int H) {
-  merge_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(o_part, lse_part, splits, rows, o_lat,
-                                                           vis_stats, H);
+                  long rows, __half* o_lat, int32_t* vis_stats, int H, bool pdl) {
+  Launch L(dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, st, pdl);
+  cudaLaunchKernelEx(&L.cfg, merge_kernel, o_part, lse_part, splits, rows, o_lat, vis_stats, H);
 }
 
-void init_vis_stats(cudaStream_t st, int32_t* vis_stats, long tokens) {
-  vis_init_kernel<<<(unsigned)((tokens + 255) / 256 < 1024 ? (tokens + 255) / 256 : 1024), 256, 0, st>>>(
-      vis_stats, tokens);
+void init_vis_stats(cudaStream_t st, int32_t* vis_stats, long tokens, bool pdl) {
+  Launch L(dim3((unsigned)((tokens + 255) / 256 < 1024 ? (tokens + 255) / 256 : 1024)), dim3(256), 0,
+           st, pdl);
+  cudaLaunchKernelEx(&L.cfg, vis_init_kernel, vis_stats, tokens);
 }
 
 }  // namespace tc

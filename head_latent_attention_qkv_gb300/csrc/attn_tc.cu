@@ -324,6 +324,8 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
   cluster_sync_all();          // the peer's barriers exist before anyone multicasts to them
   tc_fence_after();
   const uint32_t tmem = B->tmem_slot;
+  if (tid == 0) pdl_trigger();
+  pdl_wait();                  // Q_abs and the block's own latents come from the kernels before
 
   if (warp == 4) {
     // the cache row of every page this CTA reads, looked up once by the warp
@@ -499,7 +501,7 @@ namespace tc {
 mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_bfloat16* q_abs,
                               const __nv_bfloat16* cache, int num_pages,
                               const mla_attn_desc_t& d, const int32_t* positions, __half* o_lat,
-                              float* part) {
+                              float* part, bool pdl) {
   const Layout& l = h->lay;
   const int ps = h->cfg.page_size;
   if (l.rkv != 512 || l.dr != 64)
@@ -540,26 +542,19 @@ mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_b
   P.rows = rows;
   P.o_part = part;
   P.lse_part = part + (size_t)splits * rows * 512;
-  if (splits > 1 && d.vis_stats) init_vis_stats(st, d.vis_stats, tokens);
+  if (splits > 1 && d.vis_stats) {
+    init_vis_stats(st, d.vis_stats, tokens, pdl);
+    pdl = true;
+  }
   static std::once_flag once;
   std::call_once(once, [] {
     cudaFuncSetAttribute(latent_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   });
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * d.num_blocks * P.tiles_per_block, splits, 1);
-  cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, latent_attn_tc_kernel, P);
+  Launch L(dim3(2 * d.num_blocks * P.tiles_per_block, splits, 1), dim3(THREADS), SMEM_BYTES, st, pdl,
+           dim3(2, 1, 1));
+  const cudaError_t e = cudaLaunchKernelEx(&L.cfg, latent_attn_tc_kernel, P);
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 attention launch");
-  if (splits > 1) merge_splits(st, P.o_part, P.lse_part, splits, rows, o_lat, d.vis_stats, l.H);
+  if (splits > 1) merge_splits(st, P.o_part, P.lse_part, splits, rows, o_lat, d.vis_stats, l.H, true);
   return MLA_OK;
 }
 

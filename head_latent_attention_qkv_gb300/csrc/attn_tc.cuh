@@ -38,13 +38,15 @@ struct AttnParams {
 // holds the partial outputs merged by log-sum-exp.
 int attn_splits(const mla_handle* h, long tokens);
 size_t attn_split_floats(const mla_handle* h, long tokens);
+// `pdl`: the kernels may start while the previous kernel of the stream
+// finishes (programmatic stream serialization; they wait for it on the device).
 mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_bfloat16* q_abs,
                               const __nv_bfloat16* cache, int num_pages,
                               const mla_attn_desc_t& desc, const int32_t* positions,
-                              __half* o_lat, float* part);
+                              __half* o_lat, float* part, bool pdl = false);
 void merge_splits(cudaStream_t st, const float* o_part, const float* lse_part, int splits,
-                  long rows, __half* o_lat, int32_t* vis_stats, int H);
-void init_vis_stats(cudaStream_t st, int32_t* vis_stats, long tokens);
+                  long rows, __half* o_lat, int32_t* vis_stats, int H, bool pdl = false);
+void init_vis_stats(cudaStream_t st, int32_t* vis_stats, long tokens, bool pdl = false);
 
 }  // namespace tc
 }  // namespace mla

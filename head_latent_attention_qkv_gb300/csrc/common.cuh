@@ -38,6 +38,19 @@ __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {
   if (status) atomicOr(status, bits);
 }
 
+// ---- programmatic dependent launch (device) -----------------------------------
+// Every kernel of the library calls pdl_wait() before it touches the outputs
+// of earlier kernels of the same call and before it exits, so that a kernel
+// started early never completes before its predecessor: completion stays
+// ordered along the stream.
+// Block until the previous kernel of the stream (when this one was launched
+// with programmatic stream serialization) has completed and its writes are
+// visible; a no-op otherwise.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next kernel of the stream start launching (its CTAs are scheduled
+// once every CTA of this grid has done this or exited).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- derived layout of one layer (host handle) ------------------------------
 struct Layout {
   int D, H, rq, rkv, dn, dr, dv, L, dqk;
@@ -52,6 +65,38 @@ struct Layout {
 bool make_layout(const mla_config_t& c, Layout* out);
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Launch configuration with optional programmatic stream serialization (the
+// kernel may start while the previous kernel of the stream finishes; it calls
+// griddepcontrol.wait before touching that kernel's outputs) and optional
+// thread-block cluster dimensions.
+struct Launch {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[2];
+  Launch(dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+         dim3 cluster = dim3(1, 1, 1)) {
+    cfg = cudaLaunchConfig_t{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    int n = 0;
+    if (cluster.x * cluster.y * cluster.z > 1) {
+      attr[n].id = cudaLaunchAttributeClusterDimension;
+      attr[n].val.clusterDim.x = cluster.x;
+      attr[n].val.clusterDim.y = cluster.y;
+      attr[n].val.clusterDim.z = cluster.z;
+      ++n;
+    }
+    if (pdl) {
+      attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[n].val.programmaticStreamSerializationAllowed = 1;
+      ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+  }
+};
 
 }  // namespace mla
 

@@ -123,6 +123,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int ng = (int)((long)(ks + 1) * ng_all / splitk) - g0;
   constexpr uint32_t TMEM_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
 
+  // B (weights) does not depend on the previous kernel: its first stages are
+  // requested before anything else, then A once that kernel has finished
+  const int first = ng < STAGES ? ng : STAGES;
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
@@ -132,17 +135,25 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     mbar_init(accum, 1);
     fence_mbar_init();
+    for (int g = 0; g < first; ++g) {
+      mbar_arrive_expect_tx(&full[g], S::STAGE_BYTES);
+      tma_load_4d(smem + g * S::STAGE_BYTES + S::A_BYTES, &tmB, &full[g], 0, n0, (g0 + g) * KBS, z);
+    }
+    pdl_trigger();
   }
   if (warp == 2) tmem_alloc(tmem_slot, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();                     // A, the gate and C belong to the kernels around this one
 
   if (warp == 0 && lane == 0) {
     // producer: one copy per operand per stage (KBS k-blocks)
+    for (int g = 0; g < first; ++g)
+      tma_load_4d(smem + g * S::STAGE_BYTES, &tmA, &full[g], 0, m0, (g0 + g) * KBS, z);
     bool ok = true;
-    for (int g = 0; g < ng && ok; ++g) {
+    for (int g = first; g < ng && ok; ++g) {
       const int s = g % STAGES;
       ok = mbar_wait(&empty[s], ((g / STAGES) & 1) ^ 1, status);
       if (!ok) break;
@@ -202,32 +213,42 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   __syncthreads();
   if (splitk > 1) cluster_sync_all();      // every partial of the cluster is in place
   // ---- sum the partials of this CTA's rows (rank order), epilogue, store:
-  // lane l of a warp holds columns 4l .. 4l+3 of every 128-column group ----
+  // work items are (row, 128-column group); lane l holds columns 4l .. 4l+3
+  // of its item; a warp takes items warp, warp + 4, ... four at a time so
+  // that their shared-memory loads are in flight together ----
+  constexpr int CG = (BN + 127) / 128, U = 4;
   const int r_lo = ks * BM / splitk, r_hi = (ks + 1) * BM / splitk;
-  for (int r = r_lo + warp; r < r_hi; r += THREADS / 32) {
-    const int row = m0 + r;
-#pragma unroll 1
-    for (int cg = 0; cg < BN; cg += 128) {
-      const int col = cg + 4 * lane;
-      if (col >= BN) break;
-      const uint32_t off = smem_u32(smem + r * S::PITCH + col * 4);
-      float4 v;
-      if (splitk > 1) {
-        // all partials first (independent loads in flight), then the sum in rank order
-        float4 t[8];
+  const int items = (r_hi - r_lo) * CG;
+  for (int base = warp; base < items; base += U * (THREADS / 32)) {
+    float4 v[U];
+    uint32_t off[U];
+    bool live[U];
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (q < splitk) t[q] = ld_peer_v4(mapa(off, (uint32_t)q));
-        v = t[0];
+    for (int u = 0; u < U; ++u) {
+      const int it = base + u * (THREADS / 32);
+      const int r = r_lo + it / CG, col = (it % CG) * 128 + 4 * lane;
+      live[u] = it < items && col < BN;
+      off[u] = smem_u32(smem + (live[u] ? r : 0) * S::PITCH + (live[u] ? col : 0) * 4);
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (splitk > 1) {
+      for (int q = 0; q < splitk; ++q) {          // rank order: the same sum in every run
+        float4 t[U];
 #pragma unroll
-        for (int q = 1; q < 8; ++q)
-          if (q < splitk) { v.x += t[q].x; v.y += t[q].y; v.z += t[q].z; v.w += t[q].w; }
-      } else {
-        v = ld_own_v4(off);
+        for (int u = 0; u < U; ++u) t[u] = ld_peer_v4(mapa(off[u], (uint32_t)q));
+#pragma unroll
+        for (int u = 0; u < U; ++u) { v[u].x += t[u].x; v[u].y += t[u].y; v[u].z += t[u].z; v[u].w += t[u].w; }
       }
-      const int n = n0 + col;
-      if (row >= M || n >= N) continue;
-      float o[4] = {v.x, v.y, v.z, v.w};
+    } else {
+#pragma unroll
+      for (int u = 0; u < U; ++u) v[u] = ld_own_v4(off[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int it = base + u * (THREADS / 32);
+      const int row = m0 + r_lo + it / CG, n = n0 + (it % CG) * 128 + 4 * lane;
+      if (!live[u] || row >= M || n >= N) continue;
+      float o[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
       if (G) {
         const float* g = G + z * sG + (long)row * ldg + n;
 #pragma unroll
@@ -312,19 +333,9 @@ mla_status_t launch(cudaStream_t st, const GemmArgs& a, int splitk, uint32_t* st
   std::call_once(once, [&] {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
   });
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.N + BN - 1) / BN, (a.M + BM - 1) / BM, a.batch * splitk);
-  cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = S::BYTES;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = splitk;
-  cfg.attrs = attr;
-  cfg.numAttrs = splitk > 1 ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, a.M, a.N, a.K, (TC*)a.C, a.ldc, a.sC,
+  Launch L(dim3((a.N + BN - 1) / BN, (a.M + BM - 1) / BM, a.batch * splitk), dim3(THREADS), S::BYTES,
+           st, a.pdl, dim3(1, 1, splitk));
+  const cudaError_t e = cudaLaunchKernelEx(&L.cfg, kern, ta, tb, a.M, a.N, a.K, (TC*)a.C, a.ldc, a.sC,
                                            a.G, a.ldg, a.sG, idesc_f16(BM, BN, a.fp16), splitk, status);
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 gemm launch");
   return MLA_OK;

@@ -17,6 +17,7 @@ struct GemmArgs {
   const void* B; long ldb, sB;   // [batch][N][K]
   void* C; long ldc, sC; Out out;
   const float* G; long ldg, sG;  // optional sigmoid gate, same indexing as C
+  bool pdl = false;              // may start while the previous kernel of the stream finishes
 };
 
 // Tile width (64, 128 or 256 columns) and split-K factor (CTAs of a cluster

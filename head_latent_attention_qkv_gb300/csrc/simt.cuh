@@ -1,4 +1,6 @@
 // SIMT (CUDA-core, fp32-accumulate) kernels of the MLA draft layer.
+// `pdl`: launch with programmatic stream serialization (the kernel waits for
+// the previous kernel of the stream with griddepcontrol.wait).
 //
 // These are the production path for the fp32 configuration (tensor-core
 // TF32 would not meet a 1e-4 relative tolerance) and the first, plain
@@ -27,18 +29,19 @@ void gemm_nt(cudaStream_t st, int M, int N, int K, int batch,
 // cache[slot] = [RMSNorm(kv[:rkv]) * gamma | RoPE(kv[rkv:], pos)].
 template <typename T>
 void kv_finish(cudaStream_t st, const mla_handle* h, const float* kv, long ld, int n,
-               const int32_t* positions, const int64_t* slots, T* cache, long num_slots);
+               const int32_t* positions, const int64_t* slots, T* cache, long num_slots,
+               bool pdl = false);
 
 // out[m][:] = RMSNorm(in[m][:n]) * gamma  (in fp32 with row stride ld).
 template <typename T>
 void rmsnorm_rows(cudaStream_t st, const float* in, long ld, int M, int n,
-                  const float* gamma, float eps, T* out);
+                  const float* gamma, float eps, T* out, bool pdl = false);
 
 // q [M, H, dqk] fp32 (row stride ldq) -> q_nope [M, H, dn] and the rotated
 // rope part into Q_abs[m, h, rkv:rkv+dr].
 template <typename TN, typename TQ>
 void q_rope_split(cudaStream_t st, const mla_handle* h, const float* q, long ldq, int M,
-                  const int32_t* positions, TN* q_nope, TQ* q_abs);
+                  const int32_t* positions, TN* q_nope, TQ* q_abs, bool pdl = false);
 
 // out[i] = (T) in[i] for n elements.
 template <typename T>

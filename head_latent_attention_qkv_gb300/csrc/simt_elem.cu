@@ -39,6 +39,8 @@ kv_finish_kernel(const float* __restrict__ kv, long ld, const int32_t* __restric
                  int rkv, int dr, float eps, const float* __restrict__ gamma,
                  const float2* __restrict__ rope, int max_pos, int interleaved,
                  uint32_t* status) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x;
   const float* row = kv + (long)t * ld;
   const long slot = slots[t];
@@ -71,6 +73,8 @@ template <typename T>
 __global__ void __launch_bounds__(ROW_THREADS)
 rmsnorm_rows_kernel(const float* __restrict__ in, long ld, int n, const float* __restrict__ gamma,
                     float eps, T* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const float* row = in + (long)blockIdx.x * ld;
   float ss = 0.f;
   for (int i = threadIdx.x; i < n; i += ROW_THREADS) ss = fmaf(row[i], row[i], ss);
@@ -88,6 +92,8 @@ q_rope_split_kernel(const float* __restrict__ q, long ldq, const int32_t* __rest
                     int M, int H, int dn, int dr, int rkv, const float2* __restrict__ rope,
                     int max_pos, int interleaved, uint32_t* status, TN* __restrict__ q_nope,
                     TQ* __restrict__ q_abs) {
+  pdl_trigger();
+  pdl_wait();
   const long w = (blockIdx.x * (long)ROW_THREADS + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
   if (w >= (long)M * H) return;
@@ -117,6 +123,7 @@ q_rope_split_kernel(const float* __restrict__ q, long ldq, const int32_t* __rest
 
 template <typename T>
 __global__ void f32_to_kernel(const float* __restrict__ in, T* __restrict__ out, long n) {
+  pdl_wait();
   for (long i = (blockIdx.x * (long)blockDim.x + threadIdx.x) * 4; i < n; i += (long)gridDim.x * blockDim.x * 4) {
     if (i + 4 <= n) {
       const float4 v = *reinterpret_cast<const float4*>(in + i);
@@ -141,46 +148,49 @@ template void f32_to<__nv_bfloat16>(cudaStream_t, const float*, __nv_bfloat16*, 
 
 template <typename T>
 void kv_finish(cudaStream_t st, const mla_handle* h, const float* kv, long ld, int n,
-               const int32_t* positions, const int64_t* slots, T* cache, long num_slots) {
+               const int32_t* positions, const int64_t* slots, T* cache, long num_slots, bool pdl) {
   if (n <= 0) return;
   const Layout& l = h->lay;
-  kv_finish_kernel<T><<<n, ROW_THREADS, 0, st>>>(
-      kv, ld, positions, slots, cache, num_slots, l.rkv, l.dr, (float)h->cfg.rms_norm_eps,
-      h->gamma_kv, h->rope, h->cfg.max_position, h->cfg.rope == MLA_ROPE_INTERLEAVED, h->status);
+  Launch L(dim3(n), dim3(ROW_THREADS), 0, st, pdl);
+  cudaLaunchKernelEx(&L.cfg, kv_finish_kernel<T>, kv, ld, positions, slots, cache, num_slots, l.rkv,
+                     l.dr, (float)h->cfg.rms_norm_eps, h->gamma_kv, h->rope, h->cfg.max_position,
+                     (int)(h->cfg.rope == MLA_ROPE_INTERLEAVED), h->status);
 }
 
 template <typename T>
 void rmsnorm_rows(cudaStream_t st, const float* in, long ld, int M, int n, const float* gamma,
-                  float eps, T* out) {
+                  float eps, T* out, bool pdl) {
   if (M <= 0) return;
-  rmsnorm_rows_kernel<T><<<M, ROW_THREADS, 0, st>>>(in, ld, n, gamma, eps, out);
+  Launch L(dim3(M), dim3(ROW_THREADS), 0, st, pdl);
+  cudaLaunchKernelEx(&L.cfg, rmsnorm_rows_kernel<T>, in, ld, n, gamma, eps, out);
 }
 
 template <typename TN, typename TQ>
 void q_rope_split(cudaStream_t st, const mla_handle* h, const float* q, long ldq, int M,
-                  const int32_t* positions, TN* q_nope, TQ* q_abs) {
+                  const int32_t* positions, TN* q_nope, TQ* q_abs, bool pdl) {
   if (M <= 0) return;
   const Layout& l = h->lay;
   const long warps = (long)M * l.H, per_block = ROW_THREADS / 32;
-  q_rope_split_kernel<TN, TQ><<<(unsigned)((warps + per_block - 1) / per_block), ROW_THREADS, 0, st>>>(
-      q, ldq, positions, M, l.H, l.dn, l.dr, l.rkv, h->rope, h->cfg.max_position,
-      h->cfg.rope == MLA_ROPE_INTERLEAVED, h->status, q_nope, q_abs);
+  Launch L(dim3((unsigned)((warps + per_block - 1) / per_block)), dim3(ROW_THREADS), 0, st, pdl);
+  cudaLaunchKernelEx(&L.cfg, q_rope_split_kernel<TN, TQ>, q, ldq, positions, M, l.H, l.dn, l.dr,
+                     l.rkv, h->rope, h->cfg.max_position, (int)(h->cfg.rope == MLA_ROPE_INTERLEAVED),
+                     h->status, q_nope, q_abs);
 }
 
 #define MLA_INST(T)                                                                          \
   template void kv_finish<T>(cudaStream_t, const mla_handle*, const float*, long, int,      \
-                             const int32_t*, const int64_t*, T*, long);                     \
+                             const int32_t*, const int64_t*, T*, long, bool);               \
   template void rmsnorm_rows<T>(cudaStream_t, const float*, long, int, int, const float*,   \
-                                float, T*);
+                                float, T*, bool);
 MLA_INST(float)
 MLA_INST(__nv_bfloat16)
 MLA_INST(__half)
 #undef MLA_INST
 template void q_rope_split<float, float>(cudaStream_t, const mla_handle*, const float*, long, int,
-                                         const int32_t*, float*, float*);
+                                         const int32_t*, float*, float*, bool);
 template void q_rope_split<__half, __nv_bfloat16>(cudaStream_t, const mla_handle*, const float*,
                                                   long, int, const int32_t*, __half*,
-                                                  __nv_bfloat16*);
+                                                  __nv_bfloat16*, bool);
 
 }  // namespace simt
 }  // namespace mla

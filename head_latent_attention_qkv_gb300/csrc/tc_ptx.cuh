@@ -320,3 +320,4 @@ __device__ __forceinline__ void tmem_st16_u(uint32_t taddr, const uint32_t* v) {
 
 }  // namespace tc
 }  // namespace mla
+
