@@ -3,20 +3,24 @@
 //   kv = hidden @ W_kva^T                     (W_kva: the kv_lora_rank + qk_rope rows)
 //   cache[slot] = [RMSNorm(kv[:512]) * gamma | RoPE(kv[512:], position)]   (bf16)
 //
-// A cluster of 3 x 2 CTAs owns 256 token rows: CTA (c, r) computes output
-// columns [192c, 192c + 192) of rows [128r, 128r + 128) in tensor memory.
+// Persistent kernel.  A cluster of 3 x 2 CTAs works on 256 token rows at a
+// time (a "cluster tile") and loops over cluster tiles: CTA (c, r) computes
+// output columns [192c, 192c + 192) of rows [128r, 128r + 128) of the tile.
 // Every 128 x 64 slice of hidden states is multicast to the three CTAs of its
 // row group and every 192 x 64 slice of weights to the two CTAs of its column
-// group, so each cluster reads its hidden rows and each weight slice once.  A
+// group, so each cluster reads its hidden rows and each weight slice once; a
 // TMA copy costs about the same SM time whatever its size, so the copies of a
 // k-block are issued by different CTAs in turn (hidden: CTA c = kb mod 3 of
-// the row group, weights: CTA r = kb mod 2 of the column group), each SM
-// issuing less than one copy per k-block.  In the epilogue every CTA adds the
-// squares of its latent columns per row, the three partial sums of a row
-// group are exchanged through distributed shared memory and added in the same
-// order everywhere, and each CTA normalises, rotates (column CTA 2 holds the
-// 64 rope columns) and stores its part of every row straight to the row's
-// cache slot.
+// the row group, weights: CTA r = kb mod 2 of the column group).
+//
+// Warp 0 streams the ring, warp 1 issues the MMAs into one of two tensor-
+// memory accumulators (192 columns each), warps 2-5 run the epilogue of the
+// previous tile meanwhile: per row the sum of squares of its latent columns,
+// exchanged with the two other column CTAs of the row group through
+// asynchronous distributed-shared-memory stores (counted on an mbarrier) and
+// added in the same order everywhere; then normalisation, RoPE (column CTA 2
+// holds the 64 rope columns), bf16 rows staged in shared memory and written
+// to the rows' cache slots as whole 384-byte segments.
 #include "append_tc.cuh"
 
 #include <mutex>
@@ -28,14 +32,20 @@ namespace mla {
 namespace tc {
 namespace {
 
-constexpr int BM = 128, BN = 192, BK = 64, THREADS = 128, STAGES = 5;
+constexpr int BM = 128, BN = 192, BK = 64, STAGES = 4;
 constexpr int CL = 3, CR = 2, NCTA = CL * CR;     // cluster: 3 column CTAs x 2 row groups
+constexpr int THREADS = 192;                      // TMA, MMA, 4 epilogue warps
+constexpr int EPI = 128;                          // epilogue threads
 constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int OFF_BAR = STAGES * STAGE_BYTES;
-constexpr int SMEM_BYTES = 1024 + OFF_BAR + 2048;
-constexpr uint32_t TMEM_COLS = 256;
 constexpr int OUT_PITCH = BN * 2 + 16;            // staged output row (bytes), bank-conflict free
-static_assert(BM * OUT_PITCH + BM * 8 <= OFF_BAR, "output staging fits in the pipeline stages");
+constexpr int OFF_OUT = STAGES * STAGE_BYTES;     // staged rows [BM][OUT_PITCH]
+constexpr int OFF_SLOT = OFF_OUT + BM * OUT_PITCH;  // cache slot per staged row [BM] (-1: none)
+constexpr int OFF_RED = OFF_SLOT + BM * 8;        // partial sums of squares [2][CL][BM]
+constexpr int OFF_GAM = OFF_RED + 2 * CL * BM * 4;  // this CTA's kv_a_layernorm gains [BN]
+constexpr int OFF_BAR = OFF_GAM + BN * 4;
+constexpr int SMEM_BYTES = 1024 + OFF_BAR + 256;
+constexpr uint32_t TMEM_COLS = 512, ACC_STRIDE = 256;   // two accumulators of BN columns
+static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 struct AppendParams {
   CUtensorMap tmA;            // hidden [M, D]
@@ -52,182 +62,255 @@ struct AppendParams {
   uint32_t* status;
 };
 
+struct Bars {
+  uint64_t full[STAGES], empty[STAGES];   // ring: bytes landed / all six CTAs done with the slot
+  uint64_t acc_full[2], acc_empty[2];     // accumulator b written (MMA) / read (epilogue)
+  uint64_t red_full[2];                   // the two peers' partial sums of tile parity b landed
+  uint64_t red_free[2];                   // the two peers have read what this CTA sent them
+  uint64_t drain;                         // every MMA of the CTA complete
+  uint32_t tmem_slot;
+  int abort;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+// Bounded waits that give up at once after any earlier timeout of this CTA.
+__device__ __forceinline__ bool wait_bar(Bars* B, uint64_t* bar, uint32_t parity, uint32_t* st) {
+  if (*(volatile int*)&B->abort) return false;
+  if (mbar_wait_cluster(bar, parity, st)) return true;
+  B->abort = 1;
+  return false;
+}
+
+__device__ __forceinline__ void st_async_b32(uint32_t remote_addr, float v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+               ::"r"(remote_addr), "r"(__float_as_uint(v)), "r"(remote_bar) : "memory");
+}
+// Barrier 1 among the 128 epilogue threads only.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 __global__ void __launch_bounds__(THREADS, 1) kv_append_tc_kernel(const __grid_constant__ AppendParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t* full = (uint64_t*)(smem + OFF_BAR);
-  uint64_t* empty = full + STAGES;
-  uint64_t* accum = empty + STAGES;
-  uint32_t* tmem_slot = (uint32_t*)(accum + 1);
-  float* red = (float*)(smem + OFF_BAR + 256);     // per-row partial sum of squares [128]
-  float* gam = red + BM;                           // this CTA's kv_a_layernorm gains [BN]
+  Bars* B = (Bars*)(smem + OFF_BAR);
+  float* red = (float*)(smem + OFF_RED);
+  float* gam = (float*)(smem + OFF_GAM);
 
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const uint32_t rank = cluster_ctarank();         // c + 3 r
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const uint32_t rank = cluster_ctarank();           // c + 3 r
   const int c = (int)rank % CL, rg = (int)rank / CL; // column group (== blockIdx.x), row group
-  const int m0 = blockIdx.y * BM, n0 = c * BN;
+  const int n0 = c * BN;
   const int nk = (P.K + BK - 1) / BK;
-  // a slot is refilled once all six CTAs are done with it
+  const int n_ct = (P.M + CR * BM - 1) / (CR * BM);  // cluster tiles of 256 rows
+  const int cid = blockIdx.y / CR, ncl = gridDim.y / CR;
   const uint16_t all_mask = (uint16_t)((1u << NCTA) - 1);
   const uint16_t row_mask = (uint16_t)(0x7u << (CL * rg));            // CTAs of this row group
   const uint16_t col_mask = (uint16_t)((1u << c) | (1u << (c + CL)));  // CTAs of this column group
 
-  if (threadIdx.x == 0) {
-    prefetch_tmap(&P.tmA);
-    prefetch_tmap(&P.tmB);
+  if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], NCTA);
+      mbar_init(&B->full[s], 1);
+      mbar_init(&B->empty[s], NCTA);
     }
-    mbar_init(accum, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&B->acc_full[b], 1);
+      mbar_init(&B->acc_empty[b], EPI);
+      mbar_init(&B->red_full[b], 1);
+      mbar_init(&B->red_free[b], 2 * (EPI / 32));   // 4 warps of each of the two peers
+    }
+    mbar_init(&B->drain, 1);
+    B->abort = 0;
     fence_mbar_init();
+    // the first use of each partial-sum buffer expects both peers' rows
+    for (int b = 0; b < 2; ++b) mbar_arrive_expect_tx(&B->red_full[b], 2 * BM * 4);
   }
-  if (warp == 2) tmem_alloc(tmem_slot, TMEM_COLS);
-  for (int i = threadIdx.x; i < BN; i += THREADS) gam[i] = n0 + i < 512 ? P.gamma[n0 + i] : 0.f;
+  for (int i = tid; i < BN; i += THREADS) gam[i] = n0 + i < 512 ? P.gamma[n0 + i] : 0.f;
+  if (warp == 1) tmem_alloc(&B->tmem_slot, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();             // peers' barriers exist before any multicast lands
+  cluster_sync_all();             // peers' barriers exist before any multicast or remote store
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  if (threadIdx.x == 0) pdl_trigger();
+  const uint32_t tmem = B->tmem_slot;
+  if (tid == 0) pdl_trigger();
   pdl_wait();
 
-  if (warp == 0 && lane == 0) {
-    // the hidden rows of a k-block are pulled into L2 2*STAGES k-blocks ahead
-    // of their load, by the CTA that will load them
-    auto prefetch = [&](int kb) {
-      if (kb < nk && kb % CL == c) tma_prefetch_3d(&P.tmA, kb * BK, m0, 0);
-    };
-    for (int kb = STAGES; kb < 2 * STAGES; ++kb) prefetch(kb);
-    bool ok = true;
-    for (int kb = 0; kb < nk && ok; ++kb) {
-      const int s = kb % STAGES;
-      ok = mbar_wait_cluster(&empty[s], ((kb / STAGES) & 1) ^ 1, P.status);
-      if (!ok) break;
-      uint8_t* a = smem + s * STAGE_BYTES;
-      mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-      if (kb % CL == c) tma_load_3d_mc(a, &P.tmA, &full[s], kb * BK, m0, 0, row_mask);
-      if (kb % CR == rg) tma_load_3d_mc(a + A_BYTES, &P.tmB, &full[s], kb * BK, n0, 0, col_mask);
-      prefetch(kb + 2 * STAGES);
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- TMA producer ----
+      prefetch_tmap(&P.tmA);
+      prefetch_tmap(&P.tmB);
+      int g = 0;
+      bool ok = true;
+      for (int ct = cid; ct < n_ct && ok; ct += ncl) {
+        const int m0 = (ct * CR + rg) * BM;
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int s = g % STAGES;
+          if (!wait_bar(B, &B->empty[s], ((g / STAGES) & 1) ^ 1, P.status)) { ok = false; break; }
+          uint8_t* a = smem + s * STAGE_BYTES;
+          mbar_arrive_expect_tx(&B->full[s], STAGE_BYTES);
+          if (kb % CL == c) tma_load_3d_mc(a, &P.tmA, &B->full[s], kb * BK, m0, 0, row_mask);
+          if (kb % CR == rg) tma_load_3d_mc(a + A_BYTES, &P.tmB, &B->full[s], kb * BK, n0, 0, col_mask);
+          // the hidden rows of a later k-block are pulled into L2 by their loader
+          const int kp = kb + 2 * STAGES;
+          if (kp < nk && kp % CL == c) tma_prefetch_3d(&P.tmA, kp * BK, m0, 0);
+        }
+      }
+      // every copy into this CTA has landed before it may exit
+      for (int i = max(0, g - STAGES); i < g; ++i) mbar_wait_cluster(&B->full[i % STAGES], (i / STAGES) & 1, P.status);
     }
-    for (int kb = max(0, nk - STAGES); kb < nk; ++kb)
-      mbar_wait_cluster(&full[kb % STAGES], (kb / STAGES) & 1, P.status);
-  } else if (warp == 1 && lane == 0) {
-    const uint32_t idesc = idesc_f16(BM, BN, false);
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % STAGES;
-      if (!mbar_wait_cluster(&full[s], (kb / STAGES) & 1, P.status)) break;
-      tc_fence_after();
-      const uint8_t* a = smem + s * STAGE_BYTES;
-      const uint64_t da = smem_desc_sw128(a), db = smem_desc_sw128(a + A_BYTES);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer ----
+      const uint32_t idesc = idesc_f16(BM, BN, false);
+      int g = 0, i = 0;
+      bool ok = true;
+      for (int ct = cid; ct < n_ct && ok; ct += ncl, ++i) {
+        const int b = i & 1;
+        if (!wait_bar(B, &B->acc_empty[b], ((i >> 1) & 1) ^ 1, P.status)) break;   // epilogue done with it
+        tc_fence_after();
+        const uint32_t d = tmem + b * ACC_STRIDE;
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int s = g % STAGES;
+          if (!wait_bar(B, &B->full[s], (g / STAGES) & 1, P.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint8_t* a = smem + s * STAGE_BYTES;
+          const uint64_t da = smem_desc_sw128(a), db = smem_desc_sw128(a + A_BYTES);
 #pragma unroll
-      for (int k = 0; k < BK / 16; ++k) mma_f16(tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
-      mma_commit_mc(&empty[s], all_mask);
+          for (int k = 0; k < BK / 16; ++k) mma_f16(d, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+          mma_commit_mc(&B->empty[s], all_mask);
+        }
+        if (ok) mma_commit(&B->acc_full[b]);
+      }
+      // no MMA of this CTA may still run when its tensor memory is freed
+      mma_commit(&B->drain);
+      mbar_wait(&B->drain, 0, P.status);
     }
-    mma_commit(accum);
+  } else {
+    // ---- epilogue (warps 2-5): thread = accumulator row = TMEM lane ----
+    const int q = warp % 4, r = q * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const int lat_cols = c < 2 ? BN : 512 - 2 * BN;    // latent columns held here (rest: rope)
+    uint8_t* out_tile = smem + OFF_OUT;
+    long* out_slot = (long*)(smem + OFF_SLOT);
+    uint4* orow = reinterpret_cast<uint4*>(out_tile + r * OUT_PITCH);
+    int i = 0;
+    for (int ct = cid; ct < n_ct; ct += ncl, ++i) {
+      const int b = i & 1;
+      const uint32_t ph = (i >> 1) & 1;
+      const int m = (ct * CR + rg) * BM + r;
+      // waits that give up leave garbage, but every thread still runs the
+      // same sequence of epilogue barriers
+      const bool have = wait_bar(B, &B->acc_full[b], ph, P.status);
+      tc_fence_after();
+      const uint32_t lane_addr = tmem + b * ACC_STRIDE + lane_off;
+      float ss = 0.f;
+#pragma unroll 1
+      for (int col = 0; col < lat_cols; col += 32) {
+        float v[32];
+        tmem_ld32(lane_addr + col, v);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) ss = fmaf(v[k], v[k], ss);
+      }
+      // partial sum of squares: own slot locally, the two peers' by async stores
+      wait_bar(B, &B->red_free[b], ph ^ 1, P.status);
+      float* rb = red + b * CL * BM;
+      rb[c * BM + r] = ss;
+#pragma unroll
+      for (int k = 1; k < CL; ++k) {
+        const uint32_t peer = (uint32_t)(CL * rg + (c + k) % CL);
+        st_async_b32(mapa(smem_u32(&rb[c * BM + r]), peer), ss, mapa(smem_u32(&B->red_full[b]), peer));
+      }
+      wait_bar(B, &B->red_full[b], ph, P.status);
+      const float tot = (rb[r] + rb[BM + r]) + rb[2 * BM + r];     // same order in all three
+      // this warp is done reading the peers' partials of parity b
+      __syncwarp();
+      if (lane == 0) {
+#pragma unroll
+        for (int k = 1; k < CL; ++k) mbar_arrive_remote(mapa(smem_u32(&B->red_free[b]), (uint32_t)(CL * rg + (c + k) % CL)));
+      }
+      if (r == 0) mbar_arrive_expect_tx(&B->red_full[b], 2 * BM * 4);   // armed for tile i + 2
+      const float rstd = 1.f / sqrtf(tot / 512.f + P.eps);
+      const bool row_ok = have && m < P.M;
+      long slot = 0;
+      int pos = 0;
+      if (row_ok) {
+        slot = P.slots[m];
+        pos = P.positions[m];
+      }
+      const bool bad_slot = row_ok && (slot < 0 || slot >= P.num_slots);
+      const bool bad_pos = row_ok && c == CL - 1 && (pos < 0 || pos >= P.max_pos);
+      if (bad_slot || bad_pos)
+        set_status(P.status, (bad_slot ? MLA_DEV_BAD_SLOT : 0) | (bad_pos ? MLA_DEV_BAD_POSITION : 0));
+      const bool store = row_ok && !bad_slot && !bad_pos;
+      // the row's 192 bf16 outputs -> shared memory
+#pragma unroll 1
+      for (int col = 0; col < lat_cols; col += 32) {
+        float v[32];
+        tmem_ld32(lane_addr + col, v);
+#pragma unroll
+        for (int k = 0; k < 32; k += 8) {
+          __nv_bfloat162 h2[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            h2[u] = __floats2bfloat162_rn(v[k + 2 * u] * rstd * gam[col + k + 2 * u],
+                                          v[k + 2 * u + 1] * rstd * gam[col + k + 2 * u + 1]);
+          orow[(col + k) / 8] = *reinterpret_cast<uint4*>(h2);
+        }
+      }
+      if (c == CL - 1) {
+        // rope columns 512..575 = local 128..191: pair k is (2k, 2k+1) interleaved
+        // or (k, k + 32) NeoX, rotated by angle k of the position
+        float a[32], bb[32];
+        tmem_ld32(lane_addr + lat_cols, a);
+        tmem_ld32(lane_addr + lat_cols + 32, bb);
+        float o[64];
+        const float2* cs = P.rope + (long)(store ? pos : 0) * 32;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          float x, y;
+          if (P.interleaved) {
+            x = k < 16 ? a[2 * k] : bb[2 * k - 32];
+            y = k < 16 ? a[2 * k + 1] : bb[2 * k - 31];
+          } else {
+            x = a[k];
+            y = bb[k];
+          }
+          const float2 t = cs[k];
+          const float rx = x * t.x - y * t.y, ry = y * t.x + x * t.y;
+          if (P.interleaved) { o[2 * k] = rx; o[2 * k + 1] = ry; }
+          else { o[k] = rx; o[k + 32] = ry; }
+        }
+#pragma unroll
+        for (int k = 0; k < 64; k += 8) {
+          __nv_bfloat162 h2[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) h2[u] = __floats2bfloat162_rn(o[k + 2 * u], o[k + 2 * u + 1]);
+          orow[(lat_cols + k) / 8] = *reinterpret_cast<uint4*>(h2);
+        }
+      }
+      // accumulator b may be overwritten by tile i + 2
+      tc_fence_before();
+      mbar_arrive(&B->acc_empty[b]);
+      out_slot[r] = store ? slot : -1;
+      epi_sync();
+      // epilogue warp e writes rows 32e .. 32e+31, lanes 0..23 one 16-byte piece each
+      const int e = warp - 2;
+#pragma unroll 1
+      for (int k = 0; k < 32; ++k) {
+        const int row = e * 32 + k;
+        const long sl = out_slot[row];
+        if (sl >= 0 && lane < BN * 2 / 16)
+          reinterpret_cast<uint4*>(P.cache + sl * 576 + n0)[lane] =
+              reinterpret_cast<const uint4*>(out_tile + row * OUT_PITCH)[lane];
+      }
+      epi_sync();                 // the staging area is free for the next tile
+    }
   }
   __syncwarp();
-
-  // ---- epilogue: RMSNorm across the cluster, RoPE, rows to cache slots ----
-  const bool have = mbar_wait(accum, 0, P.status);
-  tc_fence_after();
-  const int r = warp * 32 + lane, m = m0 + r;
-  const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-  const int lat_cols = c < 2 ? BN : 512 - 2 * BN;      // latent columns held here (rest: rope)
-  float ss = 0.f;
-#pragma unroll 1
-  for (int col = 0; col < BN; col += 32) {
-    float v[32];
-    tmem_ld32(lane_addr + col, v);
-    if (col < lat_cols) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) ss = fmaf(v[i], v[i], ss);
-    }
-  }
-  red[r] = ss;
-  cluster_sync_all();
-  float tot = 0.f;
-#pragma unroll
-  for (int q = 0; q < CL; ++q) tot += ld_cluster_f32(mapa(smem_u32(&red[r]), CL * rg + q));  // same order in all three
-  const float rstd = 1.f / sqrtf(tot / 512.f + P.eps);
-  const bool row_ok = have && m < P.M;
-  long slot = 0;
-  int pos = 0;
-  if (row_ok) {
-    slot = P.slots[m];
-    pos = P.positions[m];
-  }
-  const bool bad_slot = row_ok && (slot < 0 || slot >= P.num_slots);
-  const bool bad_pos = row_ok && c == CL - 1 && (pos < 0 || pos >= P.max_pos);
-  if (bad_slot || bad_pos)
-    set_status(P.status, (bad_slot ? MLA_DEV_BAD_SLOT : 0) | (bad_pos ? MLA_DEV_BAD_POSITION : 0));
-  const bool store = row_ok && !bad_slot && !bad_pos;
-  // the row's 192 bf16 outputs go to shared memory first (the pipeline stages
-  // are free once the accumulator is complete); rows then leave as whole
-  // 384-byte segments written by a warp together
-  uint8_t* out_tile = smem;                                  // [BM][OUT_PITCH]
-  long* out_slot = (long*)(smem + BM * OUT_PITCH);           // [BM], -1 = not stored
-  uint4* orow = reinterpret_cast<uint4*>(out_tile + r * OUT_PITCH);
-#pragma unroll 1
-  for (int col = 0; col < lat_cols; col += 32) {
-    float v[32];
-    tmem_ld32(lane_addr + col, v);
-#pragma unroll
-    for (int i = 0; i < 32; i += 8) {
-      __nv_bfloat162 h2[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        h2[u] = __floats2bfloat162_rn(v[i + 2 * u] * rstd * gam[col + i + 2 * u],
-                                      v[i + 2 * u + 1] * rstd * gam[col + i + 2 * u + 1]);
-      orow[(col + i) / 8] = *reinterpret_cast<uint4*>(h2);
-    }
-  }
-  if (c == CL - 1) {
-    // rope columns 512..575 = local 128..191: pair k is (2k, 2k+1) interleaved
-    // or (k, k + 32) NeoX, rotated by angle k of the position
-    float a[32], b[32];
-    tmem_ld32(lane_addr + lat_cols, a);
-    tmem_ld32(lane_addr + lat_cols + 32, b);
-    float o[64];
-    const float2* cs = P.rope + (long)(store ? pos : 0) * 32;
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      float x, y;
-      if (P.interleaved) {
-        x = k < 16 ? a[2 * k] : b[2 * k - 32];
-        y = k < 16 ? a[2 * k + 1] : b[2 * k - 31];
-      } else {
-        x = a[k];
-        y = b[k];
-      }
-      const float2 t = cs[k];
-      const float rx = x * t.x - y * t.y, ry = y * t.x + x * t.y;
-      if (P.interleaved) { o[2 * k] = rx; o[2 * k + 1] = ry; }
-      else { o[k] = rx; o[k + 32] = ry; }
-    }
-#pragma unroll
-    for (int i = 0; i < 64; i += 8) {
-      __nv_bfloat162 h2[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) h2[u] = __floats2bfloat162_rn(o[i + 2 * u], o[i + 2 * u + 1]);
-      orow[(lat_cols + i) / 8] = *reinterpret_cast<uint4*>(h2);
-    }
-  }
-  out_slot[r] = store ? slot : -1;
-  __syncthreads();
-  // warp w writes rows 32w .. 32w+31, lanes 0..23 one 16-byte piece each
-#pragma unroll 1
-  for (int i = 0; i < 32; ++i) {
-    const int row = warp * 32 + i;
-    const long sl = out_slot[row];
-    if (sl >= 0 && lane < BN * 2 / 16)
-      reinterpret_cast<uint4*>(P.cache + sl * 576 + n0)[lane] =
-          reinterpret_cast<const uint4*>(out_tile + row * OUT_PITCH)[lane];
-  }
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();             // no CTA leaves while a peer may still read its partials
-  if (warp == 2) tmem_dealloc(tmem, TMEM_COLS);
+  cluster_sync_all();             // no CTA leaves while a peer may still multicast, commit or store to it
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
 }  // namespace
@@ -260,8 +343,31 @@ mla_status_t kv_append(cudaStream_t st, const mla_handle* h, const __nv_bfloat16
   std::call_once(once, [] {
     cudaFuncSetAttribute(kv_append_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   });
-  Launch L(dim3(CL, CR * ((M + CR * BM - 1) / (CR * BM)), 1), dim3(THREADS), SMEM_BYTES, st, pdl,
-           dim3(CL, CR, 1));
+  // persistent: as many clusters as fit on the GPU at once, at most one per cluster tile
+  static std::once_flag once_occ;
+  static int max_clusters = 0;
+  std::call_once(once_occ, [] {
+    cudaLaunchConfig_t c = {};
+    c.gridDim = dim3(CL, CR, 1);
+    c.blockDim = dim3(THREADS, 1, 1);
+    c.dynamicSmemBytes = SMEM_BYTES;
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = CL;
+    a[0].val.clusterDim.y = CR;
+    a[0].val.clusterDim.z = 1;
+    c.attrs = a;
+    c.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kv_append_tc_kernel, &c) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      n = 16;
+    }
+    max_clusters = n;
+  });
+  const int n_ct = (M + CR * BM - 1) / (CR * BM);
+  const int ncl = n_ct < max_clusters ? n_ct : max_clusters;
+  Launch L(dim3(CL, CR * ncl, 1), dim3(THREADS), SMEM_BYTES, st, pdl, dim3(CL, CR, 1));
   const cudaError_t e = cudaLaunchKernelEx(&L.cfg, kv_append_tc_kernel, P);
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 append launch");
   return MLA_OK;
