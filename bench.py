@@ -21,7 +21,6 @@ import os
 import statistics
 import subprocess
 import sys
-import threading
 import time
 
 import numpy as np
@@ -69,34 +68,37 @@ def algorithmic_flops(wl):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms by a
+    background nvidia-smi while the GPU runs the warm-up and timed steps."""
     Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index=0):
-        self.samples, self.index, self.stop = [], index, threading.Event()
-
-    def _run(self):
-        while not self.stop.is_set():
-            try:
-                out = subprocess.run(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                      "--format=csv,noheader,nounits"], capture_output=True,
-                                     text=True, timeout=5).stdout.strip()
-                if out:
-                    self.samples.append([x.strip() for x in out.split(",")])
-            except Exception:
-                pass
-            time.sleep(0.2)
+        self.samples, self.index, self.proc = [], index, None
 
     def __enter__(self):
-        self.t = threading.Thread(target=self._run, daemon=True)
-        self.t.start()
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
         return self
 
     def __exit__(self, *a):
-        self.stop.set()
-        self.t.join(timeout=10)
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 6:
+                self.samples.append(f)
 
     def summary(self):
         if not self.samples:
@@ -109,6 +111,28 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
                 "samples": len(self.samples)}
+
+
+def append_traffic():
+    """DRAM bytes per launch of the append kernel from the committed ncu
+    summary, or None when the kernel source changed since that capture."""
+    import hashlib
+    src = os.path.join(ROOT, "head_latent_attention_qkv_gb300", "csrc", "append_tc.cu")
+    summ = os.path.join(ROOT, "profiles", "ncu_kv_append_qwen3_4b_prefill.md")
+    if not (os.path.exists(src) and os.path.exists(summ)):
+        return None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    vals = {}
+    for line in open(summ):
+        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "kernel_source_sha256")):
+            k, v = line.split(":", 1)
+            vals[k.strip().strip("-* `")] = v.strip().strip("` ")
+    if vals.get("kernel_source_sha256") != digest:
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 def measured_peaks():
@@ -144,6 +168,8 @@ def run_ours(args, rank, world):
     append()
     forward()
     launches = int(api._lib.lib.mla_kernel_launches(dev.handle.h) - n0)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.__enter__()
     for _ in range(args.warmup):
         append()
         forward()
@@ -168,15 +194,15 @@ def run_ours(args, rank, world):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(torch.cuda.current_device()) as clocks:
-        for k in range(args.steps):
-            flush.fill_(k & 0xFF)                      # evict L2 between steps (untimed)
-            ev[k][0].record(stream)
-            run_a()
-            ev[k][1].record(stream)
-            run_f()
-            ev[k][2].record(stream)
-        torch.cuda.synchronize()
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)                      # evict L2 between steps (untimed)
+        ev[k][0].record(stream)
+        run_a()
+        ev[k][1].record(stream)
+        run_f()
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    clocks.__exit__(None, None, None)
     t_step = [e[0].elapsed_time(e[2]) for e in ev]
     t_app = [e[0].elapsed_time(e[1]) for e in ev]
     ms = sum(t_step) / len(t_step)
@@ -270,7 +296,7 @@ def base_line(args, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-graph", action="store_true")
@@ -323,7 +349,8 @@ def main():
         "pct_hbm_cache_read": 100 * fl["cache_bytes"] / (r["ms"] * 1e-3) / 1e9 / hbm,
         "roofline": {"kernel": rl_kernel,
                      "bound": "tensor", "achieved": ach, "peak": bf16, "unit": "TFLOP/s",
-                     "frac": ach / bf16, "traffic": None,
+                     "frac": ach / bf16,
+                     "traffic": append_traffic() if fl["append"] and args.workload == WORKLOAD else None,
                      "peak_source": f"{src} bf16 burst"},
         "e2e": {"value": world * fl["block_tokens"] / e2e_s, "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
