@@ -69,19 +69,33 @@ def algorithmic_flops(wl):
 
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons, sampled every 20 ms by a
-    background nvidia-smi while the GPU runs the warm-up and timed steps."""
+    background nvidia-smi while the GPU runs the warm-up and timed steps
+    (started, and its first line awaited, before the warm-up)."""
     Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index=0):
-        self.samples, self.index, self.proc = [], index, None
+        self.samples, self.index, self.proc, self.reader = [], index, None, None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 6:
+                self.samples.append(f)
 
     def __enter__(self):
+        import threading
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+            t0 = time.time()
+            while not self.samples and time.time() - t0 < 3.0:
+                time.sleep(0.01)
+            self.samples.clear()          # drop the idle sample taken before the load
         except Exception:
             self.proc = None
         return self
@@ -91,14 +105,11 @@ class ClockSampler:
             return
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=10)
+            self.proc.wait(timeout=10)
         except Exception:
             self.proc.kill()
-            out, _ = self.proc.communicate()
-        for line in out.splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) >= 6:
-                self.samples.append(f)
+        if self.reader is not None:
+            self.reader.join(timeout=5)
 
     def summary(self):
         if not self.samples:
