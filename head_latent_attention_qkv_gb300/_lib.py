@@ -63,6 +63,8 @@ def _load():
         "mla_forward_workspace_bytes": (SZ, [P, I32]),
         "mla_latent_cache_append": (I32, [P, P, P, P, I32, P, I32, P, SZ, P]),
         "mla_draft_forward": (I32, [P, P, P, P, P, I32, C.POINTER(mla_attn_desc_t), P, P, SZ, P]),
+        "mla_draft_forward_after": (I32, [P, P, P, P, P, I32, C.POINTER(mla_attn_desc_t), P, P, SZ,
+                                          P, P]),
         "mla_get_device_status": (I32, [P, P, C.POINTER(I32)]),
         "mla_draft_destroy": (None, [P]),
         "mla_kernel_launches": (C.c_ulonglong, [P]),

@@ -115,6 +115,23 @@ def mla_draft_forward(h: Handle, hidden, positions, block_slot_mapping, cache, d
     return out
 
 
+def mla_draft_forward_after(h: Handle, hidden, positions, block_slot_mapping, cache, desc,
+                            cache_ready=None, out=None, stream=None, workspace=None):
+    """mla_draft_forward whose attention waits for ``cache_ready`` (a
+    recorded torch.cuda.Event, or None)."""
+    M = desc.num_blocks * desc.block_len
+    if out is None:
+        out = torch.empty(M, h.dims.hidden_size, dtype=torch_dtype(h.dims), device=h.device)
+    need = lib.mla_forward_workspace_bytes(h.h, M)
+    ws = workspace if workspace is not None else h.workspace(need)
+    ev = None if cache_ready is None else C.c_void_p(cache_ready.cuda_event)
+    check(lib.mla_draft_forward_after(h.h, _ptr(hidden), _ptr(positions), _ptr(block_slot_mapping),
+                                      _ptr(cache), cache.shape[0], C.byref(desc), _ptr(out),
+                                      _ptr(ws), ws.numel(), _stream(stream), ev),
+          "mla_draft_forward_after")
+    return out
+
+
 def mla_get_device_status(h: Handle, stream=None) -> int:
     bits = C.c_int32(0)
     lib.mla_get_device_status(h.h, _stream(stream), C.byref(bits))

@@ -270,7 +270,7 @@ namespace mla {
 namespace {
 
 struct FwdWs {
-  size_t a_out, q_cn, q_raw, q_nope, q_abs, o_lat, o, part, total;
+  size_t a_out, q_cn, q_raw, q_nope, q_abs, o_lat, o, total;
 };
 
 FwdWs forward_ws(const mla_handle* h, long M) {
@@ -284,8 +284,6 @@ FwdWs forward_ws(const mla_handle* h, long M) {
   w.q_abs = o;  o = align256(o + (size_t)M * l.H * l.L * l.elt);
   w.o_lat = o;  o = align256(o + (size_t)M * l.H * l.rkv * l.elt);
   w.o = o;      o = align256(o + (size_t)M * l.H * l.dv * l.elt);
-  // split-KV partial outputs of the tensor-core attention (bf16 layers)
-  w.part = o;   o = align256(o + (h->cfg.dtype == MLA_BF16 ? tc::attn_split_floats(h, M) * 4 : 0));
   w.total = o;
   return w;
 }
@@ -396,7 +394,7 @@ namespace {
 template <typename TX, typename TI>
 mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* pos, const int64_t* bslots,
                   void* cache, int num_pages, const mla_attn_desc_t& d, void* out, char* ws,
-                  cudaStream_t st) {
+                  cudaStream_t st, cudaEvent_t kv_ready) {
   const Layout& l = h->lay;
   const int M = d.num_blocks * d.block_len;
   const FwdWs w = forward_ws(h, M);
@@ -454,14 +452,15 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
                    (const TI*)h->WUKT, l.dn, (long)l.rkv * l.dn, q_abs, (long)l.H * l.L, l.L);
   if (s != MLA_OK) return s;
   TI* o_lat = (TI*)(ws + w.o_lat);
+  // the cache writes of another stream the attention depends on (a plain
+  // launch after the wait: no programmatic edge crosses it)
+  if (kv_ready) MLA_CUDA_TRY(cudaStreamWaitEvent(st, kv_ready, 0));
   if constexpr (std::is_same<TX, float>::value) {
     simt::latent_attention<TI, TX>(st, h, q_abs, (const TX*)cache, num_pages, d, pos, o_lat);
   } else {
     s = tc::latent_attention(st, h, q_abs, (const TX*)cache, num_pages, d, pos, o_lat,
-                             (float*)(ws + w.part), pdl);
+                             pdl && !kv_ready);
     if (s != MLA_OK) return s;
-    const int sp = tc::attn_splits(h, M);
-    h->launches += (sp > 1) + (sp > 1 && d.vis_stats);   // merge, visibility-stat init
   }
   // o[h] = o_lat[h] @ W_UV[h]^T (* sigmoid(gate))
   TI* o = (TI*)(ws + w.o);
@@ -481,12 +480,13 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
 }  // namespace
 }  // namespace mla
 
-extern "C" mla_status_t mla_draft_forward(mla_handle_t* h, const void* hidden,
-                                          const int32_t* positions,
-                                          const int64_t* block_slot_mapping, void* cache,
-                                          int32_t num_pages, const mla_attn_desc_t* desc,
-                                          void* out, void* workspace, size_t workspace_bytes,
-                                          void* stream) {
+extern "C" mla_status_t mla_draft_forward_after(mla_handle_t* h, const void* hidden,
+                                                const int32_t* positions,
+                                                const int64_t* block_slot_mapping, void* cache,
+                                                int32_t num_pages, const mla_attn_desc_t* desc,
+                                                void* out, void* workspace,
+                                                size_t workspace_bytes, void* stream,
+                                                void* cache_ready) {
   if (!h || !desc) return fail(MLA_ERR_INVALID_ARG, "forward: null handle or descriptor");
   const mla_attn_desc_t& d = *desc;
   if (d.num_blocks < 0 || d.block_len <= 0 || d.max_pages <= 0)
@@ -502,15 +502,26 @@ extern "C" mla_status_t mla_draft_forward(mla_handle_t* h, const void* hidden,
     return fail(MLA_ERR_INVALID_ARG, "forward: workspace smaller than mla_forward_workspace_bytes()");
   if ((uintptr_t)workspace % 256) return fail(MLA_ERR_INVALID_ARG, "forward: workspace must be 256-byte aligned");
   cudaStream_t st = (cudaStream_t)stream;
+  const cudaEvent_t ev = (cudaEvent_t)cache_ready;
   const mla_status_t s =
       h->cfg.dtype == MLA_BF16
           ? forward_impl<__nv_bfloat16, __half>(h, hidden, positions, block_slot_mapping, cache,
-                                                num_pages, d, out, (char*)workspace, st)
+                                                num_pages, d, out, (char*)workspace, st, ev)
           : forward_impl<float, float>(h, hidden, positions, block_slot_mapping, cache,
-                                       num_pages, d, out, (char*)workspace, st);
+                                       num_pages, d, out, (char*)workspace, st, ev);
   if (s != MLA_OK) return s;
   MLA_CUDA_TRY(cudaGetLastError());
   return MLA_OK;
+}
+
+extern "C" mla_status_t mla_draft_forward(mla_handle_t* h, const void* hidden,
+                                          const int32_t* positions,
+                                          const int64_t* block_slot_mapping, void* cache,
+                                          int32_t num_pages, const mla_attn_desc_t* desc,
+                                          void* out, void* workspace, size_t workspace_bytes,
+                                          void* stream) {
+  return mla_draft_forward_after(h, hidden, positions, block_slot_mapping, cache, num_pages, desc,
+                                 out, workspace, workspace_bytes, stream, nullptr);
 }
 
 extern "C" mla_status_t mla_get_device_status(mla_handle_t* h, void* stream, int32_t* bits) {

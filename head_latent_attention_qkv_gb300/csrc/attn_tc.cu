@@ -33,9 +33,14 @@
 //                  fp32 in the exp2 domain (O rescaled in tensor memory only
 //                  when the running max grows by more than 2^8), P -> bf16
 //   TMA warp     : page rows of the key range (once), Q, key chunks, values
-// The key range of a unit may be split across clusters (grid y) when units
-// alone do not fill the GPU; splits write normalised partial outputs and
-// their log2-sum-exp, merged by merge_splits().
+// The key range of a unit may be split (grid y) when units alone do not fill
+// the GPU ([MLA] forward_mqa num_kv_splits); the pairs of one unit then form
+// one cluster of 2 x splits CTAs.  Every CTA stages its normalised partial
+// output, its log2-sum-exp and visibility counts in its own shared memory
+// (over the Q and V buffers, free after the last P V); after a cluster
+// barrier split s combines rows [128 s / splits, 128 (s + 1) / splits) of its
+// value half from all splits, in split order, by log-sum-exp ([MLA]
+// forward_mha merge_attn_states) and writes them as fp16 whole rows.
 #include "attn_tc.cuh"
 
 #include <mutex>
@@ -62,6 +67,15 @@ constexpr int MAX_PG = 176;                               // pages held there (e
 constexpr int SMEM_BYTES = 1024 + OFF_PG + MAX_PG * 4;
 constexpr uint32_t TMEM_COLS = 512, TM_O = 0, TM_S = 256, TM_P = 384, TM_Q = 448;
 constexpr float RESCALE_LOG2 = 8.f;                       // lazy rescale threshold (factor 256)
+constexpr int MAX_SPLITS = 4;                             // clusters of at most 8 CTAs
+// epilogue staging (over the Q and V buffers): fp32 rows of this CTA's 256
+// value dims (pitch 260 floats: conflict-free 16-byte row-per-thread
+// stores), then the rows' log2-sum-exp and visibility counts
+constexpr int STG_PITCH = 256 + 4;
+constexpr int OFF_STG = 0;
+constexpr int OFF_LSE = OFF_STG + QROWS * STG_PITCH * 4;
+constexpr int OFF_VS = OFF_LSE + QROWS * 4;
+static_assert(OFF_VS + QROWS * 12 <= OFF_K, "staging fits over Q and V");
 
 struct Bars {
   uint64_t q_full;                    // Q chunks in shared memory (TMA)
@@ -103,14 +117,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 // Warps 0-3: thread r owns accumulator row r (TMEM lane r) of the unit.
-__device__ __forceinline__ void softmax_and_store(const AttnParams& P, Bars* B, uint8_t* smem,
-                                                  uint32_t tmem, int half, int b, int qt,
-                                                  long row0, int kvl, int W, int j_lo, int nt) {
+__device__ __forceinline__ void softmax_and_stage(const AttnParams& P, Bars* B, uint8_t* smem,
+                                                  uint32_t tmem, int b, int qt, long row0, int kvl,
+                                                  int W, int j_lo, int nt) {
   const int r = threadIdx.x;
   const uint32_t lane_base = (uint32_t)((r / 32) * 32) << 16;
   const int row_in_block = qt * QROWS + r;
-  const int tok = row_in_block / P.H, head = row_in_block % P.H;
-  const long m = (long)b * P.T + tok;
+  const long m = (long)b * P.T + row_in_block / P.H;
   const int p = P.positions[m];
   const bool qv = P.q_visible ? P.q_visible[m] != 0 : true;
   // the keys this query sees form one interval [vlo, vhi): j < kv_len and, for
@@ -219,52 +232,108 @@ __device__ __forceinline__ void softmax_and_store(const AttnParams& P, Bars* B, 
     tc_fence_before();
     mbar_arrive(&B->p_full);
   }
-  // epilogue: O / l -> latent output columns [256 half, 256 half + 256)
+  // stage this split's partial: O / l in fp32, log2-sum-exp, visibility counts
   if (nt > 0) wait_bar(B, &B->o_done, (nt - 1) & 1, P.status);
   tc_fence_after();
   const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
   const bool any = nt > 0 && lsum > 0.f;
-  if (P.splits == 1) {
-    __half* dst = P.o_lat + (row0 + r) * 512 + half * 256;
+  float* prow = (float*)(smem + OFF_STG) + r * STG_PITCH;
 #pragma unroll 1
-    for (int c = 0; c < 256; c += 32) {
-      float o[32];
-      if (nt > 0) tmem_ld32(tmem + TM_O + lane_base + c, o);
+  for (int c = 0; c < 256; c += 32) {
+    float o[32];
+    if (nt > 0) tmem_ld32(tmem + TM_O + lane_base + c, o);
 #pragma unroll
-      for (int i = 0; i < 32; i += 8) {
-        __half2 h2[4];
+    for (int i = 0; i < 32; i += 4)
+      *reinterpret_cast<float4*>(prow + c + i) =
+          any ? make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv)
+              : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  ((float*)(smem + OFF_LSE))[r] = any ? mrun + log2f(lsum) : -INFINITY;
+  int* vs = (int*)(smem + OFF_VS) + 3 * r;
+  vs[0] = cnt;
+  vs[1] = first;
+  vs[2] = last;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+
+// All warps, after every split has staged: rows [128 split / S, 128 (split +
+// 1) / S) of value half `half`.  The merged row is sum_s w_s o_s / sum_s w_s,
+// w_s = 2^(lse_s - max lse), added in split order; a row no split saw stays
+// exactly zero.  Lane l writes value dims 8 l .. 8 l + 7 (a warp per row: one
+// 512-byte write).  CTA (half h, split s) is cluster rank h + 2 s.
+__device__ __forceinline__ void reduce_splits(const AttnParams& P, uint8_t* smem, int half,
+                                              int split, int b, int qt, long row0) {
+  const int S = P.splits;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int r_lo = split * QROWS / S, r_hi = (split + 1) * QROWS / S;
+  const uint32_t stg = smem_u32(smem + OFF_STG), lse_a = smem_u32(smem + OFF_LSE),
+                 vs_a = smem_u32(smem + OFF_VS);
+  for (int r = r_lo + warp; r < r_hi; r += THREADS / 32) {
+    const uint32_t off = stg + (uint32_t)(r * STG_PITCH + 8 * lane) * 4;
+    float lse[MAX_SPLITS];
+    float4 v[MAX_SPLITS][2];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          h2[u] = any ? __floats2half2_rn(o[i + 2 * u] * inv, o[i + 2 * u + 1] * inv)
-                      : __floats2half2_rn(0.f, 0.f);
-        *reinterpret_cast<uint4*>(dst + c + i) = *reinterpret_cast<uint4*>(h2);
+    for (int s = 0; s < MAX_SPLITS; ++s) {
+      if (s < S) {
+        const uint32_t rank = (uint32_t)(half + 2 * s);
+        lse[s] = ld_cluster_f32(mapa(lse_a + 4 * r, rank));
+        v[s][0] = ld_cluster_v4(mapa(off, rank));
+        v[s][1] = ld_cluster_v4(mapa(off + 16, rank));
       }
     }
-  } else {
-    // normalised partial output and its log2-sum-exp, merged by merge_splits()
-    const long prow = (long)blockIdx.y * P.rows + row0 + r;
-    float* dst = P.o_part + prow * 512 + half * 256;
-#pragma unroll 1
-    for (int c = 0; c < 256; c += 32) {
-      float o[32];
-      if (nt > 0) tmem_ld32(tmem + TM_O + lane_base + c, o);
+    float mx = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 32; i += 4)
-        *reinterpret_cast<float4*>(dst + c + i) =
-            any ? make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv)
-                : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < MAX_SPLITS; ++s)
+      if (s < S) mx = fmaxf(mx, lse[s]);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, den = 0.f;
+#pragma unroll
+    for (int s = 0; s < MAX_SPLITS; ++s) {
+      if (s < S) {
+        const float w = mx == -INFINITY ? 0.f : exp2f(lse[s] - mx);
+        den += w;
+        acc[0] += w * v[s][0].x; acc[1] += w * v[s][0].y; acc[2] += w * v[s][0].z; acc[3] += w * v[s][0].w;
+        acc[4] += w * v[s][1].x; acc[5] += w * v[s][1].y; acc[6] += w * v[s][1].z; acc[7] += w * v[s][1].w;
+      }
     }
-    if (half == 0) P.lse_part[prow] = any ? mrun + log2f(lsum) : -INFINITY;
-  }
-  if (P.vis_stats && half == 0 && head == 0) {
-    if (P.splits == 1) {
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    __half2 h2[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) h2[u] = __floats2half2_rn(acc[2 * u] * inv, acc[2 * u + 1] * inv);
+    *reinterpret_cast<uint4*>(P.o_lat + (row0 + r) * 512 + half * 256 + 8 * lane) =
+        *reinterpret_cast<uint4*>(h2);
+    // visibility statistics of the row's token (from the head-0 row, value half 0)
+    const int row_in_block = qt * QROWS + r;
+    if (P.vis_stats && half == 0 && row_in_block % P.H == 0 && lane == 0) {
+      int cnt = 0, first = -1, last = -1;
+      for (int s = 0; s < S; ++s) {
+        const uint32_t a = mapa(vs_a + 12 * r, (uint32_t)(2 * s));
+        const int c = ld_cluster_s32(a), f = ld_cluster_s32(a + 4), l = ld_cluster_s32(a + 8);
+        if (c) {
+          first = cnt ? min(first, f) : f;
+          last = max(last, l);
+          cnt += c;
+        }
+      }
+      const long m = (long)b * P.T + row_in_block / P.H;
       P.vis_stats[m * 3 + 0] = cnt;
       P.vis_stats[m * 3 + 1] = cnt ? first : -1;
       P.vis_stats[m * 3 + 2] = cnt ? last : -1;
-    } else if (cnt) {
-      atomicAdd(&P.vis_stats[m * 3 + 0], cnt);
-      atomicMin(&P.vis_stats[m * 3 + 1], first);
-      atomicMax(&P.vis_stats[m * 3 + 2], last);
     }
   }
 }
@@ -274,7 +343,9 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   Bars* B = (Bars*)(smem + OFF_BAR);
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int half = (int)cluster_ctarank();             // == blockIdx.x & 1
+  const int rank = (int)cluster_ctarank();             // half + 2 * split
+  const int half = rank & 1, split = rank >> 1;         // split == blockIdx.y
+  const uint16_t pair = (uint16_t)(3u << (2 * split));  // this unit's two CTAs
   const int unit = blockIdx.x >> 1;
   const int b = unit / P.tiles_per_block, qt = unit % P.tiles_per_block;
   const long row0 = ((long)b * P.tiles_per_block + qt) * QROWS;   // first Q_abs row of the unit
@@ -380,7 +451,6 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
         }
         return y0;
       };
-      const uint16_t both = 3;
       bool ok = true;
       int g = 0;             // key chunks issued so far (ring position)
       // V(tv): this CTA's four value chunks, once P(tv - 1) V(tv - 1) has freed the buffer
@@ -411,11 +481,11 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
           if ((g & 1) == half) {   // the CTAs take turns; each copy lands in both
             uint8_t* dst = smem + OFF_K + sl * KV_CH_BYTES;
             if (y0 >= 0) {
-              tma_load_3d_mc(dst, &P.tmK, &B->k_full[sl], c * DCH, y0, 0, both);
+              tma_load_3d_mc(dst, &P.tmK, &B->k_full[sl], c * DCH, y0, 0, pair);
             } else {
               for (int seg = 0; seg < nseg; ++seg)
                 tma_load_3d_mc(dst + seg * R * 128, &P.tmKs, &B->k_full[sl], c * DCH,
-                               cache_row(j_lo + t * KT + seg * R), 0, both);
+                               cache_row(j_lo + t * KT + seg * R), 0, pair);
             }
           }
           ++g;
@@ -452,7 +522,7 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
 #pragma unroll
             for (int k = 0; k < DCH / 16; ++k) mma_f16(tmem + TM_S, da + 2 * k, db + 2 * k, idesc_qk, 1);
           }
-          mma_commit_mc(&B->k_empty[sl], 3);   // this slot is free in both CTAs' eyes
+          mma_commit_mc(&B->k_empty[sl], pair);   // this slot is free in both CTAs' eyes
         }
         mma_commit(&B->s_full);
         return true;
@@ -476,14 +546,16 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
       mbar_wait(&B->drain, 0, P.status);
     }
   } else {
-    softmax_and_store(P, B, smem, tmem, half, b, qt, row0, kvl, W, j_lo, nt);
+    softmax_and_stage(P, B, smem, tmem, b, qt, row0, kvl, W, j_lo, nt);
   }
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();          // no CTA leaves while its peer may still multicast or commit to it
+  cluster_sync_all();          // every partial is staged; no copy or commit into any CTA is in flight
   tc_fence_after();
   if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
+  reduce_splits(P, smem, half, split, b, qt, row0);
+  cluster_sync_all();          // no CTA leaves while another may still read its staged partial
 }
 
 }  // namespace
@@ -501,7 +573,7 @@ namespace tc {
 mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_bfloat16* q_abs,
                               const __nv_bfloat16* cache, int num_pages,
                               const mla_attn_desc_t& d, const int32_t* positions, __half* o_lat,
-                              float* part, bool pdl) {
+                              bool pdl) {
   const Layout& l = h->lay;
   const int ps = h->cfg.page_size;
   if (l.rkv != 512 || l.dr != 64)
@@ -539,40 +611,27 @@ mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_b
   P.tiles_per_block = d.block_len * l.H / QROWS;
   P.scale_log2 = h->scale * 1.4426950408889634f;
   P.splits = splits;
-  P.rows = rows;
-  P.o_part = part;
-  P.lse_part = part + (size_t)splits * rows * 512;
-  if (splits > 1 && d.vis_stats) {
-    init_vis_stats(st, d.vis_stats, tokens, pdl);
-    pdl = true;
-  }
   static std::once_flag once;
   std::call_once(once, [] {
     cudaFuncSetAttribute(latent_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   });
   Launch L(dim3(2 * d.num_blocks * P.tiles_per_block, splits, 1), dim3(THREADS), SMEM_BYTES, st, pdl,
-           dim3(2, 1, 1));
+           dim3(2, splits, 1));
   const cudaError_t e = cudaLaunchKernelEx(&L.cfg, latent_attn_tc_kernel, P);
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 attention launch");
-  if (splits > 1) merge_splits(st, P.o_part, P.lse_part, splits, rows, o_lat, d.vis_stats, l.H, true);
   return MLA_OK;
 }
 
 // When the (block, 128-row, value-half) CTAs leave part of the GPU idle
 // (one CTA per SM), split each unit's key range so that the CTAs fill one
-// wave (at most 8 parts); a split that would add a partial wave only
-// lengthens the kernel.
+// wave (at most MAX_SPLITS parts: a unit's CTAs form one cluster); a split
+// that would add a partial wave only lengthens the kernel.
 int attn_splits(const mla_handle* h, long tokens) {
   const long ctas = 2 * (tokens * h->lay.H / QROWS);
   const long wave = h->num_sms;
   if (ctas <= 0 || ctas >= wave) return 1;
   const long s = wave / ctas;
-  return (int)(s < 1 ? 1 : s > 8 ? 8 : s);
-}
-
-size_t attn_split_floats(const mla_handle* h, long tokens) {
-  const int s = attn_splits(h, tokens);
-  return s > 1 ? (size_t)s * tokens * h->lay.H * (512 + 1) : 0;
+  return (int)(s < 1 ? 1 : s > MAX_SPLITS ? MAX_SPLITS : s);
 }
 
 }  // namespace tc

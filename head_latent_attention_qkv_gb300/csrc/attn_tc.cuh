@@ -20,11 +20,8 @@ struct AttnParams {
   const uint8_t* q_visible;
   const int32_t* positions;
   int32_t* vis_stats;
-  __half* o_lat;      // [rows, 512] (one split)
-  float* o_part;      // [splits, rows, 512] normalised partial outputs (splits > 1)
-  float* lse_part;    // [splits, rows] log2-sum-exp of each split (splits > 1)
-  int splits;
-  long rows;          // rows of Q_abs (tokens * heads)
+  __half* o_lat;      // [rows, 512]
+  int splits;         // key-range parts of a unit (1..4; cluster of 2 x splits CTAs)
   uint32_t* status;
   int max_pages, num_pages, page_size, seg_rows, T, H, tiles_per_block;
   float scale_log2;   // softmax scale * log2(e)
@@ -33,20 +30,16 @@ struct AttnParams {
 // Supported: kv_lora_rank 512, qk_rope 64, block_len * num_heads a multiple
 // of 128, page_size 16, 32, 64 or a multiple of 128.  Returns MLA_ERR_UNSUPPORTED
 // otherwise.
-// The key range of every (block, 128-row) unit is split in `splits` parts
-// when units alone do not fill the GPU; `part` (attn_split_floats() floats)
-// holds the partial outputs merged by log-sum-exp.
+// The key range of every (block, 128-row) unit is split in attn_splits()
+// parts when units alone do not fill the GPU; the parts are merged by
+// log-sum-exp inside the kernel (no workspace).
 int attn_splits(const mla_handle* h, long tokens);
-size_t attn_split_floats(const mla_handle* h, long tokens);
 // `pdl`: the kernels may start while the previous kernel of the stream
 // finishes (programmatic stream serialization; they wait for it on the device).
 mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_bfloat16* q_abs,
                               const __nv_bfloat16* cache, int num_pages,
                               const mla_attn_desc_t& desc, const int32_t* positions,
-                              __half* o_lat, float* part, bool pdl = false);
-void merge_splits(cudaStream_t st, const float* o_part, const float* lse_part, int splits,
-                  long rows, __half* o_lat, int32_t* vis_stats, int H, bool pdl = false);
-void init_vis_stats(cudaStream_t st, int32_t* vis_stats, long tokens, bool pdl = false);
+                              __half* o_lat, bool pdl = false);
 
 }  // namespace tc
 }  // namespace mla

@@ -360,10 +360,29 @@ int num_sms_current() {
   return num_sms;
 }
 
+// Clusters of s CTAs (one per SM) the GPU holds at once: a cluster lives in
+// one GPC and the GPCs differ in size, so this is below sms / s.
+long max_active_clusters(int s) {
+  static long cache[9] = {};
+  if (s <= 1) return num_sms_current();
+  if (s > 8) return 0;
+  if (!cache[s]) {
+    auto kern = gemm_tc_kernel<128, float>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<128>::BYTES);
+    Launch L(dim3(1, 1, s), dim3(THREADS), Smem<128>::BYTES, nullptr, false, dim3(1, 1, s));
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &L.cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = num_sms_current() / s;
+    }
+    cache[s] = n;
+  }
+  return cache[s];
+}
+
 }  // namespace
 
 void plan_gemm(int M, int N, int K, int batch, int* bn_out, int* split_out) {
-  const long sms = num_sms_current();
   const int nk = (K + BK - 1) / BK;
   const int bns[3] = {256, 128, 64};
   double best = 1e30;
@@ -373,9 +392,10 @@ void plan_gemm(int M, int N, int K, int batch, int* bn_out, int* split_out) {
     const int kbs = bn == 64 ? 4 : 2;
     const long tiles = (long)((N + bn - 1) / bn) * ((M + BM - 1) / BM) * batch;
     for (int s = 1; s <= (batch == 1 ? 8 : 1); ++s) {
-      if (s > 1 && tiles * s > sms) break;
+      const long fit = max_active_clusters(s);             // a tile is a cluster of s CTAs
+      if (s > 1 && tiles > fit) break;
       if (s > 1 && (nk + kbs - 1) / kbs < s) break;      // at least one stage per split
-      const long waves = (tiles * s + sms - 1) / sms;
+      const long waves = (tiles + fit - 1) / fit;
       const double per_cta = ((nk + s - 1) / s) * 4.0 * mma + 3000.0 + 400.0 * s;
       const double t = waves * per_cta;
       if (t < best * 0.98) { best = t; best_bn = bn; best_s = s; }

@@ -3,8 +3,11 @@
 Uploads the seeded inputs of ``workloads.Workload`` to the GPU, then runs the
 call sequence: prefilled cache entries are copied in, context tokens are
 appended with ``mla_latent_cache_append``, and every step appends its tokens
-(if any) and calls ``mla_draft_forward``.  Only data movement happens here;
-all of the layer's arithmetic runs in the library.
+(if any) and calls ``mla_draft_forward``.  ``run_step_after`` issues a step's
+cache appends on a second stream instead, so that the forward's projections
+run beside them and only its attention waits (``mla_draft_forward_after``).
+Only data movement happens here; all of the layer's arithmetic runs in the
+library.
 """
 from __future__ import annotations
 
@@ -42,6 +45,7 @@ class DeviceWorkload:
         if wl.prefill_slots is not None:
             self.prefill = (to_dev(wl.prefill_slots, None, device),
                             to_dev(wl.prefill_values, dt, device))
+        self._side_ws = None
         self.steps = []
         for s in wl.steps:
             d = dict(
@@ -78,6 +82,34 @@ class DeviceWorkload:
             api.mla_latent_cache_append(self.handle, *s["append"], self.cache)
         api.mla_draft_forward(self.handle, s["hidden"], s["positions"], s["slots"], self.cache,
                               s["desc"], out=s["out"])
+        return s["out"]
+
+    def run_step_after(self, k, side, with_context=False):
+        """Step k with its cache appends (the context first when
+        ``with_context``) on stream ``side``, forked from the current stream;
+        the forward runs on the current stream and its attention waits for
+        the appends, which also joins ``side`` back."""
+        s = self.steps[k]
+        main = torch.cuda.current_stream()
+        appends = []
+        if with_context and self.ctx is not None:
+            appends.append(self.ctx)
+        if s["append"] is not None:
+            appends.append(s["append"])
+        ready = None
+        if appends:
+            side.wait_stream(main)
+            for a in appends:
+                n = a[0].shape[0]
+                need = api.lib.mla_append_workspace_bytes(self.handle.h, n)
+                if self._side_ws is None or self._side_ws.numel() < need:
+                    self._side_ws = api._buf(need, self.device)
+                api.mla_latent_cache_append(self.handle, *a, self.cache, stream=side,
+                                            workspace=self._side_ws)
+            ready = torch.cuda.Event()
+            ready.record(side)
+        api.mla_draft_forward_after(self.handle, s["hidden"], s["positions"], s["slots"],
+                                    self.cache, s["desc"], cache_ready=ready, out=s["out"])
         return s["out"]
 
     def run_all(self):

@@ -183,6 +183,27 @@ mla_status_t mla_draft_forward(mla_handle_t *h, const void *hidden,
                                void *out, void *workspace,
                                size_t workspace_bytes, void *stream);
 
+/* mla_draft_forward whose attention waits for an event.  Everything that
+ * does not read the cache -- the projections, query RoPE and W_UK
+ * absorption, and the block's own latents when block_slot_mapping is
+ * non-NULL -- is enqueued on `stream` at once; before the attention, the
+ * stream waits for `cache_ready` (a cudaEvent_t the caller recorded after
+ * the cache writes the attention reads, typically mla_latent_cache_append
+ * of the target context on another stream).  The block's projections then
+ * run while the context is appended (the pages' draft reads the context
+ * only through the attention's keys).  The two must write disjoint slots;
+ * an append that needs a workspace needs its own.  cache_ready == NULL is
+ * exactly mla_draft_forward.  Graph-capturable: recorded into a stream
+ * capture, the event forks and joins the two streams.  Same arguments,
+ * results and errors as mla_draft_forward otherwise. */
+mla_status_t mla_draft_forward_after(mla_handle_t *h, const void *hidden,
+                                     const int32_t *positions,
+                                     const int64_t *block_slot_mapping, void *cache,
+                                     int32_t num_pages, const mla_attn_desc_t *desc,
+                                     void *out, void *workspace,
+                                     size_t workspace_bytes, void *stream,
+                                     void *cache_ready);
+
 /* Allocation-free latent-cache append.  The pages have no counterpart: this
  * is a library convenience for callers that cannot allocate device memory
  * where they append (host callbacks, allocator hooks, runtimes with a memory
