@@ -138,9 +138,10 @@ def append_traffic():
     digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
     vals = {}
     for line in open(summ):
-        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "kernel_source_sha256")):
-            k, v = line.split(":", 1)
-            vals[k.strip().strip("-* `")] = v.strip().strip("` ")
+        key = line.strip().lstrip("-* `")
+        if ":" in key and key.startswith(("traffic_bytes_per_launch", "kernel_source_sha256")):
+            k, v = key.split(":", 1)
+            vals[k.strip().strip("`")] = v.strip().strip("` ")
     if vals.get("kernel_source_sha256") != digest:
         return None
     try:

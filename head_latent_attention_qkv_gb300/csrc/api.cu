@@ -345,7 +345,8 @@ mla_status_t append_impl(mla_handle_t* h, const void* hidden, const int32_t* pos
   // kv = hidden @ W_kva^T : W_kva = first L rows of W_A
   if constexpr (std::is_same<T, __nv_bfloat16>::value) {
     h->launches += 1;
-    return tc::kv_append(st, h, (const T*)hidden, n, positions, slots, (T*)cache, num_slots);
+    return tc::kv_append(st, h, (const T*)hidden, n, positions, slots, (T*)cache, num_slots,
+                         true);
   } else {
     mla_status_t s = proj<T, float>(h, st, false, n, l.L, l.D, 1, (const T*)hidden, l.D, 0,
                                     (const T*)h->WA, l.D, 0, kv_ws, l.L, 0);
@@ -410,11 +411,12 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
   const long num_slots = (long)num_pages * h->cfg.page_size;
   const bool fused_kv = kBf16 && bslots && 3L * ((M + 127) / 128) >= h->num_sms;
   const int r0 = (bslots && !fused_kv) ? 0 : l.L;
-  // the first kernel of the call waits for everything before it; the others
-  // may start early (programmatic dependent launch, bf16 layers) and wait for
-  // their predecessor on the device
+  // every kernel (bf16 layers) may start while the previous kernel of the
+  // stream finishes (programmatic dependent launch) and waits for it on the
+  // device before it reads anything but the weights; a first kernel behind a
+  // copy or an event wait starts as a plain launch
   constexpr bool pdl = kBf16;
-  mla_status_t s = proj<TX, float>(h, st, false, M, l.NA - r0, l.D, 1, x, l.D, 0,
+  mla_status_t s = proj<TX, float>(h, st, pdl, M, l.NA - r0, l.D, 1, x, l.D, 0,
                                    WA + (long)r0 * l.D, l.D, 0, a_out + r0, l.NA, 0);
   if (s != MLA_OK) return s;
   if (bslots) {

@@ -284,6 +284,31 @@ __device__ __forceinline__ void reduce_splits(const AttnParams& P, uint8_t* smem
   const int r_lo = split * QROWS / S, r_hi = (split + 1) * QROWS / S;
   const uint32_t stg = smem_u32(smem + OFF_STG), lse_a = smem_u32(smem + OFF_LSE),
                  vs_a = smem_u32(smem + OFF_VS);
+  if (S == 1) {
+    // one split: this CTA's own rows, normalised already
+    const float* lse = (const float*)(smem + OFF_LSE);
+    const int* vs = (const int*)(smem + OFF_VS);
+    for (int r = warp; r < QROWS; r += THREADS / 32) {
+      const float4* src = (const float4*)(smem + OFF_STG + (r * STG_PITCH + 8 * lane) * 4);
+      const float4 a = src[0], c = src[1];
+      const bool any = lse[r] != -INFINITY;
+      __half2 h2[4] = {__floats2half2_rn(any ? a.x : 0.f, any ? a.y : 0.f),
+                       __floats2half2_rn(any ? a.z : 0.f, any ? a.w : 0.f),
+                       __floats2half2_rn(any ? c.x : 0.f, any ? c.y : 0.f),
+                       __floats2half2_rn(any ? c.z : 0.f, any ? c.w : 0.f)};
+      *reinterpret_cast<uint4*>(P.o_lat + (row0 + r) * 512 + half * 256 + 8 * lane) =
+          *reinterpret_cast<uint4*>(h2);
+      const int row_in_block = qt * QROWS + r;
+      if (P.vis_stats && half == 0 && row_in_block % P.H == 0 && lane == 0) {
+        const long m = (long)b * P.T + row_in_block / P.H;
+        const int cnt = vs[3 * r];
+        P.vis_stats[m * 3 + 0] = cnt;
+        P.vis_stats[m * 3 + 1] = cnt ? vs[3 * r + 1] : -1;
+        P.vis_stats[m * 3 + 2] = cnt ? vs[3 * r + 2] : -1;
+      }
+    }
+    return;
+  }
   for (int r = r_lo + warp; r < r_hi; r += THREADS / 32) {
     const uint32_t off = stg + (uint32_t)(r * STG_PITCH + 8 * lane) * 4;
     float lse[MAX_SPLITS];
@@ -551,11 +576,12 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();          // every partial is staged; no copy or commit into any CTA is in flight
+  if (P.splits > 1) cluster_sync_all();   // every split's partial is staged
   tc_fence_after();
   if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
   reduce_splits(P, smem, half, split, b, qt, row0);
-  cluster_sync_all();          // no CTA leaves while another may still read its staged partial
+  cluster_sync_all();          // no CTA leaves while another may still read its staged partial,
+                               // multicast into it or commit to its barriers
 }
 
 }  // namespace
