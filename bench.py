@@ -296,8 +296,10 @@ def cpu_baseline(workload=WORKLOAD, budget_s=15.0):
     dt = time.perf_counter() - t0
     cores = len(os.sched_getaffinity(0))
     return dict(value=done * wl.block_len / dt, unit="tokens/s", cores=cores, kind="oracle",
-                sample=f"{done} of {len(step.kv_len)} blocks (each: {len(rows)} context-token "
-                       f"appends + one 16-token block forward), fp64 numpy, {dt:.1f} s")
+                sample=f"{done} of {len(step.kv_len)} blocks of the first step (each: "
+                       f"{len(rows)} context-token appends, the block's own "
+                       f"{wl.block_len if step.append_hidden is not None else 0}-token append "
+                       f"and its {wl.block_len}-token forward), fp64 numpy, {dt:.1f} s")
 
 
 def base_line(args, world):
@@ -306,7 +308,8 @@ def base_line(args, world):
             "qwen3_4b_prefill": "8 x (2048 context + 16-token block), full mask",
             "qwen3_4b_sliding_gate": "16 x (8192 context + 16), sliding 512, gate, masked rows",
             "qwen3_4b_cached_decode": "64 seqs, cache pre-filled, 2 consecutive 16-token blocks",
-            "deepseek_v3_block_parallel": "4 x 1024 proposals of 16 over a 4096 context, gate"}
+            "deepseek_v3_block_parallel": "4 x 1024 proposals of 16 over a 4096 context, gate",
+            "qwen3_4b_decode_t1": "64 seqs, cache pre-filled, 2 consecutive one-token steps"}
     return {"metric": METRIC, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "data": "synthetic (seeded N(0,1) hidden, N(0,0.02) weights)",

@@ -123,9 +123,11 @@ __device__ __forceinline__ void softmax_and_stage(const AttnParams& P, Bars* B, 
   const int r = threadIdx.x;
   const uint32_t lane_base = (uint32_t)((r / 32) * 32) << 16;
   const int row_in_block = qt * QROWS + r;
-  const long m = (long)b * P.T + row_in_block / P.H;
+  // rows past the block's T x H (a partial last tile) are padding: fully masked
+  const bool live = row_in_block < P.T * P.H;
+  const long m = (long)b * P.T + (live ? row_in_block / P.H : 0);
   const int p = P.positions[m];
-  const bool qv = P.q_visible ? P.q_visible[m] != 0 : true;
+  const bool qv = live && (P.q_visible ? P.q_visible[m] != 0 : true);
   // the keys this query sees form one interval [vlo, vhi): j < kv_len and, for
   // a sliding window, p - j < W; a fully masked query sees none
   const int vlo = W > 0 ? max(0, p - W + 1) : 0;
@@ -140,7 +142,7 @@ __device__ __forceinline__ void softmax_and_stage(const AttnParams& P, Bars* B, 
       uint32_t w[32];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const uint4 v = __ldg(src + c * 8 + i);
+        const uint4 v = live ? __ldg(src + c * 8 + i) : make_uint4(0, 0, 0, 0);
         w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
       }
       tmem_st32_u(tmem + TM_Q + 32 * c + lane_base, w);
@@ -288,7 +290,8 @@ __device__ __forceinline__ void reduce_splits(const AttnParams& P, uint8_t* smem
     // one split: this CTA's own rows, normalised already
     const float* lse = (const float*)(smem + OFF_LSE);
     const int* vs = (const int*)(smem + OFF_VS);
-    for (int r = warp; r < QROWS; r += THREADS / 32) {
+    const int rows = min(QROWS, P.T * P.H - qt * QROWS);   // live rows of this tile
+    for (int r = warp; r < rows; r += THREADS / 32) {
       const float4* src = (const float4*)(smem + OFF_STG + (r * STG_PITCH + 8 * lane) * 4);
       const float4 a = src[0], c = src[1];
       const bool any = lse[r] != -INFINITY;
@@ -309,7 +312,8 @@ __device__ __forceinline__ void reduce_splits(const AttnParams& P, uint8_t* smem
     }
     return;
   }
-  for (int r = r_lo + warp; r < r_hi; r += THREADS / 32) {
+  const int rows = min(r_hi, P.T * P.H - qt * QROWS);   // live rows of this tile
+  for (int r = r_lo + warp; r < rows; r += THREADS / 32) {
     const uint32_t off = stg + (uint32_t)(r * STG_PITCH + 8 * lane) * 4;
     float lse[MAX_SPLITS];
     float4 v[MAX_SPLITS][2];
@@ -373,7 +377,7 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
   const uint16_t pair = (uint16_t)(3u << (2 * split));  // this unit's two CTAs
   const int unit = blockIdx.x >> 1;
   const int b = unit / P.tiles_per_block, qt = unit % P.tiles_per_block;
-  const long row0 = ((long)b * P.tiles_per_block + qt) * QROWS;   // first Q_abs row of the unit
+  const long row0 = (long)b * P.T * P.H + (long)qt * QROWS;       // first Q_abs row of the unit
 
   // key range of this unit: [j_lo, kvl) in 128-key tiles (identical in both halves)
   int kvl = P.kv_len[b];
@@ -385,7 +389,7 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
   const int W = P.window ? P.window[b] : 0;
   int j_lo = 0;
   if (W > 0) {
-    const int t_first = (qt * QROWS) / P.H, t_last = (qt * QROWS + QROWS - 1) / P.H;
+    const int t_first = (qt * QROWS) / P.H, t_last = min(P.T - 1, (qt * QROWS + QROWS - 1) / P.H);
     int pmin = 0x7fffffff;
     for (int t = t_first; t <= t_last; ++t) pmin = min(pmin, P.positions[(long)b * P.T + t]);
     j_lo = max(0, pmin - W + 1) / KT * KT;
@@ -604,13 +608,10 @@ mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_b
   const int ps = h->cfg.page_size;
   if (l.rkv != 512 || l.dr != 64)
     return fail(MLA_ERR_UNSUPPORTED, "tcgen05 attention: needs kv_lora_rank 512, qk_rope_head_dim 64");
-  if ((d.block_len * l.H) % QROWS)
-    return fail(MLA_ERR_UNSUPPORTED, "tcgen05 attention: block_len * num_heads must be a multiple of 128");
   if (ps % 16 || (ps < KT && KT % ps) || (ps > KT && ps % KT))
     return fail(MLA_ERR_UNSUPPORTED, "tcgen05 attention: page_size must be 16, 32, 64 or a multiple of 128");
   if (d.num_blocks <= 0) return MLA_OK;
-  const long tokens = (long)d.num_blocks * d.block_len;
-  const int splits = attn_splits(h, tokens);
+  const int splits = attn_splits(h, d.num_blocks, d.block_len);
   AttnParams P;
   const long rows = (long)d.num_blocks * d.block_len * l.H;
   const long slots = (long)num_pages * ps;
@@ -634,7 +635,7 @@ mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_b
   P.seg_rows = ps < KT ? ps : KT;
   P.T = d.block_len;
   P.H = l.H;
-  P.tiles_per_block = d.block_len * l.H / QROWS;
+  P.tiles_per_block = (d.block_len * l.H + QROWS - 1) / QROWS;
   P.scale_log2 = h->scale * 1.4426950408889634f;
   P.splits = splits;
   static std::once_flag once;
@@ -652,8 +653,8 @@ mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_b
 // (one CTA per SM), split each unit's key range so that the CTAs fill one
 // wave (at most MAX_SPLITS parts: a unit's CTAs form one cluster); a split
 // that would add a partial wave only lengthens the kernel.
-int attn_splits(const mla_handle* h, long tokens) {
-  const long ctas = 2 * (tokens * h->lay.H / QROWS);
+int attn_splits(const mla_handle* h, long num_blocks, int block_len) {
+  const long ctas = 2 * num_blocks * ((block_len * h->lay.H + QROWS - 1) / QROWS);
   const long wave = h->num_sms;
   if (ctas <= 0 || ctas >= wave) return 1;
   const long s = wave / ctas;

@@ -27,13 +27,13 @@ struct AttnParams {
   float scale_log2;   // softmax scale * log2(e)
 };
 
-// Supported: kv_lora_rank 512, qk_rope 64, block_len * num_heads a multiple
-// of 128, page_size 16, 32, 64 or a multiple of 128.  Returns MLA_ERR_UNSUPPORTED
-// otherwise.
+// Supported: kv_lora_rank 512, qk_rope 64, page_size 16, 32, 64 or a multiple
+// of 128 (any block_len: a block's block_len * num_heads rows are processed in
+// tiles of 128, the last one padded).  Returns MLA_ERR_UNSUPPORTED otherwise.
 // The key range of every (block, 128-row) unit is split in attn_splits()
 // parts when units alone do not fill the GPU; the parts are merged by
 // log-sum-exp inside the kernel (no workspace).
-int attn_splits(const mla_handle* h, long tokens);
+int attn_splits(const mla_handle* h, long num_blocks, int block_len);
 // `pdl`: the kernels may start while the previous kernel of the stream
 // finishes (programmatic stream serialization; they wait for it on the device).
 mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_bfloat16* q_abs,

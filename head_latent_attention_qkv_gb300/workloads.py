@@ -354,7 +354,7 @@ def cached_decode_workload(name: str, d: MLADims, seed: int, batch: int, prefill
 # The named workloads (full sizes) and their shrunken parity variants
 # --------------------------------------------------------------------------
 WORKLOADS = ("tiny_fp32", "qwen3_4b_prefill", "qwen3_4b_sliding_gate",
-             "qwen3_4b_cached_decode", "deepseek_v3_block_parallel")
+             "qwen3_4b_cached_decode", "deepseek_v3_block_parallel", "qwen3_4b_decode_t1")
 
 
 def make_workload(name: str, scale: str = "full") -> Workload:
@@ -391,6 +391,17 @@ def make_workload(name: str, scale: str = "full") -> Workload:
         return cached_decode_workload(name, d, 3, batch=64, prefill_len=4096, len_lo=1024,
                                       len_hi=4096, block_len=16, num_blocks=2, page_size=128,
                                       description="64 seqs, prefilled 4096, L~U[1024,4096], 2 blocks")
+    if name == "qwen3_4b_decode_t1":
+        # one query token per step (block_len 1): 32 query rows per sequence, the
+        # regime where the cache stream, not the tensor pipe, bounds the attention
+        d = QWEN3_4B_MLA
+        if small:
+            return cached_decode_workload(name, d, 5, batch=5, prefill_len=512, len_lo=100,
+                                          len_hi=512, block_len=1, num_blocks=2, page_size=32,
+                                          description="5 seqs, prefilled 512, 2 one-token steps")
+        return cached_decode_workload(name, d, 5, batch=64, prefill_len=4096, len_lo=1024,
+                                      len_hi=4096, block_len=1, num_blocks=2, page_size=128,
+                                      description="64 seqs, prefilled 4096, L~U[1024,4096], 2 one-token steps")
     if name == "deepseek_v3_block_parallel":
         d = DEEPSEEK_V3_MLA
         if small:

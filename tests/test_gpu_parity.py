@@ -39,7 +39,7 @@ def _sample_blocks(wl, per_step, seed=0):
 
 
 FULL = [("tiny_fp32", None), ("qwen3_4b_prefill", None), ("qwen3_4b_sliding_gate", None),
-        ("qwen3_4b_cached_decode", 8), ("deepseek_v3_block_parallel", 8)]
+        ("qwen3_4b_cached_decode", 8), ("deepseek_v3_block_parallel", 8), ("qwen3_4b_decode_t1", 8)]
 
 
 @pytest.mark.parametrize("name,per_step", FULL)
@@ -52,3 +52,20 @@ def test_full_size_workload_matches_oracle_on_sampled_blocks(name, per_step):
         step = wl.steps[0]
         sample = [sorted(set(sample[0]) | {0, 1, len(step.kv_len) - 1})]
     check_workload(wl, sample)
+
+
+@pytest.mark.parametrize("case", ["decode_T6", "sliding_T5_gate"])
+def test_partial_query_tiles_match_oracle(case):
+    """block_len x num_heads not a multiple of the 128-row attention tile: the
+    last tile of every block is padded (its extra rows masked and not written)."""
+    from tests.parity import check_workload
+    W = workloads
+    if case == "decode_T6":          # 192 rows per block: one full and one half tile
+        wl = W.cached_decode_workload(case, W.QWEN3_4B_MLA, 6, batch=3, prefill_len=256,
+                                      len_lo=60, len_hi=250, block_len=6, num_blocks=2,
+                                      page_size=64)
+    else:                            # 160 rows, sliding window, gate, NeoX, a masked row
+        d = W.QWEN3_4B_MLA.replace(use_output_gate=True, rope_style="neox")
+        wl = W.prefill_workload(case, d, 7, [300, 129, 17], 5, page_size=128, window=100,
+                                masked_rows=lambda s: (1,) if s == 1 else ())
+    check_workload(wl)
