@@ -19,8 +19,10 @@
 // exchanged with the two other column CTAs of the row group through
 // asynchronous distributed-shared-memory stores (counted on an mbarrier) and
 // added in the same order everywhere; then normalisation, RoPE (column CTA 2
-// holds the 64 rope columns), bf16 rows staged in shared memory and written
-// to the rows' cache slots as whole 384-byte segments.
+// holds the 64 rope columns); each epilogue warp stages its own 32 rows 64
+// columns at a time in shared memory and writes them to the rows' cache
+// slots as whole 128-byte pieces (small staging leaves room for a 5-stage
+// ring: a stage's refill takes longer than 4 stages of MMAs).
 #include "append_tc.cuh"
 
 #include <mutex>
@@ -32,15 +34,15 @@ namespace mla {
 namespace tc {
 namespace {
 
-constexpr int BM = 128, BN = 192, BK = 64, STAGES = 4;
+constexpr int BM = 128, BN = 192, BK = 64, STAGES = 5;
 constexpr int CL = 3, CR = 2, NCTA = CL * CR;     // cluster: 3 column CTAs x 2 row groups
 constexpr int THREADS = 192;                      // TMA, MMA, 4 epilogue warps
 constexpr int EPI = 128;                          // epilogue threads
 constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int OUT_PITCH = BN * 2 + 16;            // staged output row (bytes), bank-conflict free
-constexpr int OFF_OUT = STAGES * STAGE_BYTES;     // staged rows [BM][OUT_PITCH]
-constexpr int OFF_SLOT = OFF_OUT + BM * OUT_PITCH;  // cache slot per staged row [BM] (-1: none)
-constexpr int OFF_RED = OFF_SLOT + BM * 8;        // partial sums of squares [2][CL][BM]
+constexpr int GC = 64;                            // columns staged at a time
+constexpr int OUT_PITCH = GC * 2 + 16;            // staged output row (bytes), bank-conflict free
+constexpr int OFF_OUT = STAGES * STAGE_BYTES;     // per epilogue warp: 32 staged rows [32][OUT_PITCH]
+constexpr int OFF_RED = OFF_OUT + BM * OUT_PITCH; // partial sums of squares [2][CL][BM]
 constexpr int OFF_GAM = OFF_RED + 2 * CL * BM * 4;  // this CTA's kv_a_layernorm gains [BN]
 constexpr int OFF_BAR = OFF_GAM + BN * 4;
 constexpr int SMEM_BYTES = 1024 + OFF_BAR + 256;
@@ -85,8 +87,6 @@ __device__ __forceinline__ void st_async_b32(uint32_t remote_addr, float v, uint
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
                ::"r"(remote_addr), "r"(__float_as_uint(v)), "r"(remote_bar) : "memory");
 }
-// Barrier 1 among the 128 epilogue threads only.
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 __global__ void __launch_bounds__(THREADS, 1) kv_append_tc_kernel(const __grid_constant__ AppendParams P) {
   extern __shared__ uint8_t smem_raw[];
@@ -189,9 +189,8 @@ __global__ void __launch_bounds__(THREADS, 1) kv_append_tc_kernel(const __grid_c
     const int q = warp % 4, r = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const int lat_cols = c < 2 ? BN : 512 - 2 * BN;    // latent columns held here (rest: rope)
-    uint8_t* out_tile = smem + OFF_OUT;
-    long* out_slot = (long*)(smem + OFF_SLOT);
-    uint4* orow = reinterpret_cast<uint4*>(out_tile + r * OUT_PITCH);
+    uint8_t* wst = smem + OFF_OUT + q * 32 * OUT_PITCH;   // this warp's staged rows
+    uint4* orow = reinterpret_cast<uint4*>(wst + lane * OUT_PITCH);
     int i = 0;
     for (int ct = cid; ct < n_ct; ct += ncl, ++i) {
       const int b = i & 1;
@@ -241,68 +240,55 @@ __global__ void __launch_bounds__(THREADS, 1) kv_append_tc_kernel(const __grid_c
       if (bad_slot || bad_pos)
         set_status(P.status, (bad_slot ? MLA_DEV_BAD_SLOT : 0) | (bad_pos ? MLA_DEV_BAD_POSITION : 0));
       const bool store = row_ok && !bad_slot && !bad_pos;
-      // the row's 192 bf16 outputs -> shared memory
+      const long my_slot = store ? slot : -1;
+      // 64 columns at a time: the rows' bf16 values -> this warp's staging
+      // rows -> global, lanes 8k .. 8k+7 writing one 128-byte row piece
 #pragma unroll 1
-      for (int col = 0; col < lat_cols; col += 32) {
-        float v[32];
+      for (int col = 0; col < BN; col += GC) {
+        float v[GC];
         tmem_ld32(lane_addr + col, v);
+        tmem_ld32(lane_addr + col + 32, v + 32);
+        if (col < lat_cols) {
 #pragma unroll
-        for (int k = 0; k < 32; k += 8) {
-          __nv_bfloat162 h2[4];
+          for (int k = 0; k < GC; ++k) v[k] *= rstd * gam[col + k];
+        } else {
+          // rope columns 512..575 (local 128..191 of column CTA 2): pair k is
+          // (2k, 2k+1) interleaved or (k, k + 32) NeoX, rotated by angle k
+          const float2* cs = P.rope + (long)(store ? pos : 0) * 32;
+          float o[GC];
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            h2[u] = __floats2bfloat162_rn(v[k + 2 * u] * rstd * gam[col + k + 2 * u],
-                                          v[k + 2 * u + 1] * rstd * gam[col + k + 2 * u + 1]);
-          orow[(col + k) / 8] = *reinterpret_cast<uint4*>(h2);
-        }
-      }
-      if (c == CL - 1) {
-        // rope columns 512..575 = local 128..191: pair k is (2k, 2k+1) interleaved
-        // or (k, k + 32) NeoX, rotated by angle k of the position
-        float a[32], bb[32];
-        tmem_ld32(lane_addr + lat_cols, a);
-        tmem_ld32(lane_addr + lat_cols + 32, bb);
-        float o[64];
-        const float2* cs = P.rope + (long)(store ? pos : 0) * 32;
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          float x, y;
-          if (P.interleaved) {
-            x = k < 16 ? a[2 * k] : bb[2 * k - 32];
-            y = k < 16 ? a[2 * k + 1] : bb[2 * k - 31];
-          } else {
-            x = a[k];
-            y = bb[k];
+          for (int k = 0; k < 32; ++k) {
+            const float x = P.interleaved ? v[2 * k] : v[k];
+            const float y = P.interleaved ? v[2 * k + 1] : v[k + 32];
+            const float2 t = cs[k];
+            const float rx = x * t.x - y * t.y, ry = y * t.x + x * t.y;
+            if (P.interleaved) { o[2 * k] = rx; o[2 * k + 1] = ry; }
+            else { o[k] = rx; o[k + 32] = ry; }
           }
-          const float2 t = cs[k];
-          const float rx = x * t.x - y * t.y, ry = y * t.x + x * t.y;
-          if (P.interleaved) { o[2 * k] = rx; o[2 * k + 1] = ry; }
-          else { o[k] = rx; o[k + 32] = ry; }
+#pragma unroll
+          for (int k = 0; k < GC; ++k) v[k] = o[k];
         }
 #pragma unroll
-        for (int k = 0; k < 64; k += 8) {
+        for (int k = 0; k < GC; k += 8) {
           __nv_bfloat162 h2[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) h2[u] = __floats2bfloat162_rn(o[k + 2 * u], o[k + 2 * u + 1]);
-          orow[(lat_cols + k) / 8] = *reinterpret_cast<uint4*>(h2);
+          for (int u = 0; u < 4; ++u) h2[u] = __floats2bfloat162_rn(v[k + 2 * u], v[k + 2 * u + 1]);
+          orow[k / 8] = *reinterpret_cast<uint4*>(h2);
         }
+        __syncwarp();
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int row = 4 * it + lane / 8, piece = lane % 8;
+          const long sl = __shfl_sync(0xffffffffu, my_slot, row);
+          if (sl >= 0)
+            reinterpret_cast<uint4*>(P.cache + sl * 576 + n0 + col)[piece] =
+                reinterpret_cast<const uint4*>(wst + row * OUT_PITCH)[piece];
+        }
+        __syncwarp();                 // the staging rows are rewritten by the next group
       }
       // accumulator b may be overwritten by tile i + 2
       tc_fence_before();
       mbar_arrive(&B->acc_empty[b]);
-      out_slot[r] = store ? slot : -1;
-      epi_sync();
-      // epilogue warp e writes rows 32e .. 32e+31, lanes 0..23 one 16-byte piece each
-      const int e = warp - 2;
-#pragma unroll 1
-      for (int k = 0; k < 32; ++k) {
-        const int row = e * 32 + k;
-        const long sl = out_slot[row];
-        if (sl >= 0 && lane < BN * 2 / 16)
-          reinterpret_cast<uint4*>(P.cache + sl * 576 + n0)[lane] =
-              reinterpret_cast<const uint4*>(out_tile + row * OUT_PITCH)[lane];
-      }
-      epi_sync();                 // the staging area is free for the next tile
     }
   }
   __syncwarp();
