@@ -149,9 +149,6 @@ __global__ void __launch_bounds__(THREADS, 1) kv_append_tc_kernel(const __grid_c
           mbar_arrive_expect_tx(&B->full[s], STAGE_BYTES);
           if (kb % CL == c) tma_load_3d_mc(a, &P.tmA, &B->full[s], kb * BK, m0, 0, row_mask);
           if (kb % CR == rg) tma_load_3d_mc(a + A_BYTES, &P.tmB, &B->full[s], kb * BK, n0, 0, col_mask);
-          // the hidden rows of a later k-block are pulled into L2 by their loader
-          const int kp = kb + 2 * STAGES;
-          if (kp < nk && kp % CL == c) tma_prefetch_3d(&P.tmA, kp * BK, m0, 0);
         }
       }
       // every copy into this CTA has landed before it may exit
