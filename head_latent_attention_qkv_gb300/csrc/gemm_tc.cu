@@ -11,6 +11,8 @@
 // whatever its size, so few large copies keep the tensor pipe fed).  Warp 1
 // (one lane) issues tcgen05.mma (M=128, N=BN, K=16) into a TMEM accumulator
 // and frees each stage with tcgen05.commit; warp 2 owns the TMEM allocation.
+// All eight warps run the epilogue (with one warp per scheduler its store
+// loop was latency-bound: a CTA wrote ~4.6 bytes per cycle).
 //
 // Split-K (small M): the K range is divided among the `splitk` CTAs of a
 // cluster along z.  Every CTA writes its fp32 partial tile to its own shared
@@ -31,7 +33,7 @@ namespace mla {
 namespace tc {
 namespace {
 
-constexpr int BM = 128, BK = 64, THREADS = 128;
+constexpr int BM = 128, BK = 64, THREADS = 256;   // 8 warps: all run the epilogue
 
 // k-blocks per stage and stages by tile width: about 192 KB of ring
 template <int BN> struct Cfg;
@@ -78,25 +80,28 @@ __device__ __forceinline__ float4 ld_own_v4(uint32_t addr) {
   return v;
 }
 
-template <typename TC> __device__ __forceinline__ void store4(TC* dst, float a, float b, float c, float d);
+// One 16-byte store of VALS = 16 / sizeof(TC) values.
+template <typename TC> __device__ __forceinline__ void store16(TC* dst, const float* o);
 template <>
-__device__ __forceinline__ void store4<float>(float* dst, float a, float b, float c, float d) {
-  *reinterpret_cast<float4*>(dst) = make_float4(a, b, c, d);
+__device__ __forceinline__ void store16<float>(float* dst, const float* o) {
+  *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
 }
 template <typename T16>
-__device__ __forceinline__ void store4_16(T16* dst, float a, float b, float c, float d) {
-  T16 h[4] = {from_f32<T16>(a), from_f32<T16>(b), from_f32<T16>(c), from_f32<T16>(d)};
-  uint2 u;
-  memcpy(&u, h, 8);
-  *reinterpret_cast<uint2*>(dst) = u;
+__device__ __forceinline__ void store16_16(T16* dst, const float* o) {
+  T16 h[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) h[i] = from_f32<T16>(o[i]);
+  uint4 u;
+  memcpy(&u, h, 16);
+  *reinterpret_cast<uint4*>(dst) = u;
 }
 template <>
-__device__ __forceinline__ void store4<__half>(__half* dst, float a, float b, float c, float d) {
-  store4_16(dst, a, b, c, d);
+__device__ __forceinline__ void store16<__half>(__half* dst, const float* o) {
+  store16_16(dst, o);
 }
 template <>
-__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float a, float b, float c, float d) {
-  store4_16(dst, a, b, c, d);
+__device__ __forceinline__ void store16<__nv_bfloat16>(__nv_bfloat16* dst, const float* o) {
+  store16_16(dst, o);
 }
 
 template <int BN, typename TC>
@@ -192,11 +197,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const bool have = ng > 0 && mbar_wait(accum, 0, status);
   tc_fence_after();
   {
-    const int r = warp * 32 + lane;
-    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    // warp w reads TMEM lanes 32 (w % 4) .. + 31 (its sub-partition), half
+    // w / 4 of the columns
+    const int q = warp % 4, r = q * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
     float* prow = (float*)(smem + r * S::PITCH);
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = (warp / 4) * (BN / 2); c < (warp / 4 + 1) * (BN / 2); c += 32) {
       float v[32];
       if (have) {
         tmem_ld32(lane_addr + c, v);
@@ -216,50 +223,80 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   // work items are (row, 128-column group); lane l holds columns 4l .. 4l+3
   // of its item; a warp takes items warp, warp + 4, ... four at a time so
   // that their shared-memory loads are in flight together ----
-  constexpr int CG = (BN + 127) / 128, U = 4;
+  // work items: VALS consecutive outputs per lane (one 16-byte store), LPR
+  // lanes per output row; an item is one warp-wide store of RPI rows (or of
+  // one of the CG 32-lane column groups of a row)
+  constexpr int VALS = 16 / (int)sizeof(TC), H4 = VALS / 4;
+  constexpr int LPR = BN / VALS;
+  constexpr int RPI = LPR >= 32 ? 1 : 32 / LPR, CG = LPR >= 32 ? LPR / 32 : 1;
+  constexpr int U = VALS == 4 ? 2 : 1, NW = THREADS / 32, MAXS = 8;
   const int r_lo = ks * BM / splitk, r_hi = (ks + 1) * BM / splitk;
-  const int items = (r_hi - r_lo) * CG;
-  for (int base = warp; base < items; base += U * (THREADS / 32)) {
-    float4 v[U];
+  const int items = ((r_hi - r_lo + RPI - 1) / RPI) * CG;
+  const int sub = LPR >= 32 ? 0 : lane / LPR;
+  const int lcol = (LPR >= 32 ? lane : lane % LPR) * VALS;
+  for (int base = warp; base < items; base += U * NW) {
+    float acc[U][VALS];
     uint32_t off[U];
+    int rr[U], cc[U];
     bool live[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int it = base + u * (THREADS / 32);
-      const int r = r_lo + it / CG, col = (it % CG) * 128 + 4 * lane;
-      live[u] = it < items && col < BN;
-      off[u] = smem_u32(smem + (live[u] ? r : 0) * S::PITCH + (live[u] ? col : 0) * 4);
-      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int it = base + u * NW;
+      rr[u] = r_lo + (it / CG) * RPI + sub;
+      cc[u] = (it % CG) * 32 * VALS + lcol;
+      live[u] = it < items && rr[u] < r_hi;
+      off[u] = smem_u32(smem + (live[u] ? rr[u] : r_lo) * S::PITCH + (live[u] ? cc[u] : 0) * 4);
+#pragma unroll
+      for (int i = 0; i < VALS; ++i) acc[u][i] = 0.f;
     }
     if (splitk > 1) {
-      for (int q = 0; q < splitk; ++q) {          // rank order: the same sum in every run
-        float4 t[U];
+      // every peer's partial in flight at once, then added in rank order
+      // (the same sum in every run)
+      float4 t[MAXS][U][H4];
 #pragma unroll
-        for (int u = 0; u < U; ++u) t[u] = ld_peer_v4(mapa(off[u], (uint32_t)q));
+      for (int q = 0; q < MAXS; ++q)
+        if (q < splitk) {
 #pragma unroll
-        for (int u = 0; u < U; ++u) { v[u].x += t[u].x; v[u].y += t[u].y; v[u].z += t[u].z; v[u].w += t[u].w; }
-      }
+          for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int h = 0; h < H4; ++h) t[q][u][h] = ld_peer_v4(mapa(off[u] + 16 * h, (uint32_t)q));
+        }
+#pragma unroll
+      for (int q = 0; q < MAXS; ++q)
+        if (q < splitk) {
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int h = 0; h < H4; ++h) {
+              acc[u][4 * h] += t[q][u][h].x; acc[u][4 * h + 1] += t[q][u][h].y;
+              acc[u][4 * h + 2] += t[q][u][h].z; acc[u][4 * h + 3] += t[q][u][h].w;
+            }
+        }
     } else {
 #pragma unroll
-      for (int u = 0; u < U; ++u) v[u] = ld_own_v4(off[u]);
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int h = 0; h < H4; ++h) {
+          const float4 t = ld_own_v4(off[u] + 16 * h);
+          acc[u][4 * h] = t.x; acc[u][4 * h + 1] = t.y; acc[u][4 * h + 2] = t.z; acc[u][4 * h + 3] = t.w;
+        }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int it = base + u * (THREADS / 32);
-      const int row = m0 + r_lo + it / CG, n = n0 + (it % CG) * 128 + 4 * lane;
+      const int row = m0 + rr[u], n = n0 + cc[u];
       if (!live[u] || row >= M || n >= N) continue;
-      float o[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      float* o = acc[u];
       if (G) {
         const float* g = G + z * sG + (long)row * ldg + n;
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < VALS; ++i)
           if (n + i < N) o[i] = o[i] / (1.f + expf(-g[i]));
       }
       TC* dst = C + z * sC + (long)row * ldc + n;
-      if (n + 4 <= N) {
-        store4<TC>(dst, o[0], o[1], o[2], o[3]);
+      if (n + VALS <= N) {
+        store16<TC>(dst, o);
       } else {
-        for (int i = 0; i < 4 && n + i < N; ++i) dst[i] = from_f32<TC>(o[i]);
+        for (int i = 0; i < VALS && n + i < N; ++i) dst[i] = from_f32<TC>(o[i]);
       }
     }
   }
@@ -382,7 +419,7 @@ long max_active_clusters(int s) {
 
 }  // namespace
 
-void plan_gemm(int M, int N, int K, int batch, int* bn_out, int* split_out) {
+void plan_gemm(int M, int N, int K, int batch, int out_bytes, int* bn_out, int* split_out) {
   const int nk = (K + BK - 1) / BK;
   const int bns[3] = {256, 128, 64};
   double best = 1e30;
@@ -396,7 +433,14 @@ void plan_gemm(int M, int N, int K, int batch, int* bn_out, int* split_out) {
       if (s > 1 && tiles > fit) break;
       if (s > 1 && (nk + kbs - 1) / kbs < s) break;      // at least one stage per split
       const long waves = (tiles + fit - 1) / fit;
-      const double per_cta = ((nk + s - 1) / s) * 4.0 * mma + 3000.0 + 400.0 * s;
+      // measured per-CTA costs (cycles): MMAs of its K share; launch,
+      // prologue and first copies; with split-K the fp32 partial tile read
+      // back through DSMEM (~15 B/cycle) and a cluster barrier per peer;
+      // the rows it stores (~14 B/cycle, 16-byte lanes)
+      const double mainloop = ((nk + s - 1) / s) * 4.0 * mma;
+      const double reduce = s > 1 ? BM * bn * 4.0 / 15.0 + 600.0 * s : 0.0;
+      const double store = (double)BM / s * bn * out_bytes / 14.0;
+      const double per_cta = mainloop + 3000.0 + reduce + store;
       const double t = waves * per_cta;
       if (t < best * 0.98) { best = t; best_bn = bn; best_s = s; }
     }
@@ -408,13 +452,14 @@ void plan_gemm(int M, int N, int K, int batch, int* bn_out, int* split_out) {
 mla_status_t gemm(cudaStream_t st, const GemmArgs& a, uint32_t* status) {
   if (a.M <= 0 || a.N <= 0 || a.batch <= 0) return MLA_OK;
   const bool ok = a.K % 64 == 0 && a.lda % 8 == 0 && a.ldb % 8 == 0 && a.sA % 8 == 0 &&
-                  a.sB % 8 == 0 && a.ldc % 4 == 0 && a.sC % 4 == 0 &&
+                  a.sB % 8 == 0 && a.ldc % (a.out == Out::F32 ? 4 : 8) == 0 &&
+                  a.sC % (a.out == Out::F32 ? 4 : 8) == 0 &&
                   (uintptr_t)a.A % 16 == 0 && (uintptr_t)a.B % 16 == 0 &&
                   (uintptr_t)a.C % 16 == 0;
   if (!ok) return fail(MLA_ERR_UNSUPPORTED, "tcgen05 gemm: K must be a multiple of 64, leading dims "
-                                             "multiples of 8 and pointers 16-byte aligned");
+                                             "and strides 16-byte multiples, pointers 16-byte aligned");
   int bn = 64, splitk = 1;
-  plan_gemm(a.M, a.N, a.K, a.batch, &bn, &splitk);
+  plan_gemm(a.M, a.N, a.K, a.batch, a.out == Out::F32 ? 4 : 2, &bn, &splitk);
   switch (a.out) {
     case Out::F32: return launch_bn<float>(st, a, bn, splitk, status);
     case Out::F16: return launch_bn<__half>(st, a, bn, splitk, status);

@@ -22,7 +22,7 @@ struct GemmArgs {
 
 // Tile width (64, 128 or 256 columns) and split-K factor (CTAs of a cluster
 // along K, 1 = none) the launcher uses for this shape.
-void plan_gemm(int M, int N, int K, int batch, int* bn, int* splitk);
+void plan_gemm(int M, int N, int K, int batch, int out_bytes, int* bn, int* splitk);
 
 // Enqueue C = A B^T (* sigmoid(G)) on `st`.  When the output tiles alone do
 // not fill the GPU (and batch == 1) K is split over a cluster of CTAs whose
