@@ -84,6 +84,8 @@ def test_null_handle_calls_return_invalid_arg():
     desc = _lib.mla_attn_desc_t(num_blocks=1, block_len=16, max_pages=1)
     assert lib.mla_draft_forward(None, None, None, None, None, 1, C.byref(desc), None, None, 0, None) \
         == _lib.MLA_ERR_INVALID_ARG
+    assert lib.mla_draft_forward_after(None, None, None, None, None, 1, C.byref(desc), None, None, 0,
+                                       None, None) == _lib.MLA_ERR_INVALID_ARG
     assert lib.mla_get_device_status(None, None, None) == _lib.MLA_ERR_INVALID_ARG
     assert lib.mla_append_workspace_bytes(None, 4) == 0
     lib.mla_draft_destroy(None)
