@@ -69,3 +69,15 @@ def test_partial_query_tiles_match_oracle(case):
         wl = W.prefill_workload(case, d, 7, [300, 129, 17], 5, page_size=128, window=100,
                                 masked_rows=lambda s: (1,) if s == 1 else ())
     check_workload(wl)
+
+
+@pytest.mark.parametrize("page_size", [16, 256])
+def test_page_sizes_match_oracle(page_size):
+    """Pages smaller than the 128-key tile (one copy per page segment) and
+    larger ones (several tiles per page), with ragged contexts and permuted
+    physical pages."""
+    from tests.parity import check_workload
+    W = workloads
+    wl = W.prefill_workload(f"pages{page_size}", W.QWEN3_4B_MLA, 9, [150, 40, 333], 16,
+                            page_size=page_size)
+    check_workload(wl)
