@@ -345,6 +345,8 @@ def main():
             per.append(cpu_baseline(args.workload, budget_s=max(2.0, 60.0 / max(args.steps, 1))))
         v = statistics.median(p["value"] for p in per)
         line = base_line(args, 1)
+        line["config"].update({"schedule": "fp64 oracle, one sampled block at a time, host cores",
+                               "l2": "n/a (CPU)"})
         line.update({"impl": "reference", "value": v, "ms_per_step": None,
                      "dtype": "f64", "cpu_baseline": dict(per[-1], value=v),
                      "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
