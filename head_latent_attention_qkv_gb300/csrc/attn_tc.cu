@@ -4,7 +4,9 @@
 // 512-wide latent value space).
 //
 // Work unit: one query block and 128 consecutive rows of Q_abs (rows are
-// (token, head) pairs, token-major), handled by a cluster of two CTAs, one per
+// (token, head) pairs, token-major; a block's last tile is padded when
+// block_len x heads is not a multiple of 128: its extra rows are fully masked
+// and written nowhere), handled by a cluster of two CTAs, one per
 // half of the 512 latent value dims.  A 128 x 512 fp32 accumulator would fill
 // all of an SM's tensor memory, so each CTA keeps O for its 256 value dims and
 // computes the full 576-wide scores itself (QK^T is repeated by the two
@@ -34,12 +36,12 @@
 //                  when the running max grows by more than 2^8), P -> bf16
 //   TMA warp     : page rows of the key range (once), Q, key chunks, values
 // The key range of a unit may be split (grid y) when units alone do not fill
-// the GPU ([MLA] forward_mqa num_kv_splits); the pairs of one unit then form
+// the GPU (the blog's forward_mqa num_kv_splits); the pairs of one unit then form
 // one cluster of 2 x splits CTAs.  Every CTA stages its normalised partial
 // output, its log2-sum-exp and visibility counts in its own shared memory
 // (over the Q and V buffers, free after the last P V); after a cluster
 // barrier split s combines rows [128 s / splits, 128 (s + 1) / splits) of its
-// value half from all splits, in split order, by log-sum-exp ([MLA]
+// value half from all splits, in split order, by log-sum-exp (the blog's
 // forward_mha merge_attn_states) and writes them as fp16 whole rows.
 #include "attn_tc.cuh"
 

@@ -19,9 +19,9 @@
 // memory; CTA j of the cluster then adds the partials of rows
 // [128 j / splitk, 128 (j+1) / splitk) from all of them through distributed
 // shared memory, always in rank order (deterministic), applies the epilogue
-// and stores.  Without split-K the CTA stages its own tile the same way.  The
-// store is done row by row by whole warps, so each row leaves as a coalesced
-// write.
+// and stores.  Without split-K the CTA stages its own tile the same way.  Each
+// lane stores 16 bytes and a warp covers whole row pieces (256 to 512 bytes),
+// so every store instruction is a coalesced write.
 #include "gemm_tc.cuh"
 
 #include <mutex>
