@@ -175,7 +175,12 @@ mla_status_t mla_latent_cache_append(mla_handle_t *h, const void *hidden,
  * block_slot_mapping: device int64 [nb*T] -- when non-NULL the block's own
  * latents are written to the cache there before attending; when NULL they
  * must already be in the cache (mla_latent_cache_append).  out: device
- * [nb*T, hidden_size].  Fully masked query rows come out as exact +0. */
+ * [nb*T, hidden_size].  Fully masked query rows come out as exact +0.
+ * Any block_len.  bf16 layers run the tensor-core kernels, which need
+ * kv_lora_rank 512, qk_rope_head_dim 64, a page_size of 16, 32, 64 or a
+ * multiple of 128, hidden_size / q_lora_rank / H*v_head multiples of 64;
+ * other bf16 shapes return MLA_ERR_UNSUPPORTED before any launch (the fp32
+ * layer has no such limits).  The workspace must be 256-byte aligned. */
 mla_status_t mla_draft_forward(mla_handle_t *h, const void *hidden,
                                const int32_t *positions,
                                const int64_t *block_slot_mapping, void *cache,
