@@ -189,6 +189,18 @@ mla_status_t validate(const mla_config_t& c, const mla_weights_t& w, Layout* l) 
     return fail(MLA_ERR_UNSUPPORTED, "kv_lora_rank must be a multiple of 16 and at most 512");
   if (l->L > 1024)
     return fail(MLA_ERR_UNSUPPORTED, "kv_lora_rank + qk_rope_head_dim must be at most 1024");
+  if (c.dtype == MLA_BF16) {
+    // the tensor-core kernels: latent attention on 512 + 64 dims, 64-wide K
+    // slices in every projection, 16-byte output rows
+    const int ps = c.page_size;
+    if (l->rkv != 512 || l->dr != 64)
+      return fail(MLA_ERR_UNSUPPORTED, "bf16 layers: kv_lora_rank 512 and qk_rope_head_dim 64");
+    if (ps % 16 || (ps < 128 && 128 % ps) || (ps > 128 && ps % 128))
+      return fail(MLA_ERR_UNSUPPORTED, "bf16 layers: page_size 16, 32, 64 or a multiple of 128");
+    if (l->D % 64 || l->rq % 64 || l->dn % 64 || (l->H * l->dv) % 64 || l->dv % 8)
+      return fail(MLA_ERR_UNSUPPORTED, "bf16 layers: hidden_size, q_lora_rank, qk_nope_head_dim and "
+                                       "num_heads * v_head_dim multiples of 64, v_head_dim of 8");
+  }
   return MLA_OK;
 }
 

@@ -178,9 +178,10 @@ mla_status_t mla_latent_cache_append(mla_handle_t *h, const void *hidden,
  * [nb*T, hidden_size].  Fully masked query rows come out as exact +0.
  * Any block_len.  bf16 layers run the tensor-core kernels, which need
  * kv_lora_rank 512, qk_rope_head_dim 64, a page_size of 16, 32, 64 or a
- * multiple of 128, hidden_size / q_lora_rank / H*v_head multiples of 64;
- * other bf16 shapes return MLA_ERR_UNSUPPORTED before any launch (the fp32
- * layer has no such limits).  The workspace must be 256-byte aligned. */
+ * multiple of 128, hidden_size, q_lora_rank, qk_nope_head_dim and
+ * num_heads * v_head_dim multiples of 64; mla_draft_init rejects other bf16
+ * shapes with MLA_ERR_UNSUPPORTED (the fp32 layer has no such limits).  The
+ * workspace must be 256-byte aligned. */
 mla_status_t mla_draft_forward(mla_handle_t *h, const void *hidden,
                                const int32_t *positions,
                                const int64_t *block_slot_mapping, void *cache,

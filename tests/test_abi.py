@@ -70,6 +70,17 @@ def test_invalid_config_is_rejected(field, value):
     assert lib.mla_last_error()
 
 
+@pytest.mark.parametrize("field,value", [("kv_lora_rank", 256), ("qk_rope_head_dim", 32),
+                                         ("page_size", 48), ("page_size", 192), ("hidden_size", 2600)])
+def test_bf16_shapes_without_a_kernel_are_unsupported_at_init(field, value):
+    cfg = api.make_config(QWEN3_4B_MLA, 64)
+    setattr(cfg, field, value)
+    w = _lib.mla_weights_t(**{k: 256 for k in _lib.WEIGHT_FIELDS})   # non-NULL, never read
+    h = C.c_void_p()
+    st = lib.mla_draft_init(C.byref(cfg), C.byref(w), C.c_void_p(256), 1 << 40, None, C.byref(h))
+    assert st == _lib.MLA_ERR_UNSUPPORTED and not h.value, lib.mla_last_error()
+
+
 def test_missing_weights_are_rejected_before_any_device_work():
     cfg = api.make_config(QWEN3_4B_MLA, 64)
     w = _lib.mla_weights_t()          # every pointer NULL
