@@ -158,6 +158,23 @@ def measured_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def max_over_ranks(x, world):
+    """Largest value of x over the ranks (the job is as fast as its slowest
+    replica); works on the process group's backend, gloo or NCCL."""
+    if world <= 1:
+        return x
+    import torch
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_replica, world, seconds):
+    """Whole-job throughput: every replica processed its own full workload."""
+    return world * tokens_per_replica / seconds
+
+
 def run_ours(args, rank, world):
     import torch
     from head_latent_attention_qkv_gb300 import api, workloads
@@ -229,13 +246,10 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize()
         t_app = [e[0].elapsed_time(e[1]) for e in ev]
     clocks.__exit__(None, None, None)
-    ms = sum(t_step) / len(t_step)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(sum(t_step) / len(t_step), world)
     assert api.mla_get_device_status(dev.handle) == 0, "device status word set"
-    e2e = measure_e2e(args, dev, step, torch)
+    e2e_s, h2d, d2h = measure_e2e(args, dev, step, torch)
+    e2e = (max_over_ranks(e2e_s, world), h2d, d2h)
     return dict(ms=ms, ms_append=sum(t_app) / len(t_app) if t_app else None, flops=fl,
                 clocks=clocks.summary(), e2e=e2e, graphs=not args.no_graph, launches=launches)
 
@@ -363,7 +377,7 @@ def main():
         return
     hbm, bf16, bf16_sus, src = measured_peaks()
     fl = r["flops"]
-    value = world * fl["block_tokens"] / (r["ms"] * 1e-3)
+    value = job_tokens_per_s(fl["block_tokens"], world, r["ms"] * 1e-3)
     tflops = fl["total"] / (r["ms"] * 1e-3) / 1e12
     if fl["append"]:
         t_app = r["ms_append"] * 1e-3
@@ -383,7 +397,7 @@ def main():
                      "frac": ach / bf16,
                      "traffic": append_traffic() if fl["append"] and args.workload == WORKLOAD else None,
                      "peak_source": f"{src} bf16 burst"},
-        "e2e": {"value": world * fl["block_tokens"] / e2e_s, "unit": "tokens/s",
+        "e2e": {"value": job_tokens_per_s(fl["block_tokens"], world, e2e_s), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": r["launches"] * args.steps,
         "cuda_graphs": r["graphs"],
