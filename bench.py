@@ -72,8 +72,9 @@ def algorithmic_flops(wl):
 
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons, sampled every 20 ms by a
-    background nvidia-smi while the GPU runs the warm-up and timed steps
-    (started, and its first line awaited, before the warm-up)."""
+    background nvidia-smi while the GPU runs the warm-up, the timed steps and
+    untimed replays of the same step just before and after them (started, and
+    its first line awaited, before the warm-up)."""
     Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
@@ -224,6 +225,19 @@ def run_ours(args, rank, world):
             for g in graphs:
                 g.replay()
         run_s, run_a = graphs[0].replay, graphs[1].replay
+
+    def hold_load(n_more, limit_s=2.0):
+        # untimed replays of the same step until the clock sampler (20 ms
+        # period) has n_more samples of this load: a short timed region
+        # alone can end before its first sample
+        if clocks.proc is None:
+            return
+        target, t0 = len(clocks.samples) + n_more, time.time()
+        while len(clocks.samples) < target and time.time() - t0 < limit_s:
+            run_s()
+            torch.cuda.synchronize()
+
+    hold_load(1)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -245,6 +259,7 @@ def run_ours(args, rank, world):
             ev[k][1].record(stream)
         torch.cuda.synchronize()
         t_app = [e[0].elapsed_time(e[1]) for e in ev]
+    hold_load(2)
     clocks.__exit__(None, None, None)
     ms = max_over_ranks(sum(t_step) / len(t_step), world)
     assert api.mla_get_device_status(dev.handle) == 0, "device status word set"
