@@ -43,10 +43,6 @@ template <typename TN, typename TQ>
 void q_rope_split(cudaStream_t st, const mla_handle* h, const float* q, long ldq, int M,
                   const int32_t* positions, TN* q_nope, TQ* q_abs, bool pdl = false);
 
-// out[i] = (T) in[i] for n elements.
-template <typename T>
-void f32_to(cudaStream_t st, const float* in, T* out, long n);
-
 // Latent attention: O_lat[m, h, :rkv] = sum_j p_j c_j over the visible keys of
 // each query's block, scores scale * <Q_abs[m,h,:], entry_j>.
 template <typename TQ, typename TC>

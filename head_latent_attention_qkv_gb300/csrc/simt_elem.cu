@@ -121,30 +121,7 @@ q_rope_split_kernel(const float* __restrict__ q, long ldq, const int32_t* __rest
   }
 }
 
-template <typename T>
-__global__ void f32_to_kernel(const float* __restrict__ in, T* __restrict__ out, long n) {
-  pdl_wait();
-  for (long i = (blockIdx.x * (long)blockDim.x + threadIdx.x) * 4; i < n; i += (long)gridDim.x * blockDim.x * 4) {
-    if (i + 4 <= n) {
-      const float4 v = *reinterpret_cast<const float4*>(in + i);
-      out[i] = from_f32<T>(v.x); out[i + 1] = from_f32<T>(v.y);
-      out[i + 2] = from_f32<T>(v.z); out[i + 3] = from_f32<T>(v.w);
-    } else {
-      for (long k = i; k < n; ++k) out[k] = from_f32<T>(in[k]);
-    }
-  }
-}
-
 }  // namespace
-
-template <typename T>
-void f32_to(cudaStream_t st, const float* in, T* out, long n) {
-  if (n <= 0) return;
-  const long blocks = (n / 4 + 255) / 256;
-  f32_to_kernel<T><<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(in, out, n);
-}
-template void f32_to<float>(cudaStream_t, const float*, float*, long);
-template void f32_to<__nv_bfloat16>(cudaStream_t, const float*, __nv_bfloat16*, long);
 
 template <typename T>
 void kv_finish(cudaStream_t st, const mla_handle* h, const float* kv, long ld, int n,
