@@ -132,6 +132,36 @@ def mla_draft_forward_after(h: Handle, hidden, positions, block_slot_mapping, ca
     return out
 
 
+def mla_latent_cache_append_noalloc(h: Handle, hidden, positions, slot_mapping, cache,
+                                    stream=None):
+    """The allocation-free append (library-owned fixed scratch; at most
+    mla_append_noalloc_max_tokens(h) tokens per call)."""
+    check(lib.mla_latent_cache_append_noalloc(h.h, _ptr(hidden), _ptr(positions),
+                                              _ptr(slot_mapping), hidden.shape[0], _ptr(cache),
+                                              cache.shape[0], _stream(stream)),
+          "mla_latent_cache_append_noalloc")
+
+
+def mla_append_noalloc_max_tokens(h: Handle) -> int:
+    return int(lib.mla_append_noalloc_max_tokens(h.h))
+
+
+def mla_kernel_launches(h: Handle) -> int:
+    return int(lib.mla_kernel_launches(h.h))
+
+
+def mla_cache_entry_dim(dims, page_size: int = 64) -> int:
+    return int(lib.mla_cache_entry_dim(C.byref(make_config(dims, page_size))))
+
+
+def mla_cache_page_bytes(dims, page_size: int) -> int:
+    return int(lib.mla_cache_page_bytes(C.byref(make_config(dims, page_size))))
+
+
+def mla_weight_arena_bytes(dims, page_size: int = 64) -> int:
+    return int(lib.mla_weight_arena_bytes(C.byref(make_config(dims, page_size))))
+
+
 def mla_get_device_status(h: Handle, stream=None) -> int:
     bits = C.c_int32(0)
     lib.mla_get_device_status(h.h, _stream(stream), C.byref(bits))
