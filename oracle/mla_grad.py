@@ -19,6 +19,11 @@ A fully masked query row outputs exactly zero, so nothing flows back through
 it; a key no query sees receives no gradient.  The tests pin this module to
 ``oracle.mla`` by value (forward) and by central finite differences of
 ``oracle.mla``'s forward (gradients), not to itself.
+
+``latent_attention_backward`` states the attention part alone in the latent
+space (what a backward kernel over the latent cache computes: dQ_abs and the
+gradient of the cache entries, which are keys and values at once), written as
+explicit formulas and pinned by finite differences and by autograd.
 """
 from __future__ import annotations
 
@@ -117,3 +122,47 @@ def block_gradients(d, weights, x, positions, ctx, ctx_positions, vis, grad_out)
     grads = {n: (np.zeros(tuple(t.shape)) if gi is None else gi.detach().numpy())
              for n, t, gi in zip(names, [xt, ct] + list(w.values()), g)}
     return out.detach().numpy(), grads
+
+
+# ---------------------------------------------------------------------------
+# The latent-space attention and its backward (what an attention-backward
+# kernel over the latent cache computes)
+# ---------------------------------------------------------------------------
+def latent_attention(q_abs, entries, vis, scale, rkv):
+    """Absorbed attention over the latent cache (MLA blog, forward_mqa): rows
+    of Q_abs [R, L] score every cache entry [J, L] (L = rkv + rope), softmax
+    over the visible ones (vis [R, J]), output the probability-weighted latent
+    c = entries[:, :rkv]; a row with no visible key is exactly zero.
+    Returns (o_lat [R, rkv], p [R, J])."""
+    q = np.asarray(q_abs, np.float64)
+    e = np.asarray(entries, np.float64)
+    s = np.where(vis, (q @ e.T) * scale, -np.inf)
+    any_key = vis.any(axis=1)
+    m = np.where(any_key, s.max(axis=1), 0.0)
+    with np.errstate(invalid="ignore"):
+        p = np.where(vis, np.exp(s - m[:, None]), 0.0)
+    l = p.sum(axis=1)
+    p = np.where(any_key[:, None], p / np.where(any_key, l, 1.0)[:, None], 0.0)
+    return p @ e[:, :rkv], p
+
+
+def latent_attention_backward(q_abs, entries, vis, scale, rkv, d_o_lat):
+    """Gradients of sum(o_lat * d_o_lat) for ``latent_attention``.
+
+    With P the probabilities, V = entries[:, :rkv] and dO = d_o_lat:
+      dP = dO V^T;  dS = P * (dP - rowsum(dP * P))   (softmax derivative,
+      rowsum(dP * P) = rowsum(dO * o_lat));
+      dQ_abs = scale * dS E;  dE = scale * dS^T Q_abs, plus P^T dO on the
+      first rkv columns (the entries are both keys and values).
+    Rows with no visible key have P = 0 and pass nothing back.
+    Returns (dQ_abs [R, L], dE [J, L])."""
+    q = np.asarray(q_abs, np.float64)
+    e = np.asarray(entries, np.float64)
+    do = np.asarray(d_o_lat, np.float64)
+    o, p = latent_attention(q, e, vis, scale, rkv)
+    dp = do @ e[:, :rkv].T
+    ds = p * (dp - np.sum(do * o, axis=1, keepdims=True))
+    dq = scale * (ds @ e)
+    de = scale * (ds.T @ q)
+    de[:, :rkv] += p.T @ do
+    return dq, de

@@ -159,3 +159,71 @@ def test_planted_mistakes_fail_the_pins(monkeypatch, mutation):
         orig = torch.sigmoid
         monkeypatch.setattr(mla_grad.torch, "sigmoid", lambda t: orig(t).detach())
     assert not _pins_pass()
+
+
+def _latent_problem(seed=3, R=6, J=9, rkv=8, dr=4):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((R, rkv + dr))
+    e = rng.standard_normal((J, rkv + dr))
+    vis = rng.random((R, J)) < 0.7
+    vis[2] = False                       # a row that sees nothing
+    vis[0] = True
+    do = rng.standard_normal((R, rkv))
+    return q, e, vis, 0.4, rkv, do, rng
+
+
+def test_latent_attention_backward_matches_finite_differences():
+    q, e, vis, scale, rkv, do, rng = _latent_problem()
+    dq, de = mla_grad.latent_attention_backward(q, e, vis, scale, rkv, do)
+    f = lambda qq, ee: np.sum(mla_grad.latent_attention(qq, ee, vis, scale, rkv)[0] * do)
+    eps = 1e-6
+    for which, grad in (("q", dq), ("e", de)):
+        for _ in range(3):
+            d = rng.standard_normal(q.shape if which == "q" else e.shape)
+            if which == "q":
+                fd = (f(q + eps * d, e) - f(q - eps * d, e)) / (2 * eps)
+            else:
+                fd = (f(q, e + eps * d) - f(q, e - eps * d)) / (2 * eps)
+            an = float(np.sum(grad * d))
+            assert abs(fd - an) <= 1e-7 * max(1.0, abs(an)), (which, fd, an)
+
+
+def test_latent_attention_forward_matches_a_per_row_softmax():
+    # scores, softmax over the visible keys and latent average, row by row
+    q, e, vis, scale, rkv, do, _ = _latent_problem()
+    o, p = mla_grad.latent_attention(q, e, vis, scale, rkv)
+    s = np.where(vis, (q @ e.T) * scale, -np.inf)
+    for r in range(q.shape[0]):
+        if not vis[r].any():
+            assert np.all(o[r] == 0.0)
+            continue
+        w = np.exp(s[r] - s[r][vis[r]].max())
+        w[~vis[r]] = 0.0
+        np.testing.assert_allclose(o[r], (w / w.sum()) @ e[:, :rkv], rtol=1e-13, atol=1e-15)
+
+
+def test_latent_attention_backward_agrees_with_autograd():
+    import torch
+    q, e, vis, scale, rkv, do, _ = _latent_problem(seed=5)
+    dq, de = mla_grad.latent_attention_backward(q, e, vis, scale, rkv, do)
+    qt = torch.tensor(q, requires_grad=True)
+    et = torch.tensor(e, requires_grad=True)
+    vt = torch.tensor(vis)
+    s = torch.where(vt, (qt @ et.T) * scale, torch.full((q.shape[0], e.shape[0]), -torch.inf,
+                                                        dtype=torch.float64))
+    anyk = vt.any(dim=1, keepdim=True)
+    p = torch.softmax(torch.where(anyk, s, torch.zeros_like(s)), dim=1) * anyk
+    (gq, ge) = torch.autograd.grad(((p @ et[:, :rkv]) * torch.tensor(do)).sum(), [qt, et])
+    np.testing.assert_allclose(dq, gq.numpy(), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(de, ge.numpy(), rtol=1e-12, atol=1e-14)
+
+
+def test_latent_attention_backward_ignores_rows_without_keys():
+    q, e, vis, scale, rkv, do, rng = _latent_problem()
+    dq1, de1 = mla_grad.latent_attention_backward(q, e, vis, scale, rkv, do)
+    do2 = do.copy()
+    do2[2] = 50 * rng.standard_normal(rkv)
+    dq2, de2 = mla_grad.latent_attention_backward(q, e, vis, scale, rkv, do2)
+    np.testing.assert_array_equal(dq1, dq2)
+    np.testing.assert_array_equal(de1, de2)
+    assert np.all(dq1[2] == 0.0)
