@@ -37,6 +37,11 @@
  *    message is available from mla_last_error().  Index errors found on the
  *    device (slot, page or position out of range) skip the offending access
  *    and set a bit in a device status word read by mla_get_device_status().
+ *  - Devices: one GPU per process.  A handle works on the device that was
+ *    current at mla_draft_init, which must be current for every call; the
+ *    library keeps per-process launch settings (kernel shared-memory limits,
+ *    the SM count and cluster occupancy) taken from the first device it
+ *    runs on.  The multi-GPU model is one process per GPU.
  */
 #ifndef MLA_DRAFT_H
 #define MLA_DRAFT_H
