@@ -66,8 +66,11 @@ class OracleRun:
             need[self.key_slots(step, b)[vis]] = True
         return need
 
-    def forward_blocks(self, step, blocks, write_block_latents=True):
-        """Oracle output rows [T, D] for each block in ``blocks`` (dict)."""
+    def forward_blocks(self, step, blocks, write_block_latents=True, round_output=True):
+        """Oracle output rows [T, D] for each block in ``blocks`` (dict), held
+        in the layer dtype (``round_output=False``: the fp64 values before
+        that storage rounding)."""
+        rnd = (lambda x: mla.round_to_dtype(self.d, x)) if round_output else (lambda x: x)
         d, w, T = self.d, self.wl.weights, self.wl.block_len
         blocks = list(blocks)
         if write_block_latents and step.block_slots is not None and blocks:
@@ -94,11 +97,10 @@ class OracleRun:
             x = step.block_hidden[rows]
             if not segs:
                 o = np.zeros((T, d.num_heads, d.v_head_dim))
-                out[b] = mla.round_to_dtype(d, mla.output_projection(d, w, x, o))
+                out[b] = rnd(mla.output_projection(d, w, x, o))
                 continue
             v = vis[:, np.concatenate(cols)]
-            out[b] = mla.round_to_dtype(
-                d, mla.block_forward(d, w, x, step.block_positions[rows], segs, v))
+            out[b] = rnd(mla.block_forward(d, w, x, step.block_positions[rows], segs, v))
         return out
 
 
