@@ -3,26 +3,25 @@
 //   kv = hidden @ W_kva^T                     (W_kva: the kv_lora_rank + qk_rope rows)
 //   cache[slot] = [RMSNorm(kv[:512]) * gamma | RoPE(kv[512:], position)]   (bf16)
 //
-// Persistent kernel.  A cluster of 3 x 2 CTAs works on 256 token rows at a
-// time (a "cluster tile") and loops over cluster tiles: CTA (c, r) computes
-// output columns [192c, 192c + 192) of rows [128r, 128r + 128) of the tile.
-// Every 128 x 64 slice of hidden states is multicast to the three CTAs of its
-// row group and every 192 x 64 slice of weights to the two CTAs of its column
-// group, so each cluster reads its hidden rows and each weight slice once; a
-// TMA copy costs about the same SM time whatever its size, so the copies of a
-// k-block are issued by different CTAs in turn (hidden: CTA c = kb mod 3 of
-// the row group, weights: CTA r = kb mod 2 of the column group).
+// Persistent kernel.  A cluster of 3 CTAs works on 128 token rows at a time
+// (a "tile") and loops over tiles: CTA c computes output columns
+// [192c, 192c + 192) of the tile's rows.  Every CTA streams its own operands
+// with TMA: the tile's hidden-state rows (the three CTAs of a cluster read the
+// same rows, so two of the three reads hit L2) and its 192 weight rows (read
+// by every cluster, L2-resident).  One ring stage holds KBS consecutive
+// 64-wide k-blocks of both operands, each brought by a single chunked copy.
 //
-// Warp 0 streams the ring, warp 1 issues the MMAs into one of two tensor-
-// memory accumulators (192 columns each), warps 2-5 run the epilogue of the
+// Warps 0 and 6 stream the ring (hidden states and weights: a TMA copy keeps
+// its issuing thread for about 550 cycles whatever its size, while copies of
+// different warps proceed side by side), warp 1 issues the MMAs into one of
+// two tensor-memory accumulators (192 columns each), warps 2-5 run the epilogue of the
 // previous tile meanwhile: per row the sum of squares of its latent columns,
-// exchanged with the two other column CTAs of the row group through
-// asynchronous distributed-shared-memory stores (counted on an mbarrier) and
-// added in the same order everywhere; then normalisation, RoPE (column CTA 2
-// holds the 64 rope columns); each epilogue warp stages its own 32 rows 64
-// columns at a time in shared memory and writes them to the rows' cache
-// slots as whole 128-byte pieces (small staging leaves room for a 5-stage
-// ring: a stage's refill takes longer than 4 stages of MMAs).
+// exchanged with the two other CTAs of the cluster through asynchronous
+// distributed-shared-memory stores (counted on an mbarrier) and added in the
+// same order everywhere; then normalisation, RoPE (CTA 2 holds the 64 rope
+// columns); each epilogue warp stages its own 32 rows 64 columns at a time in
+// shared memory and writes them to the rows' cache slots as whole 128-byte
+// pieces.
 #include "append_tc.cuh"
 
 #include <mutex>
@@ -34,11 +33,17 @@ namespace mla {
 namespace tc {
 namespace {
 
-constexpr int BM = 128, BN = 192, BK = 64, STAGES = 5;
-constexpr int CL = 3, CR = 2, NCTA = CL * CR;     // cluster: 3 column CTAs x 2 row groups
-constexpr int THREADS = 192;                      // TMA, MMA, 4 epilogue warps
+#ifndef MLA_APPEND_KBS
+#define MLA_APPEND_KBS 1
+#endif
+constexpr int BM = 128, BN = 192, BK = 64;
+constexpr int KBS = MLA_APPEND_KBS;               // k-blocks per ring stage (one copy per operand)
+constexpr int STAGES = KBS == 1 ? 5 : KBS == 2 ? 2 : 1;
+constexpr int CL = 3;                             // cluster: the 3 column CTAs of a row tile
+constexpr int THREADS = 224;                      // TMA (A), MMA, 4 epilogue warps, TMA (B)
 constexpr int EPI = 128;                          // epilogue threads
-constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int A_BYTES = KBS * BM * BK * 2, B_BYTES = KBS * BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int GC = 64;                            // columns staged at a time
 constexpr int OUT_PITCH = GC * 2 + 16;            // staged output row (bytes), bank-conflict free
 constexpr int OFF_OUT = STAGES * STAGE_BYTES;     // per epilogue warp: 32 staged rows [32][OUT_PITCH]
@@ -50,8 +55,8 @@ constexpr uint32_t TMEM_COLS = 512, ACC_STRIDE = 256;   // two accumulators of B
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 struct AppendParams {
-  CUtensorMap tmA;            // hidden [M, D]
-  CUtensorMap tmB;            // W_kva [576, D]
+  CUtensorMap tmA;            // hidden [M, D], chunked view, box 128 rows x KBS k-blocks
+  CUtensorMap tmB;            // W_kva [576, D], chunked view, box 192 rows x KBS k-blocks
   int M, K;
   const int32_t* positions;
   const int64_t* slots;
@@ -65,7 +70,7 @@ struct AppendParams {
 };
 
 struct Bars {
-  uint64_t full[STAGES], empty[STAGES];   // ring: bytes landed / all six CTAs done with the slot
+  uint64_t full[STAGES], empty[STAGES];   // ring: both copies landed / this CTA's MMAs done with the slot
   uint64_t acc_full[2], acc_empty[2];     // accumulator b written (MMA) / read (epilogue)
   uint64_t red_full[2];                   // the two peers' partial sums of tile parity b landed
   uint64_t red_free[2];                   // the two peers have read what this CTA sent them
@@ -96,20 +101,17 @@ __global__ void __launch_bounds__(THREADS, 1) kv_append_tc_kernel(const __grid_c
   float* gam = (float*)(smem + OFF_GAM);
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const uint32_t rank = cluster_ctarank();           // c + 3 r
-  const int c = (int)rank % CL, rg = (int)rank / CL; // column group (== blockIdx.x), row group
+  const int c = (int)cluster_ctarank();              // column group (== blockIdx.x)
   const int n0 = c * BN;
   const int nk = (P.K + BK - 1) / BK;
-  const int n_ct = (P.M + CR * BM - 1) / (CR * BM);  // cluster tiles of 256 rows
-  const int cid = blockIdx.y / CR, ncl = gridDim.y / CR;
-  const uint16_t all_mask = (uint16_t)((1u << NCTA) - 1);
-  const uint16_t row_mask = (uint16_t)(0x7u << (CL * rg));            // CTAs of this row group
-  const uint16_t col_mask = (uint16_t)((1u << c) | (1u << (c + CL)));  // CTAs of this column group
+  const int ns = (nk + KBS - 1) / KBS;               // ring stages per tile
+  const int n_ct = (P.M + BM - 1) / BM;              // row tiles of 128
+  const int cid = blockIdx.y, ncl = gridDim.y;
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&B->full[s], 1);
-      mbar_init(&B->empty[s], NCTA);
+      mbar_init(&B->full[s], 2);          // one arrival per producer warp
+      mbar_init(&B->empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&B->acc_full[b], 1);
@@ -127,32 +129,32 @@ __global__ void __launch_bounds__(THREADS, 1) kv_append_tc_kernel(const __grid_c
   if (warp == 1) tmem_alloc(&B->tmem_slot, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();             // peers' barriers exist before any multicast or remote store
+  cluster_sync_all();             // peers' barriers exist before any remote store
   tc_fence_after();
   const uint32_t tmem = B->tmem_slot;
   if (tid == 0) pdl_trigger();
   pdl_wait();
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 6) {
     if (lane == 0) {
-      // ---- TMA producer ----
-      prefetch_tmap(&P.tmA);
-      prefetch_tmap(&P.tmB);
+      // ---- TMA producers: warp 0 the hidden-state rows, warp 6 the weights ----
+      const bool is_a = warp == 0;
+      const CUtensorMap* map = is_a ? &P.tmA : &P.tmB;
+      prefetch_tmap(map);
       int g = 0;
       bool ok = true;
       for (int ct = cid; ct < n_ct && ok; ct += ncl) {
-        const int m0 = (ct * CR + rg) * BM;
-        for (int kb = 0; kb < nk; ++kb, ++g) {
+        const int row = is_a ? ct * BM : n0;
+        for (int ks = 0; ks < ns; ++ks, ++g) {
           const int s = g % STAGES;
           if (!wait_bar(B, &B->empty[s], ((g / STAGES) & 1) ^ 1, P.status)) { ok = false; break; }
           uint8_t* a = smem + s * STAGE_BYTES;
-          mbar_arrive_expect_tx(&B->full[s], STAGE_BYTES);
-          if (kb % CL == c) tma_load_3d_mc(a, &P.tmA, &B->full[s], kb * BK, m0, 0, row_mask);
-          if (kb % CR == rg) tma_load_3d_mc(a + A_BYTES, &P.tmB, &B->full[s], kb * BK, n0, 0, col_mask);
+          mbar_arrive_expect_tx(&B->full[s], is_a ? A_BYTES : B_BYTES);
+          tma_load_3d(is_a ? a : a + A_BYTES, map, &B->full[s], 0, row, ks * KBS);
         }
       }
       // every copy into this CTA has landed before it may exit
-      for (int i = max(0, g - STAGES); i < g; ++i) mbar_wait_cluster(&B->full[i % STAGES], (i / STAGES) & 1, P.status);
+      for (int i = max(0, g - STAGES); i < g; ++i) mbar_wait(&B->full[i % STAGES], (i / STAGES) & 1, P.status);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -165,15 +167,20 @@ __global__ void __launch_bounds__(THREADS, 1) kv_append_tc_kernel(const __grid_c
         if (!wait_bar(B, &B->acc_empty[b], ((i >> 1) & 1) ^ 1, P.status)) break;   // epilogue done with it
         tc_fence_after();
         const uint32_t d = tmem + b * ACC_STRIDE;
-        for (int kb = 0; kb < nk; ++kb, ++g) {
+        for (int ks = 0; ks < ns; ++ks, ++g) {
           const int s = g % STAGES;
           if (!wait_bar(B, &B->full[s], (g / STAGES) & 1, P.status)) { ok = false; break; }
           tc_fence_after();
           const uint8_t* a = smem + s * STAGE_BYTES;
-          const uint64_t da = smem_desc_sw128(a), db = smem_desc_sw128(a + A_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) mma_f16(d, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
-          mma_commit_mc(&B->empty[s], all_mask);
+          for (int i = 0; i < KBS; ++i) {
+            if (ks * KBS + i >= nk) break;      // k-blocks past K were zero-filled by TMA
+            const uint64_t da = smem_desc_sw128(a + i * BM * BK * 2);
+            const uint64_t db = smem_desc_sw128(a + A_BYTES + i * BN * BK * 2);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) mma_f16(d, da + 2 * k, db + 2 * k, idesc, (ks | i | k) != 0);
+          }
+          mma_commit(&B->empty[s]);
         }
         if (ok) mma_commit(&B->acc_full[b]);
       }
@@ -192,7 +199,7 @@ __global__ void __launch_bounds__(THREADS, 1) kv_append_tc_kernel(const __grid_c
     for (int ct = cid; ct < n_ct; ct += ncl, ++i) {
       const int b = i & 1;
       const uint32_t ph = (i >> 1) & 1;
-      const int m = (ct * CR + rg) * BM + r;
+      const int m = ct * BM + r;
       // waits that give up leave garbage, but every thread still runs the
       // same sequence of epilogue barriers
       const bool have = wait_bar(B, &B->acc_full[b], ph, P.status);
@@ -212,7 +219,7 @@ __global__ void __launch_bounds__(THREADS, 1) kv_append_tc_kernel(const __grid_c
       rb[c * BM + r] = ss;
 #pragma unroll
       for (int k = 1; k < CL; ++k) {
-        const uint32_t peer = (uint32_t)(CL * rg + (c + k) % CL);
+        const uint32_t peer = (uint32_t)((c + k) % CL);
         st_async_b32(mapa(smem_u32(&rb[c * BM + r]), peer), ss, mapa(smem_u32(&B->red_full[b]), peer));
       }
       wait_bar(B, &B->red_full[b], ph, P.status);
@@ -221,7 +228,7 @@ __global__ void __launch_bounds__(THREADS, 1) kv_append_tc_kernel(const __grid_c
       __syncwarp();
       if (lane == 0) {
 #pragma unroll
-        for (int k = 1; k < CL; ++k) mbar_arrive_remote(mapa(smem_u32(&B->red_free[b]), (uint32_t)(CL * rg + (c + k) % CL)));
+        for (int k = 1; k < CL; ++k) mbar_arrive_remote(mapa(smem_u32(&B->red_free[b]), (uint32_t)((c + k) % CL)));
       }
       if (r == 0) mbar_arrive_expect_tx(&B->red_full[b], 2 * BM * 4);   // armed for tile i + 2
       const float rstd = 1.f / sqrtf(tot / 512.f + P.eps);
@@ -291,7 +298,7 @@ __global__ void __launch_bounds__(THREADS, 1) kv_append_tc_kernel(const __grid_c
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();             // no CTA leaves while a peer may still multicast, commit or store to it
+  cluster_sync_all();             // no CTA leaves while a peer may still store to it or arrive on its barriers
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
@@ -307,8 +314,8 @@ mla_status_t kv_append(cudaStream_t st, const mla_handle* h, const __nv_bfloat16
   if (l.D % 8) return fail(MLA_ERR_UNSUPPORTED, "tcgen05 append: hidden_size must be a multiple of 8");
   if (M <= 0) return MLA_OK;
   AppendParams P;
-  if (!make_tmap_2d(&P.tmA, false, hidden, M, l.D, l.D, BM) ||
-      !make_tmap_2d(&P.tmB, false, h->WA, 576, l.D, l.D, BN))
+  if (!make_tmap_chunked(&P.tmA, false, hidden, M, l.D, l.D, BM, KBS) ||
+      !make_tmap_chunked(&P.tmB, false, h->WA, 576, l.D, l.D, BN, KBS))
     return fail(MLA_ERR_CUDA, "tcgen05 append: cuTensorMapEncodeTiled failed");
   P.M = M;
   P.K = l.D;
@@ -331,13 +338,13 @@ mla_status_t kv_append(cudaStream_t st, const mla_handle* h, const __nv_bfloat16
   static int max_clusters = 0;
   std::call_once(once_occ, [] {
     cudaLaunchConfig_t c = {};
-    c.gridDim = dim3(CL, CR, 1);
+    c.gridDim = dim3(CL, 1, 1);
     c.blockDim = dim3(THREADS, 1, 1);
     c.dynamicSmemBytes = SMEM_BYTES;
     cudaLaunchAttribute a[1];
     a[0].id = cudaLaunchAttributeClusterDimension;
     a[0].val.clusterDim.x = CL;
-    a[0].val.clusterDim.y = CR;
+    a[0].val.clusterDim.y = 1;
     a[0].val.clusterDim.z = 1;
     c.attrs = a;
     c.numAttrs = 1;
@@ -348,9 +355,9 @@ mla_status_t kv_append(cudaStream_t st, const mla_handle* h, const __nv_bfloat16
     }
     max_clusters = n;
   });
-  const int n_ct = (M + CR * BM - 1) / (CR * BM);
+  const int n_ct = (M + BM - 1) / BM;
   const int ncl = n_ct < max_clusters ? n_ct : max_clusters;
-  Launch L(dim3(CL, CR * ncl, 1), dim3(THREADS), SMEM_BYTES, st, pdl, dim3(CL, CR, 1));
+  Launch L(dim3(CL, ncl, 1), dim3(THREADS), SMEM_BYTES, st, pdl, dim3(CL, 1, 1));
   const cudaError_t e = cudaLaunchKernelEx(&L.cfg, kv_append_tc_kernel, P);
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 append launch");
   return MLA_OK;

@@ -4,11 +4,13 @@
 // epilogue that optionally multiplies by sigmoid(G) before storing fp32,
 // fp16 or bf16.
 //
-// One CTA computes a 128 x BN tile.  Warp 0 (one lane) streams A and B
-// through a shared-memory ring with TMA; one stage holds KBS consecutive
-// 64-wide K slices of each operand and arrives in a single copy per operand
-// (a chunked 4-D view of the matrix: a TMA copy costs about the same SM time
-// whatever its size, so few large copies keep the tensor pipe fed).  Warp 1
+// One CTA computes a 128 x BN tile.  Warps 0 and 3 (one lane each) stream A
+// and B through a shared-memory ring with TMA; one stage holds KBS
+// consecutive 64-wide K slices of each operand and arrives in a single copy
+// per operand (a chunked 4-D view of the matrix: a TMA copy holds its issuing
+// thread for about the same time whatever its size, and copies of different
+// warps proceed side by side, so each operand has its own issuing warp and
+// few large copies keep the tensor pipe fed).  Warp 1
 // (one lane) issues tcgen05.mma (M=128, N=BN, K=16) into a TMEM accumulator
 // and frees each stage with tcgen05.commit; warp 2 owns the TMEM allocation.
 // All eight warps run the epilogue (with one warp per scheduler its store
@@ -135,13 +137,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 2);             // one arrival per operand's producer
       mbar_init(&empty[s], 1);
     }
     mbar_init(accum, 1);
     fence_mbar_init();
     for (int g = 0; g < first; ++g) {
-      mbar_arrive_expect_tx(&full[g], S::STAGE_BYTES);
+      mbar_arrive_expect_tx(&full[g], S::B_BYTES);
       tma_load_4d(smem + g * S::STAGE_BYTES + S::A_BYTES, &tmB, &full[g], 0, n0, (g0 + g) * KBS, z);
     }
     pdl_trigger();
@@ -153,19 +155,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const uint32_t tmem = *tmem_slot;
   pdl_wait();                     // A, the gate and C belong to the kernels around this one
 
-  if (warp == 0 && lane == 0) {
-    // producer: one copy per operand per stage (KBS k-blocks)
-    for (int g = 0; g < first; ++g)
-      tma_load_4d(smem + g * S::STAGE_BYTES, &tmA, &full[g], 0, m0, (g0 + g) * KBS, z);
+  if ((warp == 0 || warp == 3) && lane == 0) {
+    // producers, one copy per stage (KBS k-blocks) each: warp 0 the A
+    // operand, warp 3 the B operand past the stages requested above
+    const bool is_a = warp == 0;
     bool ok = true;
-    for (int g = first; g < ng && ok; ++g) {
+    for (int g = is_a ? 0 : first; g < ng && ok; ++g) {
       const int s = g % STAGES;
-      ok = mbar_wait(&empty[s], ((g / STAGES) & 1) ^ 1, status);
+      if (g >= first) ok = mbar_wait(&empty[s], ((g / STAGES) & 1) ^ 1, status);
       if (!ok) break;
       uint8_t* a = smem + s * S::STAGE_BYTES;
-      mbar_arrive_expect_tx(&full[s], S::STAGE_BYTES);
-      tma_load_4d(a, &tmA, &full[s], 0, m0, (g0 + g) * KBS, z);
-      tma_load_4d(a + S::A_BYTES, &tmB, &full[s], 0, n0, (g0 + g) * KBS, z);
+      if (is_a) {
+        mbar_arrive_expect_tx(&full[s], S::A_BYTES);
+        tma_load_4d(a, &tmA, &full[s], 0, m0, (g0 + g) * KBS, z);
+      } else {
+        mbar_arrive_expect_tx(&full[s], S::B_BYTES);
+        tma_load_4d(a + S::A_BYTES, &tmB, &full[s], 0, n0, (g0 + g) * KBS, z);
+      }
     }
     // drain: the last loads of every slot have landed before the CTA can exit
     for (int g = max(0, ng - STAGES); g < ng; ++g)

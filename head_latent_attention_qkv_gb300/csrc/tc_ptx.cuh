@@ -41,9 +41,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
   return ok != 0;
 }
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
-  for (uint32_t i = 0; i < kWaitBudget; ++i)
+// Bounded wait for the phase with the given parity to complete: gives up
+// after `budget` try_wait rounds, setting MLA_DEV_TIMEOUT.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                          uint32_t budget = kWaitBudget) {
+  for (uint32_t i = 0; i < budget; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   set_status(status, MLA_DEV_TIMEOUT);
   return false;
@@ -217,26 +219,10 @@ __host__ __device__ constexpr uint32_t idesc_f16_bmn(int M, int N, bool fp16_ope
 }  // namespace tc
 }  // namespace mla
 
-// ---- multicast within a cluster (this GPU's own memory only) -------------------
+// ---- distributed shared memory loads ------------------------------------------
 namespace mla {
 namespace tc {
 
-// TMA tile load delivered to the same shared offset (and barrier offset) in
-// every CTA of `mask`.
-__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                               int x, int y, int z, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;"
-      ::"r"(smem_u32(dst)), "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)),
-        "h"(mask) : "memory");
-}
-// tcgen05.commit arriving on the barrier at the same offset in every CTA of `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)), "h"(mask) : "memory");
-}
 __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
