@@ -16,6 +16,8 @@ MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA, MLA_ERR_DEVICE_C
 MLA_BF16, MLA_FP32 = 0, 1
 MLA_ROPE_NEOX, MLA_ROPE_INTERLEAVED = 0, 1
 MLA_DEV_BAD_SLOT, MLA_DEV_BAD_POSITION, MLA_DEV_BAD_PAGE, MLA_DEV_TIMEOUT, MLA_DEV_BAD_LENGTH = 1, 2, 4, 8, 16
+MLA_DEV_BAD_WINDOW = 32
+MLA_WS_Q_ABS, MLA_WS_O_LAT = 0, 1
 
 
 class mla_config_t(C.Structure):
@@ -70,6 +72,9 @@ def _load():
         "mla_kernel_launches": (C.c_ulonglong, [P]),
         "mla_latent_cache_append_noalloc": (I32, [P, P, P, P, I32, P, I32, P]),
         "mla_append_noalloc_max_tokens": (C.c_int64, [P]),
+        "mla_forward_workspace_offset": (SZ, [P, I32, I32]),
+        "mla_latent_attention": (I32, [P, P, P, P, I32, C.POINTER(mla_attn_desc_t), P, P, P]),
+        "mla_check_wait_timeout": (I32, [P, C.c_uint32, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)

@@ -132,6 +132,31 @@ def mla_draft_forward_after(h: Handle, hidden, positions, block_slot_mapping, ca
     return out
 
 
+def mla_latent_attention(h: Handle, q_abs, positions, cache, desc, o_lat=None, lse=None,
+                         stream=None):
+    """The latent attention step alone: ``o_lat`` [rows, kv_lora_rank] (fp16
+    for bf16 layers) and, when ``lse`` is given, its fp32 [rows] log-sum-exp."""
+    rows = desc.num_blocks * desc.block_len * h.dims.num_heads
+    if o_lat is None:
+        dt = torch.float16 if h.dims.dtype == "bf16" else torch.float32
+        o_lat = torch.empty(rows, h.dims.kv_lora_rank, dtype=dt, device=h.device)
+    check(lib.mla_latent_attention(h.h, _ptr(q_abs), _ptr(positions), _ptr(cache),
+                                   cache.shape[0], C.byref(desc), _ptr(o_lat), _ptr(lse),
+                                   _stream(stream)), "mla_latent_attention")
+    return o_lat
+
+
+def mla_check_wait_timeout(h: Handle, max_rounds: int, gave_up, stream=None):
+    """Self-check of the bounded-wait failure path (``gave_up``: a device
+    int32 tensor of one element, set to 1 when the wait gave up)."""
+    check(lib.mla_check_wait_timeout(h.h, max_rounds, _ptr(gave_up), _stream(stream)),
+          "mla_check_wait_timeout")
+
+
+def mla_forward_workspace_offset(h: Handle, num_tokens: int, part: int) -> int:
+    return int(lib.mla_forward_workspace_offset(h.h, num_tokens, part))
+
+
 def mla_latent_cache_append_noalloc(h: Handle, hidden, positions, slot_mapping, cache,
                                     stream=None):
     """The allocation-free append (library-owned fixed scratch; at most

@@ -472,7 +472,7 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
   if constexpr (std::is_same<TX, float>::value) {
     simt::latent_attention<TI, TX>(st, h, q_abs, (const TX*)cache, num_pages, d, pos, o_lat);
   } else {
-    s = tc::latent_attention(st, h, q_abs, (const TX*)cache, num_pages, d, pos, o_lat,
+    s = tc::latent_attention(st, h, q_abs, (const TX*)cache, num_pages, d, pos, o_lat, nullptr,
                              pdl && !kv_ready);
     if (s != MLA_OK) return s;
   }
@@ -536,6 +536,48 @@ extern "C" mla_status_t mla_draft_forward(mla_handle_t* h, const void* hidden,
                                           void* stream) {
   return mla_draft_forward_after(h, hidden, positions, block_slot_mapping, cache, num_pages, desc,
                                  out, workspace, workspace_bytes, stream, nullptr);
+}
+
+extern "C" size_t mla_forward_workspace_offset(const mla_handle_t* h, int32_t num_tokens,
+                                               int32_t part) {
+  if (!h || num_tokens < 0) return (size_t)-1;
+  const FwdWs w = forward_ws(h, num_tokens);
+  switch (part) {
+    case MLA_WS_Q_ABS: return w.q_abs;
+    case MLA_WS_O_LAT: return w.o_lat;
+    default: return (size_t)-1;
+  }
+}
+
+extern "C" mla_status_t mla_latent_attention(mla_handle_t* h, const void* q_abs,
+                                             const int32_t* positions, const void* cache,
+                                             int32_t num_pages, const mla_attn_desc_t* desc,
+                                             void* o_lat, float* lse, void* stream) {
+  if (!h || !desc) return fail(MLA_ERR_INVALID_ARG, "attention: null handle or descriptor");
+  const mla_attn_desc_t& d = *desc;
+  if (d.num_blocks < 0 || d.block_len <= 0 || d.max_pages <= 0)
+    return fail(MLA_ERR_INVALID_ARG, "attention: num_blocks >= 0, block_len > 0, max_pages > 0");
+  if (d.num_blocks == 0) return MLA_OK;
+  if ((long)d.num_blocks * d.block_len * h->lay.H > 0x7fffffffL)
+    return fail(MLA_ERR_INVALID_ARG, "attention: too many rows");
+  if (!q_abs || !positions || !cache || !o_lat || !d.block_table || !d.kv_len)
+    return fail(MLA_ERR_INVALID_ARG, "attention: null pointer");
+  if (num_pages <= 0) return fail(MLA_ERR_INVALID_ARG, "attention: num_pages <= 0");
+  if ((uintptr_t)q_abs % 16 || (uintptr_t)o_lat % 16 || (uintptr_t)cache % 16)
+    return fail(MLA_ERR_INVALID_ARG, "attention: q_abs, cache and o_lat must be 16-byte aligned");
+  cudaStream_t st = (cudaStream_t)stream;
+  h->launches += 1;
+  if (h->cfg.dtype == MLA_BF16) {
+    const mla_status_t s = tc::latent_attention(st, h, (const __nv_bfloat16*)q_abs,
+                                                (const __nv_bfloat16*)cache, num_pages, d,
+                                                positions, (__half*)o_lat, lse, false);
+    if (s != MLA_OK) return s;
+  } else {
+    simt::latent_attention<float, float>(st, h, (const float*)q_abs, (const float*)cache,
+                                         num_pages, d, positions, (float*)o_lat, lse);
+  }
+  MLA_CUDA_TRY(cudaGetLastError());
+  return MLA_OK;
 }
 
 extern "C" mla_status_t mla_get_device_status(mla_handle_t* h, void* stream, int32_t* bits) {

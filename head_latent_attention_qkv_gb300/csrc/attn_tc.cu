@@ -6,35 +6,41 @@
 // Work unit: one query block and 128 consecutive rows of Q_abs (rows are
 // (token, head) pairs, token-major; a block's last tile is padded when
 // block_len x heads is not a multiple of 128: its extra rows are fully masked
-// and written nowhere), handled by a cluster of two CTAs, one per
-// half of the 512 latent value dims.  A 128 x 512 fp32 accumulator would fill
-// all of an SM's tensor memory, so each CTA keeps O for its 256 value dims and
-// computes the full 576-wide scores itself (QK^T is repeated by the two
-// halves; nothing is exchanged but the cache tiles both read).  Keys go in
-// tiles of 128 (one MMA costs about the same for any N up to 128, so narrower
-// score tiles waste the tensor pipe).
+// and written nowhere), handled by a cluster of two CTAs, one per half of the
+// 512 latent value dims.  A 128 x 512 fp32 accumulator would fill all of an
+// SM's tensor memory, so each CTA keeps O for its 256 value dims and computes
+// the full 576-wide scores itself (QK^T is repeated by the two halves).  Keys
+// go in tiles of 128 (one MMA costs about the same for any N up to 128, so
+// narrower score tiles waste the tensor pipe).
+//
+// The cache entries are keys and values at once: the four 64-dim chunks of a
+// tile that hold this CTA's value half ("value chunks") arrive in one copy
+// into the V buffer and serve both as B operand of QK^T (K-major) and of P V
+// (MN-major); the other five chunks of the tile stream through a 5-slot ring.
+// Each tile thus reads its 128 cache rows once per CTA, and the ring is deep
+// enough that a slot's refill (its copy holds the issuing thread ~550 cycles,
+// then lands ~1 k cycles later) is hidden behind the MMAs of the other slots.
 //
 // Tensor memory (512 columns): O at 0..255, S (fp32, 128 keys) at 256..383,
-// P (bf16 pairs) at 384..447, Q_abs dims 0..127 (bf16 pairs, the A operand of
-// the first two score chunks) at 448..511.
-// Shared memory: Q_abs dims 128..575 (seven 64-dim chunks, one TMA copy), a
-// V buffer (this CTA's four value chunks of one tile, MN-major operand of
-// P V, one TMA copy) and a 3-slot ring of 64-dim key chunks (nine per tile).
-// A TMA copy costs about the same SM time whatever its size, so copies are as
-// large as the layout allows: the two CTAs of a cluster take turns loading
-// the key chunks and multicast each one to both, and a tile whose 128 cache
-// rows are contiguous (adjacent pages) comes in one copy per chunk.
+// P (bf16 pairs, written over the first half of S once the softmax has read
+// it) at 256..319, Q_abs dims 0..255 (bf16 pairs, A operand of four score
+// chunks) at 384..511.
+// Shared memory: Q_abs dims 256..575 (five chunks, one TMA copy), the V
+// buffer (four value chunks of one tile, one copy), the 5-slot ring.
 //
-// Tensor-pipe order: S(0), S(1), PV(0), S(2), PV(1), ...  The softmax reads
-// S(t) into registers and releases it at once, so S(t+1) runs while the
-// softmax works on tile t; V(t) is loaded while S(t+1) runs.
+// Per tile t the tensor pipe runs S(t) over the ring chunks, then over the
+// value chunks, then (once the softmax has written P(t)) O += P(t) V(t);
+// S(t + 1)'s ring chunks are already resident by then, and V(t + 1) is
+// copied while they are multiplied.
 //   MMA warp     : S(t) = Q K(t)^T (36 MMAs, N = 128); O += P(t) V(t) (8 MMAs,
 //                  N = 256, P read from tensor memory)
 //   softmax warps: thread r owns row r (TMEM lane r): mask by logical
 //                  position (one visible interval per row), online softmax in
 //                  fp32 in the exp2 domain (O rescaled in tensor memory only
 //                  when the running max grows by more than 2^8), P -> bf16
-//   TMA warp     : page rows of the key range (once), Q, key chunks, values
+//   TMA warps    : warp 4 the page rows of the key range (once), Q, V(t);
+//                  warps 6 and 7 the ring chunks (copies of different warps
+//                  proceed side by side)
 // The key range of a unit may be split (grid y) when units alone do not fill
 // the GPU (the blog's forward_mqa num_kv_splits); the pairs of one unit then form
 // one cluster of 2 x splits CTAs.  Every CTA stages its normalised partial
@@ -54,22 +60,25 @@ namespace tc {
 namespace {
 
 constexpr int QROWS = 128, KT = 128, DCH = 64, NCH = 9;  // rows, keys per tile, dims per chunk
-constexpr int NQT = 2;                                    // Q chunks held in tensor memory
+constexpr int NQT = 4;                                    // Q chunks held in tensor memory
 constexpr int NQS = NCH - NQT;                            // Q chunks held in shared memory
-constexpr int KSLOTS = 3;                                 // key-chunk ring
-constexpr int THREADS = 192;                              // softmax x4, TMA, MMA
+constexpr int NVC = 4;                                    // value chunks of this CTA's half
+constexpr int NRC = NCH - NVC;                            // ring chunks per tile
+constexpr int RSLOTS = NRC;                               // ring slot i holds ring chunk i
+constexpr int THREADS = 256;                              // softmax x4, TMA, MMA, TMA x2
 constexpr int Q_CH_BYTES = QROWS * DCH * 2;               // 16 KiB
 constexpr int KV_CH_BYTES = KT * DCH * 2;                 // 16 KiB
 constexpr int OFF_Q = 0;
 constexpr int OFF_V = OFF_Q + NQS * Q_CH_BYTES;
-constexpr int OFF_K = OFF_V + 4 * KV_CH_BYTES;
-constexpr int OFF_BAR = OFF_K + KSLOTS * KV_CH_BYTES;
+constexpr int OFF_K = OFF_V + NVC * KV_CH_BYTES;
+constexpr int OFF_BAR = OFF_K + RSLOTS * KV_CH_BYTES;
 constexpr int OFF_PG = OFF_BAR + 256;                     // cache row of each page of the key range
 constexpr int MAX_PG = 176;                               // pages held there (else looked up per load)
 constexpr int SMEM_BYTES = 1024 + OFF_PG + MAX_PG * 4;
-constexpr uint32_t TMEM_COLS = 512, TM_O = 0, TM_S = 256, TM_P = 384, TM_Q = 448;
+constexpr uint32_t TMEM_COLS = 512, TM_O = 0, TM_S = 256, TM_P = 256, TM_Q = 384;
 constexpr float RESCALE_LOG2 = 8.f;                       // lazy rescale threshold (factor 256)
 constexpr int MAX_SPLITS = 4;                             // clusters of at most 8 CTAs
+constexpr float kLn2 = 0.6931471805599453f;
 // epilogue staging (over the Q and V buffers): fp32 rows of this CTA's 256
 // value dims (pitch 260 floats: conflict-free 16-byte row-per-thread
 // stores), then the rows' log2-sum-exp and visibility counts
@@ -79,15 +88,21 @@ constexpr int OFF_LSE = OFF_STG + QROWS * STG_PITCH * 4;
 constexpr int OFF_VS = OFF_LSE + QROWS * 4;
 static_assert(OFF_VS + QROWS * 12 <= OFF_K, "staging fits over Q and V");
 
+// Cache chunk held by ring slot i for value half h: the chunks outside
+// [4h, 4h + 4), in increasing order.
+__device__ __forceinline__ int ring_chunk(int i, int half) {
+  return half == 0 ? NVC + i : (i < NVC ? i : NCH - 1);
+}
+
 struct Bars {
   uint64_t q_full;                    // Q chunks in shared memory (TMA)
   uint64_t q_tmem;                    // Q chunks in tensor memory (128 arrivals)
-  uint64_t k_full[KSLOTS];            // key chunk landed (own arm + multicast bytes)
-  uint64_t k_empty[KSLOTS];           // both CTAs' MMAs done with the slot (2 commits)
+  uint64_t r_full[RSLOTS];            // ring chunk landed (phase t)
+  uint64_t r_empty[RSLOTS];           // the MMAs reading the slot are done (phase t)
   uint64_t v_full;                    // V(t) landed (phase t)
-  uint64_t s_full, s_free;            // S(t) written / read into registers (phase t)
+  uint64_t s_full;                    // S(t) complete (phase t); also P(t - 1) V(t - 1)
   uint64_t p_full;                    // P(t) written (phase t)
-  uint64_t o_done;                    // P(t) V(t) complete (phase t)
+  uint64_t o_done;                    // P(t) V(t) complete (phase t): the V buffer is free
   uint64_t drain;                     // every MMA of the CTA complete
   uint32_t tmem_slot;
   int abort;
@@ -102,14 +117,6 @@ __device__ __forceinline__ bool wait_bar(Bars* B, uint64_t* bar, uint32_t parity
   B->abort = 1;
   return false;
 }
-// The same on a barrier that the peer CTA also signals (acquire at cluster scope).
-__device__ __forceinline__ bool wait_bar_cl(Bars* B, uint64_t* bar, uint32_t parity, uint32_t* st) {
-  if (*(volatile int*)&B->abort) return false;
-  if (mbar_wait_cluster(bar, parity, st)) return true;
-  B->abort = 1;
-  return false;
-}
-
 // 2^x by the hardware approximation (relative error ~2^-22, far below the
 // bf16 rounding P gets); 2^-inf = 0.
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -137,7 +144,7 @@ __device__ __forceinline__ void softmax_and_stage(const AttnParams& P, Bars* B, 
   float mrun = -INFINITY, lsum = 0.f;
   int cnt = 0, first = -1, last = -1;
   if (nt > 0) {
-    // Q_abs dims 0..127 of this row -> tensor memory (bf16 pairs, low half = even dim)
+    // Q_abs dims 0..255 of this row -> tensor memory (bf16 pairs, low half = even dim)
     const uint4* src = reinterpret_cast<const uint4*>(P.q_abs + (row0 + r) * 576);
 #pragma unroll 1
     for (int c = 0; c < NQT; ++c) {
@@ -156,12 +163,11 @@ __device__ __forceinline__ void softmax_and_stage(const AttnParams& P, Bars* B, 
     const uint32_t ph = t & 1;
     const int j0 = j_lo + t * KT;
     float s[KT];
+    // S(t) complete (and, the MMAs completing in order, P(t - 1) V(t - 1))
     wait_bar(B, &B->s_full, ph, P.status);
     tc_fence_after();
 #pragma unroll
     for (int c = 0; c < KT; c += 32) tmem_ld32(tmem + TM_S + c + lane_base, s + c);
-    tc_fence_before();
-    mbar_arrive(&B->s_free);
     // mask by logical position (a warp whose rows all see the whole tile skips it)
     const int lo = max(vlo - j0, 0), hi = min(vhi - j0, KT);   // visible columns [lo, hi)
     if (hi > lo) {
@@ -193,36 +199,33 @@ __device__ __forceinline__ void softmax_and_stage(const AttnParams& P, Bars* B, 
     }
     const float psum = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
     const float alpha = (grow && mrun != -INFINITY) ? exp2f(mrun - m_new) : 1.f;
-    // P(t-1) V(t-1) has finished: P may be overwritten and O rescaled
-    if (t > 0) {
-      wait_bar(B, &B->o_done, ph ^ 1, P.status);
-      tc_fence_after();
-      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+    // P(t - 1) V(t - 1) has completed (before S(t)): O may be rescaled
+    if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
-          float o[32];
-          tmem_ld32(tmem + TM_O + lane_base + c, o);
+      for (int c = 0; c < 256; c += 32) {
+        float o[32];
+        tmem_ld32(tmem + TM_O + lane_base + c, o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st32(tmem + TM_O + lane_base + c, o);
-        }
+        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+        tmem_st32(tmem + TM_O + lane_base + c, o);
       }
     }
     lsum = lsum * alpha + psum;
     mrun = m_new;
-    // value rows of keys past kv_len may hold anything: once V(t) has landed,
-    // zero those rows (last tile only)
+    // value rows of keys past kv_len may hold anything: S(t) is done with the
+    // V buffer, zero those rows before P V reads them (last tile only)
     if (j0 + KT > kvl) {
       wait_bar(B, &B->v_full, ph, P.status);
       uint8_t* vbase = smem + OFF_V;
-      const int z0 = max(0, kvl - j0), pieces = (KT - z0) * 4 * 8;
+      const int z0 = max(0, kvl - j0), pieces = (KT - z0) * NVC * 8;
       for (int idx = r; idx < pieces; idx += QROWS) {
         const int key = z0 + idx / 32, ch = (idx % 32) / 8, q = idx % 8;
         *reinterpret_cast<uint4*>(vbase + ch * KV_CH_BYTES + key * 128 + q * 16) = make_uint4(0, 0, 0, 0);
       }
       fence_proxy_async_smem();
     }
-    // P row in bf16 pairs: key 2c in the low half of column c
+    // P row in bf16 pairs over S (this thread has read its lane): key 2c in
+    // the low half of column c
 #pragma unroll
     for (int c = 0; c < KT / 2; c += 32) {
       uint32_t pw[32];
@@ -259,11 +262,6 @@ __device__ __forceinline__ void softmax_and_stage(const AttnParams& P, Bars* B, 
   vs[2] = last;
 }
 
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
 __device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
   int v;
   asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
@@ -304,6 +302,7 @@ __device__ __forceinline__ void reduce_splits(const AttnParams& P, uint8_t* smem
       *reinterpret_cast<uint4*>(P.o_lat + (row0 + r) * 512 + half * 256 + 8 * lane) =
           *reinterpret_cast<uint4*>(h2);
       const int row_in_block = qt * QROWS + r;
+      if (P.lse && half == 0 && lane == 0) P.lse[row0 + r] = any ? lse[r] * kLn2 : -INFINITY;
       if (P.vis_stats && half == 0 && row_in_block % P.H == 0 && lane == 0) {
         const long m = (long)b * P.T + row_in_block / P.H;
         const int cnt = vs[3 * r];
@@ -343,6 +342,8 @@ __device__ __forceinline__ void reduce_splits(const AttnParams& P, uint8_t* smem
       }
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
+    if (P.lse && half == 0 && lane == 0)
+      P.lse[row0 + r] = den > 0.f ? (mx + log2f(den)) * kLn2 : -INFINITY;
     __half2 h2[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) h2[u] = __floats2half2_rn(acc[2 * u] * inv, acc[2 * u + 1] * inv);
@@ -376,7 +377,6 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int rank = (int)cluster_ctarank();             // half + 2 * split
   const int half = rank & 1, split = rank >> 1;         // split == blockIdx.y
-  const uint16_t pair = (uint16_t)(3u << (2 * split));  // this unit's two CTAs
   const int unit = blockIdx.x >> 1;
   const int b = unit / P.tiles_per_block, qt = unit % P.tiles_per_block;
   const long row0 = (long)b * P.T * P.H + (long)qt * QROWS;       // first Q_abs row of the unit
@@ -389,6 +389,10 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
     kvl = max(0, min(kvl, cap));
   }
   const int W = P.window ? P.window[b] : 0;
+  if (W < 0) {                 // rejected: the block's rows see no key (exact zeros)
+    if (tid == 0 && half == 0 && blockIdx.y == 0) set_status(P.status, MLA_DEV_BAD_WINDOW);
+    kvl = 0;
+  }
   int j_lo = 0;
   if (W > 0) {
     const int t_first = (qt * QROWS) / P.H, t_last = min(P.T - 1, (qt * QROWS + QROWS - 1) / P.H);
@@ -407,13 +411,12 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
   if (tid == 0) {
     mbar_init(&B->q_full, 1);
     mbar_init(&B->q_tmem, QROWS);
-    for (int s = 0; s < KSLOTS; ++s) {
-      mbar_init(&B->k_full[s], 1);
-      mbar_init(&B->k_empty[s], 2);
+    for (int s = 0; s < RSLOTS; ++s) {
+      mbar_init(&B->r_full[s], 1);
+      mbar_init(&B->r_empty[s], 1);
     }
     mbar_init(&B->v_full, 1);
     mbar_init(&B->s_full, 1);
-    mbar_init(&B->s_free, QROWS);
     mbar_init(&B->p_full, QROWS);
     mbar_init(&B->o_done, 1);
     mbar_init(&B->drain, 1);
@@ -423,21 +426,21 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
   if (warp == 5) tmem_alloc(&B->tmem_slot, TMEM_COLS);
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();          // the peer's barriers exist before anyone multicasts to them
+  cluster_sync_all();          // every CTA of the cluster is resident before any DSMEM access
   tc_fence_after();
   const uint32_t tmem = B->tmem_slot;
   if (tid == 0) pdl_trigger();
   pdl_wait();                  // Q_abs and the block's own latents come from the kernels before
 
-  if (warp == 4) {
-    // the cache row of every page this CTA reads, looked up once by the warp
+  if (warp == 4 || warp >= 6) {
+    // the cache row of every page this CTA reads, looked up once by warp 4
     // (past_end for a page the table marks invalid: TMA then reads zeros)
     const int ps = P.page_size, past_end = P.num_pages * ps;
     const int p0 = j_lo / ps;
     const int npg = nt > 0 ? (min(kvl, j_lo + nt * KT) - 1) / ps - p0 + 1 : 0;
     int* pg_row = (int*)(smem + OFF_PG);
     const bool table = npg <= MAX_PG;
-    if (table) {
+    if (warp == 4 && table) {
       for (int i = lane; i < npg; i += 32) {
         const int pg = P.block_table[(long)b * P.max_pages + p0 + i];
         const bool okp = pg >= 0 && pg < P.num_pages;
@@ -445,15 +448,9 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
         pg_row[i] = okp ? pg * ps : past_end;
       }
     }
-    __syncwarp();
+    // the three producer warps (4, 6, 7) see the table before any copy
+    asm volatile("bar.sync 1, 96;" ::: "memory");
     if (lane == 0 && nt > 0) {
-      // ---- TMA producer ----
-      prefetch_tmap(&P.tmQ);
-      prefetch_tmap(&P.tmK);
-      prefetch_tmap(&P.tmKs);
-      prefetch_tmap(&P.tmV);
-      mbar_arrive_expect_tx(&B->q_full, NQS * Q_CH_BYTES);
-      tma_load_3d(smem + OFF_Q, &P.tmQ, &B->q_full, 0, (int)row0, NQT);
       const int R = P.seg_rows, nseg = KT / R;
       // cache row of key j (beyond the cache when j is past kv_len or its page
       // is invalid: TMA then fills zeros)
@@ -482,88 +479,94 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
         }
         return y0;
       };
-      bool ok = true;
-      int g = 0;             // key chunks issued so far (ring position)
-      // V(tv): this CTA's four value chunks, once P(tv - 1) V(tv - 1) has freed the buffer
-      auto load_v = [&](int tv) -> bool {
-        if (tv >= 1 && !wait_bar(B, &B->o_done, (tv - 1) & 1, P.status)) return false;
-        mbar_arrive_expect_tx(&B->v_full, 4 * KV_CH_BYTES);
-        const int y0 = tile_run(tv);
-        if (y0 >= 0) {
-          tma_load_3d(smem + OFF_V, &P.tmV, &B->v_full, 0, y0, 4 * half);
-        } else {
-          for (int i = 0; i < 4; ++i)
-            for (int seg = 0; seg < nseg; ++seg)
-              tma_load_3d(smem + OFF_V + i * KV_CH_BYTES + seg * R * 128, &P.tmKs, &B->v_full,
-                          (4 * half + i) * DCH, cache_row(j_lo + tv * KT + seg * R), 0);
+      if (warp == 4) {
+        // ---- Q once, then V(t) for every tile, each as soon as P(t - 1) V(t - 1)
+        // has freed the buffer ----
+        prefetch_tmap(&P.tmQ);
+        prefetch_tmap(&P.tmV);
+        prefetch_tmap(&P.tmKs);
+        mbar_arrive_expect_tx(&B->q_full, NQS * Q_CH_BYTES);
+        tma_load_3d(smem + OFF_Q, &P.tmQ, &B->q_full, 0, (int)row0, NQT);
+        for (int t = 0; t < nt; ++t) {
+          if (t >= 1 && !wait_bar(B, &B->o_done, (t - 1) & 1, P.status)) break;
+          mbar_arrive_expect_tx(&B->v_full, NVC * KV_CH_BYTES);
+          const int y0 = tile_run(t);
+          if (y0 >= 0) {
+            tma_load_3d(smem + OFF_V, &P.tmV, &B->v_full, 0, y0, NVC * half);
+          } else {
+            for (int i = 0; i < NVC; ++i)
+              for (int seg = 0; seg < nseg; ++seg)
+                tma_load_3d(smem + OFF_V + i * KV_CH_BYTES + seg * R * 128, &P.tmKs, &B->v_full,
+                            (NVC * half + i) * DCH, cache_row(j_lo + t * KT + seg * R), 0);
+          }
         }
-        return true;
-      };
-      for (int t = 0; t <= nt && ok; ++t) {
-        const int y0 = t < nt ? tile_run(t) : -1;
-        for (int c = 0; c < NCH && t < nt && ok; ++c) {
-          // V(t - 1) goes after the first ring-full of tile t's key chunks
-          if (c == KSLOTS && t >= 1) ok = load_v(t - 1);
-          if (!ok) break;
-          const int sl = g % KSLOTS;
-          // both CTAs are done with the slot's previous chunk
-          if (!wait_bar_cl(B, &B->k_empty[sl], ((g / KSLOTS) & 1) ^ 1, P.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&B->k_full[sl], KV_CH_BYTES);
-          if ((g & 1) == half) {   // the CTAs take turns; each copy lands in both
-            uint8_t* dst = smem + OFF_K + sl * KV_CH_BYTES;
+        // every copy into this CTA has landed before it may exit
+        mbar_wait(&B->q_full, 0, P.status);
+        mbar_wait(&B->v_full, (nt - 1) & 1, P.status);
+      } else {
+        // ---- ring: warp 6 refills slots 0, 2, 4, warp 7 slots 1, 3 ----
+        prefetch_tmap(&P.tmK);
+        prefetch_tmap(&P.tmKs);
+        const int s0 = warp - 6;
+        bool ok = true;
+        for (int t = 0; t < nt && ok; ++t) {
+          const int y0 = tile_run(t);
+          for (int i = s0; i < RSLOTS; i += 2) {
+            if (!wait_bar(B, &B->r_empty[i], (t & 1) ^ 1, P.status)) { ok = false; break; }
+            mbar_arrive_expect_tx(&B->r_full[i], KV_CH_BYTES);
+            uint8_t* dst = smem + OFF_K + i * KV_CH_BYTES;
+            const int c = ring_chunk(i, half);
             if (y0 >= 0) {
-              tma_load_3d_mc(dst, &P.tmK, &B->k_full[sl], c * DCH, y0, 0, pair);
+              tma_load_3d(dst, &P.tmK, &B->r_full[i], c * DCH, y0, 0);
             } else {
               for (int seg = 0; seg < nseg; ++seg)
-                tma_load_3d_mc(dst + seg * R * 128, &P.tmKs, &B->k_full[sl], c * DCH,
-                               cache_row(j_lo + t * KT + seg * R), 0, pair);
+                tma_load_3d(dst + seg * R * 128, &P.tmKs, &B->r_full[i], c * DCH,
+                            cache_row(j_lo + t * KT + seg * R), 0);
             }
           }
-          ++g;
         }
-        if (t == nt && ok) ok = load_v(nt - 1);
+        for (int i = s0; i < RSLOTS; i += 2) mbar_wait(&B->r_full[i], (nt - 1) & 1, P.status);
       }
-      // every copy into this CTA has landed before it may exit (the peer's
-      // multicast copies included: k_full counts them)
-      mbar_wait(&B->q_full, 0, P.status);
-      for (int i = max(0, g - KSLOTS); i < g; ++i) mbar_wait(&B->k_full[i % KSLOTS], (i / KSLOTS) & 1, P.status);
-      mbar_wait(&B->v_full, (nt - 1) & 1, P.status);
     }
   } else if (warp == 5) {
     if (lane == 0 && nt > 0) {
       // ---- MMA issuer ----
       const uint32_t idesc_qk = idesc_f16(QROWS, KT, false);
       const uint32_t idesc_pv = idesc_f16_bmn(QROWS, 256, false);
-      const bool have_q = wait_bar(B, &B->q_full, 0, P.status) && wait_bar(B, &B->q_tmem, 0, P.status);
-      int g = 0;
-      // S(t) = Q K(t)^T, chunk by chunk from the ring
-      auto issue_qk = [&](int t) -> bool {
-        if (t >= 1 && !wait_bar(B, &B->s_free, (t - 1) & 1, P.status)) return false;
-        for (int c = 0; c < NCH; ++c, ++g) {
-          const int sl = g % KSLOTS;
-          if (!wait_bar_cl(B, &B->k_full[sl], (g / KSLOTS) & 1, P.status)) return false;
-          tc_fence_after();
-          const uint64_t db = smem_desc_sw128(smem + OFF_K + sl * KV_CH_BYTES);
-          if (c < NQT) {
+      bool ok = wait_bar(B, &B->q_full, 0, P.status) && wait_bar(B, &B->q_tmem, 0, P.status);
+      // S += Q[:, chunk c] K(chunk c)^T, B operand at `kb` (K-major, 128 keys)
+      auto qk_chunk = [&](int c, const uint8_t* kb, bool first) {
+        const uint64_t db = smem_desc_sw128(kb);
+        if (c < NQT) {
 #pragma unroll
-            for (int k = 0; k < DCH / 16; ++k)
-              mma_f16_ts(tmem + TM_S, tmem + TM_Q + 32 * c + 8 * k, db + 2 * k, idesc_qk, (c | k) != 0);
-          } else {
-            const uint64_t da = smem_desc_sw128(smem + OFF_Q + (c - NQT) * Q_CH_BYTES);
+          for (int k = 0; k < DCH / 16; ++k)
+            mma_f16_ts(tmem + TM_S, tmem + TM_Q + 32 * c + 8 * k, db + 2 * k, idesc_qk, !(first && k == 0));
+        } else {
+          const uint64_t da = smem_desc_sw128(smem + OFF_Q + (c - NQT) * Q_CH_BYTES);
 #pragma unroll
-            for (int k = 0; k < DCH / 16; ++k) mma_f16(tmem + TM_S, da + 2 * k, db + 2 * k, idesc_qk, 1);
-          }
-          mma_commit_mc(&B->k_empty[sl], pair);   // this slot is free in both CTAs' eyes
+          for (int k = 0; k < DCH / 16; ++k)
+            mma_f16(tmem + TM_S, da + 2 * k, db + 2 * k, idesc_qk, !(first && k == 0));
         }
-        mma_commit(&B->s_full);
-        return true;
       };
-      bool ok = have_q && issue_qk(0);
       for (int t = 0; t < nt && ok; ++t) {
-        // the next tile's scores overlap this tile's softmax
-        if (t + 1 < nt && !issue_qk(t + 1)) break;
-        if (!wait_bar(B, &B->p_full, t & 1, P.status)) break;
-        if (!wait_bar(B, &B->v_full, t & 1, P.status)) break;
+        const uint32_t ph = t & 1;
+        // S(t): the ring chunks, then the value chunks (P(t - 1) V(t - 1),
+        // issued before, has read P out of these columns: same issuing
+        // thread, executed in order)
+        for (int i = 0; i < RSLOTS && ok; ++i) {
+          ok = wait_bar(B, &B->r_full[i], ph, P.status);
+          if (!ok) break;
+          tc_fence_after();
+          qk_chunk(ring_chunk(i, half), smem + OFF_K + i * KV_CH_BYTES, i == 0);
+          mma_commit(&B->r_empty[i]);          // the slot may be refilled
+        }
+        if (!ok || !(ok = wait_bar(B, &B->v_full, ph, P.status))) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int i = 0; i < NVC; ++i) qk_chunk(NVC * half + i, smem + OFF_V + i * KV_CH_BYTES, false);
+        mma_commit(&B->s_full);
+        // O += P(t) V(t)
+        if (!(ok = wait_bar(B, &B->p_full, ph, P.status))) break;
         tc_fence_after();
         const uint64_t dv = smem_desc_sw128_mn(smem + OFF_V, KV_CH_BYTES);
 #pragma unroll
@@ -586,8 +589,7 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
   tc_fence_after();
   if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
   reduce_splits(P, smem, half, split, b, qt, row0);
-  cluster_sync_all();          // no CTA leaves while another may still read its staged partial,
-                               // multicast into it or commit to its barriers
+  cluster_sync_all();          // no CTA leaves while another may still read its staged partial
 }
 
 }  // namespace
@@ -605,7 +607,7 @@ namespace tc {
 mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_bfloat16* q_abs,
                               const __nv_bfloat16* cache, int num_pages,
                               const mla_attn_desc_t& d, const int32_t* positions, __half* o_lat,
-                              bool pdl) {
+                              float* lse, bool pdl) {
   const Layout& l = h->lay;
   const int ps = h->cfg.page_size;
   if (l.rkv != 512 || l.dr != 64)
@@ -630,6 +632,7 @@ mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_b
   P.positions = positions;
   P.vis_stats = d.vis_stats;
   P.o_lat = o_lat;
+  P.lse = lse;
   P.status = h->status;
   P.max_pages = d.max_pages;
   P.num_pages = num_pages;

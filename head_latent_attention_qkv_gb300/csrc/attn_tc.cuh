@@ -21,6 +21,7 @@ struct AttnParams {
   const int32_t* positions;
   int32_t* vis_stats;
   __half* o_lat;      // [rows, 512]
+  float* lse;         // [rows] natural-log sum of exp of the scaled scores, or NULL
   int splits;         // key-range parts of a unit (1..4; cluster of 2 x splits CTAs)
   uint32_t* status;
   int max_pages, num_pages, page_size, seg_rows, T, H, tiles_per_block;
@@ -36,10 +37,12 @@ struct AttnParams {
 int attn_splits(const mla_handle* h, long num_blocks, int block_len);
 // `pdl`: the kernels may start while the previous kernel of the stream
 // finishes (programmatic stream serialization; they wait for it on the device).
+// `lse` (nullable): per Q_abs row, log of the sum over visible keys of
+// exp(scale * score), -inf for a row that sees no key.
 mla_status_t latent_attention(cudaStream_t st, const mla_handle* h, const __nv_bfloat16* q_abs,
                               const __nv_bfloat16* cache, int num_pages,
                               const mla_attn_desc_t& desc, const int32_t* positions,
-                              __half* o_lat, bool pdl = false);
+                              __half* o_lat, float* lse = nullptr, bool pdl = false);
 
 }  // namespace tc
 }  // namespace mla

@@ -44,11 +44,12 @@ void q_rope_split(cudaStream_t st, const mla_handle* h, const float* q, long ldq
                   const int32_t* positions, TN* q_nope, TQ* q_abs, bool pdl = false);
 
 // Latent attention: O_lat[m, h, :rkv] = sum_j p_j c_j over the visible keys of
-// each query's block, scores scale * <Q_abs[m,h,:], entry_j>.
+// each query's block, scores scale * <Q_abs[m,h,:], entry_j>; optionally the
+// rows' log-sum-exp of the scaled scores (lse[m * H + h], -inf without keys).
 template <typename TQ, typename TC>
 void latent_attention(cudaStream_t st, const mla_handle* h, const TQ* q_abs,
                       const TC* cache, int num_pages, const mla_attn_desc_t& desc,
-                      const int32_t* positions, TQ* o_lat);
+                      const int32_t* positions, TQ* o_lat, float* lse = nullptr);
 
 }  // namespace simt
 }  // namespace mla

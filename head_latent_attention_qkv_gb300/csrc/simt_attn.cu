@@ -41,7 +41,7 @@ latent_attn_kernel(const TQ* __restrict__ q_abs, const TC* __restrict__ cache, i
                    const int32_t* __restrict__ kv_len, const int32_t* __restrict__ window,
                    const uint8_t* __restrict__ q_visible, const int32_t* __restrict__ positions,
                    int Tb, int H, int rkv, int L, float scale, uint32_t* status,
-                   int32_t* vis_stats, TQ* __restrict__ o_lat) {
+                   int32_t* vis_stats, TQ* __restrict__ o_lat, float* __restrict__ lse) {
   extern __shared__ float sm[];
   float* Qs = sm;                      // [QT][L]
   float* Ks = Qs + QT * L;             // [KT][L + 1]
@@ -59,6 +59,10 @@ latent_attn_kernel(const TQ* __restrict__ q_abs, const TC* __restrict__ cache, i
     kvl = max(0, min(kvl, max_pages * page_size));
   }
   const int W = window ? window[b] : 0;
+  if (W < 0) {                 // rejected: the block's rows see no key (exact zeros)
+    if (tid == 0 && h == 0 && blockIdx.z == 0) set_status(status, MLA_DEV_BAD_WINDOW);
+    kvl = 0;
+  }
   // first key any query of this chunk can see
   int j_lo = 0;
   if (W > 0) {
@@ -133,6 +137,7 @@ latent_attn_kernel(const TQ* __restrict__ q_abs, const TC* __restrict__ cache, i
 #pragma unroll
     for (int i = 0; i < MAX_OUT; ++i)
       if (i < nout) dst[c0 + 16 * i] = from_f32<TQ>(lrow > 0.f ? o[i] * inv : 0.f);
+    if (lse && c0 == 0) lse[m * H + h] = lrow > 0.f ? mrow + logf(lrow) : -INFINITY;
   }
   const int tot = hsumi16(cnt), hi = hmaxi16(last), lo = -hmaxi16(-first);
   if (vis_stats && h == 0 && row_ok && c0 == 0) {
@@ -147,7 +152,7 @@ latent_attn_kernel(const TQ* __restrict__ q_abs, const TC* __restrict__ cache, i
 template <typename TQ, typename TC>
 void latent_attention(cudaStream_t st, const mla_handle* h, const TQ* q_abs, const TC* cache,
                       int num_pages, const mla_attn_desc_t& desc, const int32_t* positions,
-                      TQ* o_lat) {
+                      TQ* o_lat, float* lse) {
   const Layout& l = h->lay;
   if (desc.num_blocks <= 0 || desc.block_len <= 0) return;
   const size_t smem = sizeof(float) * (QT * l.L + KT * (l.L + 1) + QT * KT);
@@ -161,11 +166,11 @@ void latent_attention(cudaStream_t st, const mla_handle* h, const TQ* q_abs, con
   latent_attn_kernel<TQ, TC><<<grid, A_THREADS, smem, st>>>(
       q_abs, cache, num_pages, h->cfg.page_size, desc.block_table, desc.max_pages, desc.kv_len,
       desc.window, desc.q_visible, positions, desc.block_len, l.H, l.rkv, l.L, h->scale,
-      h->status, desc.vis_stats, o_lat);
+      h->status, desc.vis_stats, o_lat, lse);
 }
 
 template void latent_attention<float, float>(cudaStream_t, const mla_handle*, const float*,
                                              const float*, int, const mla_attn_desc_t&,
-                                             const int32_t*, float*);
+                                             const int32_t*, float*, float*);
 }  // namespace simt
 }  // namespace mla

@@ -350,6 +350,19 @@ def cached_decode_workload(name: str, d: MLADims, seed: int, batch: int, prefill
                     prefill_values=pre_vals, steps=steps, description=description)
 
 
+def attention_inputs(wl: Workload, step: Step, seed: int):
+    """Seeded inputs for the latent attention step alone: absorbed query rows
+    ``[tokens * heads, cache_dim]`` (token-major, N(0, 1)) and every slot of
+    the paged cache ``[num_pages * page_size, cache_dim]`` (N(0, 1)), both
+    rounded to the layer dtype."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    d = wl.dims
+    rows = len(step.block_positions) * d.num_heads
+    q = _normal(rng, (rows, d.cache_dim), 1.0, 0.0, d.dtype)
+    cache = _normal(rng, (wl.num_pages * wl.page_size, d.cache_dim), 1.0, 0.0, d.dtype)
+    return q, cache
+
+
 # --------------------------------------------------------------------------
 # The named workloads (full sizes) and their shrunken parity variants
 # --------------------------------------------------------------------------

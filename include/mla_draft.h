@@ -72,8 +72,13 @@ enum {
   MLA_DEV_BAD_POSITION = 2,  /* position < 0 or >= max_position               */
   MLA_DEV_BAD_PAGE = 4,      /* block_table entry outside [0, num_pages)      */
   MLA_DEV_TIMEOUT = 8,       /* a bounded mbarrier wait gave up               */
-  MLA_DEV_BAD_LENGTH = 16    /* kv_len < 0 or > max_pages * page_size         */
+  MLA_DEV_BAD_LENGTH = 16,   /* kv_len < 0 or > max_pages * page_size         */
+  MLA_DEV_BAD_WINDOW = 32    /* window < 0 (the block's rows are zeroed)      */
 };
+
+/* Intermediate tensors the forward leaves in its workspace
+ * (mla_forward_workspace_offset). */
+enum { MLA_WS_Q_ABS = 0, MLA_WS_O_LAT = 1 };
 
 /* Layer configuration.  Structural dims follow the HF DeepSeek-V2/V3 fields;
  * q_lora_rank == 0 selects the non-low-rank path (q_proj +
@@ -110,7 +115,9 @@ typedef struct {
  * j%page_size.  Key j is visible to query i of block b iff
  *   q_visible[i] != 0  &&  j < kv_len[b]  &&
  *   (window[b] == 0 || positions[i] - j < window[b]).
- * A query with no visible key produces an exact zero output row. */
+ * A query with no visible key produces an exact zero output row.  A negative
+ * window is rejected on the device: MLA_DEV_BAD_WINDOW is set and the block's
+ * rows see no key. */
 typedef struct {
   int32_t num_blocks, block_len, max_pages, reserved;
   const int32_t *block_table;  /* [num_blocks, max_pages]                      */
@@ -239,10 +246,54 @@ mla_status_t mla_latent_cache_append_noalloc(mla_handle_t *h, const void *hidden
                                              void *cache, int32_t num_pages, void *stream);
 int64_t mla_append_noalloc_max_tokens(const mla_handle_t *h);
 
+/* Byte offset inside a forward workspace (sized for num_tokens block tokens)
+ * of an intermediate the forward leaves there: MLA_WS_Q_ABS, the absorbed
+ * queries [num_tokens, H, kv_lora_rank + qk_rope_head_dim] in the cache dtype,
+ * or MLA_WS_O_LAT, the latent attention output [num_tokens, H, kv_lora_rank]
+ * (fp16 for bf16 layers, fp32 for fp32 layers).  Valid after the forward's
+ * work on the stream has completed, until the workspace is reused.  Returns
+ * (size_t)-1 for a NULL handle, a negative count or an unknown part. */
+size_t mla_forward_workspace_offset(const mla_handle_t *h, int32_t num_tokens,
+                                    int32_t part);
+
+/* The latent attention step alone (MLA blog, forward_mqa and the Triton
+ * decode_attention_fwd it calls, which returns the output and the
+ * log-sum-exp of each query row; PR #758 / PR #1026 masks and zeroing):
+ * for every row m = (token, head) of q_abs,
+ *   s_j = scale * <q_abs[m], cache entry of key j>   over the visible keys j
+ *   o_lat[m] = sum_j softmax(s)_j * entry_j[:kv_lora_rank]
+ *   lse[m]   = log sum_j exp(s_j)                     (natural log)
+ * with visibility and the key -> cache-slot walk of mla_attn_desc_t.  A row
+ * that sees no key gets o_lat = +0 exactly and lse = -inf.
+ * q_abs: device [nb*T, H, kv_lora_rank + qk_rope_head_dim] in the cache dtype
+ * (bf16 or fp32), 16-byte aligned; positions: device int32 [nb*T]; cache as
+ * for the forward; o_lat: device [nb*T, H, kv_lora_rank], fp16 for bf16
+ * layers (the forward's intermediate type), fp32 for fp32 layers; lse:
+ * device fp32 [nb*T, H] or NULL.  The cache is only read.  Asynchronous on
+ * `stream`; no workspace, no allocation.  Index errors are reported through
+ * the device status word like the forward's. */
+mla_status_t mla_latent_attention(mla_handle_t *h, const void *q_abs,
+                                  const int32_t *positions, const void *cache,
+                                  int32_t num_pages, const mla_attn_desc_t *desc,
+                                  void *o_lat, float *lse, void *stream);
+
 /* Synchronise `stream`, read and clear the device status word.  Returns
  * MLA_OK, MLA_ERR_TIMEOUT (MLA_DEV_TIMEOUT set) or MLA_ERR_DEVICE_CHECK; the
  * raw bits go to *bits when non-NULL. */
 mla_status_t mla_get_device_status(mla_handle_t *h, void *stream, int32_t *bits);
+
+/* Self-check of the failure path (no counterpart on the pages: a test aid
+ * for the bounded waits every kernel of the library uses).  Enqueues one
+ * single-thread kernel that waits, with the library's bounded mbarrier wait,
+ * on a barrier nothing ever arrives on; after max_rounds try_wait rounds
+ * (1 .. 2^24; the kernels themselves use 2^26) the wait gives up, sets
+ * MLA_DEV_TIMEOUT in the handle's device status word and writes 1 to
+ * *gave_up (device int32).  The kernel issues no copies and holds no tensor
+ * memory, so nothing is in flight when it returns and the handle stays
+ * usable: mla_get_device_status then returns MLA_ERR_TIMEOUT once and clears
+ * the word.  Asynchronous on `stream`. */
+mla_status_t mla_check_wait_timeout(mla_handle_t *h, uint32_t max_rounds,
+                                    int32_t *gave_up, void *stream);
 
 /* Number of CUDA kernels this handle has enqueued so far (host counter;
  * launches replayed from a captured CUDA graph are not counted). */

@@ -146,6 +146,24 @@ def latent_attention(q_abs, entries, vis, scale, rkv):
     return p @ e[:, :rkv], p
 
 
+def latent_lse(q_abs, entries, vis, scale):
+    """Per row, the natural log of the sum over visible keys of exp(scale *
+    score): what the decode attention returns beside its output (MLA blog,
+    forward_mqa: decode_attention_fwd fills ``lse``), the statistic that
+    merges attention over disjoint key ranges (forward_mha,
+    merge_attn_states).  Computed as max + log(sum(exp(s - max))); -inf for a
+    row with no visible key.  Returns lse [R]."""
+    q = np.asarray(q_abs, np.float64)
+    e = np.asarray(entries, np.float64)
+    s = np.where(vis, (q @ e.T) * scale, -np.inf)
+    any_key = vis.any(axis=1)
+    m = np.where(any_key, s.max(axis=1), 0.0)
+    with np.errstate(invalid="ignore"):
+        l = np.where(vis, np.exp(s - m[:, None]), 0.0).sum(axis=1)
+    with np.errstate(divide="ignore"):
+        return np.where(any_key, m + np.log(np.where(any_key, l, 1.0)), -np.inf)
+
+
 def latent_attention_backward(q_abs, entries, vis, scale, rkv, d_o_lat):
     """Gradients of sum(o_lat * d_o_lat) for ``latent_attention``.
 

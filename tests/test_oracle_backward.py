@@ -227,3 +227,39 @@ def test_latent_attention_backward_ignores_rows_without_keys():
     np.testing.assert_array_equal(dq1, dq2)
     np.testing.assert_array_equal(de1, de2)
     assert np.all(dq1[2] == 0.0)
+
+
+def test_latent_lse_matches_library_logsumexp_and_closed_forms():
+    from scipy.special import logsumexp
+    q, e, vis, scale, rkv, do, _ = _latent_problem(seed=7)
+    lse = mla_grad.latent_lse(q, e, vis, scale)
+    s = (q @ e.T) * scale
+    for r in range(q.shape[0]):
+        if not vis[r].any():
+            assert lse[r] == -np.inf
+        else:
+            assert abs(lse[r] - logsumexp(s[r][vis[r]])) <= 1e-12 * max(1.0, abs(lse[r]))
+    # one visible key: the scaled score itself; n equal scores: score + log n
+    one = np.zeros_like(vis)
+    one[:, 4] = True
+    np.testing.assert_allclose(mla_grad.latent_lse(q, e, one, scale), s[:, 4], rtol=1e-14)
+    e_eq = np.repeat(e[:1], e.shape[0], axis=0)
+    full = np.ones_like(vis)
+    np.testing.assert_allclose(mla_grad.latent_lse(q, e_eq, full, scale),
+                               (q @ e[0]) * scale + np.log(e.shape[0]), rtol=1e-13)
+    # the output and the lse together: exp(s - lse) are the probabilities
+    o, p = mla_grad.latent_attention(q, e, vis, scale, rkv)
+    rows = vis.any(axis=1)
+    np.testing.assert_allclose(np.where(vis[rows], np.exp(s[rows] - lse[rows, None]), 0.0),
+                               p[rows], rtol=1e-12, atol=1e-15)
+
+
+def test_latent_lse_mutation_is_caught():
+    # natural log against log2 (a plausible slip in an exp2-domain kernel)
+    from scipy.special import logsumexp
+    q, e, vis, scale, rkv, do, _ = _latent_problem(seed=8)
+    lse = mla_grad.latent_lse(q, e, vis, scale)
+    wrong = lse / np.log(2.0)
+    r = int(np.nonzero(vis.any(axis=1))[0][0])
+    good = logsumexp(((q @ e.T) * scale)[r][vis[r]])
+    assert abs(lse[r] - good) < 1e-12 and abs(wrong[r] - good) > 1e-6
