@@ -81,3 +81,61 @@ def test_page_sizes_match_oracle(page_size):
     wl = W.prefill_workload(f"pages{page_size}", W.QWEN3_4B_MLA, 9, [150, 40, 333], 16,
                             page_size=page_size)
     check_workload(wl)
+
+
+def _scaled_workload(gain_q, gain_kv, seed=12):
+    """Config 1 small with the RMSNorm gains scaled and hidden states carrying
+    +-1e3 outliers (bf16-representable values on both sides)."""
+    import dataclasses
+    W = workloads
+    wl = W.make_workload("qwen3_4b_prefill", "small")
+    rnd = lambda x: W.bf16_bits_to_f32(W.bf16_bits(np.asarray(x, np.float32)))
+    w = dict(wl.weights)
+    w["q_a_layernorm"] = rnd(w["q_a_layernorm"] * gain_q)
+    w["kv_a_layernorm"] = rnd(w["kv_a_layernorm"] * gain_kv)
+    rng = np.random.default_rng(seed)
+    ctx = wl.ctx_hidden.copy()
+    ctx[rng.integers(0, ctx.shape[0], 40), rng.integers(0, ctx.shape[1], 40)] = rng.choice([-1e3, 1e3], 40)
+    step = wl.steps[0]
+    blk = step.block_hidden.copy()
+    blk[rng.integers(0, blk.shape[0], 8), rng.integers(0, blk.shape[1], 8)] = rng.choice([-1e3, 1e3], 8)
+    return dataclasses.replace(wl, name=f"gains{gain_q}x{gain_kv}_outliers", weights=w,
+                               ctx_hidden=ctx, steps=[dataclasses.replace(step, block_hidden=blk)])
+
+
+def test_fp16_intermediates_stay_in_range_with_large_gains_and_outliers():
+    """The bf16 layer keeps the normalised q_c, q_nope, o_lat and o (and the
+    weights they meet) in fp16, whose largest finite value is 65504.  Bounds
+    that follow from the RMSNorm (an element of a normalised row is at most
+    sqrt(width) times its gain): |q_c| <= sqrt(q_lora_rank) max|gamma_q|,
+    |o_lat| <= sqrt(kv_lora_rank) max|gamma_kv| (a convex combination of
+    normalised latents).  With both gains scaled 30x and +-1e3 outliers in the
+    hidden states every intermediate stays finite and inside these bounds."""
+    from head_latent_attention_qkv_gb300 import _lib, api
+    from head_latent_attention_qkv_gb300.runner import DeviceWorkload
+    wl = _scaled_workload(30.0, 30.0)
+    dev = DeviceWorkload(wl)
+    out = dev.run_all()[0]
+    torch.cuda.synchronize()
+    assert api.mla_get_device_status(dev.handle) == 0
+    assert torch.isfinite(out.float()).all()
+    d = wl.dims
+    M = out.shape[0]
+    ws = dev.handle._ws
+    oo = api.mla_forward_workspace_offset(dev.handle, M, _lib.MLA_WS_O_LAT)
+    qo = api.mla_forward_workspace_offset(dev.handle, M, _lib.MLA_WS_Q_ABS)
+    o_lat = ws[oo:oo + M * d.num_heads * d.kv_lora_rank * 2].view(torch.float16).float()
+    q_abs = ws[qo:qo + M * d.num_heads * d.cache_dim * 2].view(torch.bfloat16).float()
+    assert torch.isfinite(o_lat).all() and torch.isfinite(q_abs).all()
+    bound = np.sqrt(d.kv_lora_rank) * float(np.abs(wl.weights["kv_a_layernorm"]).max())
+    assert float(o_lat.abs().max()) <= bound * (1 + 2.0 ** -10) < 65504.0
+    cache = dev.cache.float()
+    assert torch.isfinite(cache[~torch.isnan(cache)]).all()
+    dev.handle.close()
+
+
+def test_large_query_gain_and_hidden_outliers_match_oracle():
+    """q_a_layernorm scaled 30x (logits about 30x larger) and +-1e3 outliers in
+    the hidden states: parity within the usual tolerance."""
+    from tests.parity import check_workload
+    check_workload(_scaled_workload(30.0, 1.0))
