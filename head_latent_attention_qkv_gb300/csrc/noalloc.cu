@@ -24,7 +24,9 @@ std::mutex g_mu;
 std::unordered_map<int, float*> g_scratch_addr;  // device ordinal -> address of the array
 
 // The array's name is only a host-side stand-in in host code; its device
-// address is looked up once per device, with that device current.
+// address is looked up once per device, with that device current, and kept for
+// the life of the process (a device reset would destroy the array; the header
+// rules out calls after one).
 mla_status_t scratch_for_current_device(float** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);

@@ -235,7 +235,9 @@ mla_status_t mla_draft_forward_after(mla_handle_t *h, const void *hidden,
  *    larger n returns MLA_ERR_INVALID_ARG with a message, nothing launched;
  *  - the handle's device must be current; the first call on each device
  *    looks up the array's device address (cudaGetSymbolAddress), so make
- *    that first call before any stream capture;
+ *    that first call before any stream capture; the address is kept for the
+ *    life of the process, so this entry point must not be used after the
+ *    device has been reset (cudaDeviceReset destroys the array);
  *  - every call shares the one array per device: calls whose work overlaps
  *    on the GPU (other streams, other handles, other threads) race on it and
  *    must be ordered by the caller.  Nothing in it needs to start at zero.
