@@ -17,9 +17,11 @@
 // tile that hold this CTA's value half ("value chunks") arrive in one copy
 // into the V buffer and serve both as B operand of QK^T (K-major) and of P V
 // (MN-major); the other five chunks of the tile stream through a 5-slot ring.
-// Each tile thus reads its 128 cache rows once per CTA, and the ring is deep
-// enough that a slot's refill (its copy holds the issuing thread ~550 cycles,
-// then lands ~1 k cycles later) is hidden behind the MMAs of the other slots.
+// Each tile thus reads its 128 cache rows once per CTA; the ring holds a
+// whole tile's five chunks, refilled as soon as the tile's MMAs are done with
+// it, so that the next tile's chunks are resident long before they are read
+// (one barrier for the ring: each mbarrier check costs the single MMA-issuing
+// thread about 200 cycles, each tcgen05.mma about 110).
 //
 // Tensor memory (512 columns): O at 0..255, S (fp32, 128 keys) at 256..383,
 // P (bf16 pairs, written over the first half of S once the softmax has read
@@ -97,8 +99,8 @@ __device__ __forceinline__ int ring_chunk(int i, int half) {
 struct Bars {
   uint64_t q_full;                    // Q chunks in shared memory (TMA)
   uint64_t q_tmem;                    // Q chunks in tensor memory (128 arrivals)
-  uint64_t r_full[RSLOTS];            // ring chunk landed (phase t)
-  uint64_t r_empty[RSLOTS];           // the MMAs reading the slot are done (phase t)
+  uint64_t r_full;                    // the tile's ring chunks landed (phase t; two producers)
+  uint64_t r_empty;                   // the MMAs reading the ring are done (phase t)
   uint64_t v_full;                    // V(t) landed (phase t)
   uint64_t s_full;                    // S(t) complete (phase t); also P(t - 1) V(t - 1)
   uint64_t p_full;                    // P(t) written (phase t)
@@ -167,7 +169,10 @@ __device__ __forceinline__ void softmax_and_stage(const AttnParams& P, Bars* B, 
     wait_bar(B, &B->s_full, ph, P.status);
     tc_fence_after();
 #pragma unroll
-    for (int c = 0; c < KT; c += 32) tmem_ld32(tmem + TM_S + c + lane_base, s + c);
+    for (int c = 0; c < KT; c += 32) tmem_ld32_nowait(tmem + TM_S + c + lane_base, s + c);
+    tmem_ld_wait();
+#pragma unroll
+    for (int c = 0; c < KT; c += 32) tmem_reg_fence32(s + c);
     // mask by logical position (a warp whose rows all see the whole tile skips it)
     const int lo = max(vlo - j0, 0), hi = min(vhi - j0, KT);   // visible columns [lo, hi)
     if (hi > lo) {
@@ -411,10 +416,8 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
   if (tid == 0) {
     mbar_init(&B->q_full, 1);
     mbar_init(&B->q_tmem, QROWS);
-    for (int s = 0; s < RSLOTS; ++s) {
-      mbar_init(&B->r_full[s], 1);
-      mbar_init(&B->r_empty[s], 1);
-    }
+    mbar_init(&B->r_full, 2);
+    mbar_init(&B->r_empty, 1);
     mbar_init(&B->v_full, 1);
     mbar_init(&B->s_full, 1);
     mbar_init(&B->p_full, QROWS);
@@ -504,28 +507,29 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
         mbar_wait(&B->q_full, 0, P.status);
         mbar_wait(&B->v_full, (nt - 1) & 1, P.status);
       } else {
-        // ---- ring: warp 6 refills slots 0, 2, 4, warp 7 slots 1, 3 ----
+        // ---- ring: warp 6 refills slots 0, 2, 4, warp 7 slots 1, 3, each
+        // once the MMAs of the previous tile are done with the whole ring ----
         prefetch_tmap(&P.tmK);
         prefetch_tmap(&P.tmKs);
         const int s0 = warp - 6;
         bool ok = true;
         for (int t = 0; t < nt && ok; ++t) {
           const int y0 = tile_run(t);
+          if (!wait_bar(B, &B->r_empty, (t & 1) ^ 1, P.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&B->r_full, (s0 == 0 ? 3 : 2) * KV_CH_BYTES);
           for (int i = s0; i < RSLOTS; i += 2) {
-            if (!wait_bar(B, &B->r_empty[i], (t & 1) ^ 1, P.status)) { ok = false; break; }
-            mbar_arrive_expect_tx(&B->r_full[i], KV_CH_BYTES);
             uint8_t* dst = smem + OFF_K + i * KV_CH_BYTES;
             const int c = ring_chunk(i, half);
             if (y0 >= 0) {
-              tma_load_3d(dst, &P.tmK, &B->r_full[i], c * DCH, y0, 0);
+              tma_load_3d(dst, &P.tmK, &B->r_full, c * DCH, y0, 0);
             } else {
               for (int seg = 0; seg < nseg; ++seg)
-                tma_load_3d(dst + seg * R * 128, &P.tmKs, &B->r_full[i], c * DCH,
+                tma_load_3d(dst + seg * R * 128, &P.tmKs, &B->r_full, c * DCH,
                             cache_row(j_lo + t * KT + seg * R), 0);
             }
           }
         }
-        for (int i = s0; i < RSLOTS; i += 2) mbar_wait(&B->r_full[i], (nt - 1) & 1, P.status);
+        mbar_wait(&B->r_full, (nt - 1) & 1, P.status);
       }
     }
   } else if (warp == 5) {
@@ -553,14 +557,12 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
         // S(t): the ring chunks, then the value chunks (P(t - 1) V(t - 1),
         // issued before, has read P out of these columns: same issuing
         // thread, executed in order)
-        for (int i = 0; i < RSLOTS && ok; ++i) {
-          ok = wait_bar(B, &B->r_full[i], ph, P.status);
-          if (!ok) break;
-          tc_fence_after();
-          qk_chunk(ring_chunk(i, half), smem + OFF_K + i * KV_CH_BYTES, i == 0);
-          mma_commit(&B->r_empty[i]);          // the slot may be refilled
-        }
-        if (!ok || !(ok = wait_bar(B, &B->v_full, ph, P.status))) break;
+        if (!(ok = wait_bar(B, &B->r_full, ph, P.status))) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int i = 0; i < RSLOTS; ++i) qk_chunk(ring_chunk(i, half), smem + OFF_K + i * KV_CH_BYTES, i == 0);
+        mma_commit(&B->r_empty);               // the ring may be refilled
+        if (!(ok = wait_bar(B, &B->v_full, ph, P.status))) break;
         tc_fence_after();
 #pragma unroll 1
         for (int i = 0; i < NVC; ++i) qk_chunk(NVC * half + i, smem + OFF_V + i * KV_CH_BYTES, false);
