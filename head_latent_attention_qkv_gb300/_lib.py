@@ -75,6 +75,8 @@ def _load():
         "mla_forward_workspace_offset": (SZ, [P, I32, I32]),
         "mla_latent_attention": (I32, [P, P, P, P, I32, C.POINTER(mla_attn_desc_t), P, P, P]),
         "mla_check_wait_timeout": (I32, [P, C.c_uint32, P, P]),
+        "mla_latent_attention_backward": (I32, [P, P, P, P, I32, C.POINTER(mla_attn_desc_t), P, P,
+                                                P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)

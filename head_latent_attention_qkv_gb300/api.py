@@ -146,6 +146,16 @@ def mla_latent_attention(h: Handle, q_abs, positions, cache, desc, o_lat=None, l
     return o_lat
 
 
+def mla_latent_attention_backward(h: Handle, q_abs, positions, cache, desc, o_lat, lse, d_o_lat,
+                                  d_q_abs, d_cache, stream=None):
+    """Gradients of the latent attention step: d_q_abs (written) and d_cache
+    (added to; fp32, zeroed by the caller)."""
+    check(lib.mla_latent_attention_backward(h.h, _ptr(q_abs), _ptr(positions), _ptr(cache),
+                                            cache.shape[0], C.byref(desc), _ptr(o_lat), _ptr(lse),
+                                            _ptr(d_o_lat), _ptr(d_q_abs), _ptr(d_cache),
+                                            _stream(stream)), "mla_latent_attention_backward")
+
+
 def mla_check_wait_timeout(h: Handle, max_rounds: int, gave_up, stream=None):
     """Self-check of the bounded-wait failure path (``gave_up``: a device
     int32 tensor of one element, set to 1 when the wait gave up)."""

@@ -363,6 +363,15 @@ def attention_inputs(wl: Workload, step: Step, seed: int):
     return q, cache
 
 
+def attention_grad_inputs(wl: Workload, step: Step, seed: int):
+    """Seeded upstream gradient of the latent attention output:
+    ``[tokens * heads, kv_lora_rank]`` float32, N(0, 1)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    d = wl.dims
+    rows = len(step.block_positions) * d.num_heads
+    return _normal(rng, (rows, d.kv_lora_rank), 1.0, 0.0, "fp32")
+
+
 # --------------------------------------------------------------------------
 # The named workloads (full sizes) and their shrunken parity variants
 # --------------------------------------------------------------------------

@@ -279,6 +279,31 @@ mla_status_t mla_latent_attention(mla_handle_t *h, const void *q_abs,
                                   int32_t num_pages, const mla_attn_desc_t *desc,
                                   void *o_lat, float *lse, void *stream);
 
+/* Backward of the latent attention step (the draft layer is trained through
+ * it: "Add config-selectable MLA draft attention" (SpecForge PR #758),
+ * Validation, gradient parity; forward = mla_latent_attention).  With
+ * P = exp(scale * <q_abs[i], e_j> - lse[i]) over the visible keys j of row
+ * i, dP = d_o_lat[i] . e_j[:kv_lora_rank], D = d_o_lat[i] . o_lat[i] and
+ * dS = P (dP - D):
+ *   d_q_abs[i] = scale * sum_j dS_ij e_j                        (written)
+ *   d_cache[slot(j)] += scale * sum_i dS_ij q_abs[i]
+ *                       + sum_i P_ij d_o_lat[i] on its first kv_lora_rank
+ *                         columns (the entries are keys and values at once)
+ * over every block of `desc` (blocks whose keys share cache pages add into
+ * the same slots; the caller zeroes d_cache before the first call).  Rows
+ * without a visible key pass nothing back.  q_abs, positions, cache, desc as
+ * for mla_latent_attention; o_lat and lse are that call's outputs; d_o_lat,
+ * d_q_abs: device fp32 [nb*T, H, ...]; d_cache: device fp32 [num_pages *
+ * page_size, kv_lora_rank + qk_rope_head_dim].  SIMT kernels, fp32
+ * arithmetic; entries at most 640 wide (MLA_ERR_UNSUPPORTED otherwise).
+ * Asynchronous on `stream`; no allocation. */
+mla_status_t mla_latent_attention_backward(mla_handle_t *h, const void *q_abs,
+                                           const int32_t *positions, const void *cache,
+                                           int32_t num_pages, const mla_attn_desc_t *desc,
+                                           const void *o_lat, const float *lse,
+                                           const float *d_o_lat, float *d_q_abs,
+                                           float *d_cache, void *stream);
+
 /* Synchronise `stream`, read and clear the device status word.  Returns
  * MLA_OK, MLA_ERR_TIMEOUT (MLA_DEV_TIMEOUT set) or MLA_ERR_DEVICE_CHECK; the
  * raw bits go to *bits when non-NULL. */
