@@ -217,12 +217,12 @@ class Session:
     most of its work (the context append and the last step's attention) as
     launches of their own on the step's inputs."""
 
-    def __init__(self, name, overlap=False):
+    def __init__(self, name, overlap=False, scale="full"):
         import torch
         from head_latent_attention_qkv_gb300 import _lib, api, workloads
         from head_latent_attention_qkv_gb300.runner import DeviceWorkload
         self.name, self.overlap = name, overlap
-        self.wl = workloads.make_workload(name)
+        self.wl = workloads.make_workload(name, scale)
         self.fl = algorithmic_flops(self.wl)
         self.dev = DeviceWorkload(self.wl)
         self.side = torch.cuda.Stream()
@@ -276,7 +276,7 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-    S = Session(args.workload, args.overlap)
+    S = Session(args.workload, args.overlap, args.scale)
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.__enter__()
     for _ in range(args.warmup):
@@ -321,7 +321,7 @@ def run_ours(args, rank, world):
     S.close()
     del S
     torch.cuda.empty_cache()
-    if args.workload == WORKLOAD and not args.no_decode:
+    if args.workload == WORKLOAD and args.scale == "full" and not args.no_decode:
         res["decode"] = [decode_line(name, args, flush, stream) for name in DECODE_WORKLOADS]
     return res
 
@@ -432,7 +432,8 @@ def base_line(args, world):
     return {"metric": METRIC, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "data": "synthetic (seeded N(0,1) hidden, N(0,0.02) weights)",
-            "config": {"workload": args.workload, "shape": DESC.get(args.workload, ""),
+            "config": {"workload": args.workload if args.scale == "full" else f"{args.workload} ({args.scale})",
+                       "shape": DESC.get(args.workload, ""),
                        "parallelism": f"replicas x{world}",
                        "l2": "flushed (256 MB write) between steps",
                        "schedule": "append on a second stream beside the forward's projections"
@@ -452,6 +453,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true",
                     help="skip the cached-decode lines of the default workload")
     ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--scale", default="full", choices=["full", "medium"],
+                    help="medium: the DeepSeek-V3-shaped layer on 1/64 of its batch (profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -382,7 +382,9 @@ WORKLOADS = ("tiny_fp32", "qwen3_4b_prefill", "qwen3_4b_sliding_gate",
 def make_workload(name: str, scale: str = "full") -> Workload:
     """Build a named workload.  ``scale='small'`` keeps the layer dims but
     shrinks batch/context so the fp64 oracle runs the whole thing in seconds,
-    with ragged context lengths that leave partial tiles and pages."""
+    with ragged context lengths that leave partial tiles and pages;
+    ``scale='medium'`` (DeepSeek-V3-shaped layer only) keeps the per-block
+    shapes at 1/64 of the batch."""
     small = scale == "small"
     if name == "tiny_fp32":
         return prefill_workload(name, TINY_FP32_MLA, 0, [64], 8, page_size=16,
@@ -426,6 +428,13 @@ def make_workload(name: str, scale: str = "full") -> Workload:
                                       description="64 seqs, prefilled 4096, L~U[1024,4096], 2 one-token steps")
     if name == "deepseek_v3_block_parallel":
         d = DEEPSEEK_V3_MLA
+        if scale == "medium":
+            # the same per-block work (16 x 128 query rows over a 4096-token
+            # context) on one sequence of 64 proposals: absorbed queries of
+            # 151 MB, more than L2, a few GB in all (profiling captures)
+            return block_parallel_workload(name, d, 4, batch=1, ctx_len=4096, blocks_per_seq=64,
+                                           block_len=16, page_size=128, windows=(0, 1024),
+                                           description="1 x 64 proposals of 16 over 4096 context")
         if small:
             return block_parallel_workload(name, d, 4, batch=2, ctx_len=192, blocks_per_seq=3,
                                            block_len=16, page_size=64, windows=(0, 100),

@@ -9,9 +9,13 @@ attention; the forward is the MLA blog's forward_mqa).  Inputs are seeded
 synthetic query rows, cache entries and upstream gradients; the oracle is
 ``oracle.mla_grad.latent_attention_backward`` (explicit formulas pinned by
 finite differences and autograd), run per block and summed over blocks that
-share cache slots.  Bar: 2e-2 of the rms for the largest and 2e-3 for the
-mean error of both gradients (1e-4 for the fp32 layer); rows without a
-visible key get exactly zero.
+share cache slots.  Bars: the mean error of both gradients within 2e-3 of
+their rms (1e-4 for the fp32 layer); per element, for bf16 layers, the
+forward's output o_lat is an fp16 tensor, so D_i = <dO_i, O_i> carries an
+error of at most 2^-11 sum_d |dO_id O_id| that every dS_ij of the row
+inherits times P_ij: an element may differ by scale |dD_i| sum_j P_ij |e_jd|
+(dQ) or scale sum_i P_ij |dD_i| |q_id| (dE) plus 2e-2 of the rms (the fp32
+layer: 1e-4 of the rms).  Rows without a visible key get exactly zero.
 """
 import numpy as np
 import pytest
@@ -28,12 +32,14 @@ def _cuda():
         pytest.skip("no CUDA device")
 
 
-def _check(got, ref, tol_max, tol_mean, what):
+def _check(got, ref, tol_max, tol_mean, what, extra=0.0):
     rms = np.sqrt(np.mean(ref ** 2))
     err = np.abs(got - ref)
     assert np.all(np.isfinite(got)), what
-    assert err.max() <= tol_max * rms and err.mean() <= tol_mean * rms, (
-        f"{what}: max {err.max() / rms:.3e} mean {err.mean() / rms:.3e} of rms {rms:.3e}")
+    over = err > tol_max * rms + extra
+    assert not over.any() and err.mean() <= tol_mean * rms, (
+        f"{what}: max {err.max() / rms:.3e} mean {err.mean() / rms:.3e} of rms {rms:.3e}, "
+        f"{int(over.sum())} elements beyond the bound")
 
 
 @pytest.mark.parametrize("name", ["tiny_fp32", "qwen3_4b_prefill", "qwen3_4b_sliding_gate",
@@ -68,6 +74,9 @@ def test_attention_backward_matches_gradient_oracle(name):
     scale = mla.softmax_scale(d)
     ref_q = np.zeros_like(q, dtype=np.float64)
     ref_c = np.zeros(cache_vals.shape)
+    fp16_o = d.dtype == "bf16"
+    bnd_q = np.zeros_like(ref_q)
+    bnd_c = np.zeros_like(ref_c)
     for b in range(len(step.kv_len)):
         n = int(step.kv_len[b])
         slots = np.array([int(step.block_table[b][j // P]) * P + j % P for j in range(n)])
@@ -80,11 +89,17 @@ def test_attention_backward_matches_gradient_oracle(name):
                                                     d.kv_lora_rank, d_o[r])
         ref_q[r] = dq
         np.add.at(ref_c, slots, de)
+        if fp16_o:
+            o_ref, p_ref = mla_grad.latent_attention(q[r], cache_vals[slots], vis_rows, scale,
+                                                     d.kv_lora_rank)
+            dD = 2.0 ** -11 * np.sum(np.abs(d_o[r] * o_ref), axis=1)          # [rows]
+            bnd_q[r] = scale * dD[:, None] * (p_ref @ np.abs(cache_vals[slots]))
+            np.add.at(bnd_c, slots, scale * (p_ref * dD[:, None]).T @ np.abs(q[r]))
         dead = ~vis_rows.any(axis=1)
         assert np.all(d_q[r][dead] == 0.0), "rows without keys must pass nothing back"
     tm, tn = (1e-4, 1e-4) if d.dtype == "fp32" else (2e-2, 2e-3)
-    _check(d_q, ref_q, tm, tn, f"{name} dQ_abs")
+    _check(d_q, ref_q, tm, tn, f"{name} dQ_abs", bnd_q)
     touched = np.abs(ref_c).sum(axis=1) > 0
     assert np.all(d_cache[~touched] == 0.0), "a slot no visible key uses received a gradient"
-    _check(d_cache[touched], ref_c[touched], tm, tn, f"{name} dEntries")
+    _check(d_cache[touched], ref_c[touched], tm, tn, f"{name} dEntries", bnd_c[touched])
     dev.handle.close()
