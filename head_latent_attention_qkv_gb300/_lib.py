@@ -73,7 +73,8 @@ def _load():
         "mla_latent_cache_append_noalloc": (I32, [P, P, P, P, I32, P, I32, P]),
         "mla_append_noalloc_max_tokens": (C.c_int64, [P]),
         "mla_forward_workspace_offset": (SZ, [P, I32, I32]),
-        "mla_latent_attention": (I32, [P, P, P, P, I32, C.POINTER(mla_attn_desc_t), P, P, P]),
+        "mla_latent_attention": (I32, [P, P, P, P, I32, C.POINTER(mla_attn_desc_t), P, P, P, SZ, P]),
+        "mla_latent_attention_workspace_bytes": (SZ, [P, C.POINTER(mla_attn_desc_t)]),
         "mla_check_wait_timeout": (I32, [P, C.c_uint32, P, P]),
         "mla_latent_attention_backward": (I32, [P, P, P, P, I32, C.POINTER(mla_attn_desc_t), P, P,
                                                 P, P, P, P]),

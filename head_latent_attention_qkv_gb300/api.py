@@ -133,17 +133,25 @@ def mla_draft_forward_after(h: Handle, hidden, positions, block_slot_mapping, ca
 
 
 def mla_latent_attention(h: Handle, q_abs, positions, cache, desc, o_lat=None, lse=None,
-                         stream=None):
+                         stream=None, workspace=None):
     """The latent attention step alone: ``o_lat`` [rows, kv_lora_rank] (fp16
-    for bf16 layers) and, when ``lse`` is given, its fp32 [rows] log-sum-exp."""
+    for bf16 layers) and, when ``lse`` is given, its fp32 [rows] log-sum-exp.
+    The workspace the few-row kernel needs comes from the handle unless given."""
     rows = desc.num_blocks * desc.block_len * h.dims.num_heads
     if o_lat is None:
         dt = torch.float16 if h.dims.dtype == "bf16" else torch.float32
         o_lat = torch.empty(rows, h.dims.kv_lora_rank, dtype=dt, device=h.device)
+    need = lib.mla_latent_attention_workspace_bytes(h.h, C.byref(desc))
+    ws = workspace if workspace is not None else (h.workspace(need) if need else None)
     check(lib.mla_latent_attention(h.h, _ptr(q_abs), _ptr(positions), _ptr(cache),
                                    cache.shape[0], C.byref(desc), _ptr(o_lat), _ptr(lse),
-                                   _stream(stream)), "mla_latent_attention")
+                                   _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)),
+          "mla_latent_attention")
     return o_lat
+
+
+def mla_latent_attention_workspace_bytes(h: Handle, desc) -> int:
+    return int(lib.mla_latent_attention_workspace_bytes(h.h, C.byref(desc)))
 
 
 def mla_latent_attention_backward(h: Handle, q_abs, positions, cache, desc, o_lat, lse, d_o_lat,

@@ -10,6 +10,7 @@
 #include "common.cuh"
 #include "append_tc.cuh"
 #include "attn_tc.cuh"
+#include "decode_tc.cuh"
 #include "gemm_tc.cuh"
 #include "simt.cuh"
 
@@ -282,8 +283,18 @@ namespace mla {
 namespace {
 
 struct FwdWs {
-  size_t a_out, q_cn, q_raw, q_nope, q_abs, o_lat, o, total;
+  size_t a_out, q_cn, q_raw, q_nope, q_abs, o_lat, o, dec, dec_bytes, total;
 };
+
+// Bytes the few-row attention may need for a forward of M block tokens: it
+// applies only when block_len * num_heads <= 32 (so num_heads <= 32 and at
+// most M blocks), and then runs at most 4 x num_sms + M (block, split)
+// parts.
+size_t decode_ws_bound(const mla_handle* h, long M) {
+  if (h->cfg.dtype != MLA_BF16 || h->lay.H > 32 || h->cfg.page_size % 128) return 0;
+  const long parts = 4L * h->num_sms + M;
+  return align256(parts * 32 * 512 * 4) + align256(parts * 32 * 4) + align256(parts * 32 * 3 * 4);
+}
 
 FwdWs forward_ws(const mla_handle* h, long M) {
   const Layout& l = h->lay;
@@ -296,6 +307,7 @@ FwdWs forward_ws(const mla_handle* h, long M) {
   w.q_abs = o;  o = align256(o + (size_t)M * l.H * l.L * l.elt);
   w.o_lat = o;  o = align256(o + (size_t)M * l.H * l.rkv * l.elt);
   w.o = o;      o = align256(o + (size_t)M * l.H * l.dv * l.elt);
+  w.dec = o;    w.dec_bytes = decode_ws_bound(h, M); o = align256(o + w.dec_bytes);
   w.total = o;
   return w;
 }
@@ -471,6 +483,12 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
   if (kv_ready) MLA_CUDA_TRY(cudaStreamWaitEvent(st, kv_ready, 0));
   if constexpr (std::is_same<TX, float>::value) {
     simt::latent_attention<TI, TX>(st, h, q_abs, (const TX*)cache, num_pages, d, pos, o_lat);
+  } else if (tc::decode_applies(h, d.block_len)) {
+    // few query rows per block: keys in the MMA's M dimension, splits merged after
+    s = tc::latent_decode(st, h, q_abs, (const TX*)cache, num_pages, d, pos, o_lat, nullptr,
+                          ws + w.dec, w.dec_bytes, pdl && !kv_ready);
+    if (s != MLA_OK) return s;
+    h->launches += 1;     // the merge
   } else {
     s = tc::latent_attention(st, h, q_abs, (const TX*)cache, num_pages, d, pos, o_lat, nullptr,
                              pdl && !kv_ready);
@@ -549,10 +567,17 @@ extern "C" size_t mla_forward_workspace_offset(const mla_handle_t* h, int32_t nu
   }
 }
 
+extern "C" size_t mla_latent_attention_workspace_bytes(const mla_handle_t* h,
+                                                      const mla_attn_desc_t* desc) {
+  if (!h || !desc || desc->num_blocks <= 0 || desc->block_len <= 0 || desc->max_pages <= 0) return 0;
+  return tc::decode_applies(h, desc->block_len) ? tc::decode_workspace_bytes(h, *desc) : 0;
+}
+
 extern "C" mla_status_t mla_latent_attention(mla_handle_t* h, const void* q_abs,
                                              const int32_t* positions, const void* cache,
                                              int32_t num_pages, const mla_attn_desc_t* desc,
-                                             void* o_lat, float* lse, void* stream) {
+                                             void* o_lat, float* lse, void* workspace,
+                                             size_t workspace_bytes, void* stream) {
   if (!h || !desc) return fail(MLA_ERR_INVALID_ARG, "attention: null handle or descriptor");
   const mla_attn_desc_t& d = *desc;
   if (d.num_blocks < 0 || d.block_len <= 0 || d.max_pages <= 0)
@@ -567,7 +592,17 @@ extern "C" mla_status_t mla_latent_attention(mla_handle_t* h, const void* q_abs,
     return fail(MLA_ERR_INVALID_ARG, "attention: q_abs, cache and o_lat must be 16-byte aligned");
   cudaStream_t st = (cudaStream_t)stream;
   h->launches += 1;
-  if (h->cfg.dtype == MLA_BF16) {
+  if (h->cfg.dtype == MLA_BF16 && tc::decode_applies(h, d.block_len)) {
+    const size_t need = tc::decode_workspace_bytes(h, d);
+    if (!workspace || workspace_bytes < need || (uintptr_t)workspace % 256)
+      return fail(MLA_ERR_INVALID_ARG,
+                  "attention: workspace smaller than mla_latent_attention_workspace_bytes() or not 256-byte aligned");
+    const mla_status_t s = tc::latent_decode(st, h, (const __nv_bfloat16*)q_abs,
+                                             (const __nv_bfloat16*)cache, num_pages, d, positions,
+                                             (__half*)o_lat, lse, workspace, workspace_bytes, false);
+    if (s != MLA_OK) return s;
+    h->launches += 1;
+  } else if (h->cfg.dtype == MLA_BF16) {
     const mla_status_t s = tc::latent_attention(st, h, (const __nv_bfloat16*)q_abs,
                                                 (const __nv_bfloat16*)cache, num_pages, d,
                                                 positions, (__half*)o_lat, lse, false);

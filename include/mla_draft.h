@@ -271,13 +271,21 @@ size_t mla_forward_workspace_offset(const mla_handle_t *h, int32_t num_tokens,
  * (bf16 or fp32), 16-byte aligned; positions: device int32 [nb*T]; cache as
  * for the forward; o_lat: device [nb*T, H, kv_lora_rank], fp16 for bf16
  * layers (the forward's intermediate type), fp32 for fp32 layers; lse:
- * device fp32 [nb*T, H] or NULL.  The cache is only read.  Asynchronous on
- * `stream`; no workspace, no allocation.  Index errors are reported through
- * the device status word like the forward's. */
+ * device fp32 [nb*T, H] or NULL.  The cache is only read.  Blocks of at
+ * most 32 query rows (block_len * num_heads <= 32, bf16, page_size a
+ * multiple of 128) run a kernel for few rows that splits every block's keys
+ * across the SMs and merges the splits by log-sum-exp (the blog's
+ * forward_mqa num_kv_splits / merge_attn_states); it needs a device
+ * workspace of mla_latent_attention_workspace_bytes() (256-byte aligned;
+ * MLA_ERR_INVALID_ARG when smaller), other shapes need none (workspace may be
+ * NULL).  Asynchronous on `stream`; no allocation.  Index errors are
+ * reported through the device status word like the forward's. */
+size_t mla_latent_attention_workspace_bytes(const mla_handle_t *h, const mla_attn_desc_t *desc);
 mla_status_t mla_latent_attention(mla_handle_t *h, const void *q_abs,
                                   const int32_t *positions, const void *cache,
                                   int32_t num_pages, const mla_attn_desc_t *desc,
-                                  void *o_lat, float *lse, void *stream);
+                                  void *o_lat, float *lse, void *workspace,
+                                  size_t workspace_bytes, void *stream);
 
 /* Backward of the latent attention step (the draft layer is trained through
  * it: "Add config-selectable MLA draft attention" (SpecForge PR #758),

@@ -144,3 +144,11 @@ def test_negative_window_is_rejected_on_the_device():
     rows = wl.block_len * wl.dims.num_heads
     assert torch.all(o[rows:2 * rows] == 0) and torch.all(torch.isneginf(lse[rows:2 * rows]))
     dev.handle.close()
+
+
+@pytest.mark.parametrize("case", ["t1_ragged", "t1_window_masked", "t3_h8"])
+def test_attention_entry_few_row_blocks_match_oracle(case):
+    """The few-row kernel through the entry point: o_lat and LSE against the
+    oracle, split merge included."""
+    from tests.test_gpu_parity import _few_row_case
+    _run(_few_row_case(case))

@@ -132,3 +132,43 @@ def test_fp16_intermediates_stay_in_range_with_large_gains_and_outliers():
     cache = dev.cache.float()
     assert torch.isfinite(cache[~torch.isnan(cache)]).all()
     dev.handle.close()
+
+
+def _few_row_case(case):
+    """Workloads that run the few-row attention (block_len x heads <= 32,
+    128-token pages): ragged lengths leave partial last tiles and many key
+    splits per block."""
+    import dataclasses
+    W = workloads
+    if case == "t1_ragged":
+        return W.cached_decode_workload(case, W.QWEN3_4B_MLA, 11, batch=5, prefill_len=700,
+                                        len_lo=60, len_hi=700, block_len=1, num_blocks=2,
+                                        page_size=128)
+    if case == "t1_window_masked":
+        wl = W.cached_decode_workload(case, W.QWEN3_4B_MLA.replace(rope_style="neox",
+                                                                   use_output_gate=True),
+                                      12, batch=4, prefill_len=900, len_lo=300, len_hi=900,
+                                      block_len=1, num_blocks=1, page_size=128)
+        s = wl.steps[0]
+        win = s.window.copy()
+        win[1], win[3] = 200, 1
+        qv = s.q_visible.copy()
+        qv[2] = 0
+        return dataclasses.replace(wl, steps=[dataclasses.replace(s, window=win, q_visible=qv)])
+    if case == "t2_h16":
+        return W.cached_decode_workload(case, W.QWEN3_4B_MLA.replace(num_heads=16), 13, batch=4,
+                                        prefill_len=600, len_lo=100, len_hi=600, block_len=2,
+                                        num_blocks=2, page_size=256)
+    if case == "t3_h8":
+        return W.prefill_workload(case, W.QWEN3_4B_MLA.replace(num_heads=8), 14, [300, 129, 650],
+                                  3, page_size=128)
+    raise KeyError(case)
+
+
+@pytest.mark.parametrize("case", ["t1_ragged", "t1_window_masked", "t2_h16", "t3_h8"])
+def test_few_row_blocks_match_oracle(case):
+    """Blocks of at most 32 query rows take the few-row kernel (keys in the
+    MMA's M dimension, every block's keys split across the SMs and merged by
+    log-sum-exp)."""
+    from tests.parity import check_workload
+    check_workload(_few_row_case(case))
