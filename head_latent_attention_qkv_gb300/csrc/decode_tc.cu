@@ -137,6 +137,17 @@ __global__ void __launch_bounds__(THREADS, 1) latent_decode_tc_kernel(const __gr
   const int nt = max(0, min(nt_all, t_begin + P.tiles_per_split) - t_begin);
   const int k_begin = j_lo + t_begin * KT;                // first key of this split
   const int k_end = min(kvl, k_begin + nt * KT);
+  const long part_base = ((long)b * P.splits + split) * NR;   // partial rows of this split
+  if (nt == 0) {
+    // a split past the block's keys: an empty partial the merge skips
+    pdl_wait();
+    if (tid < R) P.part_lse[part_base + tid] = -INFINITY;
+    if (tid < P.T) {
+      int* vs = P.part_vis + (((long)b * P.splits + split) * P.T + tid) * 3;
+      vs[0] = 0; vs[1] = -1; vs[2] = -1;
+    }
+    return;
+  }
 
   if (tid == 0) {
     mbar_init(&B->q_full, 1);
@@ -158,8 +169,6 @@ __global__ void __launch_bounds__(THREADS, 1) latent_decode_tc_kernel(const __gr
   const uint32_t tmem = B->tmem_slot;
   if (tid == 0) pdl_trigger();
   pdl_wait();
-
-  const long part_base = ((long)b * P.splits + split) * NR;   // partial rows of this split
 
   if (warp == 4 || warp == 6) {
     if (lane == 0 && nt > 0) {
@@ -399,45 +408,63 @@ __global__ void __launch_bounds__(THREADS, 1) latent_decode_tc_kernel(const __gr
   if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-// One CTA per block: rows r < R, value dims d: the splits' partials combined by
-// log-sum-exp in split order; a row no split saw stays exactly zero.
-__global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant__ DecodeParams P) {
-  const int b = blockIdx.x, R = P.T * P.H;
-  for (int idx = threadIdx.x; idx < R * 512; idx += blockDim.x) {
-    const int r = idx / 512, d = idx % 512;
-    const long base = (long)b * P.splits * NR;
+// One CTA per (block, row): the splits' partials of the row combined by
+// log-sum-exp in split order (empty splits, lse = -inf, skipped); a row no
+// split saw stays exactly zero.  Thread i handles value dims 4i .. 4i + 3.
+constexpr int MERGE_THREADS = 128, MAX_MERGE_SPLITS = 64;
+__global__ void __launch_bounds__(MERGE_THREADS) decode_merge_kernel(const __grid_constant__ DecodeParams P) {
+  const int R = P.T * P.H;
+  const int b = blockIdx.x / R, r = blockIdx.x % R;
+  const long base = (long)b * P.splits * NR + r;          // partial row of split s: base + s * NR
+  __shared__ float w_s[MAX_MERGE_SPLITS];
+  __shared__ float den_s, mx_s;
+  if (threadIdx.x < 32) {
     float mx = -INFINITY;
-    for (int s = 0; s < P.splits; ++s) mx = fmaxf(mx, P.part_lse[base + s * NR + r]);
-    float acc = 0.f, den = 0.f;
-    if (mx != -INFINITY) {
-      for (int s = 0; s < P.splits; ++s) {
-        const float l = P.part_lse[base + s * NR + r];
-        if (l == -INFINITY) continue;
-        const float w = exp2f(l - mx);
-        den += w;
-        acc += w * P.part[(base + s * NR + r) * 512 + d];
-      }
+    for (int s = threadIdx.x; s < P.splits; s += 32) mx = fmaxf(mx, P.part_lse[base + s * NR]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float den = 0.f;
+    for (int s = threadIdx.x; s < P.splits; s += 32) {
+      const float l = P.part_lse[base + s * NR];
+      const float w = (mx == -INFINITY || l == -INFINITY) ? 0.f : exp2f(l - mx);
+      w_s[s] = w;
+      den += w;
     }
-    const long row = (long)b * R + r;
-    P.o_lat[row * 512 + d] = __float2half_rn(den > 0.f ? acc / den : 0.f);
-    if (d == 0 && P.lse) P.lse[row] = den > 0.f ? (mx + log2f(den)) * 0.6931471805599453f : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    if (threadIdx.x == 0) { den_s = den; mx_s = mx; }
   }
-  if (P.vis_stats) {
-    for (int t = threadIdx.x; t < P.T; t += blockDim.x) {
-      int cnt = 0, first = -1, last = -1;
-      for (int s = 0; s < P.splits; ++s) {
-        const int* vs = P.part_vis + (((long)b * P.splits + s) * P.T + t) * 3;
-        if (vs[0] > 0) {
-          first = cnt ? min(first, vs[1]) : vs[1];
-          last = max(last, vs[2]);
-          cnt += vs[0];
-        }
+  __syncthreads();
+  const float den = den_s;
+  const int d = 4 * threadIdx.x;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < P.splits; ++s) {
+    const float w = w_s[s];
+    if (w == 0.f) continue;
+    const float4 v = *reinterpret_cast<const float4*>(P.part + (base + s * NR) * 512 + d);
+    acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  const long row = (long)b * R + r;
+  __half2 h2[2] = {__floats2half2_rn(acc.x * inv, acc.y * inv), __floats2half2_rn(acc.z * inv, acc.w * inv)};
+  *reinterpret_cast<uint2*>(P.o_lat + row * 512 + d) = *reinterpret_cast<uint2*>(h2);
+  if (threadIdx.x == 0 && P.lse) P.lse[row] = den > 0.f ? (mx_s + log2f(den)) * 0.6931471805599453f : -INFINITY;
+  // visibility statistics of the row's token (from its head-0 row)
+  if (threadIdx.x == 0 && P.vis_stats && r % P.H == 0) {
+    const int t = r / P.H;
+    int cnt = 0, first = -1, last = -1;
+    for (int s = 0; s < P.splits; ++s) {
+      const int* vs = P.part_vis + (((long)b * P.splits + s) * P.T + t) * 3;
+      if (vs[0] > 0) {
+        first = cnt ? min(first, vs[1]) : vs[1];
+        last = max(last, vs[2]);
+        cnt += vs[0];
       }
-      const long m = (long)b * P.T + t;
-      P.vis_stats[m * 3 + 0] = cnt;
-      P.vis_stats[m * 3 + 1] = cnt ? first : -1;
-      P.vis_stats[m * 3 + 2] = cnt ? last : -1;
     }
+    const long m = (long)b * P.T + t;
+    P.vis_stats[m * 3 + 0] = cnt;
+    P.vis_stats[m * 3 + 1] = cnt ? first : -1;
+    P.vis_stats[m * 3 + 2] = cnt ? last : -1;
   }
 }
 
@@ -457,6 +484,9 @@ static int tiles_per_split(const mla_handle* h, const mla_attn_desc_t& d) {
   long tps = (units + target - 1) / target;
   if (tps < 1) tps = 1;
   if (tps > max_tiles) tps = max_tiles;
+  // the merge holds at most MAX_MERGE_SPLITS splits of a block
+  const long min_tps = (max_tiles + MAX_MERGE_SPLITS - 1) / MAX_MERGE_SPLITS;
+  if (tps < min_tps) tps = min_tps;
   return (int)tps;
 }
 
@@ -517,7 +547,7 @@ mla_status_t latent_decode(cudaStream_t st, const mla_handle* h, const __nv_bflo
   Launch L(dim3((unsigned)parts), dim3(THREADS), SMEM_BYTES, st, pdl);
   cudaError_t e = cudaLaunchKernelEx(&L.cfg, latent_decode_tc_kernel, P);
   if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
-  decode_merge_kernel<<<d.num_blocks, 256, 0, st>>>(P);
+  decode_merge_kernel<<<d.num_blocks * d.block_len * l.H, MERGE_THREADS, 0, st>>>(P);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "decode merge launch");
   return MLA_OK;

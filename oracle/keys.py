@@ -104,12 +104,14 @@ class OracleRun:
         return out
 
 
-def run_workload(wl, blocks_per_step=None, ctx_all=False):
+def run_workload(wl, blocks_per_step=None, ctx_all=False, round_output=True):
     """Run the oracle over ``wl``.
 
     ``blocks_per_step[k]``: blocks of step k to evaluate (default: all).
     Context latents are computed only where a selected block can see them
-    unless ``ctx_all``.  Returns (OracleRun, [dict block -> out rows]).
+    unless ``ctx_all``.  ``round_output=False`` returns the fp64 outputs
+    before their storage rounding to the layer dtype.  Returns (OracleRun,
+    [dict block -> out rows]).
     """
     run = OracleRun(wl)
     outs = []
@@ -124,5 +126,5 @@ def run_workload(wl, blocks_per_step=None, ctx_all=False):
             run.append(wl.ctx_hidden, wl.ctx_positions, wl.ctx_slots, rows)
         if step.append_hidden is not None:
             run.append(step.append_hidden, step.append_positions, step.append_slots)
-        outs.append(run.forward_blocks(step, blocks))
+        outs.append(run.forward_blocks(step, blocks, round_output=round_output))
     return run, outs
