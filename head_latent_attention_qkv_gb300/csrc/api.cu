@@ -287,13 +287,11 @@ struct FwdWs {
 };
 
 // Bytes the few-row attention may need for a forward of M block tokens: it
-// applies only when block_len * num_heads <= 32 (so num_heads <= 32 and at
-// most M blocks), and then runs at most 4 x num_sms + M (block, split)
-// parts.
+// applies only when block_len * num_heads <= 32 (so at most M blocks of at
+// most 32 tokens).
 size_t decode_ws_bound(const mla_handle* h, long M) {
   if (h->cfg.dtype != MLA_BF16 || h->lay.H > 32 || h->cfg.page_size % 128) return 0;
-  const long parts = 4L * h->num_sms + M;
-  return align256(parts * 32 * 512 * 4) + align256(parts * 32 * 4) + align256(parts * 32 * 3 * 4);
+  return tc::decode_workspace_bound(h, M, 32);
 }
 
 FwdWs forward_ws(const mla_handle* h, long M) {

@@ -14,26 +14,31 @@
 // P^T is the B operand, written by the softmax into shared memory as P
 // [row][key] (K-major, 128-byte swizzle).
 //
-// Work unit: (block, key split).  A split covers `tiles_per_split` 128-key
-// tiles; every split writes its normalised partial output (fp32), its
-// log2-sum-exp and visibility counts into the workspace, and the merge
-// kernel combines the splits of a block in split order (the blog's
-// forward_mha merge_attn_states).  Splits are many and short (about four
-// tiles) so that the SMs stay busy whatever the mix of sequence lengths.
+// Work split: one persistent CTA per SM.  The U 128-key tiles of all blocks,
+// in block order, are cut into G = min(gridDim.x, U) equal ranges (none
+// empty); CTA c < G takes range c, which covers the tail of one block, whole
+// blocks and the head of another.  Each (block, CTA) piece is a segment; it
+// writes its normalised partial output (fp32), log2-sum-exp and visibility
+// counts to partial slot block + c (distinct for every segment: along the
+// tile order neither the block nor the CTA ever decreases and one of them
+// grows), and the merge kernel combines the segments of a block in CTA order
+// (the blog's forward_mha merge_attn_states).
 //
-// Shared memory: the nine 64-dim chunks of one key tile (one slot each,
-// slot c = chunk c), Q (nine chunks of 32 rows), P (two 64-key chunks).
-// Per tile the tensor pipe runs S^T over chunks 8, 0-3 (group A), 4-5 (B),
-// 6-7 (C), then, once the softmax has written P, O^T by value group 0..3;
-// each group's chunks are refilled for the next tile as soon as the O^T
-// group that reads them is done (chunk 8 with group A), so the next tile's
-// copies run under the current tile's O^T.
+// Pipeline.  The tensor pipe runs, per segment of n tiles,
+//   S^T(0) S^T(1) O^T(0) S^T(2) O^T(1) ... S^T(n-1) O^T(n-2) O^T(n-1)
+// so the scores of tile t + 1 are computed while the softmax of tile t runs
+// (S^T and P double-buffered).  The cache streams through a ring of five
+// 32 KiB slots (two 64-dim chunks each) in exactly that order: per tile the
+// key items (chunk pairs 0-1, 2-3, 4-5, 6-7, then the rope chunk 8) and, one
+// tile later, the value items (pairs 0-1 .. 6-7, read again, now from L2).
 //   warps 0-3 : softmax, thread = key (TMEM lane); row maxima by a butterfly
 //               transpose reduction across the warp and a 4-warp combine;
-//               running max per row kept identically by every thread (lazy
-//               rescale beyond 2^8); row sums kept per thread until the end
-//   warp 4    : page rows, Q, group A copies      warp 6: groups B, C copies
-//   warp 5    : tensor-memory allocation, MMA issue
+//               each row's running max and rescale factor kept once in
+//               shared memory (lazy rescale beyond 2^8); segment epilogue
+//   warp 4    : tensor-memory allocation, MMA issue
+//   warps 5-6 : ring copies (slots 0, 2, 4 / slots 1, 3)
+//   warp 7    : Q of each segment; zeroes the value rows past kv_len of a
+//               block's last tile (they may hold anything) before O^T reads them
 #include "decode_tc.cuh"
 
 #include <mutex>
@@ -46,27 +51,54 @@ namespace tc {
 namespace {
 
 constexpr int KT = 128, DCH = 64, NCH = 9, NR = 32;   // keys per tile, dims per chunk, rows (N)
-constexpr int THREADS = 224;                           // softmax x4, TMA, MMA, TMA
+constexpr int THREADS = 256;
+constexpr int NSLOT = 5;                               // ring slots (chunk pairs)
 constexpr int KV_CH_BYTES = KT * DCH * 2;              // 16 KiB
+constexpr int SLOT_BYTES = 2 * KV_CH_BYTES;            // 32 KiB
 constexpr int Q_CH_BYTES = NR * DCH * 2;               // 4 KiB
 constexpr int P_CH_BYTES = NR * DCH * 2;               // 4 KiB (64 keys)
-constexpr int OFF_K = 0;
-constexpr int OFF_Q = OFF_K + NCH * KV_CH_BYTES;
+constexpr int P_BYTES = 2 * P_CH_BYTES;                // one tile's P
+constexpr int K_ITEMS = 5, V_ITEMS = 4;                // ring items per tile
+constexpr int OFF_RING = 0;
+constexpr int OFF_Q = OFF_RING + NSLOT * SLOT_BYTES;
 constexpr int OFF_P = OFF_Q + NCH * Q_CH_BYTES;
-constexpr int OFF_RED = OFF_P + 2 * P_CH_BYTES;        // reduction scratch
-constexpr int OFF_BAR = OFF_RED + 2048;
+constexpr int OFF_RED = OFF_P + 2 * P_BYTES;
+constexpr int RED_BYTES = 2048;
+constexpr int OFF_BAR = OFF_RED + RED_BYTES;
 constexpr int SMEM_BYTES = 1024 + OFF_BAR + 256;
-constexpr uint32_t TMEM_COLS = 256, TM_S = 0, TM_O = 32;    // O^T group g at TM_O + 32 g
+// TMEM: S^T double buffer by tile (2 x 32 columns), O^T double buffer by segment (2 x 128)
+constexpr uint32_t TMEM_COLS = 512, TM_S = 0, TM_O = 64;
 constexpr float RESCALE_LOG2 = 8.f;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
+// shared reduction area (4-byte words)
+constexpr int RD_WPART = 0;      // [4][32] per-warp row values
+constexpr int RD_M = 128;        // [32] running row max (log2 domain)
+constexpr int RD_ALPHA = 160;    // [32] rescale factor of the current tile
+constexpr int RD_INVL = 192;     // [32] 1 / row sum
+constexpr int RD_LO = 224;       // [32] first visible key of each row
+constexpr int RD_HI = 256;       // [32] end of each row's visible keys
+constexpr int RD_FLAG = 288;     // some row rescaled in this tile
+constexpr int RD_SCH = 320;      // [8] scan partials, [8..9] first block / tile of the range
+static_assert((RD_SCH + 16) * 4 <= RED_BYTES, "reduction area");
+
+// Every barrier is waited on phase by phase by its one consumer role, and
+// the producer side can run at most one phase ahead of that wait (the
+// parity test tells only two consecutive phases apart).  Hence the S^T and
+// P barriers are doubled by tile parity (S^T(g + 1) may complete before the
+// softmax of tile g starts), the epilogue has its own per-segment barrier,
+// and the value rows past kv_len are zeroed only after the MMA thread, which
+// waits on every phase of the ring in order, hands their items over.
 struct Bars {
-  uint64_t q_full;
-  uint64_t g_full[3];      // key chunks landed: A = {8, 0..3}, B = {4, 5}, C = {6, 7} (phase t)
-  uint64_t g_empty[3];     // the MMAs reading the group are done (phase t)
-  uint64_t s_full;         // S^T(t) complete (and O^T(t - 1): same issuing thread)
-  uint64_t p_full;         // P(t) in shared memory (128 arrivals)
-  uint64_t o_done;         // O^T(t) complete
+  uint64_t full[NSLOT];    // ring slot landed
+  uint64_t empty[NSLOT];   // the MMAs reading the slot are done
+  uint64_t vready;         // a block's last (ragged) tile: its value items landed
+  uint64_t vfix;           // ... and their rows past kv_len are zeroed
+  uint64_t q_full, q_empty;
+  uint64_t s_full[2];      // S^T(g) complete (and every MMA issued before it), by g % 2
+  uint64_t p_full[2];      // P(g) in shared memory (128 arrivals), by g % 2
+  uint64_t o_done;         // O^T(g) complete (waited on only for a rescale)
+  uint64_t o_seg;          // the segment's last O^T complete
   uint64_t drain;
   uint32_t tmem_slot;
   int abort;
@@ -104,368 +136,712 @@ __device__ __forceinline__ float warp_transpose_reduce(float* x, int lane) {
   return x[0];
 }
 
+// Key range of block b: [j_lo, kvl), j_lo the first key any of its rows can
+// see under the sliding window, rounded down to a tile; nt tiles.  kv_len
+// outside [0, max_pages * page_size] is clamped and a negative window empties
+// the block (both reported once, by the first CTA).
+struct BlockKeys {
+  int kvl, j_lo, W, nt;
+  bool bad_len, bad_win;
+};
+__device__ __forceinline__ BlockKeys block_keys(const DecodeParams& P, int b) {
+  BlockKeys k;
+  int kvl = P.kv_len[b];
+  const int cap = P.max_pages * P.page_size;
+  k.bad_len = kvl < 0 || kvl > cap;
+  kvl = max(0, min(kvl, cap));
+  k.W = P.window ? P.window[b] : 0;
+  k.bad_win = k.W < 0;
+  if (k.bad_win) kvl = 0;
+  k.j_lo = 0;
+  if (k.W > 0) {
+    int pmin = 0x7fffffff;
+    for (int t = 0; t < P.T; ++t) pmin = min(pmin, P.positions[(long)b * P.T + t]);
+    k.j_lo = max(0, pmin - k.W + 1) / KT * KT;
+  }
+  k.kvl = kvl;
+  k.nt = kvl > k.j_lo ? (kvl - k.j_lo + KT - 1) / KT : 0;
+  return k;
+}
+
+// The CTA whose tile range [c U / G, (c + 1) U / G) holds global tile u
+// (G <= U: no range is empty).
+__device__ __forceinline__ int cta_of(long long u, long long U, int G) {
+  return (int)(((u + 1) * G - 1) / U);
+}
+
+// Segments of this CTA's range, in order: tiles [t0, t0 + n) of block b.
+struct Seg {
+  int b, t0, n;
+  BlockKeys k;
+};
+struct SegIter {
+  int b, t;        // next block to look at, first tile in it
+  long left;       // tiles of the range not yet handed out
+};
+__device__ __forceinline__ bool next_seg(const DecodeParams& P, SegIter& it, Seg& s) {
+  while (it.left > 0 && it.b < P.num_blocks) {
+    const BlockKeys k = block_keys(P, it.b);
+    if (it.t < k.nt) {
+      s.b = it.b;
+      s.t0 = it.t;
+      s.n = (int)min((long)(k.nt - it.t), it.left);
+      s.k = k;
+      it.left -= s.n;
+      ++it.b;
+      it.t = 0;
+      return true;
+    }
+    ++it.b;
+    it.t = 0;
+  }
+  return false;
+}
+// The segment's last tile ends its block and holds keys past kv_len.
+__device__ __forceinline__ bool seg_ragged_end(const Seg& s) {
+  return s.t0 + s.n == s.k.nt && (s.k.kvl - s.k.j_lo) % KT != 0;
+}
+
+// Block-wide exclusive scan over the CTA's threads (every thread calls).
+__device__ __forceinline__ int block_excl_scan(int v, int* sc, int tid, int* total) {
+  const int lane = tid % 32, warp = tid / 32;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sc[warp] = x;
+  __syncthreads();
+  int base = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < THREADS / 32; ++w) {
+    const int s = sc[w];
+    base += w < warp ? s : 0;
+    tot += s;
+  }
+  __syncthreads();
+  *total = tot;
+  return base + x - v;
+}
+
 __global__ void __launch_bounds__(THREADS, 1) latent_decode_tc_kernel(const __grid_constant__ DecodeParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   Bars* B = (Bars*)(smem + OFF_BAR);
-  float* red = (float*)(smem + OFF_RED);     // [2][4][32] warp partials, [32] combined, [32] rows' lo/hi
+  float* red = (float*)(smem + OFF_RED);
+  int* redi = (int*)red;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int b = blockIdx.x / P.splits, split = blockIdx.x % P.splits;
+  const int c = blockIdx.x, nb = P.num_blocks;
   const int R = P.T * P.H;                                  // live rows (<= 32)
-  const long row0 = (long)b * R;                           // first Q_abs row of the block
-
-  int kvl = P.kv_len[b];
-  const int cap = P.max_pages * P.page_size;
-  if (kvl < 0 || kvl > cap) {
-    if (tid == 0 && split == 0) set_status(P.status, MLA_DEV_BAD_LENGTH);
-    kvl = max(0, min(kvl, cap));
-  }
-  const int W = P.window ? P.window[b] : 0;
-  if (W < 0) {
-    if (tid == 0 && split == 0) set_status(P.status, MLA_DEV_BAD_WINDOW);
-    kvl = 0;
-  }
-  // key range of the block: [j_lo, kvl) from the first key any row sees
-  int j_lo = 0;
-  if (W > 0) {
-    int pmin = 0x7fffffff;
-    for (int t = 0; t < P.T; ++t) pmin = min(pmin, P.positions[(long)b * P.T + t]);
-    j_lo = max(0, pmin - W + 1) / KT * KT;
-  }
-  const int nt_all = kvl > j_lo ? (kvl - j_lo + KT - 1) / KT : 0;
-  const int t_begin = split * P.tiles_per_split;
-  const int nt = max(0, min(nt_all, t_begin + P.tiles_per_split) - t_begin);
-  const int k_begin = j_lo + t_begin * KT;                // first key of this split
-  const int k_end = min(kvl, k_begin + nt * KT);
-  const long part_base = ((long)b * P.splits + split) * NR;   // partial rows of this split
-  if (nt == 0) {
-    // a split past the block's keys: an empty partial the merge skips
-    pdl_wait();
-    if (tid < R) P.part_lse[part_base + tid] = -INFINITY;
-    if (tid < P.T) {
-      int* vs = P.part_vis + (((long)b * P.splits + split) * P.T + tid) * 3;
-      vs[0] = 0; vs[1] = -1; vs[2] = -1;
-    }
-    return;
-  }
 
   if (tid == 0) {
-    mbar_init(&B->q_full, 1);
-    for (int g = 0; g < 3; ++g) {
-      mbar_init(&B->g_full[g], 1);
-      mbar_init(&B->g_empty[g], 1);
+    for (int s = 0; s < NSLOT; ++s) {
+      mbar_init(&B->full[s], 1);
+      mbar_init(&B->empty[s], 1);
     }
-    mbar_init(&B->s_full, 1);
-    mbar_init(&B->p_full, 128);
+    mbar_init(&B->vready, 1);
+    mbar_init(&B->vfix, 1);
+    mbar_init(&B->q_full, 1);
+    mbar_init(&B->q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&B->s_full[i], 1);
+      mbar_init(&B->p_full[i], 128);
+    }
     mbar_init(&B->o_done, 1);
+    mbar_init(&B->o_seg, 1);
     mbar_init(&B->drain, 1);
     B->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) tmem_alloc(&B->tmem_slot, TMEM_COLS);
+  if (warp == 4) tmem_alloc(&B->tmem_slot, TMEM_COLS);
+
+  // ---- schedule: total tiles U, then the block holding this CTA's first tile
+  int* sc = redi + RD_SCH;
+  long long U = 0;
+  for (int base = 0; base < nb; base += THREADS) {
+    const int b = base + tid;
+    const int nt = b < nb ? block_keys(P, b).nt : 0;
+    int tot;
+    block_excl_scan(nt, sc, tid, &tot);
+    U += tot;
+  }
+  // the first min(gridDim, U) CTAs take one range each, so none is empty
+  const int G = (int)min((long long)gridDim.x, max(U, 1LL));
+  const long long u0 = c < G ? U * c / G : U, u1 = c < G ? U * (c + 1) / G : U;
+  if (tid == 0) { sc[8] = nb; sc[9] = 0; }
+  __syncthreads();
+  if (u1 > u0) {
+    long long run = 0;
+    for (int base = 0; base < nb; base += THREADS) {
+      const int b = base + tid;
+      const int nt = b < nb ? block_keys(P, b).nt : 0;
+      int tot;
+      const long long excl = run + block_excl_scan(nt, sc, tid, &tot);
+      if (nt > 0 && u0 >= excl && u0 < excl + nt) {
+        sc[8] = b;
+        sc[9] = (int)(u0 - excl);
+      }
+      run += tot;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = B->tmem_slot;
+  const int b_first = sc[8], t_first = sc[9];
+  const long ntiles = (long)(u1 - u0);
   if (tid == 0) pdl_trigger();
-  pdl_wait();
+  // Each role looks up what it needs from the descriptor (lengths, windows,
+  // positions, page rows: inputs of the call, not outputs of the kernels
+  // before this one) and then waits for the previous kernel before it
+  // touches Q_abs, the cache or the workspace.
 
-  if (warp == 4 || warp == 6) {
-    if (lane == 0 && nt > 0) {
-      const int ps = P.page_size, past_end = P.num_pages * ps;
-      // first cache row of tile t (past_end for an invalid page: zeros)
-      auto tile_row = [&](int t) {
-        const int j0 = k_begin + t * KT;
-        const int pg = P.block_table[(long)b * P.max_pages + j0 / ps];
-        if (pg < 0 || pg >= P.num_pages) {
-          set_status(P.status, MLA_DEV_BAD_PAGE);
-          return past_end;
-        }
-        return pg * ps + j0 % ps;
+  if (warp == 4) {
+    if (lane == 0 && ntiles > 0) {
+      // ---- MMA issuer ----
+      // One thread's issue rate is set by the instructions between its MMAs,
+      // so every shared-memory descriptor is a base computed once plus a
+      // constant offset (16-byte units) and the ring position advances by
+      // increments.
+      const uint32_t id_s = idesc_f16(128, NR, false);                 // K-major A and B
+      const uint32_t id_o = idesc_f16(128, NR, false) | (1u << 15);    // A (V^T) MN-major
+      const uint64_t dK = smem_desc_sw128(smem + OFF_RING);
+      const uint64_t dQ = smem_desc_sw128(smem + OFF_Q);
+      const uint64_t dV = smem_desc_sw128_mn(smem + OFF_RING, KV_CH_BYTES);
+      const uint64_t dP = smem_desc_sw128(smem + OFF_P);
+      constexpr uint32_t U_SLOT = SLOT_BYTES / 16, U_CH = KV_CH_BYTES / 16, U_Q = Q_CH_BYTES / 16;
+      constexpr uint32_t U_P = P_CH_BYTES / 16, U_PB = P_BYTES / 16, U_KSTEP = 16 * 128 / 16;
+      // the four 16-dim steps of one 64-dim chunk of S^T
+      auto s4 = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t acc0) {
+        mma_f16(d, a, b, id_s, acc0);
+        mma_f16(d, a + 2, b + 2, id_s, 1u);
+        mma_f16(d, a + 4, b + 4, id_s, 1u);
+        mma_f16(d, a + 6, b + 6, id_s, 1u);
       };
-      bool ok = true;
-      if (warp == 4) {
-        prefetch_tmap(&P.tmQ);
-        prefetch_tmap(&P.tmK1);
-        prefetch_tmap(&P.tmK4);
-        mbar_arrive_expect_tx(&B->q_full, NCH * Q_CH_BYTES);
-        tma_load_3d(smem + OFF_Q, &P.tmQ, &B->q_full, 0, (int)row0, 0);
-        for (int t = 0; t < nt && ok; ++t) {
-          if (!(ok = wait_bar(B, &B->g_empty[0], (t & 1) ^ 1, P.status))) break;
-          const int y0 = tile_row(t);
-          mbar_arrive_expect_tx(&B->g_full[0], 5 * KV_CH_BYTES);
-          tma_load_3d(smem + OFF_K + 8 * KV_CH_BYTES, &P.tmK1, &B->g_full[0], 8 * DCH, y0, 0);
-          tma_load_3d(smem + OFF_K, &P.tmK4, &B->g_full[0], 0, y0, 0);
+      // the eight 16-key steps of one 128-dim value group of O^T
+      auto o8 = [&](uint32_t d, uint64_t a, uint64_t p, uint32_t acc0) {
+        mma_f16(d, a, p, id_o, acc0);
+        mma_f16(d, a + U_KSTEP, p + 2, id_o, 1u);
+        mma_f16(d, a + 2 * U_KSTEP, p + 4, id_o, 1u);
+        mma_f16(d, a + 3 * U_KSTEP, p + 6, id_o, 1u);
+        mma_f16(d, a + 4 * U_KSTEP, p + U_P, id_o, 1u);
+        mma_f16(d, a + 5 * U_KSTEP, p + U_P + 2, id_o, 1u);
+        mma_f16(d, a + 6 * U_KSTEP, p + U_P + 4, id_o, 1u);
+        mma_f16(d, a + 7 * U_KSTEP, p + U_P + 6, id_o, 1u);
+      };
+      SegIter it{b_first, t_first, ntiles};
+      Seg s, nx;
+      uint32_t slot = 0, sph = 0;             // ring slot of the next item, its fill parity
+      uint32_t g = 0, kseg = 0, nfix = 0;
+      bool ok = true, have = next_seg(P, it, s);
+      pdl_wait();
+      auto advance = [&]() {
+        if (++slot == NSLOT) {
+          slot = 0;
+          sph ^= 1;
         }
-        mbar_wait(&B->q_full, 0, P.status);
-        mbar_wait(&B->g_full[0], (nt - 1) & 1, P.status);
-      } else {
-        prefetch_tmap(&P.tmK2);
-        for (int t = 0; t < nt && ok; ++t) {
-          const int y0 = tile_row(t);
-          for (int g = 1; g < 3 && ok; ++g) {
-            if (!(ok = wait_bar(B, &B->g_empty[g], (t & 1) ^ 1, P.status))) break;
-            mbar_arrive_expect_tx(&B->g_full[g], 2 * KV_CH_BYTES);
-            tma_load_3d(smem + OFF_K + (2 + 2 * g) * KV_CH_BYTES, &P.tmK2, &B->g_full[g], 0, y0, 2 + 2 * g);
+      };
+      // This thread is the ring's one consumer: every earlier item is
+      // consumed, so the next n items are at most one phase ahead and can be
+      // probed together (one probe latency instead of one per item when they
+      // have all landed, the usual case).
+      auto ready = [&](int n) {
+        uint32_t sl = slot, ph = sph;
+        bool r = true;
+#pragma unroll
+        for (int q = 0; q < K_ITEMS; ++q) {
+          if (q < n) r &= mbar_test_wait(&B->full[sl], ph);
+          if (++sl == NSLOT) {
+            sl = 0;
+            ph ^= 1;
           }
         }
-        for (int g = 1; g < 3; ++g) mbar_wait(&B->g_full[g], (nt - 1) & 1, P.status);
-      }
-    }
-  } else if (warp == 5) {
-    if (lane == 0 && nt > 0) {
-      // ---- MMA issuer ----
-      const uint32_t idesc_s = idesc_f16(128, NR, false);                 // K-major A and B
-      const uint32_t idesc_o = idesc_f16(128, NR, false) | (1u << 15);    // A (V^T) MN-major
-      bool ok = wait_bar(B, &B->q_full, 0, P.status);
-      auto s_chunk = [&](int c, bool first) {
-        const uint64_t da = smem_desc_sw128(smem + OFF_K + c * KV_CH_BYTES);
-        const uint64_t db = smem_desc_sw128(smem + OFF_Q + c * Q_CH_BYTES);
-#pragma unroll
-        for (int k = 0; k < DCH / 16; ++k)
-          mma_f16(tmem + TM_S, da + 2 * k, db + 2 * k, idesc_s, !(first && k == 0));
+        return r;
       };
-      auto o_group = [&](int g, bool first_tile) {
-        const uint64_t da = smem_desc_sw128_mn(smem + OFF_K + 2 * g * KV_CH_BYTES, KV_CH_BYTES);
-#pragma unroll
-        for (int k = 0; k < KT / 16; ++k) {
-          const uint64_t db = smem_desc_sw128(smem + OFF_P + (k / 4) * P_CH_BYTES) + 2 * (k % 4);
-          mma_f16(tmem + TM_O + 32 * g, da + (uint64_t)(16 * 128 / 16) * k, db, idesc_o,
-                  !(first_tile && k == 0));
+      auto wait_item = [&]() {
+        if (!wait_bar(B, &B->full[slot], sph, P.status)) return false;
+        tc_fence_after();
+        return true;
+      };
+      while (ok && have) {
+        const bool have_next = next_seg(P, it, nx);     // looked up ahead of its use
+        if (!(ok = wait_bar(B, &B->q_full, kseg & 1, P.status))) break;
+        tc_fence_after();
+        const uint32_t ob = tmem + TM_O + 128 * (kseg & 1);
+        const bool ragged = seg_ragged_end(s);
+        for (int t = 0; t <= s.n && ok; ++t) {
+          if (t < s.n) {
+            // S^T(g + t) into its buffer: pairs 0-1 .. 6-7, then the rope chunk
+            const uint32_t ts = tmem + TM_S + 32 * ((g + t) & 1);
+            const bool all_in = ready(K_ITEMS);
+            if (all_in) tc_fence_after();
+            for (int q = 0; q < 4; ++q) {
+              if (!all_in && !(ok = wait_item())) break;
+              const uint64_t a = dK + slot * U_SLOT, b = dQ + 2 * q * U_Q;
+              s4(ts, a, b, q == 0 ? 0u : 1u);
+              s4(ts, a + U_CH, b + U_Q, 1u);
+              mma_commit(&B->empty[slot]);
+              advance();
+            }
+            if (!ok) break;
+            if (!all_in && !(ok = wait_item())) break;
+            s4(ts, dK + slot * U_SLOT, dQ + 8 * U_Q, 1u);
+            mma_commit(&B->empty[slot]);
+            advance();
+            mma_commit(&B->s_full[(g + t) & 1]);
+            if (t == s.n - 1) mma_commit(&B->q_empty);
+          }
+          if (t >= 1) {
+            // O^T(g + t - 1) once its P is written
+            const uint32_t gg = g + t - 1;
+            const bool ragged_tile = ragged && t == s.n;
+            bool all_in = !ragged_tile && (mbar_test_wait(&B->p_full[gg & 1], (gg >> 1) & 1) & ready(V_ITEMS));
+            if (!all_in && !(ok = wait_bar(B, &B->p_full[gg & 1], (gg >> 1) & 1, P.status))) break;
+            tc_fence_after();
+            if (ragged_tile) {
+              // the block's last tile: hand its landed value items to warp 7
+              uint32_t sl = slot, ph = sph;
+              for (int q = 0; q < V_ITEMS && ok; ++q) {
+                ok = wait_bar(B, &B->full[sl], ph, P.status);
+                if (++sl == NSLOT) {
+                  sl = 0;
+                  ph ^= 1;
+                }
+              }
+              if (!ok) break;
+              mbar_arrive(&B->vready);
+              if (!(ok = wait_bar(B, &B->vfix, nfix & 1, P.status))) break;
+              ++nfix;
+              tc_fence_after();
+              all_in = true;
+            }
+            const uint64_t pb = dP + (gg & 1) * U_PB;
+            const uint32_t acc0 = t == 1 ? 0u : 1u;
+            for (int q = 0; q < V_ITEMS; ++q) {
+              if (!all_in && !(ok = wait_item())) break;
+              o8(ob + 32 * q, dV + slot * U_SLOT, pb, acc0);
+              mma_commit(&B->empty[slot]);
+              advance();
+            }
+            if (!ok) break;
+            mma_commit(&B->o_done);
+            if (t == s.n) mma_commit(&B->o_seg);
+          }
         }
-      };
-      for (int t = 0; t < nt && ok; ++t) {
-        const uint32_t ph = t & 1;
-        if (!(ok = wait_bar(B, &B->g_full[0], ph, P.status))) break;
-        tc_fence_after();
-        s_chunk(8, true);
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) s_chunk(c, false);
-        if (!(ok = wait_bar(B, &B->g_full[1], ph, P.status))) break;
-        tc_fence_after();
-        s_chunk(4, false);
-        s_chunk(5, false);
-        if (!(ok = wait_bar(B, &B->g_full[2], ph, P.status))) break;
-        tc_fence_after();
-        s_chunk(6, false);
-        s_chunk(7, false);
-        mma_commit(&B->s_full);
-        if (!(ok = wait_bar(B, &B->p_full, ph, P.status))) break;
-        tc_fence_after();
-        o_group(0, t == 0);
-        o_group(1, t == 0);
-        mma_commit(&B->g_empty[0]);
-        o_group(2, t == 0);
-        mma_commit(&B->g_empty[1]);
-        o_group(3, t == 0);
-        mma_commit(&B->g_empty[2]);
-        mma_commit(&B->o_done);
+        g += s.n;
+        ++kseg;
+        s = nx;
+        have = have_next;
       }
       mma_commit(&B->drain);
       mbar_wait(&B->drain, 0, P.status);
+    }
+  } else if (warp == 5 || warp == 6) {
+    if (lane == 0 && ntiles > 0) {
+      // ---- ring copies: this warp fills the slots s with s % 2 == p ----
+      const int p = warp - 5;
+      const int ps = P.page_size, past_end = P.num_pages * ps;
+      prefetch_tmap(&P.tmK1);
+      prefetch_tmap(&P.tmK2);
+      SegIter it{b_first, t_first, ntiles};
+      Seg s;
+      uint32_t item = 0;
+      uint32_t last_use = 0;          // bit sl: slot sl was filled; bit 8 + sl: the phase of its last fill
+      bool ok = true, waited = false;
+      auto load = [&](int y0, int q, bool value) {
+        const uint32_t slot = item % NSLOT, ph = (item / NSLOT) & 1;
+        if ((int)(slot % 2) == p) {
+          if (!(ok = wait_bar(B, &B->empty[slot], ph ^ 1, P.status))) return;
+          uint8_t* dst = smem + OFF_RING + slot * SLOT_BYTES;
+          if (!value && q == 4) {
+            mbar_arrive_expect_tx(&B->full[slot], KV_CH_BYTES);
+            tma_load_3d(dst, &P.tmK1, &B->full[slot], 8 * DCH, y0, 0);
+          } else {
+            mbar_arrive_expect_tx(&B->full[slot], SLOT_BYTES);
+            tma_load_3d(dst, &P.tmK2, &B->full[slot], 0, y0, 2 * q);
+          }
+          last_use = (last_use & ~(0x101u << slot)) | (1u << slot) | (ph << (8 + slot));
+        }
+        ++item;
+      };
+      bool have = next_seg(P, it, s);
+      while (ok && have) {
+        // first cache row of tile t of the segment (past_end for an invalid page: zeros)
+        auto tile_row = [&](int t) {
+          const int j0 = s.k.j_lo + (s.t0 + t) * KT;
+          const int pg = P.block_table[(long)s.b * P.max_pages + j0 / ps];
+          if (pg < 0 || pg >= P.num_pages) {
+            set_status(P.status, MLA_DEV_BAD_PAGE);
+            return past_end;
+          }
+          return pg * ps + j0 % ps;
+        };
+        int y_prev = 0, y = tile_row(0);
+        for (int t = 0; t <= s.n && ok; ++t) {
+          const int y_next = t + 1 < s.n ? tile_row(t + 1) : 0;   // one tile ahead
+          if (!waited) {
+            pdl_wait();
+            waited = true;
+          }
+          if (t < s.n)
+            for (int q = 0; q < K_ITEMS && ok; ++q) load(y, q, false);
+          if (t >= 1)
+            for (int q = 0; q < V_ITEMS && ok; ++q) load(y_prev, q, true);
+          y_prev = y;
+          y = y_next;
+        }
+        have = next_seg(P, it, s);
+      }
+      // the copies in flight land before the CTA exits
+      for (int sl = 0; sl < NSLOT; ++sl)
+        if (last_use & (1u << sl)) mbar_wait(&B->full[sl], (last_use >> (8 + sl)) & 1, P.status);
+    }
+  } else if (warp == 7) {
+    if (ntiles > 0) {
+      // ---- Q of each segment; value rows past kv_len zeroed ----
+      SegIter it{b_first, t_first, ntiles};
+      Seg cur, nxt;
+      bool have = next_seg(P, it, cur), ok = true;
+      uint32_t item_base = 0, kseg = 0, nq = 0, nfix = 0;
+      pdl_wait();
+      if (lane == 0) {
+        prefetch_tmap(&P.tmQ);
+        mbar_arrive_expect_tx(&B->q_full, NCH * Q_CH_BYTES);
+        tma_load_3d(smem + OFF_Q, &P.tmQ, &B->q_full, 0, cur.b * R, 0);
+      }
+      ++nq;
+      while (have && ok) {
+        const bool have_next = next_seg(P, it, nxt);
+        if (have_next) {
+          // Q of the next segment once every S^T of this one is done
+          if (lane == 0) {
+            ok = wait_bar(B, &B->q_empty, kseg & 1, P.status);
+            if (ok) {
+              mbar_arrive_expect_tx(&B->q_full, NCH * Q_CH_BYTES);
+              tma_load_3d(smem + OFF_Q, &P.tmQ, &B->q_full, 0, nxt.b * R, 0);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (ok) ++nq;
+        }
+        if (ok && seg_ragged_end(cur)) {
+          const int j0 = cur.k.j_lo + (cur.t0 + cur.n - 1) * KT;
+          const int valid = cur.k.kvl - j0;                   // 1 .. 127 live rows
+          const int units = (KT - valid) * 16;                // 16-byte units past kv_len, per item
+          ok = __all_sync(0xffffffffu, wait_bar(B, &B->vready, nfix & 1, P.status));
+          if (ok) {
+            for (int q = 0; q < V_ITEMS; ++q) {
+              const uint32_t slot = (item_base + 9 * cur.n - V_ITEMS + q) % NSLOT;
+              uint8_t* sp = smem + OFF_RING + slot * SLOT_BYTES;
+              for (int i = lane; i < units; i += 32) {
+                const int row = valid + i / 16, part = i % 16;
+                *reinterpret_cast<uint4*>(sp + (part / 8) * KV_CH_BYTES + row * 128 + (part % 8) * 16) =
+                    make_uint4(0, 0, 0, 0);
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B->vfix);
+            ++nfix;
+          }
+        }
+        item_base += 9 * cur.n;
+        cur = nxt;
+        have = have_next;
+        ++kseg;
+      }
+      if (lane == 0) mbar_wait(&B->q_full, (nq - 1) & 1, P.status);
     }
   } else {
     // ---- softmax warps: thread k = key k of the tile (TMEM lane k) ----
     const int k = tid;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    float* wpart = red;                     // [2][4][32]
-    float* comb = red + 256;                // [32] combined row values
-    int* rlo = (int*)(red + 288);           // [32] first visible key of each row
-    int* rhi = (int*)(red + 320);           // [32] end of each row's visible keys
-    if (k < NR) {
-      int lo = 0, hi = 0;
-      if (k < R) {
-        const long m = (long)b * P.T + k / P.H;
-        const int p = P.positions[m];
-        const bool qv = P.q_visible ? P.q_visible[m] != 0 : true;
-        lo = W > 0 ? max(0, p - W + 1) : 0;
-        hi = qv ? kvl : 0;
+    float* wpart = red + RD_WPART;
+    float* m_s = red + RD_M;
+    float* al_s = red + RD_ALPHA;
+    float* il_s = red + RD_INVL;
+    int* rlo = redi + RD_LO;
+    int* rhi = redi + RD_HI;
+    pdl_wait();
+    if (c == 0) {
+      // each block's segments for the merge (first CTA, count); invalid
+      // lengths and windows reported once
+      long long run = 0;
+      for (int base = 0; base < nb; base += 128) {
+        const int b = base + k;
+        BlockKeys bk{};
+        if (b < nb) {
+          bk = block_keys(P, b);
+          if (bk.bad_len) set_status(P.status, MLA_DEV_BAD_LENGTH);
+          if (bk.bad_win) set_status(P.status, MLA_DEV_BAD_WINDOW);
+        }
+        int x = bk.nt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        if (lane == 31) redi[RD_WPART + warp] = x;
+        softmax_sync();
+        int wb = 0, tot = 0;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const int sv = redi[RD_WPART + w];
+          wb += w < warp ? sv : 0;
+          tot += sv;
+        }
+        softmax_sync();
+        const long long excl = run + wb + x - bk.nt;
+        if (b < nb) {
+          const int f = bk.nt ? cta_of(excl, U, G) : 0;
+          const int l = bk.nt ? cta_of(excl + bk.nt - 1, U, G) : -1;
+          P.meta[2 * (long)b] = f;
+          P.meta[2 * (long)b + 1] = l - f + 1;
+        }
+        run += tot;
       }
-      rlo[k] = lo;
-      rhi[k] = hi;
     }
-    softmax_sync();
-    float mrow[NR], lrow[NR];
+    SegIter it{b_first, t_first, ntiles};
+    Seg s, nx;
+    uint32_t g = 0, kseg = 0;
+    bool have = next_seg(P, it, s);
+    while (have) {
+      const bool have_next = next_seg(P, it, nx);
+      const int b = s.b;
+      const long slot = (long)b + c;
+      const int k_begin = s.k.j_lo + s.t0 * KT;              // first key of the segment
+      const int k_end = min(s.k.kvl, k_begin + s.n * KT);
+      const uint32_t ob = tmem + TM_O + 128 * (kseg & 1);
+      softmax_sync();                          // the previous segment's epilogue is done with the rows
+      if (k < NR) {
+        int lo = 0, hi = 0;
+        if (k < R) {
+          const long m = (long)b * P.T + k / P.H;
+          const int pq = P.positions[m];
+          const bool qv = P.q_visible ? P.q_visible[m] != 0 : true;
+          lo = s.k.W > 0 ? max(0, pq - s.k.W + 1) : 0;
+          hi = qv ? s.k.kvl : 0;
+        }
+        rlo[k] = lo;
+        rhi[k] = hi;
+        m_s[k] = -INFINITY;
+      }
+      softmax_sync();
+      float lrow[NR];
 #pragma unroll
-    for (int r = 0; r < NR; ++r) { mrow[r] = -INFINITY; lrow[r] = 0.f; }
-    for (int t = 0; t < nt; ++t) {
-      const uint32_t ph = t & 1;
-      const int j = k_begin + t * KT + k;   // this thread's key
-      float s[NR];
-      wait_bar(B, &B->s_full, ph, P.status);
-      tc_fence_after();
-      tmem_ld32_nowait(tmem + TM_S + lane_base, s);
-      tmem_ld_wait();
-      tmem_reg_fence32(s);
-      // mask by logical position: row r sees keys [rlo, rhi)
+      for (int r = 0; r < NR; ++r) lrow[r] = 0.f;
+      for (int t = 0; t < s.n; ++t) {
+        const uint32_t gg = g + t;
+        const int j = k_begin + t * KT + k;   // this thread's key
+        float sv[NR];
+        wait_bar(B, &B->s_full[gg & 1], (gg >> 1) & 1, P.status);
+        tc_fence_after();
+        tmem_ld32_nowait(tmem + TM_S + 32 * (gg & 1) + lane_base, sv);
+        tmem_ld_wait();
+        tmem_reg_fence32(sv);
+        // mask by logical position: row r sees keys [lo_r, hi_r)
 #pragma unroll
-      for (int r = 0; r < NR; ++r) s[r] = (j >= rlo[r] && j < rhi[r]) ? s[r] : -INFINITY;
+        for (int r = 0; r < NR; r += 4) {
+          const int4 lo4 = *reinterpret_cast<const int4*>(rlo + r), hi4 = *reinterpret_cast<const int4*>(rhi + r);
+          sv[r] = (j >= lo4.x && j < hi4.x) ? sv[r] : -INFINITY;
+          sv[r + 1] = (j >= lo4.y && j < hi4.y) ? sv[r + 1] : -INFINITY;
+          sv[r + 2] = (j >= lo4.z && j < hi4.z) ? sv[r + 2] : -INFINITY;
+          sv[r + 3] = (j >= lo4.w && j < hi4.w) ? sv[r + 3] : -INFINITY;
+        }
+        float x[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) x[r] = sv[r];
+        wpart[warp * 32 + lane] = warp_transpose_reduce<true>(x, lane);   // lane l: max of row l
+        softmax_sync();
+        if (warp == 0) {
+          // row `lane`: running max (exp2 domain) and the factor for what is accumulated
+          const float cm = fmaxf(fmaxf(wpart[lane], wpart[32 + lane]), fmaxf(wpart[64 + lane], wpart[96 + lane]));
+          const float tm = cm * P.scale_log2, m_old = m_s[lane];
+          const bool grow = tm > m_old + RESCALE_LOG2;
+          const float m_new = grow ? tm : m_old;
+          const float alpha = (grow && m_old != -INFINITY) ? exp2f(m_old - m_new) : 1.f;
+          m_s[lane] = m_new;
+          al_s[lane] = alpha;
+          const bool any = __any_sync(0xffffffffu, alpha != 1.f);
+          if (lane == 0) redi[RD_FLAG] = any;
+        }
+        softmax_sync();
+        float mref[NR], alpha[NR];
+#pragma unroll
+        for (int r = 0; r < NR; r += 4) {
+          const float4 mv = *reinterpret_cast<const float4*>(m_s + r);
+          const float4 av = *reinterpret_cast<const float4*>(al_s + r);
+          mref[r] = mv.x; mref[r + 1] = mv.y; mref[r + 2] = mv.z; mref[r + 3] = mv.w;
+          alpha[r] = av.x; alpha[r + 1] = av.y; alpha[r + 2] = av.z; alpha[r + 3] = av.w;
+        }
+        const bool rescale = redi[RD_FLAG] != 0;
+        // O^T(gg - 1) is issued after S^T(gg) (and O^T(gg) only after this
+        // tile's P): a row that grew waits for it, then rescales
+        if (rescale && t > 0) {
+          wait_bar(B, &B->o_done, (gg - 1) & 1, P.status);
+          tc_fence_after();
+#pragma unroll 1
+          for (int q = 0; q < 4; ++q) {
+            float o[NR];
+            tmem_ld32_nowait(ob + 32 * q + lane_base, o);
+            tmem_ld_wait();
+            tmem_reg_fence32(o);
+#pragma unroll
+            for (int r = 0; r < NR; ++r) o[r] *= alpha[r];
+            tmem_st32(ob + 32 * q + lane_base, o);
+          }
+        }
+        // P[r][k] (bf16) into the swizzled K-major tile: 16-byte unit (k % 64) / 8
+        // of row r sits at unit ((k % 64) / 8) ^ (r % 8)
+        uint8_t* pchunk = smem + OFF_P + (gg & 1) * P_BYTES + (k / 64) * P_CH_BYTES;
+        const int kk = k % 64;
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          const float m0 = mref[r] == -INFINITY ? 0.f : mref[r];
+          const float p = fast_exp2(fmaf(sv[r], P.scale_log2, -m0));
+          lrow[r] = fmaf(lrow[r], alpha[r], p);
+          *reinterpret_cast<__nv_bfloat16*>(pchunk + r * 128 + (((kk >> 3) ^ (r & 7)) << 4) + (kk & 7) * 2) =
+              __float2bfloat16_rn(p);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&B->p_full[gg & 1]);
+      }
+      // ---- epilogue of the segment: row sums, normalised partial, lse, visibility
       float x[NR];
 #pragma unroll
-      for (int r = 0; r < NR; ++r) x[r] = s[r];
-      const float wmax = warp_transpose_reduce<true>(x, lane);   // lane l: max of row l over the warp
-      wpart[ph * 128 + warp * 32 + lane] = wmax;
+      for (int r = 0; r < NR; ++r) x[r] = lrow[r];
+      wpart[warp * 32 + lane] = warp_transpose_reduce<false>(x, lane);
       softmax_sync();
       if (warp == 0) {
-        const float* w4 = wpart + ph * 128;
-        comb[lane] = fmaxf(fmaxf(w4[lane], w4[32 + lane]), fmaxf(w4[64 + lane], w4[96 + lane]));
+        const float l = (wpart[lane] + wpart[32 + lane]) + (wpart[64 + lane] + wpart[96 + lane]);
+        il_s[lane] = l > 0.f ? 1.f / l : 0.f;
+        P.part_lse[slot * NR + lane] = l > 0.f ? m_s[lane] + log2f(l) : -INFINITY;
       }
       softmax_sync();
-      // every thread updates the rows' running maxima identically (exp2 domain)
-      float alpha[NR];
-      bool any_rescale = false;
+      float il[NR];
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        const float tm = comb[r] * P.scale_log2;
-        const bool grow = tm > mrow[r] + RESCALE_LOG2;
-        const float m_new = grow ? tm : mrow[r];
-        alpha[r] = (grow && mrow[r] != -INFINITY) ? exp2f(mrow[r] - m_new) : 1.f;
-        any_rescale |= alpha[r] != 1.f;
-        mrow[r] = m_new;
+      for (int r = 0; r < NR; r += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(il_s + r);
+        il[r] = v.x; il[r + 1] = v.y; il[r + 2] = v.z; il[r + 3] = v.w;
       }
-      // value rows of keys past kv_len may hold anything: zero this key's
-      // row in the eight value chunks before P V^T reads them
-      if (j >= kvl) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint4* rowp = reinterpret_cast<uint4*>(smem + OFF_K + c * KV_CH_BYTES + k * 128);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) rowp[q] = make_uint4(0, 0, 0, 0);
-        }
-      }
-      // P[r][k] (bf16) into the swizzled K-major tile: 16-byte unit (k % 64) / 8
-      // of row r sits at unit ((k % 64) / 8) ^ (r % 8)
-      uint8_t* pchunk = smem + OFF_P + (k / 64) * P_CH_BYTES;
-      const int kk = k % 64;
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        const float mref = mrow[r] == -INFINITY ? 0.f : mrow[r];
-        const float p = fast_exp2(fmaf(s[r], P.scale_log2, -mref));
-        lrow[r] = lrow[r] * alpha[r] + p;
-        *reinterpret_cast<__nv_bfloat16*>(pchunk + r * 128 + (((kk >> 3) ^ (r & 7)) << 4) + (kk & 7) * 2) =
-            __float2bfloat16_rn(p);
-      }
-      // O^T(t - 1) has completed (before S^T(t)): rescale the rows that grew
-      if (t > 0 && __any_sync(0xffffffffu, any_rescale)) {
+      wait_bar(B, &B->o_seg, kseg & 1, P.status);
+      tc_fence_after();
+      // thread k holds value dim 128 q + k of every row: one 128-byte row of
+      // the [dim][row] partial
 #pragma unroll 1
-        for (int g = 0; g < 4; ++g) {
-          float o[NR];
-          tmem_ld32_nowait(tmem + TM_O + 32 * g + lane_base, o);
-          tmem_ld_wait();
-          tmem_reg_fence32(o);
-#pragma unroll
-          for (int r = 0; r < NR; ++r) o[r] *= alpha[r];
-          tmem_st32(tmem + TM_O + 32 * g + lane_base, o);
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&B->p_full);
-    }
-    // rows' sums over the 128 keys of every tile (threads hold partials)
-    float x[NR];
-#pragma unroll
-    for (int r = 0; r < NR; ++r) x[r] = lrow[r];
-    const float wsum = warp_transpose_reduce<false>(x, lane);
-    softmax_sync();
-    wpart[warp * 32 + lane] = wsum;
-    softmax_sync();
-    if (warp == 0) comb[lane] = (wpart[lane] + wpart[32 + lane]) + (wpart[64 + lane] + wpart[96 + lane]);
-    softmax_sync();
-    if (nt > 0) wait_bar(B, &B->o_done, (nt - 1) & 1, P.status);
-    tc_fence_after();
-    // partial output of this split: thread k holds value dim 128 g + k of every row
-#pragma unroll 1
-    for (int g = 0; g < 4; ++g) {
-      float o[NR];
-      if (nt > 0) {
-        tmem_ld32_nowait(tmem + TM_O + 32 * g + lane_base, o);
+      for (int q = 0; q < 4; ++q) {
+        float o[NR];
+        tmem_ld32_nowait(ob + 32 * q + lane_base, o);
         tmem_ld_wait();
         tmem_reg_fence32(o);
-      }
+        float4* dst = reinterpret_cast<float4*>(P.part + (slot * 512 + 128 * q + k) * NR);
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        const float l = comb[r];
-        if (r < R) P.part[(part_base + r) * 512 + 128 * g + k] = (nt > 0 && l > 0.f) ? o[r] / l : 0.f;
+        for (int r = 0; r < NR; r += 4)
+          dst[r / 4] = make_float4(o[r] * il[r], o[r + 1] * il[r + 1], o[r + 2] * il[r + 2], o[r + 3] * il[r + 3]);
       }
-    }
-    float mk = -INFINITY;                   // row k's running max (registers indexed statically)
-#pragma unroll
-    for (int r = 0; r < NR; ++r) mk = (r == k) ? mrow[r] : mk;
-    if (k < R) P.part_lse[part_base + k] = (nt > 0 && comb[k] > 0.f) ? mk + log2f(comb[k]) : -INFINITY;
-    if (k < P.T) {   // visibility of token k over this split's keys (one interval)
-      const int lo = max(rlo[k * P.H], k_begin), hi = min(rhi[k * P.H], k_end);
-      int* vs = P.part_vis + (((long)b * P.splits + split) * P.T + k) * 3;
-      vs[0] = hi > lo ? hi - lo : 0;
-      vs[1] = hi > lo ? lo : -1;
-      vs[2] = hi > lo ? hi - 1 : -1;
+      if (k < P.T) {   // visibility of token k over this segment's keys (one interval)
+        const int lo = max(rlo[k * P.H], k_begin), hi = min(rhi[k * P.H], k_end);
+        int* vs = P.part_vis + (slot * P.T + k) * 3;
+        vs[0] = hi > lo ? hi - lo : 0;
+        vs[1] = hi > lo ? lo : -1;
+        vs[2] = hi > lo ? hi - 1 : -1;
+      }
+      tc_fence_before();
+      g += s.n;
+      ++kseg;
+      s = nx;
+      have = have_next;
     }
   }
+  pdl_wait();        // (a no-op for the threads that waited already)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
+  if (warp == 4) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-// One CTA per (block, row): the splits' partials of the row combined by
-// log-sum-exp in split order (empty splits, lse = -inf, skipped); a row no
-// split saw stays exactly zero.  Thread i handles value dims 4i .. 4i + 3.
-constexpr int MERGE_THREADS = 128, MAX_MERGE_SPLITS = 64;
+// Grid (block, value half): the segments' partials of each row combined by
+// log-sum-exp in CTA order (a row no segment saw stays exactly zero).
+// Thread i handles value dim 256 * half + i of all the block's rows.
+constexpr int MERGE_THREADS = 256;
 __global__ void __launch_bounds__(MERGE_THREADS) decode_merge_kernel(const __grid_constant__ DecodeParams P) {
+  extern __shared__ float w_s[];              // [segments][32] normalised weights
+  __shared__ float lse_s[NR];
+  const int b = blockIdx.x, half = blockIdx.y, tid = threadIdx.x;
   const int R = P.T * P.H;
-  const int b = blockIdx.x / R, r = blockIdx.x % R;
-  const long base = (long)b * P.splits * NR + r;          // partial row of split s: base + s * NR
-  __shared__ float w_s[MAX_MERGE_SPLITS];
-  __shared__ float den_s, mx_s;
-  if (threadIdx.x < 32) {
+  const int f = P.meta[2 * (long)b], cnt = P.meta[2 * (long)b + 1];
+  const long slot0 = (long)b + f;
+  if (tid < NR) {
+    const int r = tid;
     float mx = -INFINITY;
-    for (int s = threadIdx.x; s < P.splits; s += 32) mx = fmaxf(mx, P.part_lse[base + s * NR]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    for (int s = 0; s < cnt; ++s) mx = fmaxf(mx, P.part_lse[(slot0 + s) * NR + r]);
     float den = 0.f;
-    for (int s = threadIdx.x; s < P.splits; s += 32) {
-      const float l = P.part_lse[base + s * NR];
+    for (int s = 0; s < cnt; ++s) {
+      const float l = P.part_lse[(slot0 + s) * NR + r];
       const float w = (mx == -INFINITY || l == -INFINITY) ? 0.f : exp2f(l - mx);
-      w_s[s] = w;
+      w_s[s * NR + r] = w;
       den += w;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-    if (threadIdx.x == 0) { den_s = den; mx_s = mx; }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    for (int s = 0; s < cnt; ++s) w_s[s * NR + r] *= inv;
+    lse_s[r] = den > 0.f ? mx + log2f(den) : -INFINITY;
   }
   __syncthreads();
-  const float den = den_s;
-  const int d = 4 * threadIdx.x;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < P.splits; ++s) {
-    const float w = w_s[s];
-    if (w == 0.f) continue;
-    const float4 v = *reinterpret_cast<const float4*>(P.part + (base + s * NR) * 512 + d);
-    acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+  const int d = 256 * half + tid;
+  float acc[NR];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) acc[r] = 0.f;
+  for (int s = 0; s < cnt; ++s) {
+    const float4* src = reinterpret_cast<const float4*>(P.part + ((slot0 + s) * 512 + d) * NR);
+    const float4* w4 = reinterpret_cast<const float4*>(w_s + s * NR);
+#pragma unroll
+    for (int i = 0; i < NR / 4; ++i) {
+      const float4 v = src[i], w = w4[i];
+      acc[4 * i] = fmaf(w.x, v.x, acc[4 * i]);
+      acc[4 * i + 1] = fmaf(w.y, v.y, acc[4 * i + 1]);
+      acc[4 * i + 2] = fmaf(w.z, v.z, acc[4 * i + 2]);
+      acc[4 * i + 3] = fmaf(w.w, v.w, acc[4 * i + 3]);
+    }
   }
-  const float inv = den > 0.f ? 1.f / den : 0.f;
-  const long row = (long)b * R + r;
-  __half2 h2[2] = {__floats2half2_rn(acc.x * inv, acc.y * inv), __floats2half2_rn(acc.z * inv, acc.w * inv)};
-  *reinterpret_cast<uint2*>(P.o_lat + row * 512 + d) = *reinterpret_cast<uint2*>(h2);
-  if (threadIdx.x == 0 && P.lse) P.lse[row] = den > 0.f ? (mx_s + log2f(den)) * 0.6931471805599453f : -INFINITY;
-  // visibility statistics of the row's token (from its head-0 row)
-  if (threadIdx.x == 0 && P.vis_stats && r % P.H == 0) {
-    const int t = r / P.H;
-    int cnt = 0, first = -1, last = -1;
-    for (int s = 0; s < P.splits; ++s) {
-      const int* vs = P.part_vis + (((long)b * P.splits + s) * P.T + t) * 3;
+#pragma unroll
+  for (int r = 0; r < NR; ++r)
+    if (r < R) P.o_lat[((long)b * R + r) * 512 + d] = __float2half_rn(acc[r]);
+  if (half == 0 && tid < R && P.lse) {
+    const float l2 = lse_s[tid];
+    P.lse[(long)b * R + tid] = l2 == -INFINITY ? -INFINITY : l2 * 0.6931471805599453f;
+  }
+  // visibility statistics of each token
+  if (half == 0 && tid < P.T && P.vis_stats) {
+    int n = 0, first = -1, last = -1;
+    for (int s = 0; s < cnt; ++s) {
+      const int* vs = P.part_vis + ((slot0 + s) * P.T + tid) * 3;
       if (vs[0] > 0) {
-        first = cnt ? min(first, vs[1]) : vs[1];
+        first = n ? min(first, vs[1]) : vs[1];
         last = max(last, vs[2]);
-        cnt += vs[0];
+        n += vs[0];
       }
     }
-    const long m = (long)b * P.T + t;
-    P.vis_stats[m * 3 + 0] = cnt;
-    P.vis_stats[m * 3 + 1] = cnt ? first : -1;
-    P.vis_stats[m * 3 + 2] = cnt ? last : -1;
+    const long m = (long)b * P.T + tid;
+    P.vis_stats[m * 3 + 0] = n;
+    P.vis_stats[m * 3 + 1] = n ? first : -1;
+    P.vis_stats[m * 3 + 2] = n ? last : -1;
   }
+}
+
+// Workspace pieces: partial slots block + CTA < num_blocks + grid.
+size_t ws_layout(long num_blocks, int grid, int T, size_t* off_lse, size_t* off_vis, size_t* off_meta) {
+  const long slots = num_blocks + grid;
+  size_t o = align256((size_t)slots * NR * 512 * 4);
+  *off_lse = o;
+  o += align256((size_t)slots * NR * 4);
+  *off_vis = o;
+  o += align256((size_t)slots * T * 3 * 4);
+  *off_meta = o;
+  o += align256((size_t)num_blocks * 2 * 4);
+  return o;
 }
 
 }  // namespace
@@ -476,27 +852,14 @@ bool decode_applies(const mla_handle* h, int block_len) {
          h->cfg.page_size % KT == 0;
 }
 
-static int tiles_per_split(const mla_handle* h, const mla_attn_desc_t& d) {
-  const int max_tiles = (d.max_pages * h->cfg.page_size + KT - 1) / KT;
-  // about four CTAs per SM over the launch, each on a short key range
-  const long units = (long)d.num_blocks * max_tiles;
-  const long target = 4L * h->num_sms;
-  long tps = (units + target - 1) / target;
-  if (tps < 1) tps = 1;
-  if (tps > max_tiles) tps = max_tiles;
-  // the merge holds at most MAX_MERGE_SPLITS splits of a block
-  const long min_tps = (max_tiles + MAX_MERGE_SPLITS - 1) / MAX_MERGE_SPLITS;
-  if (tps < min_tps) tps = min_tps;
-  return (int)tps;
+size_t decode_workspace_bytes(const mla_handle* h, const mla_attn_desc_t& d) {
+  size_t a, b, c;
+  return ws_layout(d.num_blocks, h->num_sms, d.block_len, &a, &b, &c);
 }
 
-size_t decode_workspace_bytes(const mla_handle* h, const mla_attn_desc_t& d) {
-  const int max_tiles = (d.max_pages * h->cfg.page_size + KT - 1) / KT;
-  const int tps = tiles_per_split(h, d);
-  const long splits = (max_tiles + tps - 1) / tps;
-  const long parts = (long)d.num_blocks * splits;
-  return align256(parts * NR * 512 * 4) + align256(parts * NR * 4) +
-         align256(parts * d.block_len * 3 * 4);
+size_t decode_workspace_bound(const mla_handle* h, long max_blocks, int max_block_len) {
+  size_t a, b, c;
+  return ws_layout(max_blocks, h->num_sms, max_block_len, &a, &b, &c);
 }
 
 mla_status_t latent_decode(cudaStream_t st, const mla_handle* h, const __nv_bfloat16* q_abs,
@@ -507,24 +870,23 @@ mla_status_t latent_decode(cudaStream_t st, const mla_handle* h, const __nv_bflo
   if (!decode_applies(h, d.block_len))
     return fail(MLA_ERR_UNSUPPORTED, "decode attention: needs block_len * num_heads <= 32, page_size a multiple of 128");
   if (d.num_blocks <= 0) return MLA_OK;
-  if (workspace_bytes < decode_workspace_bytes(h, d) || (uintptr_t)workspace % 256)
+  size_t off_lse, off_vis, off_meta;
+  const int G = h->num_sms;
+  const size_t need = ws_layout(d.num_blocks, G, d.block_len, &off_lse, &off_vis, &off_meta);
+  if (workspace_bytes < need || (uintptr_t)workspace % 256)
     return fail(MLA_ERR_INVALID_ARG, "decode attention: workspace too small or not 256-byte aligned");
   DecodeParams P;
   const long rows = (long)d.num_blocks * d.block_len * l.H;
   const long slots = (long)num_pages * h->cfg.page_size;
   if (!make_tmap_chunked(&P.tmQ, false, q_abs, rows, l.L, l.L, NR, NCH) ||
       !make_tmap_2d(&P.tmK1, false, cache, slots, l.L, l.L, KT) ||
-      !make_tmap_chunked(&P.tmK2, false, cache, slots, l.L, l.L, KT, 2) ||
-      !make_tmap_chunked(&P.tmK4, false, cache, slots, l.L, l.L, KT, 4))
+      !make_tmap_chunked(&P.tmK2, false, cache, slots, l.L, l.L, KT, 2))
     return fail(MLA_ERR_CUDA, "decode attention: cuTensorMapEncodeTiled failed");
-  const int max_tiles = (d.max_pages * h->cfg.page_size + KT - 1) / KT;
-  P.tiles_per_split = tiles_per_split(h, d);
-  P.splits = (max_tiles + P.tiles_per_split - 1) / P.tiles_per_split;
-  const long parts = (long)d.num_blocks * P.splits;
   char* ws = (char*)workspace;
   P.part = (float*)ws;
-  P.part_lse = (float*)(ws + align256(parts * NR * 512 * 4));
-  P.part_vis = (int*)(ws + align256(parts * NR * 512 * 4) + align256(parts * NR * 4));
+  P.part_lse = (float*)(ws + off_lse);
+  P.part_vis = (int*)(ws + off_vis);
+  P.meta = (int*)(ws + off_meta);
   P.block_table = d.block_table;
   P.kv_len = d.kv_len;
   P.window = d.window;
@@ -534,6 +896,7 @@ mla_status_t latent_decode(cudaStream_t st, const mla_handle* h, const __nv_bflo
   P.o_lat = o_lat;
   P.lse = lse;
   P.status = h->status;
+  P.num_blocks = d.num_blocks;
   P.max_pages = d.max_pages;
   P.num_pages = num_pages;
   P.page_size = h->cfg.page_size;
@@ -544,10 +907,10 @@ mla_status_t latent_decode(cudaStream_t st, const mla_handle* h, const __nv_bflo
   std::call_once(once, [] {
     cudaFuncSetAttribute(latent_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   });
-  Launch L(dim3((unsigned)parts), dim3(THREADS), SMEM_BYTES, st, pdl);
+  Launch L(dim3((unsigned)G), dim3(THREADS), SMEM_BYTES, st, pdl);
   cudaError_t e = cudaLaunchKernelEx(&L.cfg, latent_decode_tc_kernel, P);
   if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
-  decode_merge_kernel<<<d.num_blocks * d.block_len * l.H, MERGE_THREADS, 0, st>>>(P);
+  decode_merge_kernel<<<dim3((unsigned)d.num_blocks, 2), MERGE_THREADS, (size_t)G * NR * 4, st>>>(P);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "decode merge launch");
   return MLA_OK;
