@@ -444,6 +444,7 @@ __global__ void __launch_bounds__(THREADS, 1) latent_decode_tc_kernel(const __gr
       const int ps = P.page_size, past_end = P.num_pages * ps;
       prefetch_tmap(&P.tmK1);
       prefetch_tmap(&P.tmK2);
+      const uint64_t evict_first = l2_policy_evict_first();
       SegIter it{b_first, t_first, ntiles};
       Seg s;
       uint32_t item = 0;
@@ -457,9 +458,13 @@ __global__ void __launch_bounds__(THREADS, 1) latent_decode_tc_kernel(const __gr
           if (!value && q == 4) {
             mbar_arrive_expect_tx(&B->full[slot], KV_CH_BYTES);
             tma_load_3d(dst, &P.tmK1, &B->full[slot], 8 * DCH, y0, 0);
-          } else {
+          } else if (!value) {
             mbar_arrive_expect_tx(&B->full[slot], SLOT_BYTES);
             tma_load_3d(dst, &P.tmK2, &B->full[slot], 0, y0, 2 * q);
+          } else {
+            // the value pass is the last touch of these lines: first out of L2
+            mbar_arrive_expect_tx(&B->full[slot], SLOT_BYTES);
+            tma_load_3d_hint(dst, &P.tmK2, &B->full[slot], 0, y0, 2 * q, evict_first);
           }
           last_use = (last_use & ~(0x101u << slot)) | (1u << slot) | (ph << (8 + slot));
         }
@@ -563,48 +568,57 @@ __global__ void __launch_bounds__(THREADS, 1) latent_decode_tc_kernel(const __gr
     float* il_s = red + RD_INVL;
     int* rlo = redi + RD_LO;
     int* rhi = redi + RD_HI;
-    pdl_wait();
-    if (c == 0) {
-      // each block's segments for the merge (first CTA, count); invalid
-      // lengths and windows reported once
-      long long run = 0;
-      for (int base = 0; base < nb; base += 128) {
-        const int b = base + k;
-        BlockKeys bk{};
-        if (b < nb) {
-          bk = block_keys(P, b);
-          if (bk.bad_len) set_status(P.status, MLA_DEV_BAD_LENGTH);
-          if (bk.bad_win) set_status(P.status, MLA_DEV_BAD_WINDOW);
-        }
-        int x = bk.nt;
+    // Before their first global write these warps wait for the previous
+    // kernel (the workspace may still be read by it); the first CTA then
+    // records each block's segment range for the merge.
+    bool waited = false;
+    auto first_write = [&]() {
+      if (waited) return;
+      waited = true;
+      pdl_wait();
+      if (c == 0) {
+        // each block's segments for the merge (first CTA, count); invalid
+        // lengths and windows reported once
+        long long run = 0;
+        for (int base = 0; base < nb; base += 128) {
+          const int b = base + k;
+          BlockKeys bk{};
+          if (b < nb) {
+            bk = block_keys(P, b);
+            if (bk.bad_len) set_status(P.status, MLA_DEV_BAD_LENGTH);
+            if (bk.bad_win) set_status(P.status, MLA_DEV_BAD_WINDOW);
+          }
+          int x = bk.nt;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, x, o);
-          if (lane >= o) x += y;
-        }
-        if (lane == 31) redi[RD_WPART + warp] = x;
-        softmax_sync();
-        int wb = 0, tot = 0;
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+          }
+          if (lane == 31) redi[RD_WPART + warp] = x;
+          softmax_sync();
+          int wb = 0, tot = 0;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const int sv = redi[RD_WPART + w];
-          wb += w < warp ? sv : 0;
-          tot += sv;
+          for (int w = 0; w < 4; ++w) {
+            const int sv = redi[RD_WPART + w];
+            wb += w < warp ? sv : 0;
+            tot += sv;
+          }
+          softmax_sync();
+          const long long excl = run + wb + x - bk.nt;
+          if (b < nb) {
+            const int f = bk.nt ? cta_of(excl, U, G) : 0;
+            const int l = bk.nt ? cta_of(excl + bk.nt - 1, U, G) : -1;
+            P.meta[2 * (long)b] = f;
+            P.meta[2 * (long)b + 1] = l - f + 1;
+          }
+          run += tot;
         }
-        softmax_sync();
-        const long long excl = run + wb + x - bk.nt;
-        if (b < nb) {
-          const int f = bk.nt ? cta_of(excl, U, G) : 0;
-          const int l = bk.nt ? cta_of(excl + bk.nt - 1, U, G) : -1;
-          P.meta[2 * (long)b] = f;
-          P.meta[2 * (long)b + 1] = l - f + 1;
-        }
-        run += tot;
       }
-    }
+    };
     SegIter it{b_first, t_first, ntiles};
     Seg s, nx;
     uint32_t g = 0, kseg = 0;
+    long long u_seg = u0;                     // global index of the segment's first tile
     bool have = next_seg(P, it, s);
     while (have) {
       const bool have_next = next_seg(P, it, nx);
@@ -625,7 +639,6 @@ __global__ void __launch_bounds__(THREADS, 1) latent_decode_tc_kernel(const __gr
         }
         rlo[k] = lo;
         rhi[k] = hi;
-        m_s[k] = -INFINITY;
       }
       softmax_sync();
       float lrow[NR];
@@ -657,7 +670,7 @@ __global__ void __launch_bounds__(THREADS, 1) latent_decode_tc_kernel(const __gr
         if (warp == 0) {
           // row `lane`: running max (exp2 domain) and the factor for what is accumulated
           const float cm = fmaxf(fmaxf(wpart[lane], wpart[32 + lane]), fmaxf(wpart[64 + lane], wpart[96 + lane]));
-          const float tm = cm * P.scale_log2, m_old = m_s[lane];
+          const float tm = cm * P.scale_log2, m_old = t == 0 ? -INFINITY : m_s[lane];
           const bool grow = tm > m_old + RESCALE_LOG2;
           const float m_new = grow ? tm : m_old;
           const float alpha = (grow && m_old != -INFINITY) ? exp2f(m_old - m_new) : 1.f;
@@ -667,14 +680,6 @@ __global__ void __launch_bounds__(THREADS, 1) latent_decode_tc_kernel(const __gr
           if (lane == 0) redi[RD_FLAG] = any;
         }
         softmax_sync();
-        float mref[NR], alpha[NR];
-#pragma unroll
-        for (int r = 0; r < NR; r += 4) {
-          const float4 mv = *reinterpret_cast<const float4*>(m_s + r);
-          const float4 av = *reinterpret_cast<const float4*>(al_s + r);
-          mref[r] = mv.x; mref[r + 1] = mv.y; mref[r + 2] = mv.z; mref[r + 3] = mv.w;
-          alpha[r] = av.x; alpha[r + 1] = av.y; alpha[r + 2] = av.z; alpha[r + 3] = av.w;
-        }
         const bool rescale = redi[RD_FLAG] != 0;
         // O^T(gg - 1) is issued after S^T(gg) (and O^T(gg) only after this
         // tile's P): a row that grew waits for it, then rescales
@@ -688,27 +693,43 @@ __global__ void __launch_bounds__(THREADS, 1) latent_decode_tc_kernel(const __gr
             tmem_ld_wait();
             tmem_reg_fence32(o);
 #pragma unroll
-            for (int r = 0; r < NR; ++r) o[r] *= alpha[r];
+            for (int r = 0; r < NR; r += 4) {
+              const float4 av = *reinterpret_cast<const float4*>(al_s + r);
+              o[r] *= av.x; o[r + 1] *= av.y; o[r + 2] *= av.z; o[r + 3] *= av.w;
+            }
             tmem_st32(ob + 32 * q + lane_base, o);
           }
         }
         // P[r][k] (bf16) into the swizzled K-major tile: 16-byte unit (k % 64) / 8
-        // of row r sits at unit ((k % 64) / 8) ^ (r % 8)
+        // of row r sits at unit ((k % 64) / 8) ^ (r % 8); each row's max and
+        // factor read four rows at a time (short live ranges)
         uint8_t* pchunk = smem + OFF_P + (gg & 1) * P_BYTES + (k / 64) * P_CH_BYTES;
         const int kk = k % 64;
 #pragma unroll
-        for (int r = 0; r < NR; ++r) {
-          const float m0 = mref[r] == -INFINITY ? 0.f : mref[r];
-          const float p = fast_exp2(fmaf(sv[r], P.scale_log2, -m0));
-          lrow[r] = fmaf(lrow[r], alpha[r], p);
-          *reinterpret_cast<__nv_bfloat16*>(pchunk + r * 128 + (((kk >> 3) ^ (r & 7)) << 4) + (kk & 7) * 2) =
-              __float2bfloat16_rn(p);
+        for (int r4 = 0; r4 < NR; r4 += 4) {
+          const float4 mv = *reinterpret_cast<const float4*>(m_s + r4);
+          const float4 av = *reinterpret_cast<const float4*>(al_s + r4);
+          const float mr[4] = {mv.x, mv.y, mv.z, mv.w}, ar[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = r4 + i;
+            const float m0 = mr[i] == -INFINITY ? 0.f : mr[i];
+            const float p = fast_exp2(fmaf(sv[r], P.scale_log2, -m0));
+            lrow[r] = fmaf(lrow[r], ar[i], p);
+            *reinterpret_cast<__nv_bfloat16*>(pchunk + r * 128 + (((kk >> 3) ^ (r & 7)) << 4) + (kk & 7) * 2) =
+                __float2bfloat16_rn(p);
+          }
         }
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&B->p_full[gg & 1]);
       }
-      // ---- epilogue of the segment: row sums, normalised partial, lse, visibility
+      // ---- epilogue of the segment: row sums, then either the block's final
+      // output (the block lies in this CTA alone) or a normalised partial
+      first_write();
+      const long long S_b = u_seg - s.t0;                     // the block's first tile, global order
+      const int fb = cta_of(S_b, U, G), nseg = cta_of(S_b + s.k.nt - 1, U, G) - fb + 1;
+      const bool direct = nseg == 1;
       float x[NR];
 #pragma unroll
       for (int r = 0; r < NR; ++r) x[r] = lrow[r];
@@ -717,7 +738,11 @@ __global__ void __launch_bounds__(THREADS, 1) latent_decode_tc_kernel(const __gr
       if (warp == 0) {
         const float l = (wpart[lane] + wpart[32 + lane]) + (wpart[64 + lane] + wpart[96 + lane]);
         il_s[lane] = l > 0.f ? 1.f / l : 0.f;
-        P.part_lse[slot * NR + lane] = l > 0.f ? m_s[lane] + log2f(l) : -INFINITY;
+        const float l2 = l > 0.f ? m_s[lane] + log2f(l) : -INFINITY;
+        if (!direct)
+          P.part_lse[slot * NR + lane] = l2;
+        else if (P.lse && lane < R)
+          P.lse[(long)b * R + lane] = l2 == -INFINITY ? -INFINITY : l2 * 0.6931471805599453f;
       }
       softmax_sync();
       float il[NR];
@@ -728,32 +753,46 @@ __global__ void __launch_bounds__(THREADS, 1) latent_decode_tc_kernel(const __gr
       }
       wait_bar(B, &B->o_seg, kseg & 1, P.status);
       tc_fence_after();
-      // thread k holds value dim 128 q + k of every row: one 128-byte row of
-      // the [dim][row] partial
+      // thread k holds value dim 128 q + k of every row (a row nothing was
+      // visible to stays +0)
 #pragma unroll 1
       for (int q = 0; q < 4; ++q) {
         float o[NR];
         tmem_ld32_nowait(ob + 32 * q + lane_base, o);
         tmem_ld_wait();
         tmem_reg_fence32(o);
-        float4* dst = reinterpret_cast<float4*>(P.part + (slot * 512 + 128 * q + k) * NR);
 #pragma unroll
-        for (int r = 0; r < NR; r += 4)
-          dst[r / 4] = make_float4(o[r] * il[r], o[r + 1] * il[r + 1], o[r + 2] * il[r + 2], o[r + 3] * il[r + 3]);
+        for (int r = 0; r < NR; ++r) o[r] = il[r] > 0.f ? o[r] * il[r] : 0.f;
+        if (direct) {
+#pragma unroll
+          for (int r = 0; r < NR; ++r)
+            if (r < R) P.o_lat[((long)b * R + r) * 512 + 128 * q + k] = __float2half_rn(o[r]);
+        } else {
+          // kept in L2 for the merge (the cache stream would push them out)
+          float4* dst = reinterpret_cast<float4*>(P.part + (slot * 512 + 128 * q + k) * NR);
+          const uint64_t keep = l2_policy_evict_last();
+#pragma unroll
+          for (int r = 0; r < NR; r += 4) st_global_hint(dst + r / 4, make_float4(o[r], o[r + 1], o[r + 2], o[r + 3]), keep);
+        }
       }
       if (k < P.T) {   // visibility of token k over this segment's keys (one interval)
         const int lo = max(rlo[k * P.H], k_begin), hi = min(rhi[k * P.H], k_end);
-        int* vs = P.part_vis + (slot * P.T + k) * 3;
-        vs[0] = hi > lo ? hi - lo : 0;
-        vs[1] = hi > lo ? lo : -1;
-        vs[2] = hi > lo ? hi - 1 : -1;
+        int* vs = direct ? (P.vis_stats ? P.vis_stats + ((long)b * P.T + k) * 3 : nullptr)
+                         : P.part_vis + (slot * P.T + k) * 3;
+        if (vs) {
+          vs[0] = hi > lo ? hi - lo : 0;
+          vs[1] = hi > lo ? lo : -1;
+          vs[2] = hi > lo ? hi - 1 : -1;
+        }
       }
+      u_seg += s.n;
       tc_fence_before();
       g += s.n;
       ++kseg;
       s = nx;
       have = have_next;
     }
+    first_write();
   }
   pdl_wait();        // (a no-op for the threads that waited already)
   __syncwarp();
@@ -763,61 +802,90 @@ __global__ void __launch_bounds__(THREADS, 1) latent_decode_tc_kernel(const __gr
   if (warp == 4) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-// Grid (block, value half): the segments' partials of each row combined by
-// log-sum-exp in CTA order (a row no segment saw stays exactly zero).
-// Thread i handles value dim 256 * half + i of all the block's rows.
-constexpr int MERGE_THREADS = 256;
-__global__ void __launch_bounds__(MERGE_THREADS) decode_merge_kernel(const __grid_constant__ DecodeParams P) {
-  extern __shared__ float w_s[];              // [segments][32] normalised weights
+// Grid (block, quarter of the value dims): the segments' partials of each
+// row combined by log-sum-exp in CTA order; a row no segment saw stays
+// exactly zero, a block with no keys is all zero, a block held by one CTA
+// was written directly by it.  Thread i handles value dim 128 * quarter +
+// i % 128 of rows 16 (i / 128) .. + 15 and keeps up to MERGE_LOADS
+// segments' rows in flight (the partials may have left L2: the attention
+// kernel streamed the cache through it after writing them); eight threads
+// derive the weights of each row.
+constexpr int MERGE_THREADS = 256, MERGE_SPLIT = 4, MERGE_LOADS = 4;
+constexpr int MERGE_SMEM_MAX = 200 * (NR + 3 * NR) * 4;   // up to 200 segments of 32 one-token blocks
+__global__ void __launch_bounds__(MERGE_THREADS, 2) decode_merge_kernel(const __grid_constant__ DecodeParams P) {
+  extern __shared__ float w_s[];              // [segments][32] log2-sum-exps then weights; [segments][T][3] visibility
   __shared__ float lse_s[NR];
-  const int b = blockIdx.x, half = blockIdx.y, tid = threadIdx.x;
+  const int b = blockIdx.x, part = blockIdx.y, tid = threadIdx.x;
   const int R = P.T * P.H;
   const int f = P.meta[2 * (long)b], cnt = P.meta[2 * (long)b + 1];
+  if (cnt == 1) return;
   const long slot0 = (long)b + f;
-  if (tid < NR) {
-    const int r = tid;
+  const bool lead = part == 0;
+  int* vis_s = reinterpret_cast<int*>(w_s + cnt * NR);
+  for (int i = tid; i < cnt * NR; i += MERGE_THREADS) w_s[i] = P.part_lse[slot0 * NR + i];
+  if (lead && P.vis_stats)
+    for (int i = tid; i < cnt * P.T * 3; i += MERGE_THREADS) vis_s[i] = P.part_vis[slot0 * P.T * 3 + i];
+  __syncthreads();
+  {
+    // row tid / 8, segments tid % 8 + 8 j
+    const int r = tid / 8, sl = tid % 8;
     float mx = -INFINITY;
-    for (int s = 0; s < cnt; ++s) mx = fmaxf(mx, P.part_lse[(slot0 + s) * NR + r]);
+    for (int s = sl; s < cnt; s += 8) mx = fmaxf(mx, w_s[s * NR + r]);
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     float den = 0.f;
-    for (int s = 0; s < cnt; ++s) {
-      const float l = P.part_lse[(slot0 + s) * NR + r];
+    for (int s = sl; s < cnt; s += 8) {
+      const float l = w_s[s * NR + r];
       const float w = (mx == -INFINITY || l == -INFINITY) ? 0.f : exp2f(l - mx);
       w_s[s * NR + r] = w;
       den += w;
     }
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     const float inv = den > 0.f ? 1.f / den : 0.f;
-    for (int s = 0; s < cnt; ++s) w_s[s * NR + r] *= inv;
-    lse_s[r] = den > 0.f ? mx + log2f(den) : -INFINITY;
+    for (int s = sl; s < cnt; s += 8) w_s[s * NR + r] *= inv;
+    if (sl == 0) lse_s[r] = den > 0.f ? mx + log2f(den) : -INFINITY;
   }
   __syncthreads();
-  const int d = 256 * half + tid;
-  float acc[NR];
+  const int d = 128 * part + tid % 128, r0 = 16 * (tid / 128);
+  float acc[16];
 #pragma unroll
-  for (int r = 0; r < NR; ++r) acc[r] = 0.f;
-  for (int s = 0; s < cnt; ++s) {
-    const float4* src = reinterpret_cast<const float4*>(P.part + ((slot0 + s) * 512 + d) * NR);
-    const float4* w4 = reinterpret_cast<const float4*>(w_s + s * NR);
+  for (int r = 0; r < 16; ++r) acc[r] = 0.f;
+  for (int s0 = 0; s0 < cnt; s0 += MERGE_LOADS) {
+    float4 v[MERGE_LOADS][4];
 #pragma unroll
-    for (int i = 0; i < NR / 4; ++i) {
-      const float4 v = src[i], w = w4[i];
-      acc[4 * i] = fmaf(w.x, v.x, acc[4 * i]);
-      acc[4 * i + 1] = fmaf(w.y, v.y, acc[4 * i + 1]);
-      acc[4 * i + 2] = fmaf(w.z, v.z, acc[4 * i + 2]);
-      acc[4 * i + 3] = fmaf(w.w, v.w, acc[4 * i + 3]);
-    }
+    for (int j = 0; j < MERGE_LOADS; ++j)
+      if (s0 + j < cnt) {
+        const float4* src = reinterpret_cast<const float4*>(P.part + ((slot0 + s0 + j) * 512 + d) * NR + r0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[j][i] = src[i];
+      }
+#pragma unroll
+    for (int j = 0; j < MERGE_LOADS; ++j)
+      if (s0 + j < cnt) {
+        const float4* w4 = reinterpret_cast<const float4*>(w_s + (s0 + j) * NR + r0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 w = w4[i];
+          acc[4 * i] = fmaf(w.x, v[j][i].x, acc[4 * i]);
+          acc[4 * i + 1] = fmaf(w.y, v[j][i].y, acc[4 * i + 1]);
+          acc[4 * i + 2] = fmaf(w.z, v[j][i].z, acc[4 * i + 2]);
+          acc[4 * i + 3] = fmaf(w.w, v[j][i].w, acc[4 * i + 3]);
+        }
+      }
   }
 #pragma unroll
-  for (int r = 0; r < NR; ++r)
-    if (r < R) P.o_lat[((long)b * R + r) * 512 + d] = __float2half_rn(acc[r]);
-  if (half == 0 && tid < R && P.lse) {
+  for (int r = 0; r < 16; ++r)
+    if (r0 + r < R) P.o_lat[((long)b * R + r0 + r) * 512 + d] = __float2half_rn(acc[r]);
+  if (lead && tid < R && P.lse) {
     const float l2 = lse_s[tid];
     P.lse[(long)b * R + tid] = l2 == -INFINITY ? -INFINITY : l2 * 0.6931471805599453f;
   }
   // visibility statistics of each token
-  if (half == 0 && tid < P.T && P.vis_stats) {
+  if (lead && tid < P.T && P.vis_stats) {
     int n = 0, first = -1, last = -1;
     for (int s = 0; s < cnt; ++s) {
-      const int* vs = P.part_vis + ((slot0 + s) * P.T + tid) * 3;
+      const int* vs = vis_s + (s * P.T + tid) * 3;
       if (vs[0] > 0) {
         first = n ? min(first, vs[1]) : vs[1];
         last = max(last, vs[2]);
@@ -872,6 +940,8 @@ mla_status_t latent_decode(cudaStream_t st, const mla_handle* h, const __nv_bflo
   if (d.num_blocks <= 0) return MLA_OK;
   size_t off_lse, off_vis, off_meta;
   const int G = h->num_sms;
+  if ((size_t)G * (NR + 3 * d.block_len) * 4 > (size_t)MERGE_SMEM_MAX)
+    return fail(MLA_ERR_UNSUPPORTED, "decode attention: more than 200 SMs");
   const size_t need = ws_layout(d.num_blocks, G, d.block_len, &off_lse, &off_vis, &off_meta);
   if (workspace_bytes < need || (uintptr_t)workspace % 256)
     return fail(MLA_ERR_INVALID_ARG, "decode attention: workspace too small or not 256-byte aligned");
@@ -906,11 +976,14 @@ mla_status_t latent_decode(cudaStream_t st, const mla_handle* h, const __nv_bflo
   static std::once_flag once;
   std::call_once(once, [] {
     cudaFuncSetAttribute(latent_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaFuncSetAttribute(decode_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MERGE_SMEM_MAX);
   });
   Launch L(dim3((unsigned)G), dim3(THREADS), SMEM_BYTES, st, pdl);
   cudaError_t e = cudaLaunchKernelEx(&L.cfg, latent_decode_tc_kernel, P);
   if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
-  decode_merge_kernel<<<dim3((unsigned)d.num_blocks, 2), MERGE_THREADS, (size_t)G * NR * 4, st>>>(P);
+  // (a programmatic launch of the merge measured slower: it stays a plain one)
+  const size_t merge_smem = (size_t)G * (NR + 3 * d.block_len) * 4;
+  decode_merge_kernel<<<dim3((unsigned)d.num_blocks, MERGE_SPLIT), MERGE_THREADS, merge_smem, st>>>(P);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "decode merge launch");
   return MLA_OK;

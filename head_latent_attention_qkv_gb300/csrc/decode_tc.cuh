@@ -40,7 +40,7 @@ size_t decode_workspace_bytes(const mla_handle* h, const mla_attn_desc_t& desc);
 // max_block_len tokens.
 size_t decode_workspace_bound(const mla_handle* h, long max_blocks, int max_block_len);
 // Latent attention of desc's blocks through the few-row kernel and the
-// split merge; same results as latent_attention() (o_lat, optional lse,
+// segment merge; same results as latent_attention() (o_lat, optional lse,
 // vis_stats).  MLA_ERR_UNSUPPORTED when decode_applies() is false.
 mla_status_t latent_decode(cudaStream_t st, const mla_handle* h, const __nv_bfloat16* q_abs,
                            const __nv_bfloat16* cache, int num_pages, const mla_attn_desc_t& desc,
