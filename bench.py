@@ -87,6 +87,26 @@ def algorithmic_flops(wl):
                 cache_bytes=cache_bytes, attention=attention)
 
 
+def attention_cache_bytes(wl):
+    """Cache bytes the last step's attention reads: 1152 per key a block can
+    see, once per block (from the first key any of its rows sees)."""
+    step, L = wl.steps[-1], wl.dims.cache_dim
+    total = 0
+    for b in range(len(step.kv_len)):
+        r = slice(b * wl.block_len, (b + 1) * wl.block_len)
+        w, kv = int(step.window[b]), int(step.kv_len[b])
+        lo = max(0, int(step.block_positions[r].min()) - w + 1) if w > 0 else 0
+        total += (kv - lo) * L * 2
+    return total
+
+
+def few_row_attention(wl):
+    """The library serves blocks of at most 32 query rows (bf16, 128-token
+    pages) with the few-row kernel and its segment merge."""
+    return (wl.dims.dtype == "bf16" and wl.block_len * wl.dims.num_heads <= 32
+            and wl.page_size % 128 == 0)
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons, sampled every 20 ms by a
     background nvidia-smi while the GPU runs the warm-up, the timed steps and
@@ -309,7 +329,8 @@ def run_ours(args, rank, world):
     if S.dev.ctx is not None:
         kernels["append"] = dict(ms=timed(run_a, args.steps, flush, stream), flops=S.fl["append"])
     kernels["attention"] = dict(ms=timed(run_t, args.steps, flush, stream),
-                                flops=S.fl["attention"][-1])
+                                flops=S.fl["attention"][-1], bytes=attention_cache_bytes(S.wl),
+                                few_row=few_row_attention(S.wl))
     hold_load(2)
     clocks.__exit__(None, None, None)
     ms = max_over_ranks(ms, world)
@@ -339,14 +360,7 @@ def decode_line(name, args, flush, stream):
     ms = timed(g.replay, n, flush, stream)
     ms_att = timed(ga.replay, n, flush, stream)
     fl = S.fl
-    step = S.wl.steps[-1]
-    L = S.wl.dims.cache_dim
-    att_bytes = 0
-    for b in range(len(step.kv_len)):           # the last attention's cache bytes
-        r = slice(b * S.wl.block_len, (b + 1) * S.wl.block_len)
-        w, kv = int(step.window[b]), int(step.kv_len[b])
-        lo = max(0, int(step.block_positions[r].min()) - w + 1) if w > 0 else 0
-        att_bytes += (kv - lo) * L * 2
+    att_bytes = attention_cache_bytes(S.wl)
     assert S.api.mla_get_device_status(S.dev.handle) == 0
     out = {"workload": name, "shape": DESC[name], "ms_per_step": ms,
            "block_tokens_per_s": fl["block_tokens"] / (ms * 1e-3),
@@ -498,16 +512,28 @@ def main():
     ach = k["flops"] / (k["ms"] * 1e-3) / 1e12
     line = base_line(args, world)
     e2e_s, h2d, d2h = r["e2e"]
-    roofline = {"kernel": names[dom], "bound": "tensor", "achieved": ach, "peak": bf16,
-                "unit": "TFLOP/s", "frac": ach / bf16,
-                "traffic": dram_traffic(dom, args.workload),
-                "launch_ms": k["ms"], "algorithmic_flops_per_launch": k["flops"],
-                "share_of_step": k["ms"] / r["ms"],
-                "peak_source": f"{src} bf16 burst (sustained {bf16_sus}: frac "
-                               f"{ach / bf16_sus if bf16_sus else None})"}
+    if dom == "attention" and k.get("few_row"):
+        # few query rows per block: the cache stream bounds it (60 flop per cache byte at 32 rows)
+        gbs = k["bytes"] / (k["ms"] * 1e-3) / 1e9
+        roofline = {"kernel": "latent_decode_tc_kernel + decode_merge_kernel: few-row latent attention "
+                              "(keys in the MMA's M, 32 rows in N) and its segment merge, the last step's blocks",
+                    "bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                    "traffic": dram_traffic("decode", args.workload),
+                    "launch_ms": k["ms"], "algorithmic_bytes_per_launch": k["bytes"],
+                    "share_of_step": k["ms"] / r["ms"],
+                    "peak_source": f"{src} HBM copy rate; traffic is the attention kernel's, the merge adds "
+                                   f"its fp32 partials"}
+    else:
+        roofline = {"kernel": names[dom], "bound": "tensor", "achieved": ach, "peak": bf16,
+                    "unit": "TFLOP/s", "frac": ach / bf16,
+                    "traffic": dram_traffic(dom, args.workload),
+                    "launch_ms": k["ms"], "algorithmic_flops_per_launch": k["flops"],
+                    "share_of_step": k["ms"] / r["ms"],
+                    "peak_source": f"{src} bf16 burst (sustained {bf16_sus}: frac "
+                                   f"{ach / bf16_sus if bf16_sus else None})"}
     others = {n: {"launch_ms": v["ms"], "tflops": v["flops"] / (v["ms"] * 1e-3) / 1e12,
                   "frac": v["flops"] / (v["ms"] * 1e-3) / 1e12 / bf16,
-                  "traffic": dram_traffic(n, args.workload)}
+                  "traffic": dram_traffic("decode" if v.get("few_row") else n, args.workload)}
               for n, v in r["kernels"].items() if n != dom}
     line.update({
         "value": value, "ms_per_step": r["ms"], "dtype": "bf16",
