@@ -336,7 +336,8 @@ namespace {
 template <typename TA, typename TC>
 mla_status_t proj(mla_handle_t* h, cudaStream_t st, bool pdl, int M, int N, int K, int batch,
                   const TA* A, long lda, long sA, const TA* B, long ldb, long sB, TC* C, long ldc,
-                  long sC, const float* G = nullptr, long ldg = 0, long sG = 0) {
+                  long sC, const float* G = nullptr, long ldg = 0, long sG = 0, bool gate_act = false,
+                  int sig_from = -1) {
   h->launches += (M > 0 && N > 0 && batch > 0);
   if constexpr (std::is_same<TA, float>::value) {
     simt::gemm_nt<TA, TC>(st, M, N, K, batch, A, lda, sA, B, ldb, sB, C, ldc, sC, G, ldg, sG);
@@ -345,7 +346,7 @@ mla_status_t proj(mla_handle_t* h, cudaStream_t st, bool pdl, int M, int N, int 
     tc::Out o = std::is_same<TC, float>::value ? tc::Out::F32
                 : std::is_same<TC, __half>::value ? tc::Out::F16 : tc::Out::BF16;
     tc::GemmArgs a{M, N, K, batch, std::is_same<TA, __half>::value, A, lda, sA, B, ldb, sB,
-                   C, ldc, sC, o, G, ldg, sG, pdl};
+                   C, ldc, sC, o, G, ldg, sG, pdl, gate_act, sig_from};
     return tc::gemm(st, a, h->status);
   }
 }
@@ -438,8 +439,10 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
   // device before it reads anything but the weights; a first kernel behind a
   // copy or an event wait starts as a plain launch
   constexpr bool pdl = kBf16;
+  // (tensor-core layers: the gate columns leave this GEMM as sigmoid(x W_gate^T))
   mla_status_t s = proj<TX, float>(h, st, pdl, M, l.NA - r0, l.D, 1, x, l.D, 0,
-                                   WA + (long)r0 * l.D, l.D, 0, a_out + r0, l.NA, 0);
+                                   WA + (long)r0 * l.D, l.D, 0, a_out + r0, l.NA, 0, nullptr, 0, 0,
+                                   false, l.gdim ? l.L + l.qdim - r0 : -1);
   if (s != MLA_OK) return s;
   if (bslots) {
     if (fused_kv) {
@@ -492,12 +495,13 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
                              pdl && !kv_ready);
     if (s != MLA_OK) return s;
   }
-  // o[h] = o_lat[h] @ W_UV[h]^T (* sigmoid(gate))
+  // o[h] = o_lat[h] @ W_UV[h]^T (* sigmoid(gate): computed by the A projection on
+  // tensor-core layers, by this GEMM's epilogue on the fp32 layer)
   TI* o = (TI*)(ws + w.o);
   const float* gate = l.gdim ? a_out + l.L + l.qdim : nullptr;
   s = proj<TI, TI>(h, st, pdl, M, l.dv, l.rkv, l.H, o_lat, (long)l.H * l.rkv, l.rkv,
                    (const TI*)h->WUV, l.rkv, (long)l.dv * l.rkv, o, (long)l.H * l.dv, l.dv, gate,
-                   l.NA, l.dv);
+                   l.NA, l.dv, kBf16);
   if (s != MLA_OK) return s;
   s = proj<TI, TX>(h, st, pdl, M, l.D, l.H * l.dv, 1, o, (long)l.H * l.dv, 0, (const TI*)h->Wo,
                    (long)l.H * l.dv, 0, (TX*)out, l.D, 0);

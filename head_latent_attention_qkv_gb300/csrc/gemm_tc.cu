@@ -110,8 +110,8 @@ template <int BN, typename TC>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                int M, int N, int K, TC* __restrict__ C, long ldc, long sC,
-               const float* __restrict__ G, long ldg, long sG, uint32_t idesc, int splitk,
-               int group_m, uint32_t* status) {
+               const float* __restrict__ G, long ldg, long sG, bool gate_act, int sig_from,
+               uint32_t idesc, int splitk, int group_m, uint32_t* status) {
   using S = Smem<BN>;
   constexpr int KBS = S::KBS, STAGES = S::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -309,7 +309,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const float* g = G + z * sG + (long)row * ldg + n;
 #pragma unroll
         for (int i = 0; i < VALS; ++i)
-          if (n + i < N) o[i] = o[i] / (1.f + expf(-g[i]));
+          if (n + i < N) o[i] = gate_act ? o[i] * g[i] : o[i] / (1.f + expf(-g[i]));
+      }
+      if (sig_from >= 0) {
+#pragma unroll
+        for (int i = 0; i < VALS; ++i)
+          if (n + i >= sig_from) o[i] = 1.f / (1.f + expf(-o[i]));
       }
       TC* dst = C + z * sC + (long)row * ldc + n;
       if (n + VALS <= N) {
@@ -321,6 +326,212 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
   if (splitk > 1) cluster_sync_all();      // no CTA leaves while a peer may still read its partial
   __syncthreads();
+  if (warp == 2) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// Persistent form for launches without split-K: one CTA per SM walks the
+// tiles (tile c, c + grid, ...), the ring runs on across tiles, and the
+// accumulator is double-buffered in tensor memory so that the epilogue of
+// one tile (warps 4-7, straight from tensor memory to global memory: a
+// thread holds 32 consecutive columns of its row) runs under the next
+// tile's loads and MMAs.  Same warp roles otherwise: warp 0 streams A, warp
+// 3 B, warp 1 (one lane) issues the MMAs, warp 2 owns tensor memory.
+struct PBars {
+  uint64_t acc_full[2];    // tile accumulator complete (phase per use of the buffer)
+  uint64_t acc_empty[2];   // its epilogue has read it (128 arrivals)
+  uint64_t drain;          // every MMA of the CTA complete
+  uint32_t tmem_slot;
+  int abort;
+};
+
+__device__ __forceinline__ bool pwait(PBars* B, uint64_t* bar, uint32_t parity, uint32_t* st) {
+  if (*(volatile int*)&B->abort) return false;
+  if (mbar_wait(bar, parity, st)) return true;
+  B->abort = 1;
+  return false;
+}
+
+template <int BN, typename TC>
+__global__ void __launch_bounds__(THREADS, 1)
+gemm_tc_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   int M, int N, int K, TC* __restrict__ C, long ldc, long sC,
+                   const float* __restrict__ G, long ldg, long sG, bool gate_act, int sig_from,
+                   uint32_t idesc, int group_m, int tiles_n, int tiles_m, int batch, uint32_t* status) {
+  using S = Smem<BN>;
+  constexpr int KBS = S::KBS, STAGES = S::STAGES;
+  constexpr uint32_t ACC_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+  constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* full = (uint64_t*)(smem + S::RING);
+  uint64_t* empty = full + STAGES;
+  PBars* PB = (PBars*)(empty + STAGES);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int nk = (K + BK - 1) / BK;
+  const int ng = (nk + KBS - 1) / KBS;                              // stages per tile
+  const long per_batch = (long)tiles_n * tiles_m, total = per_batch * batch;
+  // tile t -> (batch entry, row tile, column tile); row tiles in groups of
+  // group_m when that keeps B's columns shared in L2
+  auto tile_of = [&](long t, int& z, int& m0, int& n0) {
+    z = (int)(t / per_batch);
+    const long t_in = t % per_batch;
+    int tm, tn;
+    if (group_m > 1) {
+      const long per_group = (long)group_m * tiles_n;
+      const int first_m = (int)(t_in / per_group) * group_m;
+      const int gm = min(group_m, tiles_m - first_m);
+      const long r = t_in % per_group;
+      tm = first_m + (int)(r % gm);
+      tn = (int)(r / gm);
+    } else {
+      tn = (int)(t_in % tiles_n);
+      tm = (int)(t_in / tiles_n);
+    }
+    m0 = tm * BM;
+    n0 = tn * BN;
+  };
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 2);             // one arrival per operand's producer
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&PB->acc_full[i], 1);
+      mbar_init(&PB->acc_empty[i], 128);
+    }
+    mbar_init(&PB->drain, 1);
+    PB->abort = 0;
+    fence_mbar_init();
+    pdl_trigger();
+  }
+  if (warp == 2) tmem_alloc(&PB->tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = PB->tmem_slot;
+
+  if ((warp == 0 || warp == 3) && lane == 0) {
+    // producers: warp 0 the A operand (after the previous kernel), warp 3 the
+    // weights (independent of it); one copy per stage each
+    const bool is_a = warp == 0;
+    if (is_a) pdl_wait();
+    long gs = 0;
+    bool ok = true;
+    for (long t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      int z, m0, n0;
+      tile_of(t, z, m0, n0);
+      for (int g = 0; g < ng && ok; ++g, ++gs) {
+        const int s = (int)(gs % STAGES);
+        if (!(ok = pwait(PB, &empty[s], (uint32_t)((gs / STAGES) & 1) ^ 1, status))) break;
+        uint8_t* a = smem + s * S::STAGE_BYTES;
+        if (is_a) {
+          mbar_arrive_expect_tx(&full[s], S::A_BYTES);
+          tma_load_4d(a, &tmA, &full[s], 0, m0, g * KBS, z);
+        } else {
+          mbar_arrive_expect_tx(&full[s], S::B_BYTES);
+          tma_load_4d(a + S::A_BYTES, &tmB, &full[s], 0, n0, g * KBS, z);
+        }
+      }
+    }
+    // drain: the last loads of every slot have landed before the CTA can exit
+    for (long g = gs - STAGES < 0 ? 0 : gs - STAGES; g < gs; ++g)
+      mbar_wait(&full[g % STAGES], (uint32_t)((g / STAGES) & 1), status);
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer (k-blocks past K were filled with zeros by TMA and are skipped)
+    long gs = 0;
+    int j = 0;
+    bool ok = true;
+    for (long t = blockIdx.x; t < total && ok; t += gridDim.x, ++j) {
+      const int buf = j & 1;
+      if (!(ok = pwait(PB, &PB->acc_empty[buf], (uint32_t)((j >> 1) & 1) ^ 1, status))) break;
+      tc_fence_after();
+      const uint32_t d = tmem + buf * ACC_COLS;
+      for (int g = 0; g < ng; ++g, ++gs) {
+        const int s = (int)(gs % STAGES);
+        if (!(ok = pwait(PB, &full[s], (uint32_t)((gs / STAGES) & 1), status))) break;
+        tc_fence_after();
+        const uint8_t* a = smem + s * S::STAGE_BYTES;
+        const uint8_t* b = a + S::A_BYTES;
+#pragma unroll
+        for (int i = 0; i < KBS; ++i) {
+          if (g * KBS + i >= nk) break;
+          const uint64_t da = smem_desc_sw128(a + i * BM * BK * 2), db = smem_desc_sw128(b + i * BN * BK * 2);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_f16(d, da + 2 * k, db + 2 * k, idesc, (g | i | k) != 0);
+        }
+        mma_commit(&empty[s]);
+      }
+      if (!ok) break;
+      mma_commit(&PB->acc_full[buf]);
+    }
+    mma_commit(&PB->drain);
+    mbar_wait(&PB->drain, 0, status);
+  } else if (warp >= 4) {
+    // epilogue: thread = accumulator row (TMEM lane 32 (warp % 4) + lane)
+    pdl_wait();                        // C and the gate belong to the kernels around this one
+    const int q = warp % 4, r = q * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    int j = 0;
+    for (long t = blockIdx.x; t < total; t += gridDim.x, ++j) {
+      const int buf = j & 1;
+      int z, m0, n0;
+      tile_of(t, z, m0, n0);
+      const bool ok = pwait(PB, &PB->acc_full[buf], (uint32_t)((j >> 1) & 1), status);
+      tc_fence_after();
+      const int row = m0 + r;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        float v[32];
+        tmem_ld32(tmem + buf * ACC_COLS + lane_addr + c, v);
+        const int n = n0 + c;
+        if (!ok || row >= M || n >= N) continue;
+        if (G) {
+          // the row's 32 gate values (16-byte loads when the row piece is whole and aligned)
+          const float* g = G + z * sG + (long)row * ldg + n;
+          float gv[32];
+          if (n + 32 <= N && ((uintptr_t)g & 15) == 0) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              const float4 t = *reinterpret_cast<const float4*>(g + i);
+              gv[i] = t.x; gv[i + 1] = t.y; gv[i + 2] = t.z; gv[i + 3] = t.w;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) gv[i] = n + i < N ? g[i] : 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = gate_act ? v[i] * gv[i] : v[i] / (1.f + expf(-gv[i]));
+        }
+        if (sig_from >= 0) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (n + i >= sig_from) v[i] = 1.f / (1.f + expf(-v[i]));
+        }
+        TC* dst = C + z * sC + (long)row * ldc + n;
+        constexpr int VALS = 16 / (int)sizeof(TC);
+        if (n + 32 <= N) {
+#pragma unroll
+          for (int i = 0; i < 32; i += VALS) store16<TC>(dst + i, v + i);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (n + i < N) dst[i] = from_f32<TC>(v[i]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&PB->acc_empty[buf]);
+    }
+  }
+  pdl_wait();
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
   if (warp == 2) tmem_dealloc(tmem, TMEM_COLS);
 }
 
@@ -377,6 +588,8 @@ bool make_operand_map(CUtensorMap* m, bool fp16, const void* base, long rows, lo
   return encode(m, fp16, base, 4, dims, strides, box);
 }
 
+int num_sms_current();
+
 template <int BN, typename TC>
 mla_status_t launch(cudaStream_t st, const GemmArgs& a, int splitk, uint32_t* status) {
   using S = Smem<BN>;
@@ -395,9 +608,26 @@ mla_status_t launch(cudaStream_t st, const GemmArgs& a, int splitk, uint32_t* st
   // of 8 (measured on the DeepSeek-V3-shaped step: 113.3 -> 111.0 ms)
   const double b_bytes = (double)a.N * a.K * 2;
   const int group_m = (b_bytes > 48e6 && (a.M + BM - 1) / BM > 8) ? 8 : 1;
+  const int tiles_n = (a.N + BN - 1) / BN, tiles_m = (a.M + BM - 1) / BM;
+  const long tiles = (long)tiles_n * tiles_m * a.batch;
+  if (splitk == 1 && tiles > num_sms_current()) {
+    // more tiles than SMs: the persistent form, one CTA per SM
+    auto pk = gemm_tc_persistent<BN, TC>;
+    static std::once_flag once_p;
+    std::call_once(once_p, [&] {
+      cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
+    });
+    Launch P(dim3((unsigned)num_sms_current()), dim3(THREADS), S::BYTES, st, a.pdl);
+    const cudaError_t ep = cudaLaunchKernelEx(&P.cfg, pk, ta, tb, a.M, a.N, a.K, (TC*)a.C, a.ldc, a.sC,
+                                              a.G, a.ldg, a.sG, a.gate_act, a.sig_from,
+                                              idesc_f16(BM, BN, a.fp16), group_m, tiles_n, tiles_m,
+                                              a.batch, status);
+    if (ep != cudaSuccess) return cuda_fail(ep, "tcgen05 gemm launch");
+    return MLA_OK;
+  }
   const cudaError_t e = cudaLaunchKernelEx(&L.cfg, kern, ta, tb, a.M, a.N, a.K, (TC*)a.C, a.ldc, a.sC,
-                                           a.G, a.ldg, a.sG, idesc_f16(BM, BN, a.fp16), splitk, group_m,
-                                           status);
+                                           a.G, a.ldg, a.sG, a.gate_act, a.sig_from,
+                                           idesc_f16(BM, BN, a.fp16), splitk, group_m, status);
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 gemm launch");
   return MLA_OK;
 }

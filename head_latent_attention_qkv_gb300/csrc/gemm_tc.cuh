@@ -16,15 +16,18 @@ struct GemmArgs {
   const void* A; long lda, sA;   // [batch][M][K] (elements; lda, sA strides)
   const void* B; long ldb, sB;   // [batch][N][K]
   void* C; long ldc, sC; Out out;
-  const float* G; long ldg, sG;  // optional sigmoid gate, same indexing as C
+  const float* G; long ldg, sG;  // optional gate, same indexing as C: C *= sigmoid(G)
   bool pdl = false;              // may start while the previous kernel of the stream finishes
+  bool gate_act = false;         // G already holds sigmoid(gate): C *= G
+  int sig_from = -1;             // columns n >= sig_from (>= 0) of C store sigmoid(value)
 };
 
 // Tile width (64, 128 or 256 columns) and split-K factor (CTAs of a cluster
 // along K, 1 = none) the launcher uses for this shape.
 void plan_gemm(int M, int N, int K, int batch, int out_bytes, int* bn, int* splitk);
 
-// Enqueue C = A B^T (* sigmoid(G)) on `st`.  When the output tiles alone do
+// Enqueue C = A B^T (* sigmoid(G), or * G when gate_act; sigmoid applied to
+// the columns from sig_from on) on `st`.  When the output tiles alone do
 // not fill the GPU (and batch == 1) K is split over a cluster of CTAs whose
 // fp32 partials are added in shared memory, in a fixed order, before the
 // epilogue: no atomics, no zeroing, any output type.  Returns
