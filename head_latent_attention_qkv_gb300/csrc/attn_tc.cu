@@ -36,10 +36,14 @@
 // copied while they are multiplied.
 //   MMA warp     : S(t) = Q K(t)^T (36 MMAs, N = 128); O += P(t) V(t) (8 MMAs,
 //                  N = 256, P read from tensor memory)
-//   softmax warps: thread r owns row r (TMEM lane r): mask by logical
-//                  position (one visible interval per row), online softmax in
-//                  fp32 in the exp2 domain (O rescaled in tensor memory only
-//                  when the running max grows by more than 2^8), P -> bf16
+//   softmax warps (0-3 and 8-11): two threads per row r (TMEM lane r), each
+//                  on 64 of the tile's keys and 128 of the value columns,
+//                  exchanging the half maxima through shared memory: mask by
+//                  logical position (one visible interval per row), online
+//                  softmax in fp32 in the exp2 domain (O rescaled in tensor
+//                  memory only when the running max grows by more than 2^8),
+//                  P -> bf16 (one thread per row: ≈1.7 k of ≈6.2 k cycles per
+//                  tile, with the tensor pipe waiting)
 //   TMA warps    : warp 4 the page rows of the key range (once), Q, V(t);
 //                  warps 6 and 7 the ring chunks (copies of different warps
 //                  proceed side by side)
@@ -67,7 +71,7 @@ constexpr int NQS = NCH - NQT;                            // Q chunks held in sh
 constexpr int NVC = 4;                                    // value chunks of this CTA's half
 constexpr int NRC = NCH - NVC;                            // ring chunks per tile
 constexpr int RSLOTS = NRC;                               // ring slot i holds ring chunk i
-constexpr int THREADS = 256;                              // softmax x4, TMA, MMA, TMA x2
+constexpr int THREADS = 384;                              // softmax x4, TMA, MMA, TMA x2, softmax x4
 constexpr int Q_CH_BYTES = QROWS * DCH * 2;               // 16 KiB
 constexpr int KV_CH_BYTES = KT * DCH * 2;                 // 16 KiB
 constexpr int OFF_Q = 0;
@@ -76,7 +80,8 @@ constexpr int OFF_K = OFF_V + NVC * KV_CH_BYTES;
 constexpr int OFF_BAR = OFF_K + RSLOTS * KV_CH_BYTES;
 constexpr int OFF_PG = OFF_BAR + 256;                     // cache row of each page of the key range
 constexpr int MAX_PG = 176;                               // pages held there (else looked up per load)
-constexpr int SMEM_BYTES = 1024 + OFF_PG + MAX_PG * 4;
+constexpr int OFF_XM = OFF_PG + MAX_PG * 4;               // [128] a row's half maximum (or sum)
+constexpr int SMEM_BYTES = 1024 + OFF_XM + QROWS * 4 * 2;
 constexpr uint32_t TMEM_COLS = 512, TM_O = 0, TM_S = 256, TM_P = 256, TM_Q = 384;
 constexpr float RESCALE_LOG2 = 8.f;                       // lazy rescale threshold (factor 256)
 constexpr int MAX_SPLITS = 4;                             // clusters of at most 8 CTAs
@@ -127,12 +132,20 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// Warps 0-3: thread r owns accumulator row r (TMEM lane r) of the unit.
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
+
+// Warps 0-3 and 8-11: the two threads of row r (TMEM lane r; warps w and
+// w + 8 share the lane sub-partition) own key columns [64 kh, 64 kh + 64) of
+// each score tile and value columns [128 kh, 128 kh + 128) of O.  They
+// exchange their half's maximum each tile (and their half's sum at the end)
+// through shared memory.
 __device__ __forceinline__ void softmax_and_stage(const AttnParams& P, Bars* B, uint8_t* smem,
                                                   uint32_t tmem, int b, int qt, long row0, int kvl,
                                                   int W, int j_lo, int nt) {
-  const int r = threadIdx.x;
+  const int r = threadIdx.x & (QROWS - 1), kh = threadIdx.x >= 256 ? 1 : 0;
+  constexpr int KH = KT / 2;                                   // score columns per thread
   const uint32_t lane_base = (uint32_t)((r / 32) * 32) << 16;
+  float* xm = (float*)(smem + OFF_XM);                         // [2][128]
   const int row_in_block = qt * QROWS + r;
   // rows past the block's T x H (a partial last tile) are padding: fully masked
   const bool live = row_in_block < P.T * P.H;
@@ -149,7 +162,7 @@ __device__ __forceinline__ void softmax_and_stage(const AttnParams& P, Bars* B, 
     // Q_abs dims 0..255 of this row -> tensor memory (bf16 pairs, low half = even dim)
     const uint4* src = reinterpret_cast<const uint4*>(P.q_abs + (row0 + r) * 576);
 #pragma unroll 1
-    for (int c = 0; c < NQT; ++c) {
+    for (int c = kh * (NQT / 2); c < (kh + 1) * (NQT / 2); ++c) {
       uint32_t w[32];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -164,41 +177,47 @@ __device__ __forceinline__ void softmax_and_stage(const AttnParams& P, Bars* B, 
   for (int t = 0; t < nt; ++t) {
     const uint32_t ph = t & 1;
     const int j0 = j_lo + t * KT;
-    float s[KT];
+    float s[KH];
     // S(t) complete (and, the MMAs completing in order, P(t - 1) V(t - 1))
     wait_bar(B, &B->s_full, ph, P.status);
     tc_fence_after();
 #pragma unroll
-    for (int c = 0; c < KT; c += 32) tmem_ld32_nowait(tmem + TM_S + c + lane_base, s + c);
+    for (int c = 0; c < KH; c += 32) tmem_ld32_nowait(tmem + TM_S + KH * kh + c + lane_base, s + c);
     tmem_ld_wait();
 #pragma unroll
-    for (int c = 0; c < KT; c += 32) tmem_reg_fence32(s + c);
-    // mask by logical position (a warp whose rows all see the whole tile skips it)
+    for (int c = 0; c < KH; c += 32) tmem_reg_fence32(s + c);
+    // mask by logical position (a warp whose rows all see its half of the tile skips it)
     const int lo = max(vlo - j0, 0), hi = min(vhi - j0, KT);   // visible columns [lo, hi)
     if (hi > lo) {
       cnt += hi - lo;
       if (first < 0) first = j0 + lo;
       last = j0 + hi - 1;
     }
+    const int lo_h = lo - KH * kh, hi_h = hi - KH * kh;          // the same, in this half
     float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-    if (__all_sync(0xffffffffu, lo == 0 && hi == KT)) {
+    if (__all_sync(0xffffffffu, lo_h <= 0 && hi_h >= KH)) {
 #pragma unroll
-      for (int i = 0; i < KT; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
+      for (int i = 0; i < KH; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
     } else {
 #pragma unroll
-      for (int i = 0; i < KT; ++i) {
-        s[i] = (i >= lo && i < hi) ? s[i] : -INFINITY;
+      for (int i = 0; i < KH; ++i) {
+        s[i] = (i >= lo_h && i < hi_h) ? s[i] : -INFINITY;
         mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
       }
     }
-    // into the exp2 domain: the scale is positive, so it commutes with the max
-    const float tmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * P.scale_log2;
+    // the row's maximum from both halves; into the exp2 domain (the scale is
+    // positive, so it commutes with the max)
+    const float hmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+    xm[kh * QROWS + r] = hmax;
+    softmax_sync();
+    const float tmax = fmaxf(hmax, xm[(1 - kh) * QROWS + r]) * P.scale_log2;
+    softmax_sync();                                            // both halves read before the next write
     const bool grow = tmax > mrun + RESCALE_LOG2;
     const float m_new = grow ? tmax : mrun;
     const float mref = m_new == -INFINITY ? 0.f : m_new;      // all masked so far: P = 0
     float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < KT; ++i) {
+    for (int i = 0; i < KH; ++i) {
       s[i] = fast_exp2(fmaf(s[i], P.scale_log2, -mref));
       ps4[i & 3] += s[i];
     }
@@ -207,7 +226,7 @@ __device__ __forceinline__ void softmax_and_stage(const AttnParams& P, Bars* B, 
     // P(t - 1) V(t - 1) has completed (before S(t)): O may be rescaled
     if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-      for (int c = 0; c < 256; c += 32) {
+      for (int c = 128 * kh; c < 128 * kh + 128; c += 32) {
         float o[32];
         tmem_ld32(tmem + TM_O + lane_base + c, o);
 #pragma unroll
@@ -223,7 +242,7 @@ __device__ __forceinline__ void softmax_and_stage(const AttnParams& P, Bars* B, 
       wait_bar(B, &B->v_full, ph, P.status);
       uint8_t* vbase = smem + OFF_V;
       const int z0 = max(0, kvl - j0), pieces = (KT - z0) * NVC * 8;
-      for (int idx = r; idx < pieces; idx += QROWS) {
+      for (int idx = r + QROWS * kh; idx < pieces; idx += 2 * QROWS) {
         const int key = z0 + idx / 32, ch = (idx % 32) / 8, q = idx % 8;
         *reinterpret_cast<uint4*>(vbase + ch * KV_CH_BYTES + key * 128 + q * 16) = make_uint4(0, 0, 0, 0);
       }
@@ -231,27 +250,30 @@ __device__ __forceinline__ void softmax_and_stage(const AttnParams& P, Bars* B, 
     }
     // P row in bf16 pairs over S (this thread has read its lane): key 2c in
     // the low half of column c
-#pragma unroll
-    for (int c = 0; c < KT / 2; c += 32) {
+    {
       uint32_t pw[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(s[2 * (c + i)], s[2 * (c + i) + 1]);
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(s[2 * i], s[2 * i + 1]);
         pw[i] = *reinterpret_cast<uint32_t*>(&h2);
       }
-      tmem_st32_u(tmem + TM_P + c + lane_base, pw);
+      tmem_st32_u(tmem + TM_P + 32 * kh + lane_base, pw);
     }
     tc_fence_before();
     mbar_arrive(&B->p_full);
   }
   // stage this split's partial: O / l in fp32, log2-sum-exp, visibility counts
+  // (the row sum from both halves)
+  xm[kh * QROWS + r] = lsum;
+  softmax_sync();
+  lsum += xm[(1 - kh) * QROWS + r];
   if (nt > 0) wait_bar(B, &B->o_done, (nt - 1) & 1, P.status);
   tc_fence_after();
   const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
   const bool any = nt > 0 && lsum > 0.f;
   float* prow = (float*)(smem + OFF_STG) + r * STG_PITCH;
 #pragma unroll 1
-  for (int c = 0; c < 256; c += 32) {
+  for (int c = 128 * kh; c < 128 * kh + 128; c += 32) {
     float o[32];
     if (nt > 0) tmem_ld32(tmem + TM_O + lane_base + c, o);
 #pragma unroll
@@ -260,11 +282,13 @@ __device__ __forceinline__ void softmax_and_stage(const AttnParams& P, Bars* B, 
           any ? make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv)
               : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  ((float*)(smem + OFF_LSE))[r] = any ? mrun + log2f(lsum) : -INFINITY;
-  int* vs = (int*)(smem + OFF_VS) + 3 * r;
-  vs[0] = cnt;
-  vs[1] = first;
-  vs[2] = last;
+  if (kh == 0) {
+    ((float*)(smem + OFF_LSE))[r] = any ? mrun + log2f(lsum) : -INFINITY;
+    int* vs = (int*)(smem + OFF_VS) + 3 * r;
+    vs[0] = cnt;
+    vs[1] = first;
+    vs[2] = last;
+  }
 }
 
 __device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
@@ -415,12 +439,12 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
 
   if (tid == 0) {
     mbar_init(&B->q_full, 1);
-    mbar_init(&B->q_tmem, QROWS);
+    mbar_init(&B->q_tmem, 2 * QROWS);
     mbar_init(&B->r_full, 2);
     mbar_init(&B->r_empty, 1);
     mbar_init(&B->v_full, 1);
     mbar_init(&B->s_full, 1);
-    mbar_init(&B->p_full, QROWS);
+    mbar_init(&B->p_full, 2 * QROWS);
     mbar_init(&B->o_done, 1);
     mbar_init(&B->drain, 1);
     B->abort = 0;
@@ -435,7 +459,7 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
   if (tid == 0) pdl_trigger();
   pdl_wait();                  // Q_abs and the block's own latents come from the kernels before
 
-  if (warp == 4 || warp >= 6) {
+  if (warp == 4 || warp == 6 || warp == 7) {
     // the cache row of every page this CTA reads, looked up once by warp 4
     // (past_end for a page the table marks invalid: TMA then reads zeros)
     const int ps = P.page_size, past_end = P.num_pages * ps;
