@@ -310,10 +310,14 @@ FwdWs forward_ws(const mla_handle* h, long M) {
   return w;
 }
 
-// The bf16 append runs as one fused kernel; only the fp32 layer stages the
-// projection in a workspace.
+// The bf16 append runs as one fused kernel when its CTAs (3 per 128 rows)
+// fill the GPU; fewer tokens, and the fp32 layer, stage the projection (a
+// split-K GEMM) in a workspace and finish the rows with a second kernel.
+bool append_fused(const mla_handle* h, long n) {
+  return h->cfg.dtype == MLA_BF16 && 3L * ((n + 127) / 128) >= h->num_sms;
+}
 size_t append_ws(const mla_handle* h, long n) {
-  return h->cfg.dtype == MLA_BF16 ? 0 : align256((size_t)n * h->lay.L * 4);
+  return append_fused(h, n) ? 0 : align256((size_t)n * h->lay.L * 4);
 }
 
 }  // namespace
@@ -367,10 +371,13 @@ mla_status_t append_impl(mla_handle_t* h, const void* hidden, const int32_t* pos
   const Layout& l = h->lay;
   // kv = hidden @ W_kva^T : W_kva = first L rows of W_A
   if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-    h->launches += 1;
-    return tc::kv_append(st, h, (const T*)hidden, n, positions, slots, (T*)cache, num_slots,
-                         true);
-  } else {
+    if (append_fused(h, n)) {
+      h->launches += 1;
+      return tc::kv_append(st, h, (const T*)hidden, n, positions, slots, (T*)cache, num_slots,
+                           true);
+    }
+  }
+  {
     mla_status_t s = proj<T, float>(h, st, false, n, l.L, l.D, 1, (const T*)hidden, l.D, 0,
                                     (const T*)h->WA, l.D, 0, kv_ws, l.L, 0);
     if (s != MLA_OK) return s;
