@@ -341,7 +341,7 @@ template <typename TA, typename TC>
 mla_status_t proj(mla_handle_t* h, cudaStream_t st, bool pdl, int M, int N, int K, int batch,
                   const TA* A, long lda, long sA, const TA* B, long ldb, long sB, TC* C, long ldc,
                   long sC, const float* G = nullptr, long ldg = 0, long sG = 0, bool gate_act = false,
-                  int sig_from = -1) {
+                  int sig_from = -1, const tc::QSplit* qsplit = nullptr, bool* qsplit_done = nullptr) {
   h->launches += (M > 0 && N > 0 && batch > 0);
   if constexpr (std::is_same<TA, float>::value) {
     simt::gemm_nt<TA, TC>(st, M, N, K, batch, A, lda, sA, B, ldb, sB, C, ldc, sC, G, ldg, sG);
@@ -350,7 +350,7 @@ mla_status_t proj(mla_handle_t* h, cudaStream_t st, bool pdl, int M, int N, int 
     tc::Out o = std::is_same<TC, float>::value ? tc::Out::F32
                 : std::is_same<TC, __half>::value ? tc::Out::F16 : tc::Out::BF16;
     tc::GemmArgs a{M, N, K, batch, std::is_same<TA, __half>::value, A, lda, sA, B, ldb, sB,
-                   C, ldc, sC, o, G, ldg, sG, pdl, gate_act, sig_from};
+                   C, ldc, sC, o, G, ldg, sG, pdl, gate_act, sig_from, qsplit, qsplit_done};
     return tc::gemm(st, a, h->status);
   }
 }
@@ -463,13 +463,24 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
   }
   const float* q_raw;
   long ldq;
+  TI* q_nope = (TI*)(ws + w.q_nope);
+  // Q_abs shares the cache's type: the two meet in the attention contraction
+  TX* q_abs = (TX*)(ws + w.q_abs);
+  bool split_done = false;
   if (l.rq > 0) {
     TI* q_cn = (TI*)(ws + w.q_cn);
     simt::rmsnorm_rows<TI>(st, a_out + l.L, l.NA, M, l.rq, h->gamma_q, (float)h->cfg.rms_norm_eps, q_cn,
                            pdl);
     float* qr = (float*)(ws + w.q_raw);
+    // tensor-core layers: the GEMM's epilogue may split the heads and rotate
+    // the RoPE dims itself (persistent launches), else the row kernel below
+    tc::QSplit qs{};
+    if constexpr (kBf16)
+      qs = tc::QSplit{(__half*)q_nope, (__nv_bfloat16*)q_abs, pos, h->rope, l.H, l.dn, l.dr, l.L, l.rkv,
+                      h->cfg.max_position, (int)(h->cfg.rope == MLA_ROPE_INTERLEAVED)};
     s = proj<TI, float>(h, st, pdl, M, l.H * l.dqk, l.rq, 1, q_cn, l.rq, 0, (const TI*)h->Wqb, l.rq,
-                        0, qr, l.H * l.dqk, 0);
+                        0, qr, l.H * l.dqk, 0, nullptr, 0, 0, false, -1, kBf16 ? &qs : nullptr,
+                        &split_done);
     if (s != MLA_OK) return s;
     q_raw = qr;
     ldq = l.H * l.dqk;
@@ -477,10 +488,7 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
     q_raw = a_out + l.L;
     ldq = l.NA;
   }
-  TI* q_nope = (TI*)(ws + w.q_nope);
-  // Q_abs shares the cache's type: the two meet in the attention contraction
-  TX* q_abs = (TX*)(ws + w.q_abs);
-  simt::q_rope_split<TI, TX>(st, h, q_raw, ldq, M, pos, q_nope, q_abs, pdl);
+  if (!split_done) simt::q_rope_split<TI, TX>(st, h, q_raw, ldq, M, pos, q_nope, q_abs, pdl);
   // q_lat[h] = q_nope[h] @ W_UK[h]  ->  Q_abs[:, h, :rkv]
   s = proj<TI, TX>(h, st, pdl, M, l.rkv, l.dn, l.H, q_nope, (long)l.H * l.dn, l.dn,
                    (const TI*)h->WUKT, l.dn, (long)l.rkv * l.dn, q_abs, (long)l.H * l.L, l.L);
@@ -513,8 +521,8 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
   s = proj<TI, TX>(h, st, pdl, M, l.D, l.H * l.dv, 1, o, (long)l.H * l.dv, 0, (const TI*)h->Wo,
                    (long)l.H * l.dv, 0, (TX*)out, l.D, 0);
   if (s != MLA_OK) return s;
-  // non-GEMM kernels: [kv finish], [q norm], rope split, attention
-  h->launches += 2 + (bslots ? 1 : 0) + (l.rq > 0 ? 1 : 0);
+  // non-GEMM kernels: [kv finish], [q norm], [rope split], attention
+  h->launches += (split_done ? 1 : 2) + (bslots ? 1 : 0) + (l.rq > 0 ? 1 : 0);
   return MLA_OK;
 }
 

@@ -356,7 +356,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    int M, int N, int K, TC* __restrict__ C, long ldc, long sC,
                    const float* __restrict__ G, long ldg, long sG, bool gate_act, int sig_from,
-                   uint32_t idesc, int group_m, int tiles_n, int tiles_m, int batch, uint32_t* status) {
+                   uint32_t idesc, int group_m, int tiles_n, int tiles_m, int batch, QSplit qs,
+                   uint32_t* status) {
   using S = Smem<BN>;
   constexpr int KBS = S::KBS, STAGES = S::STAGES;
   constexpr uint32_t ACC_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
@@ -484,6 +485,64 @@ gemm_tc_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
       const bool ok = pwait(PB, &PB->acc_full[buf], (uint32_t)((j >> 1) & 1), status);
       tc_fence_after();
       const int row = m0 + r;
+      if (qs.q_nope) {
+        // q_b: 32-column chunks lie inside one head's no-position or RoPE dims
+        const int dqk = qs.dn + qs.dr, half = qs.dr / 2;
+        int p = 0;
+        bool bad = false;
+        if (ok && row < M) {
+          p = qs.positions[row];
+          bad = p < 0 || p >= qs.max_pos;
+          if (bad && n0 == 0) set_status(status, MLA_DEV_BAD_POSITION);
+        }
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          const int n = n0 + c, hh = n / dqk, d = n % dqk;
+          float v[32];
+          tmem_ld32(tmem + buf * ACC_COLS + lane_addr + c, v);
+          const bool second_neox = !qs.interleaved && d >= qs.dn + half;   // done with its partner
+          float u[32];
+          if (d >= qs.dn && !qs.interleaved && !second_neox)
+            tmem_ld32(tmem + buf * ACC_COLS + lane_addr + c + half, u);
+          if (!ok || row >= M || n >= N || second_neox) continue;
+          const long base = (long)row * qs.H + hh;
+          if (d < qs.dn) {
+            store16_16(qs.q_nope + base * qs.dn + d, v);
+            store16_16(qs.q_nope + base * qs.dn + d + 8, v + 8);
+            store16_16(qs.q_nope + base * qs.dn + d + 16, v + 16);
+            store16_16(qs.q_nope + base * qs.dn + d + 24, v + 24);
+            continue;
+          }
+          const int rd = d - qs.dn;                       // first RoPE dim of the chunk
+          __nv_bfloat16* dst = qs.q_abs + base * qs.L + qs.rkv + rd;
+          if (qs.interleaved) {
+            // pairs (2k, 2k + 1), k = rd / 2 + i
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 cs = bad ? make_float2(0.f, 0.f) : qs.rope[(long)p * half + rd / 2 + i];
+              const float a = v[2 * i], bb = v[2 * i + 1];
+              v[2 * i] = a * cs.x - bb * cs.y;
+              v[2 * i + 1] = bb * cs.x + a * cs.y;
+            }
+            store16_16(dst, v); store16_16(dst + 8, v + 8); store16_16(dst + 16, v + 16); store16_16(dst + 24, v + 24);
+          } else {
+            // pairs (k, k + dr / 2): this chunk holds the first halves, u the second
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float2 cs = bad ? make_float2(0.f, 0.f) : qs.rope[(long)p * half + rd + i];
+              const float a = v[i], bb = u[i];
+              v[i] = a * cs.x - bb * cs.y;
+              u[i] = bb * cs.x + a * cs.y;
+            }
+            store16_16(dst, v); store16_16(dst + 8, v + 8); store16_16(dst + 16, v + 16); store16_16(dst + 24, v + 24);
+            store16_16(dst + half, u); store16_16(dst + half + 8, u + 8);
+            store16_16(dst + half + 16, u + 16); store16_16(dst + half + 24, u + 24);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&PB->acc_empty[buf]);
+        continue;
+      }
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         float v[32];
@@ -610,6 +669,7 @@ mla_status_t launch(cudaStream_t st, const GemmArgs& a, int splitk, uint32_t* st
   const int group_m = (b_bytes > 48e6 && (a.M + BM - 1) / BM > 8) ? 8 : 1;
   const int tiles_n = (a.N + BN - 1) / BN, tiles_m = (a.M + BM - 1) / BM;
   const long tiles = (long)tiles_n * tiles_m * a.batch;
+  if (a.qsplit_done) *a.qsplit_done = false;
   if (splitk == 1 && tiles > num_sms_current()) {
     // more tiles than SMs: the persistent form, one CTA per SM
     auto pk = gemm_tc_persistent<BN, TC>;
@@ -621,8 +681,9 @@ mla_status_t launch(cudaStream_t st, const GemmArgs& a, int splitk, uint32_t* st
     const cudaError_t ep = cudaLaunchKernelEx(&P.cfg, pk, ta, tb, a.M, a.N, a.K, (TC*)a.C, a.ldc, a.sC,
                                               a.G, a.ldg, a.sG, a.gate_act, a.sig_from,
                                               idesc_f16(BM, BN, a.fp16), group_m, tiles_n, tiles_m,
-                                              a.batch, status);
+                                              a.batch, a.qsplit ? *a.qsplit : QSplit{}, status);
     if (ep != cudaSuccess) return cuda_fail(ep, "tcgen05 gemm launch");
+    if (a.qsplit && a.qsplit_done) *a.qsplit_done = true;
     return MLA_OK;
   }
   const cudaError_t e = cudaLaunchKernelEx(&L.cfg, kern, ta, tb, a.M, a.N, a.K, (TC*)a.C, a.ldc, a.sC,

@@ -10,6 +10,17 @@ namespace tc {
 
 enum class Out { F32, F16, BF16 };
 
+// q_b epilogue: for each head, the no-position dims go to q_nope (fp16)
+// and the RoPE dims, rotated by the row's position, to the tail of Q_abs
+// (bf16), instead of C.
+struct QSplit {
+  __half* q_nope;                 // [rows, H, dn]
+  __nv_bfloat16* q_abs;           // [rows, H, L]: dims rkv .. rkv + dr written
+  const int32_t* positions;       // [rows]
+  const float2* rope;             // [max_pos, dr / 2] (cos, sin)
+  int H, dn, dr, L, rkv, max_pos, interleaved;
+};
+
 struct GemmArgs {
   int M, N, K, batch;
   bool fp16;                 // operand type: fp16 (true) or bf16 (false)
@@ -20,6 +31,8 @@ struct GemmArgs {
   bool pdl = false;              // may start while the previous kernel of the stream finishes
   bool gate_act = false;         // G already holds sigmoid(gate): C *= G
   int sig_from = -1;             // columns n >= sig_from (>= 0) of C store sigmoid(value)
+  const QSplit* qsplit = nullptr;  // q_b split/rotation in the epilogue (persistent launches)
+  bool* qsplit_done = nullptr;     // set true when the launch did it (C then not written)
 };
 
 // Tile width (64, 128 or 256 columns) and split-K factor (CTAs of a cluster

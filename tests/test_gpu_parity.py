@@ -83,6 +83,20 @@ def test_page_sizes_match_oracle(page_size):
     check_workload(wl)
 
 
+@pytest.mark.parametrize("rope", ["neox", "interleaved"])
+def test_many_block_tokens_split_queries_in_the_projection(rope):
+    """1024 block tokens (64 blocks of 16): the q_b projection runs as the
+    persistent GEMM whose epilogue splits the heads and rotates the RoPE dims
+    itself (both pairings), instead of the row kernel; sampled blocks against
+    the oracle."""
+    from tests.parity import check_workload
+    W = workloads
+    wl = W.cached_decode_workload(f"q_split_{rope}", W.QWEN3_4B_MLA.replace(rope_style=rope), 21,
+                                  batch=64, prefill_len=300, len_lo=100, len_hi=300, block_len=16,
+                                  num_blocks=1, page_size=128)
+    check_workload(wl, _sample_blocks(wl, 6, seed=3))
+
+
 def _scaled_workload(gain_q, gain_kv, seed=12):
     """Config 1 small with the RMSNorm gains scaled and hidden states carrying
     +-1e3 outliers (bf16-representable values on both sides)."""
