@@ -562,19 +562,30 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
       const uint32_t idesc_qk = idesc_f16(QROWS, KT, false);
       const uint32_t idesc_pv = idesc_f16_bmn(QROWS, 256, false);
       bool ok = wait_bar(B, &B->q_full, 0, P.status) && wait_bar(B, &B->q_tmem, 0, P.status);
-      // S += Q[:, chunk c] K(chunk c)^T, B operand at `kb` (K-major, 128 keys)
-      auto qk_chunk = [&](int c, const uint8_t* kb, bool first) {
-        const uint64_t db = smem_desc_sw128(kb);
-        if (c < NQT) {
-#pragma unroll
-          for (int k = 0; k < DCH / 16; ++k)
-            mma_f16_ts(tmem + TM_S, tmem + TM_Q + 32 * c + 8 * k, db + 2 * k, idesc_qk, !(first && k == 0));
-        } else {
-          const uint64_t da = smem_desc_sw128(smem + OFF_Q + (c - NQT) * Q_CH_BYTES);
-#pragma unroll
-          for (int k = 0; k < DCH / 16; ++k)
-            mma_f16(tmem + TM_S, da + 2 * k, db + 2 * k, idesc_qk, !(first && k == 0));
-        }
+      // S += Q[:, chunk] K(chunk)^T over the 576 dims, fully unrolled from
+      // descriptors computed once (the issuing thread's rate is set by the
+      // instructions between its MMAs): A is Q chunk qc in tensor memory
+      // (dims 0..255) or smem Q chunk qs (dims 256..575), B the 128 keys'
+      // chunk (K-major).  Half 0 reads Q chunks 4..8 with its ring and 0..3
+      // with its value chunks; half 1 Q chunks 0..3 and 8 with its ring and
+      // 4..7 with its value chunks.
+      const uint64_t dK = smem_desc_sw128(smem + OFF_K), dVk = smem_desc_sw128(smem + OFF_V);
+      const uint64_t dQs = smem_desc_sw128(smem + OFF_Q);
+      const uint64_t dv = smem_desc_sw128_mn(smem + OFF_V, KV_CH_BYTES);
+      constexpr uint32_t U_CH = KV_CH_BYTES / 16, U_Q = Q_CH_BYTES / 16, U_KSTEP = 16 * 128 / 16;
+      const uint32_t tS = tmem + TM_S, tQ = tmem + TM_Q, tO = tmem + TM_O, tP = tmem + TM_P;
+      auto qk_tm = [&](int qc, uint64_t db, uint32_t acc0) {
+        mma_f16_ts(tS, tQ + 32 * qc, db, idesc_qk, acc0);
+        mma_f16_ts(tS, tQ + 32 * qc + 8, db + 2, idesc_qk, 1u);
+        mma_f16_ts(tS, tQ + 32 * qc + 16, db + 4, idesc_qk, 1u);
+        mma_f16_ts(tS, tQ + 32 * qc + 24, db + 6, idesc_qk, 1u);
+      };
+      auto qk_sm = [&](int qs, uint64_t db, uint32_t acc0) {
+        const uint64_t da = dQs + qs * U_Q;
+        mma_f16(tS, da, db, idesc_qk, acc0);
+        mma_f16(tS, da + 2, db + 2, idesc_qk, 1u);
+        mma_f16(tS, da + 4, db + 4, idesc_qk, 1u);
+        mma_f16(tS, da + 6, db + 6, idesc_qk, 1u);
       };
       for (int t = 0; t < nt && ok; ++t) {
         const uint32_t ph = t & 1;
@@ -583,22 +594,33 @@ __global__ void __launch_bounds__(THREADS, 1) latent_attn_tc_kernel(const __grid
         // thread, executed in order)
         if (!(ok = wait_bar(B, &B->r_full, ph, P.status))) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int i = 0; i < RSLOTS; ++i) qk_chunk(ring_chunk(i, half), smem + OFF_K + i * KV_CH_BYTES, i == 0);
+        if (half == 0) {
+#pragma unroll
+          for (int i = 0; i < RSLOTS; ++i) qk_sm(i, dK + i * U_CH, i == 0 ? 0u : 1u);
+        } else {
+#pragma unroll
+          for (int i = 0; i < NVC; ++i) qk_tm(i, dK + i * U_CH, i == 0 ? 0u : 1u);
+          qk_sm(NQS - 1, dK + NVC * U_CH, 1u);
+        }
         mma_commit(&B->r_empty);               // the ring may be refilled
         if (!(ok = wait_bar(B, &B->v_full, ph, P.status))) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int i = 0; i < NVC; ++i) qk_chunk(NVC * half + i, smem + OFF_V + i * KV_CH_BYTES, false);
+        if (half == 0) {
+#pragma unroll
+          for (int i = 0; i < NVC; ++i) qk_tm(i, dVk + i * U_CH, 1u);
+        } else {
+#pragma unroll
+          for (int i = 0; i < NVC; ++i) qk_sm(i, dVk + i * U_CH, 1u);
+        }
         mma_commit(&B->s_full);
         // O += P(t) V(t)
         if (!(ok = wait_bar(B, &B->p_full, ph, P.status))) break;
         tc_fence_after();
-        const uint64_t dv = smem_desc_sw128_mn(smem + OFF_V, KV_CH_BYTES);
+        const uint32_t acc0 = t ? 1u : 0u;
+        mma_f16_ts(tO, tP, dv, idesc_pv, acc0);
 #pragma unroll
-        for (int k = 0; k < KT / 16; ++k)   // 16 keys per MMA: 8 P columns, 16 V rows
-          mma_f16_ts(tmem + TM_O, tmem + TM_P + 8 * k, dv + (uint64_t)(16 * 128 / 16) * k, idesc_pv,
-                     (t | k) != 0);
+        for (int k = 1; k < KT / 16; ++k)   // 16 keys per MMA: 8 P columns, 16 V rows
+          mma_f16_ts(tO, tP + 8 * k, dv + (uint64_t)U_KSTEP * k, idesc_pv, 1u);
         mma_commit(&B->o_done);
       }
       // no MMA of this CTA may still run when its tensor memory is freed
