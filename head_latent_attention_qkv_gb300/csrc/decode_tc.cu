@@ -79,7 +79,7 @@ constexpr int RD_INVL = 192;     // [32] 1 / row sum
 constexpr int RD_LO = 224;       // [32] first visible key of each row
 constexpr int RD_HI = 256;       // [32] end of each row's visible keys
 constexpr int RD_FLAG = 288;     // some row rescaled in this tile
-constexpr int RD_SCH = 320;      // [8] scan partials, [8..9] first block / tile of the range
+constexpr int RD_SCH = 320;      // [8] scan partials, [12..13] first block / tile of the range
 static_assert((RD_SCH + 16) * 4 <= RED_BYTES, "reduction area");
 
 // Every barrier is waited on phase by phase by its one consumer role, and
@@ -256,40 +256,53 @@ __global__ void __launch_bounds__(THREADS, 1) latent_decode_tc_kernel(const __gr
   }
   if (warp == 4) tmem_alloc(&B->tmem_slot, TMEM_COLS);
 
-  // ---- schedule: total tiles U, then the block holding this CTA's first tile
+  // ---- schedule: total tiles U, then the block holding this CTA's first
+  // tile (from the same scan when every block has a thread)
   int* sc = redi + RD_SCH;
   long long U = 0;
+  int my_nt = 0, my_excl = 0;
   for (int base = 0; base < nb; base += THREADS) {
     const int b = base + tid;
     const int nt = b < nb ? block_keys(P, b).nt : 0;
     int tot;
-    block_excl_scan(nt, sc, tid, &tot);
+    const int ex = block_excl_scan(nt, sc, tid, &tot);
+    if (base == 0) {
+      my_nt = nt;
+      my_excl = ex;
+    }
     U += tot;
   }
   // the first min(gridDim, U) CTAs take one range each, so none is empty
   const int G = (int)min((long long)gridDim.x, max(U, 1LL));
   const long long u0 = c < G ? U * c / G : U, u1 = c < G ? U * (c + 1) / G : U;
-  if (tid == 0) { sc[8] = nb; sc[9] = 0; }
+  if (tid == 0) { sc[12] = nb; sc[13] = 0; }
   __syncthreads();
   if (u1 > u0) {
-    long long run = 0;
-    for (int base = 0; base < nb; base += THREADS) {
-      const int b = base + tid;
-      const int nt = b < nb ? block_keys(P, b).nt : 0;
-      int tot;
-      const long long excl = run + block_excl_scan(nt, sc, tid, &tot);
-      if (nt > 0 && u0 >= excl && u0 < excl + nt) {
-        sc[8] = b;
-        sc[9] = (int)(u0 - excl);
+    if (nb <= THREADS) {
+      if (my_nt > 0 && u0 >= my_excl && u0 < my_excl + my_nt) {
+        sc[12] = tid;
+        sc[13] = (int)(u0 - my_excl);
       }
-      run += tot;
+    } else {
+      long long run = 0;
+      for (int base = 0; base < nb; base += THREADS) {
+        const int b = base + tid;
+        const int nt = b < nb ? block_keys(P, b).nt : 0;
+        int tot;
+        const long long excl = run + block_excl_scan(nt, sc, tid, &tot);
+        if (nt > 0 && u0 >= excl && u0 < excl + nt) {
+          sc[12] = b;
+          sc[13] = (int)(u0 - excl);
+        }
+        run += tot;
+      }
     }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = B->tmem_slot;
-  const int b_first = sc[8], t_first = sc[9];
+  const int b_first = sc[12], t_first = sc[13];
   const long ntiles = (long)(u1 - u0);
   if (tid == 0) pdl_trigger();
   // Each role looks up what it needs from the descriptor (lengths, windows,
@@ -768,11 +781,12 @@ __global__ void __launch_bounds__(THREADS, 1) latent_decode_tc_kernel(const __gr
           for (int r = 0; r < NR; ++r)
             if (r < R) P.o_lat[((long)b * R + r) * 512 + 128 * q + k] = __float2half_rn(o[r]);
         } else {
-          // kept in L2 for the merge (the cache stream would push them out)
-          float4* dst = reinterpret_cast<float4*>(P.part + (slot * 512 + 128 * q + k) * NR);
+          // row-major, so that a warp's store is one 128-byte line; kept in
+          // L2 for the merge (the cache stream would push them out)
+          float* dst = P.part + slot * NR * 512 + 128 * q + k;
           const uint64_t keep = l2_policy_evict_last();
 #pragma unroll
-          for (int r = 0; r < NR; r += 4) st_global_hint(dst + r / 4, make_float4(o[r], o[r + 1], o[r + 2], o[r + 3]), keep);
+          for (int r = 0; r < NR; ++r) st_global_hint(dst + r * 512, o[r], keep);
         }
       }
       if (k < P.T) {   // visibility of token k over this segment's keys (one interval)
@@ -805,11 +819,10 @@ __global__ void __launch_bounds__(THREADS, 1) latent_decode_tc_kernel(const __gr
 // Grid (block, quarter of the value dims): the segments' partials of each
 // row combined by log-sum-exp in CTA order; a row no segment saw stays
 // exactly zero, a block with no keys is all zero, a block held by one CTA
-// was written directly by it.  Thread i handles value dim 128 * quarter +
-// i % 128 of rows 16 (i / 128) .. + 15 and keeps up to MERGE_LOADS
-// segments' rows in flight (the partials may have left L2: the attention
-// kernel streamed the cache through it after writing them); eight threads
-// derive the weights of each row.
+// was written directly by it.  Thread i handles value dims 128 * quarter +
+// 4 (i % 32) .. + 3 of rows i / 32 + 8 j (j < 4): a warp's load of one
+// row is 512 contiguous bytes; MERGE_LOADS segments' rows are in flight at
+// once.  Eight threads derive the weights of each row.
 constexpr int MERGE_THREADS = 256, MERGE_SPLIT = 4, MERGE_LOADS = 4;
 constexpr int MERGE_SMEM_MAX = 200 * (NR + 3 * NR) * 4;   // up to 200 segments of 32 one-token blocks
 __global__ void __launch_bounds__(MERGE_THREADS, 2) decode_merge_kernel(const __grid_constant__ DecodeParams P) {
@@ -847,36 +860,45 @@ __global__ void __launch_bounds__(MERGE_THREADS, 2) decode_merge_kernel(const __
     if (sl == 0) lse_s[r] = den > 0.f ? mx + log2f(den) : -INFINITY;
   }
   __syncthreads();
-  const int d = 128 * part + tid % 128, r0 = 16 * (tid / 128);
-  float acc[16];
+  const int d = 128 * part + 4 * (tid % 32), r0 = tid / 32;
+  float acc[4][4];
 #pragma unroll
-  for (int r = 0; r < 16; ++r) acc[r] = 0.f;
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
   for (int s0 = 0; s0 < cnt; s0 += MERGE_LOADS) {
     float4 v[MERGE_LOADS][4];
 #pragma unroll
-    for (int j = 0; j < MERGE_LOADS; ++j)
-      if (s0 + j < cnt) {
-        const float4* src = reinterpret_cast<const float4*>(P.part + ((slot0 + s0 + j) * 512 + d) * NR + r0);
+    for (int i = 0; i < MERGE_LOADS; ++i)
+      if (s0 + i < cnt) {
+        const float* src = P.part + ((slot0 + s0 + i) * NR + r0) * 512 + d;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) v[j][i] = src[i];
+        for (int j = 0; j < 4; ++j) v[i][j] = *reinterpret_cast<const float4*>(src + 8 * j * 512);
       }
 #pragma unroll
-    for (int j = 0; j < MERGE_LOADS; ++j)
-      if (s0 + j < cnt) {
-        const float4* w4 = reinterpret_cast<const float4*>(w_s + (s0 + j) * NR + r0);
+    for (int i = 0; i < MERGE_LOADS; ++i)
+      if (s0 + i < cnt) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 w = w4[i];
-          acc[4 * i] = fmaf(w.x, v[j][i].x, acc[4 * i]);
-          acc[4 * i + 1] = fmaf(w.y, v[j][i].y, acc[4 * i + 1]);
-          acc[4 * i + 2] = fmaf(w.z, v[j][i].z, acc[4 * i + 2]);
-          acc[4 * i + 3] = fmaf(w.w, v[j][i].w, acc[4 * i + 3]);
+        for (int j = 0; j < 4; ++j) {
+          const float w = w_s[(s0 + i) * NR + r0 + 8 * j];
+          acc[j][0] = fmaf(w, v[i][j].x, acc[j][0]);
+          acc[j][1] = fmaf(w, v[i][j].y, acc[j][1]);
+          acc[j][2] = fmaf(w, v[i][j].z, acc[j][2]);
+          acc[j][3] = fmaf(w, v[i][j].w, acc[j][3]);
         }
       }
   }
 #pragma unroll
-  for (int r = 0; r < 16; ++r)
-    if (r0 + r < R) P.o_lat[((long)b * R + r0 + r) * 512 + d] = __float2half_rn(acc[r]);
+  for (int j = 0; j < 4; ++j) {
+    const int r = r0 + 8 * j;
+    if (r < R) {
+      const __half2 lo = __floats2half2_rn(acc[j][0], acc[j][1]), hi = __floats2half2_rn(acc[j][2], acc[j][3]);
+      uint2 u;
+      u.x = *reinterpret_cast<const uint32_t*>(&lo);
+      u.y = *reinterpret_cast<const uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(P.o_lat + ((long)b * R + r) * 512 + d) = u;
+    }
+  }
   if (lead && tid < R && P.lse) {
     const float l2 = lse_s[tid];
     P.lse[(long)b * R + tid] = l2 == -INFINITY ? -INFINITY : l2 * 0.6931471805599453f;

@@ -20,7 +20,7 @@ struct DecodeParams {
   int32_t* vis_stats;
   __half* o_lat;      // [rows, 512]
   float* lse;         // [rows] or NULL
-  float* part;        // [slots, 512, 32] normalised partial outputs, value dim major
+  float* part;        // [slots, 32, 512] normalised partial outputs, row major
   float* part_lse;    // [slots, 32] log2-sum-exp of each partial row
   int* part_vis;      // [slots, T, 3]
   int* meta;          // [blocks, 2]: first CTA, segment count
