@@ -105,6 +105,31 @@ template <>
 __device__ __forceinline__ void store16<__nv_bfloat16>(__nv_bfloat16* dst, const float* o) {
   store16_16(dst, o);
 }
+// The same 16 bytes, packed for a shared-memory staging tile.
+template <typename TC> __device__ __forceinline__ uint4 pack16(const float* o) {
+  if constexpr (std::is_same<TC, float>::value) {
+    return make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]), __float_as_uint(o[3]));
+  } else {
+    TC h[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] = from_f32<TC>(o[i]);
+    uint4 u;
+    memcpy(&u, h, 16);
+    return u;
+  }
+}
+// 3-D TMA tile store from shared memory (coordinates innermost first) in the
+// thread's bulk group; the bulk-group waits below order it against the reuse
+// of the staging tile and the kernel's end.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
+               ::"l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(src)) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// at most one committed store group still reading shared memory
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// every committed store group complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 template <int BN, typename TC>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -332,10 +357,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // Persistent form for launches without split-K: one CTA per SM walks the
 // tiles (tile c, c + grid, ...), the ring runs on across tiles, and the
 // accumulator is double-buffered in tensor memory so that the epilogue of
-// one tile (warps 4-7, straight from tensor memory to global memory: a
-// thread holds 32 consecutive columns of its row) runs under the next
-// tile's loads and MMAs.  Same warp roles otherwise: warp 0 streams A, warp
-// 3 B, warp 1 (one lane) issues the MMAs, warp 2 owns tensor memory.
+// one tile (warps 4-7, a thread per row) runs under the next tile's loads
+// and MMAs.  The epilogue stages 128 bytes of each of a warp's 32 rows at a
+// time in shared memory and writes them with one TMA store (whole lines,
+// asynchronous), or, where C's layout does not suit TMA (and for the q_b
+// split), stores from registers.  Same warp roles otherwise: warp 0 streams
+// A, warp 3 B, warp 1 (one lane) issues the MMAs, warp 2 owns tensor memory.
+template <int BN>
+struct PSmem {
+  static constexpr int STG = Smem<BN>::RING + 1024;         // after the ring and the barriers
+  static constexpr int STG_TILE = 32 * 128;                 // a warp's 32 rows x 128 bytes
+  static constexpr int BYTES = 1024 + STG + 4 * 2 * STG_TILE;
+  static_assert(BYTES <= 232448, "shared memory");
+};
 struct PBars {
   uint64_t acc_full[2];    // tile accumulator complete (phase per use of the buffer)
   uint64_t acc_empty[2];   // its epilogue has read it (128 arrivals)
@@ -354,6 +388,7 @@ __device__ __forceinline__ bool pwait(PBars* B, uint64_t* bar, uint32_t parity, 
 template <int BN, typename TC>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, bool tma_store,
                    int M, int N, int K, TC* __restrict__ C, long ldc, long sC,
                    const float* __restrict__ G, long ldg, long sG, bool gate_act, int sig_from,
                    uint32_t idesc, int group_m, int tiles_n, int tiles_m, int batch, QSplit qs,
@@ -477,6 +512,34 @@ gemm_tc_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     pdl_wait();                        // C and the gate belong to the kernels around this one
     const int q = warp % 4, r = q * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    // the gate (W_UV) or the sigmoid of the gate columns (A projection) on
+    // 32 values of row `row` from column n
+    auto epi_math = [&](float* v, int z, int row, int n) {
+      if (G) {
+        // the row's 32 gate values (16-byte loads when the row piece is whole and aligned)
+        const float* g = G + z * sG + (long)row * ldg + n;
+        float gv[32];
+        if (n + 32 <= N && ((uintptr_t)g & 15) == 0) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 t4 = *reinterpret_cast<const float4*>(g + i);
+            gv[i] = t4.x; gv[i + 1] = t4.y; gv[i + 2] = t4.z; gv[i + 3] = t4.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) gv[i] = n + i < N ? g[i] : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = gate_act ? v[i] * gv[i] : v[i] / (1.f + expf(-gv[i]));
+      }
+      if (sig_from >= 0) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (n + i >= sig_from) v[i] = 1.f / (1.f + expf(-v[i]));
+      }
+    };
+    uint8_t* stg_warp = smem + PSmem<BN>::STG + q * 2 * PSmem<BN>::STG_TILE;
+    int sbuf = 0;
     int j = 0;
     for (long t = blockIdx.x; t < total; t += gridDim.x, ++j) {
       const int buf = j & 1;
@@ -543,34 +606,48 @@ gemm_tc_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         mbar_arrive(&PB->acc_empty[buf]);
         continue;
       }
+      if (tma_store) {
+        // staged: 128 bytes of each of the warp's rows per chunk into a
+        // double-buffered 4 KB tile (128-byte swizzle: 16-byte piece p of row
+        // l at p ^ (l % 8), conflict-free stores), written by one TMA store;
+        // rows and columns past M and N are clipped by the store
+        constexpr int CW = 128 / (int)sizeof(TC), VALS = 16 / (int)sizeof(TC);
+        const bool in = ok && row < M;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += CW) {
+          uint8_t* stg = stg_warp + sbuf * PSmem<BN>::STG_TILE;
+          if (lane == 0) bulk_wait_read1();     // the store that last read this tile is done with it
+          __syncwarp();
+#pragma unroll
+          for (int h = 0; h < CW; h += 32) {
+            float v[32];
+            tmem_ld32(tmem + buf * ACC_COLS + lane_addr + c0 + h, v);
+            if (in && n0 + c0 + h < N) epi_math(v, z, row, n0 + c0 + h);
+#pragma unroll
+            for (int k = 0; k < 32 / VALS; ++k) {
+              const int piece = h * (int)sizeof(TC) / 16 + k;
+              *reinterpret_cast<uint4*>(stg + lane * 128 + ((piece ^ (lane & 7)) << 4)) = pack16<TC>(v + k * VALS);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && ok) {
+            tma_store_3d(&tmC, stg, n0 + c0, m0 + 32 * q, z);
+            bulk_commit();
+          }
+          sbuf ^= 1;
+        }
+        tc_fence_before();
+        mbar_arrive(&PB->acc_empty[buf]);
+        continue;
+      }
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         float v[32];
         tmem_ld32(tmem + buf * ACC_COLS + lane_addr + c, v);
         const int n = n0 + c;
         if (!ok || row >= M || n >= N) continue;
-        if (G) {
-          // the row's 32 gate values (16-byte loads when the row piece is whole and aligned)
-          const float* g = G + z * sG + (long)row * ldg + n;
-          float gv[32];
-          if (n + 32 <= N && ((uintptr_t)g & 15) == 0) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              const float4 t = *reinterpret_cast<const float4*>(g + i);
-              gv[i] = t.x; gv[i + 1] = t.y; gv[i + 2] = t.z; gv[i + 3] = t.w;
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) gv[i] = n + i < N ? g[i] : 0.f;
-          }
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = gate_act ? v[i] * gv[i] : v[i] / (1.f + expf(-gv[i]));
-        }
-        if (sig_from >= 0) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (n + i >= sig_from) v[i] = 1.f / (1.f + expf(-v[i]));
-        }
+        epi_math(v, z, row, n);
         TC* dst = C + z * sC + (long)row * ldc + n;
         constexpr int VALS = 16 / (int)sizeof(TC);
         if (n + 32 <= N) {
@@ -585,6 +662,8 @@ gemm_tc_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
       tc_fence_before();
       mbar_arrive(&PB->acc_empty[buf]);
     }
+    if (tma_store && lane == 0) bulk_wait_all();   // the stores are complete before the CTA ends
+    __syncwarp();
   }
   pdl_wait();
   __syncwarp();
@@ -647,6 +726,27 @@ bool make_operand_map(CUtensorMap* m, bool fp16, const void* base, long rows, lo
   return encode(m, fp16, base, 4, dims, strides, box);
 }
 
+// C [batch][M][N] of TC (row stride ldc, batch stride sC elements) as a
+// 3-D store map {N, M, batch}, box 128 bytes x 32 rows, 128-byte swizzle;
+// false when C's base or strides are not 16-byte multiples (TMA's rule).
+template <typename TC>
+bool make_store_map(CUtensorMap* m, const void* C, long M, long N, long ldc, long sC, int batch) {
+  constexpr long es = sizeof(TC);
+  if ((uintptr_t)C % 16 || (ldc * es) % 16 || (batch > 1 && (sC * es) % 16)) return false;
+  EncodeFn enc = encode_fn();
+  if (!enc) return false;
+  const CUtensorMapDataType dt = std::is_same<TC, float>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : std::is_same<TC, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)batch};
+  cuuint64_t strides[2] = {(cuuint64_t)(ldc * es), (cuuint64_t)((batch > 1 ? sC : ldc * M) * es)};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / es), 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, dt, 3, const_cast<void*>(C), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int num_sms_current();
 
 template <int BN, typename TC>
@@ -675,10 +775,12 @@ mla_status_t launch(cudaStream_t st, const GemmArgs& a, int splitk, uint32_t* st
     auto pk = gemm_tc_persistent<BN, TC>;
     static std::once_flag once_p;
     std::call_once(once_p, [&] {
-      cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
+      cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, PSmem<BN>::BYTES);
     });
-    Launch P(dim3((unsigned)num_sms_current()), dim3(THREADS), S::BYTES, st, a.pdl);
-    const cudaError_t ep = cudaLaunchKernelEx(&P.cfg, pk, ta, tb, a.M, a.N, a.K, (TC*)a.C, a.ldc, a.sC,
+    CUtensorMap tc{};
+    const bool tma_store = !a.qsplit && make_store_map<TC>(&tc, a.C, a.M, a.N, a.ldc, a.sC, a.batch);
+    Launch P(dim3((unsigned)num_sms_current()), dim3(THREADS), PSmem<BN>::BYTES, st, a.pdl);
+    const cudaError_t ep = cudaLaunchKernelEx(&P.cfg, pk, ta, tb, tc, tma_store, a.M, a.N, a.K, (TC*)a.C, a.ldc, a.sC,
                                               a.G, a.ldg, a.sG, a.gate_act, a.sig_from,
                                               idesc_f16(BM, BN, a.fp16), group_m, tiles_n, tiles_m,
                                               a.batch, a.qsplit ? *a.qsplit : QSplit{}, status);
