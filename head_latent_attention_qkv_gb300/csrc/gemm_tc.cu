@@ -42,10 +42,16 @@ template <int BN> struct Cfg;
 template <> struct Cfg<64> { static constexpr int KBS = 4, STAGES = 2; };
 template <> struct Cfg<128> { static constexpr int KBS = 2, STAGES = 3; };
 template <> struct Cfg<256> { static constexpr int KBS = 2, STAGES = 2; };
+// the persistent form: the same ring in more, smaller stages, so that more of
+// it is in flight while the MMAs read one stage (its tiles run long K loops)
+template <int BN> struct PCfg;
+template <> struct PCfg<64> { static constexpr int KBS = 2, STAGES = 4; };
+template <> struct PCfg<128> { static constexpr int KBS = 1, STAGES = 6; };
+template <> struct PCfg<256> { static constexpr int KBS = 1, STAGES = 4; };
 
-template <int BN>
+template <int BN, typename CF = Cfg<BN>>
 struct Smem {
-  static constexpr int KBS = Cfg<BN>::KBS, STAGES = Cfg<BN>::STAGES;
+  static constexpr int KBS = CF::KBS, STAGES = CF::STAGES;
   static constexpr int A_BYTES = KBS * BM * BK * 2;
   static constexpr int B_BYTES = KBS * BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -365,7 +371,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // A, warp 3 B, warp 1 (one lane) issues the MMAs, warp 2 owns tensor memory.
 template <int BN>
 struct PSmem {
-  static constexpr int STG = Smem<BN>::RING + 1024;         // after the ring and the barriers
+  static constexpr int STG = Smem<BN, PCfg<BN>>::RING + 1024;   // after the ring and the barriers
   static constexpr int STG_TILE = 32 * 128;                 // a warp's 32 rows x 128 bytes
   static constexpr int BYTES = 1024 + STG + 4 * 2 * STG_TILE;
   static_assert(BYTES <= 232448, "shared memory");
@@ -393,7 +399,7 @@ gemm_tc_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                    const float* __restrict__ G, long ldg, long sG, bool gate_act, int sig_from,
                    uint32_t idesc, int group_m, int tiles_n, int tiles_m, int batch, QSplit qs,
                    uint32_t* status) {
-  using S = Smem<BN>;
+  using S = Smem<BN, PCfg<BN>>;
   constexpr int KBS = S::KBS, STAGES = S::STAGES;
   constexpr uint32_t ACC_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
   constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
@@ -777,10 +783,14 @@ mla_status_t launch(cudaStream_t st, const GemmArgs& a, int splitk, uint32_t* st
     std::call_once(once_p, [&] {
       cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, PSmem<BN>::BYTES);
     });
-    CUtensorMap tc{};
+    CUtensorMap tc{}, tpa, tpb;
     const bool tma_store = !a.qsplit && make_store_map<TC>(&tc, a.C, a.M, a.N, a.ldc, a.sC, a.batch);
+    constexpr int PK = Smem<BN, PCfg<BN>>::KBS;
+    if (!make_operand_map(&tpa, a.fp16, a.A, a.M, a.K, a.lda, a.sA, a.batch, BM, PK) ||
+        !make_operand_map(&tpb, a.fp16, a.B, a.N, a.K, a.ldb, a.sB, a.batch, BN, PK))
+      return fail(MLA_ERR_CUDA, "tcgen05 gemm: cuTensorMapEncodeTiled failed");
     Launch P(dim3((unsigned)num_sms_current()), dim3(THREADS), PSmem<BN>::BYTES, st, a.pdl);
-    const cudaError_t ep = cudaLaunchKernelEx(&P.cfg, pk, ta, tb, tc, tma_store, a.M, a.N, a.K, (TC*)a.C, a.ldc, a.sC,
+    const cudaError_t ep = cudaLaunchKernelEx(&P.cfg, pk, tpa, tpb, tc, tma_store, a.M, a.N, a.K, (TC*)a.C, a.ldc, a.sC,
                                               a.G, a.ldg, a.sG, a.gate_act, a.sig_from,
                                               idesc_f16(BM, BN, a.fp16), group_m, tiles_n, tiles_m,
                                               a.batch, a.qsplit ? *a.qsplit : QSplit{}, status);
