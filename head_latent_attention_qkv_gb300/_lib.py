@@ -42,6 +42,11 @@ class mla_attn_desc_t(C.Structure):
                 ("window", C.c_void_p), ("q_visible", C.c_void_p), ("vis_stats", C.c_void_p)]
 
 
+class mla_shared_ctx_t(C.Structure):
+    _fields_ = [("num_ctx", C.c_int32), ("ctx_rows", C.c_int32), ("ctx_len", C.c_void_p),
+                ("ctx_block_start", C.c_void_p)]
+
+
 class MLAError(RuntimeError):
     def __init__(self, status: int, where: str, msg: str):
         super().__init__(f"{where}: status {status}: {msg}")
@@ -67,6 +72,9 @@ def _load():
         "mla_draft_forward": (I32, [P, P, P, P, P, I32, C.POINTER(mla_attn_desc_t), P, P, SZ, P]),
         "mla_draft_forward_after": (I32, [P, P, P, P, P, I32, C.POINTER(mla_attn_desc_t), P, P, SZ,
                                           P, P]),
+        "mla_forward_shared_workspace_bytes": (SZ, [P, I32, I32]),
+        "mla_draft_forward_shared": (I32, [P, P, P, P, P, I32, C.POINTER(mla_attn_desc_t),
+                                           C.POINTER(mla_shared_ctx_t), P, P, SZ, P]),
         "mla_get_device_status": (I32, [P, P, C.POINTER(I32)]),
         "mla_draft_destroy": (None, [P]),
         "mla_kernel_launches": (C.c_ulonglong, [P]),

@@ -115,6 +115,30 @@ def mla_draft_forward(h: Handle, hidden, positions, block_slot_mapping, cache, d
     return out
 
 
+def make_shared_ctx(ctx_len, ctx_block_start, ctx_rows):
+    """Context list for mla_draft_forward_shared: device int32 ``ctx_len``
+    [num_ctx] and ``ctx_block_start`` [num_ctx + 1]; ``ctx_rows`` (host int)
+    is the sum of ``ctx_len``."""
+    return _lib.mla_shared_ctx_t(num_ctx=ctx_len.shape[0], ctx_rows=int(ctx_rows),
+                                 ctx_len=ctx_len.data_ptr(), ctx_block_start=ctx_block_start.data_ptr())
+
+
+def mla_draft_forward_shared(h: Handle, hidden, positions, block_slot_mapping, cache, desc, ctx,
+                             out=None, stream=None, workspace=None):
+    """mla_draft_forward for blocks that share contexts (``ctx`` from
+    make_shared_ctx): the expanded form where the layer allows it."""
+    M = desc.num_blocks * desc.block_len
+    if out is None:
+        out = torch.empty(M, h.dims.hidden_size, dtype=torch_dtype(h.dims), device=h.device)
+    need = lib.mla_forward_shared_workspace_bytes(h.h, M, ctx.ctx_rows)
+    ws = workspace if workspace is not None else h.workspace(need)
+    check(lib.mla_draft_forward_shared(h.h, _ptr(hidden), _ptr(positions), _ptr(block_slot_mapping),
+                                       _ptr(cache), cache.shape[0], C.byref(desc), C.byref(ctx),
+                                       _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+          "mla_draft_forward_shared")
+    return out
+
+
 def mla_draft_forward_after(h: Handle, hidden, positions, block_slot_mapping, cache, desc,
                             cache_ready=None, out=None, stream=None, workspace=None):
     """mla_draft_forward whose attention waits for ``cache_ready`` (a

@@ -11,6 +11,7 @@
 #include "append_tc.cuh"
 #include "attn_tc.cuh"
 #include "decode_tc.cuh"
+#include "expand_tc.cuh"
 #include "gemm_tc.cuh"
 #include "simt.cuh"
 
@@ -32,7 +33,8 @@ mla_status_t cuda_fail(cudaError_t e, const char* what) {
 
 // Arena layout: W_A [NA, D] (rows [kv | q | gate]), W_qb [H*dqk, rq],
 // gamma_q fp32 [rq], gamma_kv fp32 [rkv], W_UK^T [H, rkv, dn],
-// W_UV [H, dv, rkv], W_o [D, H*dv], rope float2 [max_pos, dr/2], status.
+// W_UV [H, dv, rkv], W_o [D, H*dv], kv_b_proj [H*(dn+dv), rkv] (the expanded
+// form's K/V expansion, layer dtype), rope float2 [max_pos, dr/2], status.
 bool make_layout(const mla_config_t& c, Layout* out) {
   Layout l;
   l.D = c.hidden_size; l.H = c.num_heads; l.rq = c.q_lora_rank; l.rkv = c.kv_lora_rank;
@@ -56,6 +58,7 @@ bool make_layout(const mla_config_t& c, Layout* out) {
   l.off_WUKT = o; o = align256(o + (size_t)l.H * l.rkv * l.dn * l.elt);
   l.off_WUV = o;  o = align256(o + (size_t)l.H * l.dv * l.rkv * l.elt);
   l.off_Wo = o;   o = align256(o + (size_t)l.D * l.H * l.dv * l.elt);
+  l.off_WKV = o;  o = align256(o + (size_t)l.H * (l.dn + l.dv) * l.rkv * l.elt);
   l.off_rope = o; o = align256(o + (size_t)c.max_position * (l.dr / 2) * sizeof(float2));
   l.off_status = o; o = align256(o + 256);
   l.total = o;
@@ -167,6 +170,8 @@ void relayout_weights(const Layout& l, const mla_weights_t& w, char* a, cudaStre
                                               l.dn, l.dv, l.rkv);
   convert_kernel<TI, TO><<<G, B, 0, st>>>((const TI*)w.o_proj, (TO*)(a + l.off_Wo),
                                           (long)l.D * l.H * l.dv);
+  convert_kernel<TI, TI><<<G, B, 0, st>>>((const TI*)w.kv_b_proj, (TI*)(a + l.off_WKV),
+                                          (long)l.H * (l.dn + l.dv) * l.rkv);
 }
 
 mla_status_t validate(const mla_config_t& c, const mla_weights_t& w, Layout* l) {
@@ -234,7 +239,7 @@ extern "C" mla_status_t mla_draft_init(const mla_config_t* cfg, const mla_weight
   h->scale = cfg->softmax_scale > 0 ? (float)cfg->softmax_scale : (float)(1.0 / sqrt((double)l.dqk));
   char* a = h->arena;
   h->WA = a + l.off_WA; h->Wqb = a + l.off_Wqb; h->WUKT = a + l.off_WUKT; h->WUV = a + l.off_WUV;
-  h->Wo = a + l.off_Wo; h->gamma_q = (float*)(a + l.off_gq); h->gamma_kv = (float*)(a + l.off_gkv);
+  h->Wo = a + l.off_Wo; h->WKV = a + l.off_WKV; h->gamma_q = (float*)(a + l.off_gq); h->gamma_kv = (float*)(a + l.off_gkv);
   h->rope = (float2*)(a + l.off_rope); h->status = (uint32_t*)(a + l.off_status);
   const size_t e = l.elt, rowb = (size_t)l.D * e;
   char* WA = a + l.off_WA;
@@ -331,6 +336,31 @@ extern "C" size_t mla_forward_workspace_bytes(const mla_handle_t* h, int32_t num
   return (h && num_tokens >= 0) ? forward_ws(h, num_tokens).total : 0;
 }
 
+namespace mla {
+namespace {
+// The expanded form's pieces after the forward's own: the gathered latent
+// rows [rows, L] (layer dtype) and their expansion [rows, H, dn + dv] (fp16).
+struct SharedWs {
+  size_t gathered, kv, total;
+};
+SharedWs shared_ws(const mla_handle* h, long num_tokens, long ctx_rows) {
+  const Layout& l = h->lay;
+  const long rows = ctx_rows + num_tokens;
+  SharedWs w;
+  size_t o = forward_ws(h, num_tokens).total;
+  w.gathered = o; o = align256(o + (size_t)rows * l.L * l.elt);
+  w.kv = o;       o = align256(o + (size_t)rows * l.H * (l.dn + l.dv) * 2);
+  w.total = o;
+  return w;
+}
+}  // namespace
+}  // namespace mla
+
+extern "C" size_t mla_forward_shared_workspace_bytes(const mla_handle_t* h, int32_t num_tokens,
+                                                     int32_t ctx_rows) {
+  return (h && num_tokens >= 0 && ctx_rows >= 0) ? shared_ws(h, num_tokens, ctx_rows).total : 0;
+}
+
 // ---------------------------------------------------------------------------
 // Projections: tcgen05 GEMM for 16-bit operands, SIMT for the fp32 layer
 // ---------------------------------------------------------------------------
@@ -425,7 +455,7 @@ namespace {
 template <typename TX, typename TI>
 mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* pos, const int64_t* bslots,
                   void* cache, int num_pages, const mla_attn_desc_t& d, void* out, char* ws,
-                  cudaStream_t st, cudaEvent_t kv_ready) {
+                  cudaStream_t st, cudaEvent_t kv_ready, const mla_shared_ctx_t* ctx = nullptr) {
   const Layout& l = h->lay;
   const int M = d.num_blocks * d.block_len;
   const FwdWs w = forward_ws(h, M);
@@ -489,6 +519,34 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
     ldq = l.NA;
   }
   if (!split_done) simt::q_rope_split<TI, TX>(st, h, q_raw, ldq, M, pos, q_nope, q_abs, pdl);
+  if constexpr (kBf16) {
+    if (ctx && tc::expand_applies(h, d.block_len)) {
+      // blocks sharing contexts, the expanded form: each context's latents and
+      // each block's own gathered once, expanded by kv_b_proj into per-head
+      // k_nope | v, then one attention of q_nope | q_pe over them (its output
+      // already o[h], times the gate); no W_UK / W_UV absorption
+      if (kv_ready) MLA_CUDA_TRY(cudaStreamWaitEvent(st, kv_ready, 0));
+      const SharedWs sw = shared_ws(h, M, ctx->ctx_rows);
+      const long rows = tc::expand_rows(*ctx, d.num_blocks, d.block_len);
+      TX* gathered = (TX*)(ws + sw.gathered);
+      __half* kvx = (__half*)(ws + sw.kv);
+      tc::expand_gather(st, h, (const TX*)cache, num_pages, d, *ctx, gathered, pdl && !kv_ready);
+      s = proj<TX, TI>(h, st, pdl, rows, l.H * (l.dn + l.dv), l.rkv, 1, gathered, l.L, 0,
+                       (const TX*)h->WKV, l.rkv, 0, (TI*)kvx, (long)l.H * (l.dn + l.dv), 0);
+      if (s != MLA_OK) return s;
+      TI* o = (TI*)(ws + w.o);
+      const float* gate = l.gdim ? a_out + l.L + l.qdim : nullptr;
+      s = tc::expanded_attention(st, h, (const __half*)q_nope, (const __nv_bfloat16*)q_abs, kvx,
+                                 gathered, rows, d, *ctx, pos, gate, l.NA, (__half*)o, pdl);
+      if (s != MLA_OK) return s;
+      s = proj<TI, TX>(h, st, pdl, M, l.D, l.H * l.dv, 1, o, (long)l.H * l.dv, 0, (const TI*)h->Wo,
+                       (long)l.H * l.dv, 0, (TX*)out, l.D, 0);
+      if (s != MLA_OK) return s;
+      // non-GEMM kernels: [kv finish], [q norm], [rope split], gather, attention
+      h->launches += (split_done ? 2 : 3) + (bslots ? 1 : 0) + (l.rq > 0 ? 1 : 0);
+      return MLA_OK;
+    }
+  }
   // q_lat[h] = q_nope[h] @ W_UK[h]  ->  Q_abs[:, h, :rkv]
   s = proj<TI, TX>(h, st, pdl, M, l.rkv, l.dn, l.H, q_nope, (long)l.H * l.dn, l.dn,
                    (const TI*)h->WUKT, l.dn, (long)l.rkv * l.dn, q_abs, (long)l.H * l.L, l.L);
@@ -558,6 +616,41 @@ extern "C" mla_status_t mla_draft_forward_after(mla_handle_t* h, const void* hid
                                                 num_pages, d, out, (char*)workspace, st, ev)
           : forward_impl<float, float>(h, hidden, positions, block_slot_mapping, cache,
                                        num_pages, d, out, (char*)workspace, st, ev);
+  if (s != MLA_OK) return s;
+  MLA_CUDA_TRY(cudaGetLastError());
+  return MLA_OK;
+}
+
+extern "C" mla_status_t mla_draft_forward_shared(mla_handle_t* h, const void* hidden,
+                                                 const int32_t* positions,
+                                                 const int64_t* block_slot_mapping, void* cache,
+                                                 int32_t num_pages, const mla_attn_desc_t* desc,
+                                                 const mla_shared_ctx_t* ctx, void* out,
+                                                 void* workspace, size_t workspace_bytes,
+                                                 void* stream) {
+  if (!h || !desc || !ctx) return fail(MLA_ERR_INVALID_ARG, "forward_shared: null handle, descriptor or context list");
+  const mla_attn_desc_t& d = *desc;
+  if (d.num_blocks < 0 || d.block_len <= 0 || d.max_pages <= 0)
+    return fail(MLA_ERR_INVALID_ARG, "forward_shared: num_blocks >= 0, block_len > 0, max_pages > 0");
+  if (d.num_blocks == 0) return MLA_OK;
+  if (ctx->num_ctx <= 0 || ctx->ctx_rows < 0 || !ctx->ctx_len || !ctx->ctx_block_start)
+    return fail(MLA_ERR_INVALID_ARG, "forward_shared: num_ctx > 0, ctx_rows >= 0, ctx_len and ctx_block_start set");
+  if ((long)d.num_blocks * d.block_len + ctx->ctx_rows > 0x7fffffffL)
+    return fail(MLA_ERR_INVALID_ARG, "forward_shared: too many tokens");
+  if (!hidden || !positions || !cache || !out || !workspace || !d.block_table || !d.kv_len)
+    return fail(MLA_ERR_INVALID_ARG, "forward_shared: null pointer");
+  if (num_pages <= 0) return fail(MLA_ERR_INVALID_ARG, "forward_shared: num_pages <= 0");
+  const int M = d.num_blocks * d.block_len;
+  if (workspace_bytes < shared_ws(h, M, ctx->ctx_rows).total)
+    return fail(MLA_ERR_INVALID_ARG, "forward_shared: workspace smaller than mla_forward_shared_workspace_bytes()");
+  if ((uintptr_t)workspace % 256) return fail(MLA_ERR_INVALID_ARG, "forward_shared: workspace must be 256-byte aligned");
+  cudaStream_t st = (cudaStream_t)stream;
+  const mla_status_t s =
+      h->cfg.dtype == MLA_BF16
+          ? forward_impl<__nv_bfloat16, __half>(h, hidden, positions, block_slot_mapping, cache,
+                                                num_pages, d, out, (char*)workspace, st, nullptr, ctx)
+          : forward_impl<float, float>(h, hidden, positions, block_slot_mapping, cache,
+                                       num_pages, d, out, (char*)workspace, st, nullptr);
   if (s != MLA_OK) return s;
   MLA_CUDA_TRY(cudaGetLastError());
   return MLA_OK;

@@ -59,7 +59,7 @@ struct Layout {
   int NA;          // rows of W_A: L + qdim + gdim, ordered [kv | q | gate]
   size_t elt;      // bytes per element of the configured dtype
   // byte offsets inside the arena
-  size_t off_WA, off_Wqb, off_gq, off_gkv, off_WUKT, off_WUV, off_Wo, off_rope, off_status, total;
+  size_t off_WA, off_Wqb, off_gq, off_gkv, off_WUKT, off_WUV, off_Wo, off_WKV, off_rope, off_status, total;
 };
 
 bool make_layout(const mla_config_t& c, Layout* out);
@@ -116,5 +116,6 @@ struct mla_handle {
   const void* WUKT;     // [H, rkv, dn]
   const void* WUV;      // [H, dv, rkv]
   const void* Wo;
+  const void* WKV;       // [H * (dn + dv), rkv] in the layer dtype: kv_b_proj (the expanded form)
   unsigned long long launches;  // kernels enqueued through this handle
 };

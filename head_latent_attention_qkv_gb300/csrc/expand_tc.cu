@@ -1,0 +1,497 @@
+// Expanded-form attention of the MLA draft layer for blocks that share a
+// context ("MLA (Multi-Head Latent Attention)" blog, forward_impl: the
+// prefill path, forward_mha, whose context keys come from the cache through
+// kv_b_proj, _compute_prefill_context, and whose new tokens attend
+// themselves, _run_prefill_new_tokens; the two merged by log-sum-exp,
+// merge_attn_states).
+//
+// When thousands of query rows meet one cached context, the absorbed form
+// pays 2 * (576 + 512) flop per key and row; the expanded form 2 * (192 +
+// 128), after kv_b_proj expands each context latent once into per-head
+// k_nope and v.  Here a context's keys and each block's own keys are
+// gathered into dense rows, expanded by one GEMM (kv_b_proj, [k_nope | v]
+// per head, fp16), and one kernel runs per (up to 128 / block_len blocks of
+// a context, head): 128 query rows against the context's key tiles and then
+// one more tile holding the blocks' own keys, masked so that each block sees
+// its own (a block-diagonal tile).  One online softmax covers both, which is
+// the log-sum-exp merge of the two parts done in place.
+//
+//   S = [q_nope | q_pe] [k_nope | k_pe]^T   (M = 128 rows, N = 128 keys,
+//        K = 128 fp16 + 64 bf16: 8 + 4 MMAs)
+//   O += P V                                (N = 128 value dims, K = 128
+//        keys: 8 MMAs, P fp16 from tensor memory)
+// O is 128 fp32 columns, so S is double-buffered in tensor memory and the
+// scores of tile t + 1 are computed while the softmax of tile t runs.
+//   warps 0-3, 8-11: softmax, two threads per row (64 keys each), half
+//                    maxima exchanged through shared memory; epilogue
+//   warp 4         : Q and the key/value tiles (TMA, two slots)
+//   warp 5         : tensor-memory allocation, MMA issue
+#include "expand_tc.cuh"
+
+#include <mutex>
+
+#include "gemm_tc.cuh"
+#include "tc_ptx.cuh"
+
+namespace mla {
+namespace tc {
+namespace {
+
+constexpr int QROWS = 128, KT = 128;
+constexpr int THREADS = 384;
+constexpr int CH = 128 * 64 * 2;                 // one 16 KiB chunk: 128 rows x 64 16-bit values
+constexpr int OFF_Q = 0;                          // q_nope (2 chunks, fp16), q_pe (bf16)
+constexpr int OFF_RING = OFF_Q + 3 * CH;          // 2 slots: k_nope (2), k_pe, v (2)
+constexpr int SLOT = 5 * CH;
+constexpr int OFF_BAR = OFF_RING + 2 * SLOT;
+constexpr int OFF_XM = OFF_BAR + 256;             // [2][128] half maxima / sums
+constexpr int OFF_RED = OFF_XM + 2 * QROWS * 4;   // [8] per-warp minima of the window starts
+constexpr int SMEM_BYTES = 1024 + OFF_RED + 64;
+constexpr uint32_t TMEM_COLS = 512, TM_O = 0, TM_S = 128;   // O 128 columns; S (and P over it) 2 x 128
+constexpr float RESCALE_LOG2 = 8.f;
+static_assert(SMEM_BYTES <= 232448, "shared memory");
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t full[2], empty[2];   // key/value slot landed / read by its last MMA (by tile parity)
+  uint64_t s_full[2];           // S(t) complete, by t % 2
+  uint64_t p_full[2];           // P(t) in tensor memory (256 arrivals), by t % 2
+  uint64_t o_free[2];           // P(t) V(t) complete, by t % 2
+  uint64_t drain;
+  uint32_t tmem_slot;
+  int abort;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+struct ExpParams {
+  CUtensorMap tmQn, tmQp, tmKV, tmKp;
+  const int32_t* positions;
+  const int32_t* kv_len;
+  const int32_t* window;
+  const uint8_t* q_visible;
+  int32_t* vis_stats;
+  const int32_t* ctx_len;
+  const int32_t* ctx_start;
+  const float* gate;
+  long ld_gate;
+  __half* o;
+  uint32_t* status;
+  int num_ctx, ctx_rows, T, H, bpu;
+  float scale_log2;
+};
+
+__device__ __forceinline__ bool wait_bar(Bars* B, uint64_t* bar, uint32_t parity, uint32_t* st) {
+  if (*(volatile int*)&B->abort) return false;
+  if (mbar_wait(bar, parity, st)) return true;
+  B->abort = 1;
+  return false;
+}
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
+
+// Unit u: blocks b0 .. b0 + nbu - 1 (at most bpu) of context c, whose keys
+// start at row coff of the gathered rows.  False past the last unit.
+__device__ __forceinline__ bool unit_of(const ExpParams& P, int u, int& c, int& b0, int& nbu, int& coff) {
+  int acc = 0;
+  coff = 0;
+  for (int cc = 0; cc < P.num_ctx; ++cc) {
+    const int s = P.ctx_start[cc], e = P.ctx_start[cc + 1];
+    const int n = e > s ? (e - s + P.bpu - 1) / P.bpu : 0;
+    if (u < acc + n) {
+      c = cc;
+      b0 = s + (u - acc) * P.bpu;
+      nbu = min(P.bpu, e - b0);
+      return true;
+    }
+    acc += n;
+    coff += P.ctx_len[cc];
+  }
+  return false;
+}
+
+__global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_constant__ ExpParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  Bars* B = (Bars*)(smem + OFF_BAR);
+  float* xm = (float*)(smem + OFF_XM);
+  int* red = (int*)(smem + OFF_RED);
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int h = blockIdx.y;
+  int c, b0, nbu, coff;
+  if (!unit_of(P, blockIdx.x, c, b0, nbu, coff)) return;       // the grid is an upper bound
+  const int T = P.T, nrows = nbu * T;
+  const long m0 = (long)b0 * T;
+  const int ctx_len = P.ctx_len[c];
+  const long own0 = (long)P.ctx_rows + m0;                      // first gathered row of the blocks' own keys
+
+  if (tid == 0) {
+    mbar_init(&B->q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&B->full[i], 1);
+      mbar_init(&B->empty[i], 1);
+      mbar_init(&B->s_full[i], 1);
+      mbar_init(&B->p_full[i], 2 * QROWS);
+      mbar_init(&B->o_free[i], 1);
+    }
+    mbar_init(&B->drain, 1);
+    B->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) tmem_alloc(&B->tmem_slot, TMEM_COLS);
+  // first context key any row of the unit can see (whole tiles below it are
+  // skipped): the least window start over the unit's rows (0 for a full mask)
+  int lo_r = 0x7fffffff;
+  if (tid < QROWS && tid < nrows) {
+    const int b = b0 + tid / T;
+    const int W = P.window ? P.window[b] : 0;
+    lo_r = W > 0 ? max(0, P.positions[m0 + tid] - W + 1) : 0;
+    if (tid % T == 0 && h == 0) {
+      if (P.kv_len[b] > ctx_len + T || P.kv_len[b] < 0) set_status(P.status, MLA_DEV_BAD_LENGTH);
+      if (W < 0) set_status(P.status, MLA_DEV_BAD_WINDOW);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lo_r = min(lo_r, __shfl_xor_sync(0xffffffffu, lo_r, o));
+  if (lane == 0 && warp < 4) red[warp] = lo_r;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const int lo_min = min(min(red[0], red[1]), min(red[2], red[3]));
+  const int j_lo = lo_min >= ctx_len ? ctx_len / KT * KT : lo_min / KT * KT;
+  const int nt_ctx = ctx_len > j_lo ? (ctx_len - j_lo + KT - 1) / KT : 0;
+  const int nt = nt_ctx + 1;                                     // + the blocks' own keys
+  const uint32_t tmem = B->tmem_slot;
+  if (tid == 0) pdl_trigger();
+
+  if (warp == 4) {
+    if (lane == 0) {
+      // ---- Q, then the key/value tiles through two slots ----
+      prefetch_tmap(&P.tmQn);
+      prefetch_tmap(&P.tmQp);
+      prefetch_tmap(&P.tmKV);
+      prefetch_tmap(&P.tmKp);
+      pdl_wait();
+      mbar_arrive_expect_tx(&B->q_full, 3 * CH);
+      tma_load_3d(smem + OFF_Q, &P.tmQn, &B->q_full, 0, (int)m0, 2 * h);
+      tma_load_3d(smem + OFF_Q + 2 * CH, &P.tmQp, &B->q_full, 0, (int)m0, 9 * h + 8);
+      bool ok = true;
+      for (int t = 0; t < nt && ok; ++t) {
+        const int s = t & 1;
+        if (!(ok = wait_bar(B, &B->empty[s], ((t >> 1) & 1) ^ 1, P.status))) break;
+        const int row = t < nt_ctx ? coff + j_lo + KT * t : (int)own0;
+        uint8_t* slot = smem + OFF_RING + s * SLOT;
+        mbar_arrive_expect_tx(&B->full[s], 5 * CH);
+        tma_load_3d(slot, &P.tmKV, &B->full[s], 0, row, 4 * h);            // k_nope (2 chunks)
+        tma_load_3d(slot + 2 * CH, &P.tmKp, &B->full[s], 0, row, 8);       // k_pe
+        tma_load_3d(slot + 3 * CH, &P.tmKV, &B->full[s], 0, row, 4 * h + 2);  // v (2 chunks)
+      }
+      // every copy into this CTA has landed before it may exit
+      mbar_wait(&B->q_full, 0, P.status);
+      for (int t = max(0, nt - 2); t < nt; ++t) mbar_wait(&B->full[t & 1], (t >> 1) & 1, P.status);
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      // ---- MMA issue: S(t) ahead of P(t - 1) V(t - 1) ----
+      const uint32_t id_s16 = idesc_f16(QROWS, KT, true), id_sbf = idesc_f16(QROWS, KT, false);
+      const uint32_t id_pv = idesc_f16_bmn(QROWS, 128, true);
+      const uint64_t dQ = smem_desc_sw128(smem + OFF_Q);
+      const uint64_t dK0 = smem_desc_sw128(smem + OFF_RING);
+      const uint64_t dV0 = smem_desc_sw128_mn(smem + OFF_RING + 3 * CH, CH);
+      constexpr uint32_t U_CH = CH / 16, U_SLOT = SLOT / 16, U_KSTEP = 16 * 128 / 16;
+      bool ok = wait_bar(B, &B->q_full, 0, P.status);
+      tc_fence_after();
+      for (int t = 0; t <= nt && ok; ++t) {
+        if (t < nt) {
+          const int s = t & 1;
+          // S buffer s: the softmax has written P(t - 2) over it (and P(t - 2)
+          // V(t - 2), issued before by this thread, reads it first)
+          if (t >= 2 && !(ok = wait_bar(B, &B->p_full[s], ((t - 2) >> 1) & 1, P.status))) break;
+          if (!(ok = wait_bar(B, &B->full[s], (t >> 1) & 1, P.status))) break;
+          tc_fence_after();
+          const uint32_t tS = tmem + TM_S + 128 * s;
+          const uint64_t dK = dK0 + s * U_SLOT;
+#pragma unroll
+          for (int ch = 0; ch < 3; ++ch) {
+            const uint32_t id = ch < 2 ? id_s16 : id_sbf;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_f16(tS, dQ + ch * U_CH + 2 * k, dK + ch * U_CH + 2 * k, id, (ch | k) ? 1u : 0u);
+          }
+          mma_commit(&B->s_full[s]);
+        }
+        if (t >= 1) {
+          const int tt = t - 1, s = tt & 1;
+          if (!(ok = wait_bar(B, &B->p_full[s], (tt >> 1) & 1, P.status))) break;
+          tc_fence_after();
+          const uint32_t tP = tmem + TM_S + 128 * s;
+          const uint64_t dV = dV0 + s * U_SLOT;
+#pragma unroll
+          for (int k = 0; k < KT / 16; ++k)   // 16 keys per MMA: 8 P columns, 16 V rows
+            mma_f16_ts(tmem + TM_O, tP + 8 * k, dV + (uint64_t)U_KSTEP * k, id_pv, (tt | k) ? 1u : 0u);
+          mma_commit(&B->empty[s]);
+          mma_commit(&B->o_free[s]);
+        }
+      }
+      mma_commit(&B->drain);
+      mbar_wait(&B->drain, 0, P.status);
+    }
+  } else if (warp < 4 || warp >= 8) {
+    // ---- softmax: row r (TMEM lane r), key columns [64 kh, 64 kh + 64) ----
+    const int r = tid & (QROWS - 1), kh = tid >= 256 ? 1 : 0;
+    constexpr int KH = KT / 2;
+    const uint32_t lane_base = (uint32_t)((r / 32) * 32) << 16;
+    const bool live = r < nrows;
+    const int bi = r / T, b = b0 + min(bi, nbu - 1);
+    const long m = m0 + (live ? r : 0);
+    const int p = P.positions[m];
+    const bool qv = live && (P.q_visible ? P.q_visible[m] != 0 : true);
+    const int W = P.window ? P.window[b] : 0;
+    const int kvl = P.kv_len[b];
+    // visible keys: context keys [vlo, min(ctx_len, kv_len)); own key i (key
+    // ctx_len + i, column bi * T + i of the last tile) for ctx_len + i in
+    // [vlo, kv_len), i < T; none for a masked or padding row or a rejected window
+    const int vlo = W > 0 ? max(0, p - W + 1) : 0;
+    const bool sees = qv && W >= 0;
+    const int ctx_hi = sees ? min(ctx_len, kvl) : 0;
+    const int own_lo = bi * T + max(0, vlo - ctx_len);
+    const int own_hi = sees ? bi * T + min(T, kvl - ctx_len) : 0;
+    float mrun = -INFINITY, lsum = 0.f;
+    for (int t = 0; t < nt; ++t) {
+      const int s = t & 1;
+      float sv[KH];
+      wait_bar(B, &B->s_full[s], (t >> 1) & 1, P.status);
+      tc_fence_after();
+#pragma unroll
+      for (int q = 0; q < KH; q += 32) tmem_ld32_nowait(tmem + TM_S + 128 * s + KH * kh + q + lane_base, sv + q);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q = 0; q < KH; q += 32) tmem_reg_fence32(sv + q);
+      int lo, hi;                                   // visible columns of this tile
+      if (t < nt_ctx) {
+        const int j0 = j_lo + KT * t;
+        lo = max(vlo - j0, 0);
+        hi = min(ctx_hi - j0, KT);
+      } else {
+        lo = own_lo;
+        hi = own_hi;
+      }
+      const int lo_h = lo - KH * kh, hi_h = hi - KH * kh;
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (__all_sync(0xffffffffu, lo_h <= 0 && hi_h >= KH)) {
+#pragma unroll
+        for (int i = 0; i < KH; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], sv[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < KH; ++i) {
+          sv[i] = (i >= lo_h && i < hi_h) ? sv[i] : -INFINITY;
+          mx4[i & 3] = fmaxf(mx4[i & 3], sv[i]);
+        }
+      }
+      const float hmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      xm[kh * QROWS + r] = hmax;
+      softmax_sync();
+      const float tmax = fmaxf(hmax, xm[(1 - kh) * QROWS + r]) * P.scale_log2;
+      softmax_sync();
+      const bool grow = tmax > mrun + RESCALE_LOG2;
+      const float m_new = grow ? tmax : mrun;
+      const float mref = m_new == -INFINITY ? 0.f : m_new;
+      float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < KH; ++i) {
+        sv[i] = fast_exp2(fmaf(sv[i], P.scale_log2, -mref));
+        ps4[i & 3] += sv[i];
+      }
+      const float psum = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+      const float alpha = (grow && mrun != -INFINITY) ? exp2f(mrun - m_new) : 1.f;
+      // P(t - 1) V(t - 1) may still run: a row that grew waits for it, then rescales
+      if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        wait_bar(B, &B->o_free[(t - 1) & 1], ((t - 1) >> 1) & 1, P.status);
+        tc_fence_after();
+#pragma unroll 1
+        for (int q = 64 * kh; q < 64 * kh + 64; q += 32) {
+          float o[32];
+          tmem_ld32(tmem + TM_O + lane_base + q, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(tmem + TM_O + lane_base + q, o);
+        }
+      }
+      lsum = lsum * alpha + psum;
+      mrun = m_new;
+      // P row in fp16 pairs over S (this thread has read its lane): key 2i in
+      // the low half of column i
+      {
+        uint32_t pw[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          __half2 h2 = __floats2half2_rn(sv[2 * i], sv[2 * i + 1]);
+          pw[i] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+        tmem_st32_u(tmem + TM_S + 128 * s + 32 * kh + lane_base, pw);
+      }
+      tc_fence_before();
+      mbar_arrive(&B->p_full[s]);
+    }
+    // visibility statistics of the row's token (head 0): its keys form one
+    // interval, [vlo, kv_len) clamped to the context and its own block_len
+    if (P.vis_stats && h == 0 && kh == 0 && live) {
+      const int hi = sees ? min(kvl, ctx_len + T) : 0;
+      const int n = max(0, hi - vlo);
+      P.vis_stats[m * 3 + 0] = n;
+      P.vis_stats[m * 3 + 1] = n ? vlo : -1;
+      P.vis_stats[m * 3 + 2] = n ? hi - 1 : -1;
+    }
+    // ---- epilogue: O / l (times the gate) -> o[m, h, 64 kh .. 64 kh + 63] ----
+    xm[kh * QROWS + r] = lsum;
+    softmax_sync();
+    lsum += xm[(1 - kh) * QROWS + r];
+    wait_bar(B, &B->o_free[(nt - 1) & 1], ((nt - 1) >> 1) & 1, P.status);
+    tc_fence_after();
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    __half* dst = P.o + (m * P.H + h) * 128 + 64 * kh;
+    const float* g = P.gate ? P.gate + m * P.ld_gate + (long)h * 128 + 64 * kh : nullptr;
+#pragma unroll 1
+    for (int q = 0; q < 64; q += 32) {
+      float o[32];
+      tmem_ld32(tmem + TM_O + lane_base + 64 * kh + q, o);
+      if (live) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) {
+          float v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) v[u] = o[i + u] * inv;
+          if (g) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] *= g[q + i + u];
+          }
+          __half2 h2[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) h2[u] = __floats2half2_rn(v[2 * u], v[2 * u + 1]);
+          *reinterpret_cast<uint4*>(dst + q + i) = *reinterpret_cast<uint4*>(h2);
+        }
+      }
+    }
+  }
+  pdl_wait();        // (a no-op for the threads that waited already)
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// One warp per gathered row: context c's key j (rows [coff_c, coff_c +
+// ctx_len_c), through the table of c's first block), then block b's own key
+// ctx_len + i (rows ctx_rows + b * T + i, zero when past kv_len[b]).
+__global__ void __launch_bounds__(256) expand_gather_kernel(
+    const __nv_bfloat16* __restrict__ cache, long num_slots, const int32_t* __restrict__ block_table,
+    int max_pages, int page_size, const int32_t* __restrict__ kv_len, const int32_t* __restrict__ ctx_len,
+    const int32_t* __restrict__ ctx_start, int num_ctx, int ctx_rows, int nb, int T,
+    __nv_bfloat16* __restrict__ out, uint32_t* status) {
+  const long r = (long)blockIdx.x * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (r >= (long)ctx_rows + (long)nb * T) return;
+  pdl_wait();
+  int b = -1, j = 0;
+  bool zero = false;
+  if (r < ctx_rows) {
+    int acc = 0;
+    for (int c = 0; c < num_ctx; ++c) {
+      if (r < acc + ctx_len[c]) {
+        b = ctx_start[c];
+        j = (int)(r - acc);
+        break;
+      }
+      acc += ctx_len[c];
+    }
+  } else {
+    const long rr = r - ctx_rows;
+    b = (int)(rr / T);
+    const int i = (int)(rr % T);
+    int c = 0;
+    while (c + 1 < num_ctx && ctx_start[c + 1] <= b) ++c;
+    j = ctx_len[c] + i;
+    zero = j >= kv_len[b];
+  }
+  uint4* dst = reinterpret_cast<uint4*>(out + r * 576);
+  long slot = -1;
+  if (b >= 0 && !zero && j / page_size < max_pages) {
+    const int pg = block_table[(long)b * max_pages + j / page_size];
+    const long sl = (long)pg * page_size + j % page_size;
+    if (pg >= 0 && sl < num_slots) slot = sl;
+  }
+  if (slot < 0 && !zero && lane == 0) set_status(status, MLA_DEV_BAD_PAGE);
+  const uint4* src = reinterpret_cast<const uint4*>(cache + (slot < 0 ? 0 : slot) * 576);
+  for (int i = lane; i < 72; i += 32) dst[i] = slot < 0 ? make_uint4(0, 0, 0, 0) : src[i];
+}
+
+}  // namespace
+
+bool expand_applies(const mla_handle* h, int block_len) {
+  const Layout& l = h->lay;
+  return h->cfg.dtype == MLA_BF16 && l.rkv == 512 && l.dr == 64 && l.dn == 128 && l.dv == 128 &&
+         block_len >= 1 && block_len <= QROWS;
+}
+
+void expand_gather(cudaStream_t st, const mla_handle* h, const __nv_bfloat16* cache, int num_pages,
+                   const mla_attn_desc_t& d, const mla_shared_ctx_t& ctx, __nv_bfloat16* out, bool pdl) {
+  const long rows = expand_rows(ctx, d.num_blocks, d.block_len);
+  Launch L(dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, st, pdl);
+  cudaLaunchKernelEx(&L.cfg, expand_gather_kernel, cache, (long)num_pages * h->cfg.page_size,
+                     d.block_table, (int)d.max_pages, (int)h->cfg.page_size, d.kv_len, ctx.ctx_len,
+                     ctx.ctx_block_start, (int)ctx.num_ctx, (int)ctx.ctx_rows, (int)d.num_blocks,
+                     (int)d.block_len, out, h->status);
+}
+
+mla_status_t expanded_attention(cudaStream_t st, const mla_handle* h, const __half* q_nope,
+                                const __nv_bfloat16* q_abs, const __half* kv,
+                                const __nv_bfloat16* gathered, long rows, const mla_attn_desc_t& d,
+                                const mla_shared_ctx_t& ctx, const int32_t* positions,
+                                const float* gate, long ld_gate, __half* o, bool pdl) {
+  const Layout& l = h->lay;
+  if (!expand_applies(h, d.block_len))
+    return fail(MLA_ERR_UNSUPPORTED, "expanded attention: needs bf16, kv_lora_rank 512, qk_rope 64, "
+                                     "qk_nope 128, v_head 128, block_len <= 128");
+  if (d.num_blocks <= 0 || ctx.num_ctx <= 0) return MLA_OK;
+  const long M = (long)d.num_blocks * d.block_len;
+  ExpParams P;
+  if (!make_tmap_chunked(&P.tmQn, true, q_nope, M, (long)l.H * 128, (long)l.H * 128, QROWS, 2) ||
+      !make_tmap_chunked(&P.tmQp, false, q_abs, M, (long)l.H * l.L, (long)l.H * l.L, QROWS, 1) ||
+      !make_tmap_chunked(&P.tmKV, true, kv, rows, (long)l.H * 256, (long)l.H * 256, KT, 2) ||
+      !make_tmap_chunked(&P.tmKp, false, gathered, rows, l.L, l.L, KT, 1))
+    return fail(MLA_ERR_CUDA, "expanded attention: cuTensorMapEncodeTiled failed");
+  P.positions = positions;
+  P.kv_len = d.kv_len;
+  P.window = d.window;
+  P.q_visible = d.q_visible;
+  P.vis_stats = d.vis_stats;
+  P.ctx_len = ctx.ctx_len;
+  P.ctx_start = ctx.ctx_block_start;
+  P.gate = gate;
+  P.ld_gate = ld_gate;
+  P.o = o;
+  P.status = h->status;
+  P.num_ctx = ctx.num_ctx;
+  P.ctx_rows = ctx.ctx_rows;
+  P.T = d.block_len;
+  P.H = l.H;
+  P.bpu = QROWS / d.block_len;
+  P.scale_log2 = h->scale * 1.4426950408889634f;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(expand_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  });
+  // units: each context's blocks in groups of bpu (at most one partial group per context)
+  const long units = (d.num_blocks + P.bpu - 1) / P.bpu + ctx.num_ctx;
+  Launch L(dim3((unsigned)units, (unsigned)l.H), dim3(THREADS), SMEM_BYTES, st, pdl);
+  const cudaError_t e = cudaLaunchKernelEx(&L.cfg, expand_attn_kernel, P);
+  if (e != cudaSuccess) return cuda_fail(e, "expanded attention launch");
+  return MLA_OK;
+}
+
+}  // namespace tc
+}  // namespace mla

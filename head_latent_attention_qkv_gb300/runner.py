@@ -3,7 +3,10 @@
 Uploads the seeded inputs of ``workloads.Workload`` to the GPU, then runs the
 call sequence: prefilled cache entries are copied in, context tokens are
 appended with ``mla_latent_cache_append``, and every step appends its tokens
-(if any) and calls ``mla_draft_forward``.  ``run_step_after`` issues a step's
+(if any) and calls ``mla_draft_forward`` -- or, when its blocks come in
+groups that share one context (consecutive blocks, at least two per
+context, each seeing its context and then its own block_len keys),
+``mla_draft_forward_shared`` with that context list.  ``run_step_after`` issues a step's
 cache appends on a second stream instead, so that the forward's projections
 run beside them and only its attention waits (``mla_draft_forward_after``).
 Only data movement happens here; all of the layer's arithmetic runs in the
@@ -15,6 +18,25 @@ import numpy as np
 import torch
 
 from . import api
+
+
+def shared_contexts(wl, step, min_blocks=2):
+    """(ctx_len [num_ctx], ctx_block_start [num_ctx + 1], ctx_rows) when the
+    step's blocks share contexts as mla_draft_forward_shared wants them,
+    else None."""
+    if wl.ctx_seq is None or step.block_seq is None:
+        return None
+    seq = np.asarray(step.block_seq)
+    n_ctx = int(seq.max()) + 1 if seq.size else 0
+    if n_ctx == 0 or np.any(np.diff(seq) < 0) or set(np.unique(seq).tolist()) != set(range(n_ctx)):
+        return None
+    ctx_len = np.bincount(np.asarray(wl.ctx_seq), minlength=n_ctx)[:n_ctx].astype(np.int32)
+    starts = np.searchsorted(seq, np.arange(n_ctx + 1)).astype(np.int32)
+    if np.min(np.diff(starts)) < min_blocks:
+        return None
+    if np.any(step.kv_len != ctx_len[seq] + wl.block_len):
+        return None
+    return ctx_len, starts, int(ctx_len.sum())
 
 
 def to_dev(a, dtype=None, device="cuda"):
@@ -64,6 +86,12 @@ class DeviceWorkload:
             d["desc"] = api.make_desc(d["block_table"], d["kv_len"], d["window"], d["q_visible"],
                                       wl.block_len, d["vis_stats"])
             d["out"] = torch.empty(len(s.block_positions), wl.dims.hidden_size, dtype=dt, device=device)
+            d["ctx"] = None
+            sc = shared_contexts(wl, s)
+            if sc is not None:
+                d["ctx_len"] = to_dev(sc[0], None, device)
+                d["ctx_start"] = to_dev(sc[1], None, device)
+                d["ctx"] = api.make_shared_ctx(d["ctx_len"], d["ctx_start"], sc[2])
             self.steps.append(d)
 
     def reset_cache(self):
@@ -80,8 +108,12 @@ class DeviceWorkload:
         s = self.steps[k]
         if s["append"] is not None:
             api.mla_latent_cache_append(self.handle, *s["append"], self.cache)
-        api.mla_draft_forward(self.handle, s["hidden"], s["positions"], s["slots"], self.cache,
-                              s["desc"], out=s["out"])
+        if s["ctx"] is not None:
+            api.mla_draft_forward_shared(self.handle, s["hidden"], s["positions"], s["slots"],
+                                         self.cache, s["desc"], s["ctx"], out=s["out"])
+        else:
+            api.mla_draft_forward(self.handle, s["hidden"], s["positions"], s["slots"], self.cache,
+                                  s["desc"], out=s["out"])
         return s["out"]
 
     def run_step_after(self, k, side, with_context=False):

@@ -130,6 +130,24 @@ typedef struct {
                                   applied them; NULL = not written            */
 } mla_attn_desc_t;
 
+/* Blocks that share a context (MLA blog, forward_impl: the prefill path,
+ * forward_mha with _compute_prefill_context, runs the expanded form when
+ * many query rows meet one cached context).  Context c's blocks are
+ * ctx_block_start[c] .. ctx_block_start[c+1]-1 (consecutive; the whole list
+ * covers blocks 0 .. num_blocks-1).  Each block b of context c sees keys
+ * 0 .. ctx_len[c]-1 as the context -- the same cache entries for all of c's
+ * blocks, read through the table of block ctx_block_start[c] -- and keys
+ * ctx_len[c] .. kv_len[b]-1 as its own, at most block_len of them
+ * (kv_len[b] <= ctx_len[c] + block_len; a longer kv_len is reported on the
+ * device as MLA_DEV_BAD_LENGTH and its extra keys are not seen).  The
+ * visibility rule of mla_attn_desc_t applies unchanged. */
+typedef struct {
+  int32_t num_ctx;                 /* contexts                                   */
+  int32_t ctx_rows;                /* host: sum of ctx_len (keys of all contexts) */
+  const int32_t *ctx_len;          /* device [num_ctx]                           */
+  const int32_t *ctx_block_start;  /* device [num_ctx + 1]                       */
+} mla_shared_ctx_t;
+
 typedef struct mla_handle mla_handle_t;
 
 /* ---- geometry (host only; no GPU needed) --------------------------------
@@ -221,6 +239,27 @@ mla_status_t mla_draft_forward_after(mla_handle_t *h, const void *hidden,
                                      void *out, void *workspace,
                                      size_t workspace_bytes, void *stream,
                                      void *cache_ready);
+
+/* mla_draft_forward for blocks that share contexts (mla_shared_ctx_t), in
+ * the expanded form when the layer allows it (bf16, qk_nope_head_dim and
+ * v_head_dim 128, block_len <= 128): each context's latents and each block's
+ * own latents are expanded once by kv_b_proj into per-head k_nope and v
+ * (MLA blog, forward_mha: kv_b_proj on the prefill context), the queries
+ * keep q_nope and q_pe (no W_UK / W_UV absorption), and one attention runs
+ * per (head, up to 128 / block_len blocks of a context): the context keys,
+ * then the blocks' own keys as one more key tile, masked to each block's
+ * own.  Other layers run mla_draft_forward.  Same results and errors as
+ * mla_draft_forward; the workspace is
+ * mla_forward_shared_workspace_bytes(h, num_tokens, ctx_rows). */
+size_t mla_forward_shared_workspace_bytes(const mla_handle_t *h, int32_t num_tokens,
+                                          int32_t ctx_rows);
+mla_status_t mla_draft_forward_shared(mla_handle_t *h, const void *hidden,
+                                      const int32_t *positions,
+                                      const int64_t *block_slot_mapping, void *cache,
+                                      int32_t num_pages, const mla_attn_desc_t *desc,
+                                      const mla_shared_ctx_t *ctx, void *out,
+                                      void *workspace, size_t workspace_bytes,
+                                      void *stream);
 
 /* Allocation-free latent-cache append.  The pages have no counterpart: this
  * is a library convenience for callers that cannot allocate device memory

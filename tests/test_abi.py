@@ -105,7 +105,8 @@ def test_null_handle_calls_return_invalid_arg():
 def test_python_binding_has_the_c_names():
     # every entry point the header declares that a Python caller uses directly
     for n in declared_functions() - {"mla_draft_destroy", "mla_status_string", "mla_last_error",
-                                      "mla_append_workspace_bytes", "mla_forward_workspace_bytes"}:
+                                      "mla_append_workspace_bytes", "mla_forward_workspace_bytes",
+                                      "mla_forward_shared_workspace_bytes"}:
         assert hasattr(api, n), f"api.{n} missing"
     assert api.mla_cache_entry_dim(QWEN3_4B_MLA) == 576
     assert api.mla_cache_page_bytes(QWEN3_4B_MLA, 64) == 64 * 576 * 2
