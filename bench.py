@@ -50,19 +50,26 @@ DESC = {"tiny_fp32": "1 x (64 context + 8-token block), fp32",
         "qwen3_4b_decode_t1": "64 seqs, cache pre-filled, 2 consecutive one-token steps"}
 
 
-def algorithmic_flops(wl):
+def algorithmic_flops(wl, shared=False):
     """Absorbed latent path: per block token 2D(r_q+L) [+2D*H*dv gate] +
     2 r_q H dqk + 2 H dn r_kv + 2 H r_kv dv + 2 H dv D, per visible key
-    H (2L + 2 r_kv); per appended token 2 D L.  Also the cache bytes the
-    attention reads (1152 B per key a block can see, once per block)."""
+    H (2L + 2 r_kv); per appended token 2 D L.  The expanded form (``shared``:
+    blocks sharing a context) instead: no W_UK / W_UV, per gathered latent row
+    (each context key once, each block token) 2 r_kv H (dn + dv), per visible
+    key H (2 dqk + 2 dv).  Also the cache bytes the attention reads (1152 B
+    per key a block can see, once per block)."""
     d = wl.dims
     H, D, L = d.num_heads, d.hidden_size, d.cache_dim
     qdim = d.q_lora_rank if d.q_lora_rank else H * d.qk_head_dim
     per_tok = 2 * D * (qdim + L) + (2 * D * H * d.v_head_dim if d.use_output_gate else 0)
     if d.q_lora_rank:
         per_tok += 2 * d.q_lora_rank * H * d.qk_head_dim
-    per_tok += 2 * H * d.qk_nope_head_dim * d.kv_lora_rank + 2 * H * d.kv_lora_rank * d.v_head_dim
+    if not shared:
+        per_tok += 2 * H * d.qk_nope_head_dim * d.kv_lora_rank + 2 * H * d.kv_lora_rank * d.v_head_dim
+    else:
+        per_tok += 2 * d.kv_lora_rank * H * (d.qk_nope_head_dim + d.v_head_dim)   # its own row
     per_tok += 2 * H * d.v_head_dim * D
+    per_key = H * (2 * d.qk_head_dim + 2 * d.v_head_dim) if shared else H * (2 * L + 2 * d.kv_lora_rank)
     T = wl.block_len
     total = block_tokens = cache_bytes = 0
     attention = []                             # per step: flops of its attention launch
@@ -76,13 +83,15 @@ def algorithmic_flops(wl):
             lo = np.maximum(0, p - w + 1) if w > 0 else np.zeros_like(p)
             keys += int(((n - lo) * step.q_visible[r]).sum())
             cache_bytes += (n - int(lo.min())) * L * 2
-        attention.append(H * (2 * L + 2 * d.kv_lora_rank) * keys)
+        attention.append(per_key * keys)
         total += per_tok * len(step.block_positions) + attention[-1]
         block_tokens += len(step.block_positions)
         if step.append_hidden is not None:
             appended += len(step.append_hidden)
     append = 2 * D * L * (0 if wl.ctx_hidden is None else len(wl.ctx_hidden))
     total += 2 * D * L * (appended - (0 if wl.ctx_hidden is None else len(wl.ctx_hidden))) + append
+    if shared:      # each context's keys expanded once per step
+        total += 2 * d.kv_lora_rank * H * (d.qk_nope_head_dim + d.v_head_dim) * len(wl.ctx_hidden) * len(wl.steps)
     return dict(total=total, append=append, block_tokens=block_tokens, ctx_tokens=appended,
                 cache_bytes=cache_bytes, attention=attention)
 
@@ -243,8 +252,12 @@ class Session:
         from head_latent_attention_qkv_gb300.runner import DeviceWorkload
         self.name, self.overlap = name, overlap
         self.wl = workloads.make_workload(name, scale)
-        self.fl = algorithmic_flops(self.wl)
         self.dev = DeviceWorkload(self.wl)
+        # blocks sharing a context run the expanded form (when the layer allows it)
+        self.shared = (self.dev.steps[-1]["ctx"] is not None and self.wl.dims.dtype == "bf16"
+                       and self.wl.dims.qk_nope_head_dim == 128 and self.wl.dims.v_head_dim == 128
+                       and self.wl.block_len <= 128)
+        self.fl = algorithmic_flops(self.wl, self.shared)
         self.side = torch.cuda.Stream()
         self.api, self.lib = api, _lib
         dev = self.dev
@@ -284,6 +297,10 @@ class Session:
 
     def attention(self):
         s = self.dev.steps[-1]
+        if self.shared:
+            # the expanded attention on the intermediates the step's forward left
+            self.api.mla_shared_attention(self.dev.handle, s["positions"], s["desc"], s["ctx"])
+            return
         self.api.mla_latent_attention(self.dev.handle, self.q_abs, s["positions"], self.dev.cache,
                                       s["desc"], o_lat=self.o_lat, lse=self.lse)
 
@@ -330,7 +347,7 @@ def run_ours(args, rank, world):
         kernels["append"] = dict(ms=timed(run_a, args.steps, flush, stream), flops=S.fl["append"])
     kernels["attention"] = dict(ms=timed(run_t, args.steps, flush, stream),
                                 flops=S.fl["attention"][-1], bytes=attention_cache_bytes(S.wl),
-                                few_row=few_row_attention(S.wl))
+                                few_row=few_row_attention(S.wl), shared=S.shared)
     hold_load(2)
     clocks.__exit__(None, None, None)
     ms = max_over_ranks(ms, world)
@@ -507,6 +524,10 @@ def main():
                        "RMSNorm/RoPE/slot scatter), the context's tokens",
              "attention": "latent_attn_tc_kernel: latent attention (tcgen05 QK^T and PV over "
                           "the 576-wide cache), the last step's blocks"}
+    if r["kernels"]["attention"].get("shared"):
+        names["attention"] = ("expand_attn_kernel: expanded attention (tcgen05 [q_nope|q_pe][k_nope|k_pe]^T "
+                              "and P V, head dims 192 / 128) over each context's keys and the blocks' own, "
+                              "the last step's blocks")
     dom = max(r["kernels"], key=lambda k: r["kernels"][k]["ms"])
     k = r["kernels"][dom]
     ach = k["flops"] / (k["ms"] * 1e-3) / 1e12
@@ -526,7 +547,7 @@ def main():
     else:
         roofline = {"kernel": names[dom], "bound": "tensor", "achieved": ach, "peak": bf16,
                     "unit": "TFLOP/s", "frac": ach / bf16,
-                    "traffic": dram_traffic(dom, args.workload),
+                    "traffic": dram_traffic("expand" if k.get("shared") else dom, args.workload),
                     "launch_ms": k["ms"], "algorithmic_flops_per_launch": k["flops"],
                     "share_of_step": k["ms"] / r["ms"],
                     "peak_source": f"{src} bf16 burst (sustained {bf16_sus}: frac "

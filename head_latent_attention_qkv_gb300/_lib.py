@@ -17,7 +17,7 @@ MLA_BF16, MLA_FP32 = 0, 1
 MLA_ROPE_NEOX, MLA_ROPE_INTERLEAVED = 0, 1
 MLA_DEV_BAD_SLOT, MLA_DEV_BAD_POSITION, MLA_DEV_BAD_PAGE, MLA_DEV_TIMEOUT, MLA_DEV_BAD_LENGTH = 1, 2, 4, 8, 16
 MLA_DEV_BAD_WINDOW = 32
-MLA_WS_Q_ABS, MLA_WS_O_LAT = 0, 1
+MLA_WS_Q_ABS, MLA_WS_O_LAT, MLA_WS_O = 0, 1, 2
 
 
 class mla_config_t(C.Structure):
@@ -75,6 +75,10 @@ def _load():
         "mla_forward_shared_workspace_bytes": (SZ, [P, I32, I32]),
         "mla_draft_forward_shared": (I32, [P, P, P, P, P, I32, C.POINTER(mla_attn_desc_t),
                                            C.POINTER(mla_shared_ctx_t), P, P, SZ, P]),
+        "mla_draft_forward_shared_after": (I32, [P, P, P, P, P, I32, C.POINTER(mla_attn_desc_t),
+                                                 C.POINTER(mla_shared_ctx_t), P, P, SZ, P, P]),
+        "mla_shared_attention": (I32, [P, P, C.POINTER(mla_attn_desc_t), C.POINTER(mla_shared_ctx_t),
+                                       P, SZ, P]),
         "mla_get_device_status": (I32, [P, P, C.POINTER(I32)]),
         "mla_draft_destroy": (None, [P]),
         "mla_kernel_launches": (C.c_ulonglong, [P]),

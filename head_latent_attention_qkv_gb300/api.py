@@ -139,6 +139,35 @@ def mla_draft_forward_shared(h: Handle, hidden, positions, block_slot_mapping, c
     return out
 
 
+def mla_draft_forward_shared_after(h: Handle, hidden, positions, block_slot_mapping, cache, desc,
+                                   ctx, cache_ready=None, out=None, stream=None, workspace=None):
+    """mla_draft_forward_shared whose attention waits for ``cache_ready``
+    (a recorded torch.cuda.Event, or None)."""
+    M = desc.num_blocks * desc.block_len
+    if out is None:
+        out = torch.empty(M, h.dims.hidden_size, dtype=torch_dtype(h.dims), device=h.device)
+    need = lib.mla_forward_shared_workspace_bytes(h.h, M, ctx.ctx_rows)
+    ws = workspace if workspace is not None else h.workspace(need)
+    ev = None if cache_ready is None else C.c_void_p(cache_ready.cuda_event)
+    check(lib.mla_draft_forward_shared_after(h.h, _ptr(hidden), _ptr(positions),
+                                             _ptr(block_slot_mapping), _ptr(cache), cache.shape[0],
+                                             C.byref(desc), C.byref(ctx), _ptr(out), _ptr(ws),
+                                             ws.numel(), _stream(stream), ev),
+          "mla_draft_forward_shared_after")
+    return out
+
+
+def mla_shared_attention(h: Handle, positions, desc, ctx, workspace=None, stream=None):
+    """The expanded attention step alone, on the intermediates the last
+    mla_draft_forward_shared left in the workspace (the handle's unless
+    given); rewrites that workspace's per-head output o."""
+    M = desc.num_blocks * desc.block_len
+    need = lib.mla_forward_shared_workspace_bytes(h.h, M, ctx.ctx_rows)
+    ws = workspace if workspace is not None else h.workspace(need)
+    check(lib.mla_shared_attention(h.h, _ptr(positions), C.byref(desc), C.byref(ctx), _ptr(ws),
+                                   ws.numel(), _stream(stream)), "mla_shared_attention")
+
+
 def mla_draft_forward_after(h: Handle, hidden, positions, block_slot_mapping, cache, desc,
                             cache_ready=None, out=None, stream=None, workspace=None):
     """mla_draft_forward whose attention waits for ``cache_ready`` (a

@@ -621,13 +621,13 @@ extern "C" mla_status_t mla_draft_forward_after(mla_handle_t* h, const void* hid
   return MLA_OK;
 }
 
-extern "C" mla_status_t mla_draft_forward_shared(mla_handle_t* h, const void* hidden,
-                                                 const int32_t* positions,
-                                                 const int64_t* block_slot_mapping, void* cache,
-                                                 int32_t num_pages, const mla_attn_desc_t* desc,
-                                                 const mla_shared_ctx_t* ctx, void* out,
-                                                 void* workspace, size_t workspace_bytes,
-                                                 void* stream) {
+extern "C" mla_status_t mla_draft_forward_shared_after(mla_handle_t* h, const void* hidden,
+                                                       const int32_t* positions,
+                                                       const int64_t* block_slot_mapping, void* cache,
+                                                       int32_t num_pages, const mla_attn_desc_t* desc,
+                                                       const mla_shared_ctx_t* ctx, void* out,
+                                                       void* workspace, size_t workspace_bytes,
+                                                       void* stream, void* cache_ready) {
   if (!h || !desc || !ctx) return fail(MLA_ERR_INVALID_ARG, "forward_shared: null handle, descriptor or context list");
   const mla_attn_desc_t& d = *desc;
   if (d.num_blocks < 0 || d.block_len <= 0 || d.max_pages <= 0)
@@ -645,12 +645,52 @@ extern "C" mla_status_t mla_draft_forward_shared(mla_handle_t* h, const void* hi
     return fail(MLA_ERR_INVALID_ARG, "forward_shared: workspace smaller than mla_forward_shared_workspace_bytes()");
   if ((uintptr_t)workspace % 256) return fail(MLA_ERR_INVALID_ARG, "forward_shared: workspace must be 256-byte aligned");
   cudaStream_t st = (cudaStream_t)stream;
+  const cudaEvent_t ev = (cudaEvent_t)cache_ready;
   const mla_status_t s =
       h->cfg.dtype == MLA_BF16
           ? forward_impl<__nv_bfloat16, __half>(h, hidden, positions, block_slot_mapping, cache,
-                                                num_pages, d, out, (char*)workspace, st, nullptr, ctx)
+                                                num_pages, d, out, (char*)workspace, st, ev, ctx)
           : forward_impl<float, float>(h, hidden, positions, block_slot_mapping, cache,
-                                       num_pages, d, out, (char*)workspace, st, nullptr);
+                                       num_pages, d, out, (char*)workspace, st, ev);
+  if (s != MLA_OK) return s;
+  MLA_CUDA_TRY(cudaGetLastError());
+  return MLA_OK;
+}
+
+extern "C" mla_status_t mla_draft_forward_shared(mla_handle_t* h, const void* hidden,
+                                                 const int32_t* positions,
+                                                 const int64_t* block_slot_mapping, void* cache,
+                                                 int32_t num_pages, const mla_attn_desc_t* desc,
+                                                 const mla_shared_ctx_t* ctx, void* out,
+                                                 void* workspace, size_t workspace_bytes,
+                                                 void* stream) {
+  return mla_draft_forward_shared_after(h, hidden, positions, block_slot_mapping, cache, num_pages,
+                                        desc, ctx, out, workspace, workspace_bytes, stream, nullptr);
+}
+
+extern "C" mla_status_t mla_shared_attention(mla_handle_t* h, const int32_t* positions,
+                                             const mla_attn_desc_t* desc, const mla_shared_ctx_t* ctx,
+                                             void* workspace, size_t workspace_bytes, void* stream) {
+  if (!h || !desc || !ctx || !positions || !workspace)
+    return fail(MLA_ERR_INVALID_ARG, "shared_attention: null pointer");
+  const mla_attn_desc_t& d = *desc;
+  if (d.num_blocks <= 0 || d.block_len <= 0 || ctx->num_ctx <= 0 || ctx->ctx_rows < 0)
+    return fail(MLA_ERR_INVALID_ARG, "shared_attention: num_blocks, block_len, num_ctx > 0, ctx_rows >= 0");
+  if (!tc::expand_applies(h, d.block_len))
+    return fail(MLA_ERR_UNSUPPORTED, "shared_attention: the layer does not run the expanded form");
+  const Layout& l = h->lay;
+  const long M = (long)d.num_blocks * d.block_len;
+  const SharedWs sw = shared_ws(h, M, ctx->ctx_rows);
+  if (workspace_bytes < sw.total)
+    return fail(MLA_ERR_INVALID_ARG, "shared_attention: workspace smaller than mla_forward_shared_workspace_bytes()");
+  const FwdWs w = forward_ws(h, M);
+  char* ws = (char*)workspace;
+  const float* gate = l.gdim ? (const float*)(ws + w.a_out) + l.L + l.qdim : nullptr;
+  const mla_status_t s = tc::expanded_attention(
+      (cudaStream_t)stream, h, (const __half*)(ws + w.q_nope), (const __nv_bfloat16*)(ws + w.q_abs),
+      (const __half*)(ws + sw.kv), (const __nv_bfloat16*)(ws + sw.gathered),
+      tc::expand_rows(*ctx, d.num_blocks, d.block_len), d, *ctx, positions, gate, l.NA,
+      (__half*)(ws + w.o), false);
   if (s != MLA_OK) return s;
   MLA_CUDA_TRY(cudaGetLastError());
   return MLA_OK;
@@ -673,6 +713,7 @@ extern "C" size_t mla_forward_workspace_offset(const mla_handle_t* h, int32_t nu
   switch (part) {
     case MLA_WS_Q_ABS: return w.q_abs;
     case MLA_WS_O_LAT: return w.o_lat;
+    case MLA_WS_O: return w.o;
     default: return (size_t)-1;
   }
 }

@@ -22,9 +22,13 @@
 //        keys: 8 MMAs, P fp16 from tensor memory)
 // O is 128 fp32 columns, so S is double-buffered in tensor memory and the
 // scores of tile t + 1 are computed while the softmax of tile t runs.
+// Keys and values stream through separate two-slot rings: a key slot is
+// refilled as soon as its scores are done, so the score chain never waits for
+// P V.
 //   warps 0-3, 8-11: softmax, two threads per row (64 keys each), half
 //                    maxima exchanged through shared memory; epilogue
-//   warp 4         : Q and the key/value tiles (TMA, two slots)
+//   warp 4         : Q and the key tiles (TMA)
+//   warp 6         : the value tiles (TMA)
 //   warp 5         : tensor-memory allocation, MMA issue
 #include "expand_tc.cuh"
 
@@ -41,9 +45,11 @@ constexpr int QROWS = 128, KT = 128;
 constexpr int THREADS = 384;
 constexpr int CH = 128 * 64 * 2;                 // one 16 KiB chunk: 128 rows x 64 16-bit values
 constexpr int OFF_Q = 0;                          // q_nope (2 chunks, fp16), q_pe (bf16)
-constexpr int OFF_RING = OFF_Q + 3 * CH;          // 2 slots: k_nope (2), k_pe, v (2)
-constexpr int SLOT = 5 * CH;
-constexpr int OFF_BAR = OFF_RING + 2 * SLOT;
+constexpr int OFF_KR = OFF_Q + 3 * CH;            // key ring, 2 slots: k_nope (2 chunks), k_pe
+constexpr int KSLOT = 3 * CH;
+constexpr int OFF_VR = OFF_KR + 2 * KSLOT;        // value ring, 2 slots: v (2 chunks)
+constexpr int VSLOT = 2 * CH;
+constexpr int OFF_BAR = OFF_VR + 2 * VSLOT;
 constexpr int OFF_XM = OFF_BAR + 256;             // [2][128] half maxima / sums
 constexpr int OFF_RED = OFF_XM + 2 * QROWS * 4;   // [8] per-warp minima of the window starts
 constexpr int SMEM_BYTES = 1024 + OFF_RED + 64;
@@ -53,7 +59,8 @@ static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 struct Bars {
   uint64_t q_full;
-  uint64_t full[2], empty[2];   // key/value slot landed / read by its last MMA (by tile parity)
+  uint64_t kfull[2], kempty[2]; // key slot landed / read by S (by tile parity)
+  uint64_t vfull[2], vempty[2]; // value slot landed / read by P V (by tile parity)
   uint64_t s_full[2];           // S(t) complete, by t % 2
   uint64_t p_full[2];           // P(t) in tensor memory (256 arrivals), by t % 2
   uint64_t o_free[2];           // P(t) V(t) complete, by t % 2
@@ -131,8 +138,10 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
   if (tid == 0) {
     mbar_init(&B->q_full, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&B->full[i], 1);
-      mbar_init(&B->empty[i], 1);
+      mbar_init(&B->kfull[i], 1);
+      mbar_init(&B->kempty[i], 1);
+      mbar_init(&B->vfull[i], 1);
+      mbar_init(&B->vempty[i], 1);
       mbar_init(&B->s_full[i], 1);
       mbar_init(&B->p_full[i], 2 * QROWS);
       mbar_init(&B->o_free[i], 1);
@@ -167,31 +176,42 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
   const uint32_t tmem = B->tmem_slot;
   if (tid == 0) pdl_trigger();
 
-  if (warp == 4) {
+  if (warp == 4 || warp == 6) {
     if (lane == 0) {
-      // ---- Q, then the key/value tiles through two slots ----
-      prefetch_tmap(&P.tmQn);
-      prefetch_tmap(&P.tmQp);
+      // ---- warp 4: Q, then the key tiles; warp 6: the value tiles ----
+      const bool keys = warp == 4;
+      if (keys) {
+        prefetch_tmap(&P.tmQn);
+        prefetch_tmap(&P.tmQp);
+        prefetch_tmap(&P.tmKp);
+      }
       prefetch_tmap(&P.tmKV);
-      prefetch_tmap(&P.tmKp);
       pdl_wait();
-      mbar_arrive_expect_tx(&B->q_full, 3 * CH);
-      tma_load_3d(smem + OFF_Q, &P.tmQn, &B->q_full, 0, (int)m0, 2 * h);
-      tma_load_3d(smem + OFF_Q + 2 * CH, &P.tmQp, &B->q_full, 0, (int)m0, 9 * h + 8);
+      if (keys) {
+        mbar_arrive_expect_tx(&B->q_full, 3 * CH);
+        tma_load_3d(smem + OFF_Q, &P.tmQn, &B->q_full, 0, (int)m0, 2 * h);
+        tma_load_3d(smem + OFF_Q + 2 * CH, &P.tmQp, &B->q_full, 0, (int)m0, 9 * h + 8);
+      }
+      uint64_t* full = keys ? B->kfull : B->vfull;
+      uint64_t* empty = keys ? B->kempty : B->vempty;
       bool ok = true;
       for (int t = 0; t < nt && ok; ++t) {
         const int s = t & 1;
-        if (!(ok = wait_bar(B, &B->empty[s], ((t >> 1) & 1) ^ 1, P.status))) break;
+        if (!(ok = wait_bar(B, &empty[s], ((t >> 1) & 1) ^ 1, P.status))) break;
         const int row = t < nt_ctx ? coff + j_lo + KT * t : (int)own0;
-        uint8_t* slot = smem + OFF_RING + s * SLOT;
-        mbar_arrive_expect_tx(&B->full[s], 5 * CH);
-        tma_load_3d(slot, &P.tmKV, &B->full[s], 0, row, 4 * h);            // k_nope (2 chunks)
-        tma_load_3d(slot + 2 * CH, &P.tmKp, &B->full[s], 0, row, 8);       // k_pe
-        tma_load_3d(slot + 3 * CH, &P.tmKV, &B->full[s], 0, row, 4 * h + 2);  // v (2 chunks)
+        if (keys) {
+          uint8_t* slot = smem + OFF_KR + s * KSLOT;
+          mbar_arrive_expect_tx(&full[s], 3 * CH);
+          tma_load_3d(slot, &P.tmKV, &full[s], 0, row, 4 * h);            // k_nope (2 chunks)
+          tma_load_3d(slot + 2 * CH, &P.tmKp, &full[s], 0, row, 8);       // k_pe
+        } else {
+          mbar_arrive_expect_tx(&full[s], 2 * CH);
+          tma_load_3d(smem + OFF_VR + s * VSLOT, &P.tmKV, &full[s], 0, row, 4 * h + 2);  // v (2 chunks)
+        }
       }
       // every copy into this CTA has landed before it may exit
-      mbar_wait(&B->q_full, 0, P.status);
-      for (int t = max(0, nt - 2); t < nt; ++t) mbar_wait(&B->full[t & 1], (t >> 1) & 1, P.status);
+      if (keys) mbar_wait(&B->q_full, 0, P.status);
+      for (int t = max(0, nt - 2); t < nt; ++t) mbar_wait(&full[t & 1], (t >> 1) & 1, P.status);
     }
   } else if (warp == 5) {
     if (lane == 0) {
@@ -199,9 +219,9 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
       const uint32_t id_s16 = idesc_f16(QROWS, KT, true), id_sbf = idesc_f16(QROWS, KT, false);
       const uint32_t id_pv = idesc_f16_bmn(QROWS, 128, true);
       const uint64_t dQ = smem_desc_sw128(smem + OFF_Q);
-      const uint64_t dK0 = smem_desc_sw128(smem + OFF_RING);
-      const uint64_t dV0 = smem_desc_sw128_mn(smem + OFF_RING + 3 * CH, CH);
-      constexpr uint32_t U_CH = CH / 16, U_SLOT = SLOT / 16, U_KSTEP = 16 * 128 / 16;
+      const uint64_t dK0 = smem_desc_sw128(smem + OFF_KR);
+      const uint64_t dV0 = smem_desc_sw128_mn(smem + OFF_VR, CH);
+      constexpr uint32_t U_CH = CH / 16, U_KSLOT = KSLOT / 16, U_VSLOT = VSLOT / 16, U_KSTEP = 16 * 128 / 16;
       bool ok = wait_bar(B, &B->q_full, 0, P.status);
       tc_fence_after();
       for (int t = 0; t <= nt && ok; ++t) {
@@ -210,10 +230,10 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
           // S buffer s: the softmax has written P(t - 2) over it (and P(t - 2)
           // V(t - 2), issued before by this thread, reads it first)
           if (t >= 2 && !(ok = wait_bar(B, &B->p_full[s], ((t - 2) >> 1) & 1, P.status))) break;
-          if (!(ok = wait_bar(B, &B->full[s], (t >> 1) & 1, P.status))) break;
+          if (!(ok = wait_bar(B, &B->kfull[s], (t >> 1) & 1, P.status))) break;
           tc_fence_after();
           const uint32_t tS = tmem + TM_S + 128 * s;
-          const uint64_t dK = dK0 + s * U_SLOT;
+          const uint64_t dK = dK0 + s * U_KSLOT;
 #pragma unroll
           for (int ch = 0; ch < 3; ++ch) {
             const uint32_t id = ch < 2 ? id_s16 : id_sbf;
@@ -221,18 +241,20 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
             for (int k = 0; k < 4; ++k)
               mma_f16(tS, dQ + ch * U_CH + 2 * k, dK + ch * U_CH + 2 * k, id, (ch | k) ? 1u : 0u);
           }
+          mma_commit(&B->kempty[s]);
           mma_commit(&B->s_full[s]);
         }
         if (t >= 1) {
           const int tt = t - 1, s = tt & 1;
           if (!(ok = wait_bar(B, &B->p_full[s], (tt >> 1) & 1, P.status))) break;
+          if (!(ok = wait_bar(B, &B->vfull[s], (tt >> 1) & 1, P.status))) break;
           tc_fence_after();
           const uint32_t tP = tmem + TM_S + 128 * s;
-          const uint64_t dV = dV0 + s * U_SLOT;
+          const uint64_t dV = dV0 + s * U_VSLOT;
 #pragma unroll
           for (int k = 0; k < KT / 16; ++k)   // 16 keys per MMA: 8 P columns, 16 V rows
             mma_f16_ts(tmem + TM_O, tP + 8 * k, dV + (uint64_t)U_KSTEP * k, id_pv, (tt | k) ? 1u : 0u);
-          mma_commit(&B->empty[s]);
+          mma_commit(&B->vempty[s]);
           mma_commit(&B->o_free[s]);
         }
       }

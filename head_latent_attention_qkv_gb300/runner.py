@@ -140,8 +140,13 @@ class DeviceWorkload:
                                             workspace=self._side_ws)
             ready = torch.cuda.Event()
             ready.record(side)
-        api.mla_draft_forward_after(self.handle, s["hidden"], s["positions"], s["slots"],
-                                    self.cache, s["desc"], cache_ready=ready, out=s["out"])
+        if s["ctx"] is not None:
+            api.mla_draft_forward_shared_after(self.handle, s["hidden"], s["positions"], s["slots"],
+                                               self.cache, s["desc"], s["ctx"], cache_ready=ready,
+                                               out=s["out"])
+        else:
+            api.mla_draft_forward_after(self.handle, s["hidden"], s["positions"], s["slots"],
+                                        self.cache, s["desc"], cache_ready=ready, out=s["out"])
         return s["out"]
 
     def run_all(self):

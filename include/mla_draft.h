@@ -78,7 +78,7 @@ enum {
 
 /* Intermediate tensors the forward leaves in its workspace
  * (mla_forward_workspace_offset). */
-enum { MLA_WS_Q_ABS = 0, MLA_WS_O_LAT = 1 };
+enum { MLA_WS_Q_ABS = 0, MLA_WS_O_LAT = 1, MLA_WS_O = 2 };
 
 /* Layer configuration.  Structural dims follow the HF DeepSeek-V2/V3 fields;
  * q_lora_rank == 0 selects the non-low-rank path (q_proj +
@@ -261,6 +261,27 @@ mla_status_t mla_draft_forward_shared(mla_handle_t *h, const void *hidden,
                                       void *workspace, size_t workspace_bytes,
                                       void *stream);
 
+/* mla_draft_forward_shared whose attention waits for an event, as
+ * mla_draft_forward_after: everything before the gather of the cache rows
+ * is enqueued at once, then the stream waits for `cache_ready`. */
+mla_status_t mla_draft_forward_shared_after(mla_handle_t *h, const void *hidden,
+                                            const int32_t *positions,
+                                            const int64_t *block_slot_mapping, void *cache,
+                                            int32_t num_pages, const mla_attn_desc_t *desc,
+                                            const mla_shared_ctx_t *ctx, void *out,
+                                            void *workspace, size_t workspace_bytes,
+                                            void *stream, void *cache_ready);
+
+/* The attention step of mla_draft_forward_shared alone, on the intermediates
+ * the last such call left in `workspace` (same handle, descriptor, context
+ * list and token count): the queries' q_nope and q_pe, the gathered latent
+ * rows and their kv_b_proj expansion, the gate.  It rewrites the workspace's
+ * per-head output o (the input of o_proj) with the same values the forward
+ * computed.  For timing and checking that step in isolation. */
+mla_status_t mla_shared_attention(mla_handle_t *h, const int32_t *positions,
+                                  const mla_attn_desc_t *desc, const mla_shared_ctx_t *ctx,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+
 /* Allocation-free latent-cache append.  The pages have no counterpart: this
  * is a library convenience for callers that cannot allocate device memory
  * where they append (host callbacks, allocator hooks, runtimes with a memory
@@ -290,8 +311,10 @@ int64_t mla_append_noalloc_max_tokens(const mla_handle_t *h);
 /* Byte offset inside a forward workspace (sized for num_tokens block tokens)
  * of an intermediate the forward leaves there: MLA_WS_Q_ABS, the absorbed
  * queries [num_tokens, H, kv_lora_rank + qk_rope_head_dim] in the cache dtype,
- * or MLA_WS_O_LAT, the latent attention output [num_tokens, H, kv_lora_rank]
- * (fp16 for bf16 layers, fp32 for fp32 layers).  Valid after the forward's
+ * MLA_WS_O_LAT, the latent attention output [num_tokens, H, kv_lora_rank]
+ * (fp16 for bf16 layers, fp32 for fp32 layers), or MLA_WS_O, the per-head
+ * output [num_tokens, H, v_head_dim] that o_proj reads (same types; in a
+ * workspace of mla_draft_forward_shared too, at the same offsets).  Valid after the forward's
  * work on the stream has completed, until the workspace is reused.  Returns
  * (size_t)-1 for a NULL handle, a negative count or an unknown part. */
 size_t mla_forward_workspace_offset(const mla_handle_t *h, int32_t num_tokens,

@@ -186,3 +186,59 @@ def test_few_row_blocks_match_oracle(case):
     log-sum-exp)."""
     from tests.parity import check_workload
     check_workload(_few_row_case(case))
+
+
+@pytest.mark.parametrize("case", ["T7_ragged_windows_masked", "T16_gate_off", "T40_one_context"])
+def test_shared_context_blocks_match_oracle(case):
+    """Blocks that share a context run the expanded form (the context's and
+    the blocks' own latents expanded by kv_b_proj, one attention over
+    q_nope|q_pe with the own keys as a block-diagonal tile): ragged context
+    lengths (not multiples of the 128-key tile), block lengths that leave a
+    unit's last rows empty, sliding windows shorter than the context and than
+    the block, masked query rows, with and without the output gate."""
+    import dataclasses
+    from tests.parity import check_workload
+    from head_latent_attention_qkv_gb300.runner import shared_contexts
+    W = workloads
+    d = W.DEEPSEEK_V3_MLA.replace(num_heads=16, hidden_size=1024)
+    if case == "T7_ragged_windows_masked":
+        wl = W.block_parallel_workload(case, d, 31, batch=3, ctx_len=320, blocks_per_seq=5,
+                                       block_len=7, page_size=64, windows=(0, 150, 3))
+        s = wl.steps[0]
+        qv = s.q_visible.copy()
+        qv[[2, 9, 33, 34, 60]] = 0
+        wl = dataclasses.replace(wl, steps=[dataclasses.replace(s, q_visible=qv)])
+    elif case == "T16_gate_off":
+        wl = W.block_parallel_workload(case, d.replace(use_output_gate=False, rope_style="neox"), 32,
+                                       batch=2, ctx_len=448, blocks_per_seq=9, block_len=16,
+                                       page_size=64, windows=(0, 200))
+    else:
+        wl = W.block_parallel_workload(case, d, 33, batch=1, ctx_len=256, blocks_per_seq=4,
+                                       block_len=40, page_size=128, windows=(0,))
+    assert shared_contexts(wl, wl.steps[0]) is not None
+    check_workload(wl)
+
+
+def test_shared_attention_entry_reproduces_the_forwards_output():
+    """mla_shared_attention re-runs the expanded attention on the shared
+    forward's intermediates: the per-head output o is the same bit for bit."""
+    from head_latent_attention_qkv_gb300 import _lib, api
+    from head_latent_attention_qkv_gb300.runner import DeviceWorkload
+    wl = workloads.make_workload("deepseek_v3_block_parallel", "small")
+    dev = DeviceWorkload(wl)
+    dev.run_all()
+    s = dev.steps[-1]
+    assert s["ctx"] is not None
+    M = s["hidden"].shape[0]
+    d = wl.dims
+    ws = dev.handle._ws
+    off = api.mla_forward_workspace_offset(dev.handle, M, _lib.MLA_WS_O)
+    n = M * d.num_heads * d.v_head_dim
+    torch.cuda.synchronize()
+    o_fwd = ws[off:off + 2 * n].clone()
+    ws[off:off + 2 * n] = 0
+    api.mla_shared_attention(dev.handle, s["positions"], s["desc"], s["ctx"])
+    torch.cuda.synchronize()
+    assert api.mla_get_device_status(dev.handle) == 0
+    assert torch.equal(ws[off:off + 2 * n], o_fwd)
+    dev.handle.close()
