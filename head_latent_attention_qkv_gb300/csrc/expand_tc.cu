@@ -29,7 +29,9 @@
 //                    maxima exchanged through shared memory; epilogue
 //   warp 4         : Q and the key tiles (TMA)
 //   warp 6         : the value tiles (TMA)
-//   warp 5         : tensor-memory allocation, MMA issue
+//   warp 5         : tensor-memory allocation, S issue
+//   warp 7         : P V issue (two issuing threads: one thread's issue
+//                    rate, not the tensor pipe, bounded the tile)
 #include "expand_tc.cuh"
 
 #include <mutex>
@@ -64,7 +66,7 @@ struct Bars {
   uint64_t s_full[2];           // S(t) complete, by t % 2
   uint64_t p_full[2];           // P(t) in tensor memory (256 arrivals), by t % 2
   uint64_t o_free[2];           // P(t) V(t) complete, by t % 2
-  uint64_t drain;
+  uint64_t drain, drain_pv;
   uint32_t tmem_slot;
   int abort;
 };
@@ -147,6 +149,7 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
       mbar_init(&B->o_free[i], 1);
     }
     mbar_init(&B->drain, 1);
+    mbar_init(&B->drain_pv, 1);
     B->abort = 0;
     fence_mbar_init();
   }
@@ -213,23 +216,22 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
       if (keys) mbar_wait(&B->q_full, 0, P.status);
       for (int t = max(0, nt - 2); t < nt; ++t) mbar_wait(&full[t & 1], (t >> 1) & 1, P.status);
     }
-  } else if (warp == 5) {
+  } else if (warp == 5 || warp == 7) {
     if (lane == 0) {
-      // ---- MMA issue: S(t) ahead of P(t - 1) V(t - 1) ----
-      const uint32_t id_s16 = idesc_f16(QROWS, KT, true), id_sbf = idesc_f16(QROWS, KT, false);
-      const uint32_t id_pv = idesc_f16_bmn(QROWS, 128, true);
-      const uint64_t dQ = smem_desc_sw128(smem + OFF_Q);
-      const uint64_t dK0 = smem_desc_sw128(smem + OFF_KR);
-      const uint64_t dV0 = smem_desc_sw128_mn(smem + OFF_VR, CH);
       constexpr uint32_t U_CH = CH / 16, U_KSLOT = KSLOT / 16, U_VSLOT = VSLOT / 16, U_KSTEP = 16 * 128 / 16;
-      bool ok = wait_bar(B, &B->q_full, 0, P.status);
-      tc_fence_after();
-      for (int t = 0; t <= nt && ok; ++t) {
-        if (t < nt) {
+      bool ok = true;
+      if (warp == 5) {
+        // ---- S(t) = [q_nope | q_pe] K(t)^T into S buffer t % 2 ----
+        const uint32_t id_s16 = idesc_f16(QROWS, KT, true), id_sbf = idesc_f16(QROWS, KT, false);
+        const uint64_t dQ = smem_desc_sw128(smem + OFF_Q);
+        const uint64_t dK0 = smem_desc_sw128(smem + OFF_KR);
+        ok = wait_bar(B, &B->q_full, 0, P.status);
+        tc_fence_after();
+        for (int t = 0; t < nt && ok; ++t) {
           const int s = t & 1;
-          // S buffer s: the softmax has written P(t - 2) over it (and P(t - 2)
-          // V(t - 2), issued before by this thread, reads it first)
-          if (t >= 2 && !(ok = wait_bar(B, &B->p_full[s], ((t - 2) >> 1) & 1, P.status))) break;
+          // S buffer s holds P(t - 2): P(t - 2) V(t - 2) (the other thread) has
+          // completed reading it
+          if (t >= 2 && !(ok = wait_bar(B, &B->o_free[s], ((t - 2) >> 1) & 1, P.status))) break;
           if (!(ok = wait_bar(B, &B->kfull[s], (t >> 1) & 1, P.status))) break;
           tc_fence_after();
           const uint32_t tS = tmem + TM_S + 128 * s;
@@ -244,22 +246,28 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
           mma_commit(&B->kempty[s]);
           mma_commit(&B->s_full[s]);
         }
-        if (t >= 1) {
-          const int tt = t - 1, s = tt & 1;
-          if (!(ok = wait_bar(B, &B->p_full[s], (tt >> 1) & 1, P.status))) break;
-          if (!(ok = wait_bar(B, &B->vfull[s], (tt >> 1) & 1, P.status))) break;
+      } else {
+        // ---- O += P(t) V(t), in tile order ----
+        const uint32_t id_pv = idesc_f16_bmn(QROWS, 128, true);
+        const uint64_t dV0 = smem_desc_sw128_mn(smem + OFF_VR, CH);
+        for (int t = 0; t < nt && ok; ++t) {
+          const int s = t & 1;
+          if (!(ok = wait_bar(B, &B->p_full[s], (t >> 1) & 1, P.status))) break;
+          if (!(ok = wait_bar(B, &B->vfull[s], (t >> 1) & 1, P.status))) break;
           tc_fence_after();
           const uint32_t tP = tmem + TM_S + 128 * s;
           const uint64_t dV = dV0 + s * U_VSLOT;
 #pragma unroll
           for (int k = 0; k < KT / 16; ++k)   // 16 keys per MMA: 8 P columns, 16 V rows
-            mma_f16_ts(tmem + TM_O, tP + 8 * k, dV + (uint64_t)U_KSTEP * k, id_pv, (tt | k) ? 1u : 0u);
+            mma_f16_ts(tmem + TM_O, tP + 8 * k, dV + (uint64_t)U_KSTEP * k, id_pv, (t | k) ? 1u : 0u);
           mma_commit(&B->vempty[s]);
           mma_commit(&B->o_free[s]);
         }
       }
-      mma_commit(&B->drain);
-      mbar_wait(&B->drain, 0, P.status);
+      // no MMA of this thread may still run when tensor memory is freed
+      uint64_t* drain = warp == 5 ? &B->drain : &B->drain_pv;
+      mma_commit(drain);
+      mbar_wait(drain, 0, P.status);
     }
   } else if (warp < 4 || warp >= 8) {
     // ---- softmax: row r (TMEM lane r), key columns [64 kh, 64 kh + 64) ----
