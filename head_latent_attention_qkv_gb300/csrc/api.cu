@@ -341,7 +341,7 @@ namespace {
 // The expanded form's pieces after the forward's own: the gathered latent
 // rows [rows, L] (layer dtype) and their expansion [rows, H, dn + dv] (fp16).
 struct SharedWs {
-  size_t gathered, kv, total;
+  size_t gathered, kv, units, total;
 };
 SharedWs shared_ws(const mla_handle* h, long num_tokens, long ctx_rows) {
   const Layout& l = h->lay;
@@ -350,6 +350,7 @@ SharedWs shared_ws(const mla_handle* h, long num_tokens, long ctx_rows) {
   size_t o = forward_ws(h, num_tokens).total;
   w.gathered = o; o = align256(o + (size_t)rows * l.L * l.elt);
   w.kv = o;       o = align256(o + (size_t)rows * l.H * (l.dn + l.dv) * 2);
+  w.units = o;    o = align256(o + (size_t)3 * num_tokens * 4);   // >= num_blocks + 2 * num_ctx ints
   w.total = o;
   return w;
 }
@@ -537,7 +538,8 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
       TI* o = (TI*)(ws + w.o);
       const float* gate = l.gdim ? a_out + l.L + l.qdim : nullptr;
       s = tc::expanded_attention(st, h, (const __half*)q_nope, (const __nv_bfloat16*)q_abs, kvx,
-                                 gathered, rows, d, *ctx, pos, gate, l.NA, (__half*)o, pdl);
+                                 gathered, rows, d, *ctx, pos, gate, l.NA, (__half*)o,
+                                 (int32_t*)(ws + sw.units), pdl);
       if (s != MLA_OK) return s;
       s = proj<TI, TX>(h, st, pdl, M, l.D, l.H * l.dv, 1, o, (long)l.H * l.dv, 0, (const TI*)h->Wo,
                        (long)l.H * l.dv, 0, (TX*)out, l.D, 0);
@@ -633,8 +635,9 @@ extern "C" mla_status_t mla_draft_forward_shared_after(mla_handle_t* h, const vo
   if (d.num_blocks < 0 || d.block_len <= 0 || d.max_pages <= 0)
     return fail(MLA_ERR_INVALID_ARG, "forward_shared: num_blocks >= 0, block_len > 0, max_pages > 0");
   if (d.num_blocks == 0) return MLA_OK;
-  if (ctx->num_ctx <= 0 || ctx->ctx_rows < 0 || !ctx->ctx_len || !ctx->ctx_block_start)
-    return fail(MLA_ERR_INVALID_ARG, "forward_shared: num_ctx > 0, ctx_rows >= 0, ctx_len and ctx_block_start set");
+  if (ctx->num_ctx <= 0 || ctx->num_ctx > d.num_blocks || ctx->ctx_rows < 0 || !ctx->ctx_len || !ctx->ctx_block_start)
+    return fail(MLA_ERR_INVALID_ARG,
+                "forward_shared: 0 < num_ctx <= num_blocks, ctx_rows >= 0, ctx_len and ctx_block_start set");
   if ((long)d.num_blocks * d.block_len + ctx->ctx_rows > 0x7fffffffL)
     return fail(MLA_ERR_INVALID_ARG, "forward_shared: too many tokens");
   if (!hidden || !positions || !cache || !out || !workspace || !d.block_table || !d.kv_len)
@@ -674,8 +677,10 @@ extern "C" mla_status_t mla_shared_attention(mla_handle_t* h, const int32_t* pos
   if (!h || !desc || !ctx || !positions || !workspace)
     return fail(MLA_ERR_INVALID_ARG, "shared_attention: null pointer");
   const mla_attn_desc_t& d = *desc;
-  if (d.num_blocks <= 0 || d.block_len <= 0 || ctx->num_ctx <= 0 || ctx->ctx_rows < 0)
-    return fail(MLA_ERR_INVALID_ARG, "shared_attention: num_blocks, block_len, num_ctx > 0, ctx_rows >= 0");
+  if (d.num_blocks <= 0 || d.block_len <= 0 || ctx->num_ctx <= 0 || ctx->num_ctx > d.num_blocks ||
+      ctx->ctx_rows < 0 || !ctx->ctx_len || !ctx->ctx_block_start)
+    return fail(MLA_ERR_INVALID_ARG,
+                "shared_attention: num_blocks, block_len > 0, 0 < num_ctx <= num_blocks, ctx_rows >= 0");
   if (!tc::expand_applies(h, d.block_len))
     return fail(MLA_ERR_UNSUPPORTED, "shared_attention: the layer does not run the expanded form");
   const Layout& l = h->lay;
@@ -690,7 +695,7 @@ extern "C" mla_status_t mla_shared_attention(mla_handle_t* h, const int32_t* pos
       (cudaStream_t)stream, h, (const __half*)(ws + w.q_nope), (const __nv_bfloat16*)(ws + w.q_abs),
       (const __half*)(ws + sw.kv), (const __nv_bfloat16*)(ws + sw.gathered),
       tc::expand_rows(*ctx, d.num_blocks, d.block_len), d, *ctx, positions, gate, l.NA,
-      (__half*)(ws + w.o), false);
+      (__half*)(ws + w.o), (int32_t*)(ws + sw.units), false);
   if (s != MLA_OK) return s;
   MLA_CUDA_TRY(cudaGetLastError());
   return MLA_OK;

@@ -22,6 +22,16 @@
 //        keys: 8 MMAs, P fp16 from tensor memory)
 // O is 128 fp32 columns, so S is double-buffered in tensor memory and the
 // scores of tile t + 1 are computed while the softmax of tile t runs.
+//
+// Units.  A context's blocks are first ordered full-mask ones before
+// windowed ones (a stable partition, expand_units_kernel), and a unit takes
+// up to 128 / block_len consecutive blocks of that order: its rows then share
+// one mask class, so a windowed unit skips the context tiles below its
+// windows and the rows of a warp agree on which keys a tile shows them.
+// The unit's query rows and own keys are then loaded block by block (one
+// block_len-row box each, at rows that keep the 128-byte swizzle's
+// 1024-byte alignment: block_len a multiple of 8 dividing 128); other block
+// lengths take consecutive blocks in their given order.
 // Keys and values stream through separate two-slot rings: a key slot is
 // refilled as soon as its scores are done, so the score chain never waits for
 // P V.
@@ -73,7 +83,10 @@ struct Bars {
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
 struct ExpParams {
-  CUtensorMap tmQn, tmQp, tmKV, tmKp;
+  CUtensorMap tmQn, tmQp, tmKV, tmKp;       // 128-row boxes (Q of a unit, context key tiles)
+  CUtensorMap tmQnT, tmQpT, tmKVT, tmKpT;   // block_len-row boxes, one chunk (grouped units)
+  const int32_t* perm;     // [num_blocks]: each context's blocks, full-mask first (NULL: given order)
+  const int32_t* ncls;     // [num_ctx][2]: full-mask and windowed block counts
   const int32_t* positions;
   const int32_t* kv_len;
   const int32_t* window;
@@ -85,7 +98,7 @@ struct ExpParams {
   long ld_gate;
   __half* o;
   uint32_t* status;
-  int num_ctx, ctx_rows, T, H, bpu;
+  int num_ctx, ctx_rows, T, H, bpu, rows, M;
   float scale_log2;
 };
 
@@ -102,24 +115,37 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 __device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
 
-// Unit u: blocks b0 .. b0 + nbu - 1 (at most bpu) of context c, whose keys
-// start at row coff of the gathered rows.  False past the last unit.
-__device__ __forceinline__ bool unit_of(const ExpParams& P, int u, int& c, int& b0, int& nbu, int& coff) {
+// Unit u: entries pstart .. pstart + nbu - 1 (at most bpu) of the block
+// order (perm, or the given order) of context c, whose keys start at row
+// coff of the gathered rows.  With perm, a unit never mixes the context's
+// full-mask and windowed blocks.  False past the last unit.
+__device__ __forceinline__ bool unit_of(const ExpParams& P, int u, int& c, int& pstart, int& nbu, int& coff) {
   int acc = 0;
   coff = 0;
   for (int cc = 0; cc < P.num_ctx; ++cc) {
     const int s = P.ctx_start[cc], e = P.ctx_start[cc + 1];
-    const int n = e > s ? (e - s + P.bpu - 1) / P.bpu : 0;
-    if (u < acc + n) {
+    const int n0 = P.perm ? P.ncls[2 * cc] : max(e - s, 0);
+    const int n1 = P.perm ? P.ncls[2 * cc + 1] : 0;
+    const int u0 = (n0 + P.bpu - 1) / P.bpu, u1 = (n1 + P.bpu - 1) / P.bpu;
+    if (u < acc + u0) {
       c = cc;
-      b0 = s + (u - acc) * P.bpu;
-      nbu = min(P.bpu, e - b0);
+      pstart = s + (u - acc) * P.bpu;
+      nbu = min(P.bpu, n0 - (u - acc) * P.bpu);
       return true;
     }
-    acc += n;
+    if (u < acc + u0 + u1) {
+      c = cc;
+      pstart = s + n0 + (u - acc - u0) * P.bpu;
+      nbu = min(P.bpu, n1 - (u - acc - u0) * P.bpu);
+      return true;
+    }
+    acc += u0 + u1;
     coff += P.ctx_len[cc];
   }
   return false;
+}
+__device__ __forceinline__ int unit_block(const ExpParams& P, int pstart, int i) {
+  return P.perm ? P.perm[pstart + i] : pstart + i;
 }
 
 __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_constant__ ExpParams P) {
@@ -130,12 +156,14 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
   int* red = (int*)(smem + OFF_RED);
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int h = blockIdx.y;
-  int c, b0, nbu, coff;
-  if (!unit_of(P, blockIdx.x, c, b0, nbu, coff)) return;       // the grid is an upper bound
+  int c, pstart, nbu, coff;
+  pdl_wait();                  // the block order comes from the kernel before this one
+  if (!unit_of(P, blockIdx.x, c, pstart, nbu, coff)) return;   // the grid is an upper bound
   const int T = P.T, nrows = nbu * T;
-  const long m0 = (long)b0 * T;
+  const bool grouped = P.perm != nullptr;
+  const long m0 = (long)pstart * T;                             // (contiguous units) first query row
   const int ctx_len = P.ctx_len[c];
-  const long own0 = (long)P.ctx_rows + m0;                      // first gathered row of the blocks' own keys
+  const long own0 = (long)P.ctx_rows + m0;                      // (contiguous units) first own-key row
 
   if (tid == 0) {
     mbar_init(&B->q_full, 1);
@@ -158,9 +186,9 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
   // skipped): the least window start over the unit's rows (0 for a full mask)
   int lo_r = 0x7fffffff;
   if (tid < QROWS && tid < nrows) {
-    const int b = b0 + tid / T;
+    const int b = unit_block(P, pstart, tid / T);
     const int W = P.window ? P.window[b] : 0;
-    lo_r = W > 0 ? max(0, P.positions[m0 + tid] - W + 1) : 0;
+    lo_r = W > 0 ? max(0, P.positions[(long)b * T + tid % T] - W + 1) : 0;
     if (tid % T == 0 && h == 0) {
       if (P.kv_len[b] > ctx_len + T || P.kv_len[b] < 0) set_status(P.status, MLA_DEV_BAD_LENGTH);
       if (W < 0) set_status(P.status, MLA_DEV_BAD_WINDOW);
@@ -190,10 +218,22 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
       }
       prefetch_tmap(&P.tmKV);
       pdl_wait();
+      const int slots = QROWS / T;                // block_len-row groups of a 128-row tile (grouped)
       if (keys) {
         mbar_arrive_expect_tx(&B->q_full, 3 * CH);
-        tma_load_3d(smem + OFF_Q, &P.tmQn, &B->q_full, 0, (int)m0, 2 * h);
-        tma_load_3d(smem + OFF_Q + 2 * CH, &P.tmQp, &B->q_full, 0, (int)m0, 9 * h + 8);
+        if (!grouped) {
+          tma_load_3d(smem + OFF_Q, &P.tmQn, &B->q_full, 0, (int)m0, 2 * h);
+          tma_load_3d(smem + OFF_Q + 2 * CH, &P.tmQp, &B->q_full, 0, (int)m0, 9 * h + 8);
+        } else {
+          // block i's rows at rows i T of the tile; the rest past the end (zeros)
+          for (int i = 0; i < slots; ++i) {
+            const int row = i < nbu ? unit_block(P, pstart, i) * T : P.M;
+            uint8_t* dst = smem + OFF_Q + i * T * 128;
+            tma_load_3d(dst, &P.tmQnT, &B->q_full, 0, row, 2 * h);
+            tma_load_3d(dst + CH, &P.tmQnT, &B->q_full, 0, row, 2 * h + 1);
+            tma_load_3d(dst + 2 * CH, &P.tmQpT, &B->q_full, 0, row, 9 * h + 8);
+          }
+        }
       }
       uint64_t* full = keys ? B->kfull : B->vfull;
       uint64_t* empty = keys ? B->kempty : B->vempty;
@@ -202,14 +242,29 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
         const int s = t & 1;
         if (!(ok = wait_bar(B, &empty[s], ((t >> 1) & 1) ^ 1, P.status))) break;
         const int row = t < nt_ctx ? coff + j_lo + KT * t : (int)own0;
-        if (keys) {
-          uint8_t* slot = smem + OFF_KR + s * KSLOT;
-          mbar_arrive_expect_tx(&full[s], 3 * CH);
-          tma_load_3d(slot, &P.tmKV, &full[s], 0, row, 4 * h);            // k_nope (2 chunks)
-          tma_load_3d(slot + 2 * CH, &P.tmKp, &full[s], 0, row, 8);       // k_pe
+        uint8_t* slot = keys ? smem + OFF_KR + s * KSLOT : smem + OFF_VR + s * VSLOT;
+        mbar_arrive_expect_tx(&full[s], (keys ? 3 : 2) * CH);
+        if (t < nt_ctx || !grouped) {
+          if (keys) {
+            tma_load_3d(slot, &P.tmKV, &full[s], 0, row, 4 * h);            // k_nope (2 chunks)
+            tma_load_3d(slot + 2 * CH, &P.tmKp, &full[s], 0, row, 8);       // k_pe
+          } else {
+            tma_load_3d(slot, &P.tmKV, &full[s], 0, row, 4 * h + 2);        // v (2 chunks)
+          }
         } else {
-          mbar_arrive_expect_tx(&full[s], 2 * CH);
-          tma_load_3d(smem + OFF_VR + s * VSLOT, &P.tmKV, &full[s], 0, row, 4 * h + 2);  // v (2 chunks)
+          // the blocks' own keys, block by block (the rest past the end: zeros)
+          for (int i = 0; i < slots; ++i) {
+            const int r = i < nbu ? P.ctx_rows + unit_block(P, pstart, i) * T : P.rows;
+            uint8_t* dst = slot + i * T * 128;
+            if (keys) {
+              tma_load_3d(dst, &P.tmKVT, &full[s], 0, r, 4 * h);
+              tma_load_3d(dst + CH, &P.tmKVT, &full[s], 0, r, 4 * h + 1);
+              tma_load_3d(dst + 2 * CH, &P.tmKpT, &full[s], 0, r, 8);
+            } else {
+              tma_load_3d(dst, &P.tmKVT, &full[s], 0, r, 4 * h + 2);
+              tma_load_3d(dst + CH, &P.tmKVT, &full[s], 0, r, 4 * h + 3);
+            }
+          }
         }
       }
       // every copy into this CTA has landed before it may exit
@@ -275,8 +330,8 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
     constexpr int KH = KT / 2;
     const uint32_t lane_base = (uint32_t)((r / 32) * 32) << 16;
     const bool live = r < nrows;
-    const int bi = r / T, b = b0 + min(bi, nbu - 1);
-    const long m = m0 + (live ? r : 0);
+    const int bi = r / T, b = unit_block(P, pstart, min(bi, nbu - 1));
+    const long m = (long)b * T + (live ? r % T : 0);
     const int p = P.positions[m];
     const bool qv = live && (P.q_visible ? P.q_visible[m] != 0 : true);
     const int W = P.window ? P.window[b] : 0;
@@ -414,6 +469,53 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
   if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// Each context's blocks in the order the units take them: full-mask ones
+// (window 0) first, then windowed ones, each class in its given order;
+// ncls[c] = (full-mask count, windowed count).  One CTA per context.
+__global__ void __launch_bounds__(256) expand_units_kernel(const int32_t* __restrict__ window,
+                                                           const int32_t* __restrict__ ctx_start,
+                                                           int32_t* __restrict__ perm, int32_t* __restrict__ ncls) {
+  __shared__ int wsum[8];
+  const int c = blockIdx.x, tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+  const int s = ctx_start[c], e = ctx_start[c + 1];
+  pdl_wait();                  // perm may still be read by the kernels before
+  int n0 = 0;
+  for (int base = s; base < e; base += 256) {
+    const int b = base + tid;
+    n0 += __syncthreads_count(b < e && (window == nullptr || window[b] == 0));
+  }
+  int run0 = 0, run1 = 0;
+  for (int base = s; base < e; base += 256) {
+    const int b = base + tid;
+    const bool in = b < e;
+    const int f = in && (window == nullptr || window[b] == 0) ? 1 : 0;
+    int x = f;                                    // inclusive scan of f over the CTA
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    int before = 0, cnt0 = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      before += w < warp ? wsum[w] : 0;
+      cnt0 += wsum[w];
+    }
+    __syncthreads();
+    const int ex0 = before + x - f;               // full-mask blocks before this one in the chunk
+    const int ex1 = min(tid, e - base) - ex0;     // windowed blocks before it
+    if (in) perm[f ? s + run0 + ex0 : s + n0 + run1 + ex1] = b;
+    run0 += cnt0;
+    run1 += min(256, e - base) - cnt0;
+  }
+  if (tid == 0) {
+    ncls[2 * c] = n0;
+    ncls[2 * c + 1] = max(e - s, 0) - n0;
+  }
+}
+
 // One warp per gathered row: context c's key j (rows [coff_c, coff_c +
 // ctx_len_c), through the table of c's first block), then block b's own key
 // ctx_len + i (rows ctx_rows + b * T + i, zero when past kv_len[b]).
@@ -481,7 +583,7 @@ mla_status_t expanded_attention(cudaStream_t st, const mla_handle* h, const __ha
                                 const __nv_bfloat16* q_abs, const __half* kv,
                                 const __nv_bfloat16* gathered, long rows, const mla_attn_desc_t& d,
                                 const mla_shared_ctx_t& ctx, const int32_t* positions,
-                                const float* gate, long ld_gate, __half* o, bool pdl) {
+                                const float* gate, long ld_gate, __half* o, int32_t* unit_ws, bool pdl) {
   const Layout& l = h->lay;
   if (!expand_applies(h, d.block_len))
     return fail(MLA_ERR_UNSUPPORTED, "expanded attention: needs bf16, kv_lora_rank 512, qk_rope 64, "
@@ -494,6 +596,31 @@ mla_status_t expanded_attention(cudaStream_t st, const mla_handle* h, const __ha
       !make_tmap_chunked(&P.tmKV, true, kv, rows, (long)l.H * 256, (long)l.H * 256, KT, 2) ||
       !make_tmap_chunked(&P.tmKp, false, gathered, rows, l.L, l.L, KT, 1))
     return fail(MLA_ERR_CUDA, "expanded attention: cuTensorMapEncodeTiled failed");
+  // units of one mask class when a block's rows fill whole 8-row groups of the tile
+  const int T = d.block_len;
+  const bool grouped = T % 8 == 0 && QROWS % T == 0;
+  P.perm = nullptr;
+  P.ncls = nullptr;
+  if (grouped) {
+    if (!make_tmap_chunked(&P.tmQnT, true, q_nope, M, (long)l.H * 128, (long)l.H * 128, T, 1) ||
+        !make_tmap_chunked(&P.tmQpT, false, q_abs, M, (long)l.H * l.L, (long)l.H * l.L, T, 1) ||
+        !make_tmap_chunked(&P.tmKVT, true, kv, rows, (long)l.H * 256, (long)l.H * 256, T, 1) ||
+        !make_tmap_chunked(&P.tmKpT, false, gathered, rows, l.L, l.L, T, 1))
+      return fail(MLA_ERR_CUDA, "expanded attention: cuTensorMapEncodeTiled failed");
+    Launch U(dim3((unsigned)ctx.num_ctx), dim3(256), 0, st, pdl);
+    const cudaError_t eu = cudaLaunchKernelEx(&U.cfg, expand_units_kernel, d.window, ctx.ctx_block_start,
+                                              unit_ws, unit_ws + d.num_blocks);
+    if (eu != cudaSuccess) return cuda_fail(eu, "expanded attention units launch");
+    P.perm = unit_ws;
+    P.ncls = unit_ws + d.num_blocks;
+  } else {
+    P.tmQnT = P.tmQn;
+    P.tmQpT = P.tmQp;
+    P.tmKVT = P.tmKV;
+    P.tmKpT = P.tmKp;
+  }
+  P.rows = (int)rows;
+  P.M = (int)M;
   P.positions = positions;
   P.kv_len = d.kv_len;
   P.window = d.window;
@@ -515,9 +642,10 @@ mla_status_t expanded_attention(cudaStream_t st, const mla_handle* h, const __ha
   std::call_once(once, [] {
     cudaFuncSetAttribute(expand_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   });
-  // units: each context's blocks in groups of bpu (at most one partial group per context)
-  const long units = (d.num_blocks + P.bpu - 1) / P.bpu + ctx.num_ctx;
-  Launch L(dim3((unsigned)units, (unsigned)l.H), dim3(THREADS), SMEM_BYTES, st, pdl);
+  // units: each context's blocks (of each mask class) in groups of bpu, at
+  // most one partial group per context and class
+  const long units = (d.num_blocks + P.bpu - 1) / P.bpu + 2L * ctx.num_ctx;
+  Launch L(dim3((unsigned)units, (unsigned)l.H), dim3(THREADS), SMEM_BYTES, st, pdl || grouped);
   const cudaError_t e = cudaLaunchKernelEx(&L.cfg, expand_attn_kernel, P);
   if (e != cudaSuccess) return cuda_fail(e, "expanded attention launch");
   return MLA_OK;

@@ -31,12 +31,14 @@ void expand_gather(cudaStream_t st, const mla_handle* h, const __nv_bfloat16* ca
 // q_abs bf16 [M, H, 576] (q_pe in dims 512..575); kv fp16 [rows, H, 256]
 // (k_nope | v of each head: the gathered rows times kv_b_proj^T); gathered
 // bf16 [rows, 576] (k_pe in dims 512..575); gate fp32 (row m, head h, dim d
-// at gate[m * ld_gate + h * 128 + d]) or NULL; o fp16 [M, H, 128].
+// at gate[m * ld_gate + h * 128 + d]) or NULL; o fp16 [M, H, 128];
+// unit_ws: device scratch of num_blocks + 2 * num_ctx int32 (the block order
+// of the units).
 mla_status_t expanded_attention(cudaStream_t st, const mla_handle* h, const __half* q_nope,
                                 const __nv_bfloat16* q_abs, const __half* kv,
                                 const __nv_bfloat16* gathered, long rows, const mla_attn_desc_t& d,
                                 const mla_shared_ctx_t& ctx, const int32_t* positions,
-                                const float* gate, long ld_gate, __half* o, bool pdl);
+                                const float* gate, long ld_gate, __half* o, int32_t* unit_ws, bool pdl);
 
 }  // namespace tc
 }  // namespace mla

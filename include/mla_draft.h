@@ -142,7 +142,8 @@ typedef struct {
  * device as MLA_DEV_BAD_LENGTH and its extra keys are not seen).  The
  * visibility rule of mla_attn_desc_t applies unchanged. */
 typedef struct {
-  int32_t num_ctx;                 /* contexts                                   */
+  int32_t num_ctx;                 /* contexts, 1 .. num_blocks (else
+                                      MLA_ERR_INVALID_ARG)                       */
   int32_t ctx_rows;                /* host: sum of ctx_len (keys of all contexts) */
   const int32_t *ctx_len;          /* device [num_ctx]                           */
   const int32_t *ctx_block_start;  /* device [num_ctx + 1]                       */

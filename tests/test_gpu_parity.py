@@ -188,14 +188,18 @@ def test_few_row_blocks_match_oracle(case):
     check_workload(_few_row_case(case))
 
 
-@pytest.mark.parametrize("case", ["T7_ragged_windows_masked", "T16_gate_off", "T40_one_context"])
+@pytest.mark.parametrize("case", ["T7_ragged_windows_masked", "T16_gate_off", "T40_one_context",
+                                  "T32_grouped_masked"])
 def test_shared_context_blocks_match_oracle(case):
     """Blocks that share a context run the expanded form (the context's and
     the blocks' own latents expanded by kv_b_proj, one attention over
     q_nope|q_pe with the own keys as a block-diagonal tile): ragged context
     lengths (not multiples of the 128-key tile), block lengths that leave a
     unit's last rows empty, sliding windows shorter than the context and than
-    the block, masked query rows, with and without the output gate."""
+    the block, masked query rows, with and without the output gate.  Block
+    lengths that divide the 128-row tile into 8-row multiples (16, 32) take
+    each context's full-mask blocks and windowed blocks in separate units, so
+    a unit's query and own-key rows come from blocks that are not adjacent."""
     import dataclasses
     from tests.parity import check_workload
     from head_latent_attention_qkv_gb300.runner import shared_contexts
@@ -212,6 +216,13 @@ def test_shared_context_blocks_match_oracle(case):
         wl = W.block_parallel_workload(case, d.replace(use_output_gate=False, rope_style="neox"), 32,
                                        batch=2, ctx_len=448, blocks_per_seq=9, block_len=16,
                                        page_size=64, windows=(0, 200))
+    elif case == "T32_grouped_masked":
+        wl = W.block_parallel_workload(case, d, 34, batch=3, ctx_len=384, blocks_per_seq=7,
+                                       block_len=32, page_size=128, windows=(0, 90, 0, 5))
+        s = wl.steps[0]
+        qv = s.q_visible.copy()
+        qv[[0, 31, 70, 300, 671]] = 0
+        wl = dataclasses.replace(wl, steps=[dataclasses.replace(s, q_visible=qv)])
     else:
         wl = W.block_parallel_workload(case, d, 33, batch=1, ctx_len=256, blocks_per_seq=4,
                                        block_len=40, page_size=128, windows=(0,))
