@@ -20,8 +20,11 @@
 //        K = 128 fp16 + 64 bf16: 8 + 4 MMAs)
 //   O += P V                                (N = 128 value dims, K = 128
 //        keys: 8 MMAs, P fp16 from tensor memory)
-// O is 128 fp32 columns, so S is double-buffered in tensor memory and the
-// scores of tile t + 1 are computed while the softmax of tile t runs.
+// O is 128 fp32 columns and S (with P over it) three buffers of 128: the
+// scores of tile t + 1 are computed while the softmax of tile t runs, and
+// S(t + 1) waits only for P V of tile t - 2, so the chain softmax -> P V ->
+// S -> softmax spans three tiles (two buffers left it on every second tile,
+// and the tile period at about half that chain).
 //
 // Units.  A context's blocks are first ordered full-mask ones before
 // windowed ones (a stable partition, expand_units_kernel), and a unit takes
@@ -62,10 +65,11 @@ constexpr int KSLOT = 3 * CH;
 constexpr int OFF_VR = OFF_KR + 2 * KSLOT;        // value ring, 2 slots: v (2 chunks)
 constexpr int VSLOT = 2 * CH;
 constexpr int OFF_BAR = OFF_VR + 2 * VSLOT;
-constexpr int OFF_XM = OFF_BAR + 256;             // [2][128] half maxima / sums
-constexpr int OFF_RED = OFF_XM + 2 * QROWS * 4;   // [8] per-warp minima of the window starts
+constexpr int OFF_XM = OFF_BAR + 256;             // [2 (tile parity)][2][128] half maxima / sums
+constexpr int OFF_RED = OFF_XM + 4 * QROWS * 4;   // [8] per-warp minima of the window starts
 constexpr int SMEM_BYTES = 1024 + OFF_RED + 64;
-constexpr uint32_t TMEM_COLS = 512, TM_O = 0, TM_S = 128;   // O 128 columns; S (and P over it) 2 x 128
+constexpr int NS = 3;                             // S buffers
+constexpr uint32_t TMEM_COLS = 512, TM_O = 0, TM_S = 128;   // O 128 columns; S (and P over it) 3 x 128
 constexpr float RESCALE_LOG2 = 8.f;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
@@ -73,9 +77,9 @@ struct Bars {
   uint64_t q_full;
   uint64_t kfull[2], kempty[2]; // key slot landed / read by S (by tile parity)
   uint64_t vfull[2], vempty[2]; // value slot landed / read by P V (by tile parity)
-  uint64_t s_full[2];           // S(t) complete, by t % 2
-  uint64_t p_full[2];           // P(t) in tensor memory (256 arrivals), by t % 2
-  uint64_t o_free[2];           // P(t) V(t) complete, by t % 2
+  uint64_t s_full[NS];          // S(t) complete, by t % NS
+  uint64_t p_full[NS];          // P(t) in tensor memory (256 arrivals), by t % NS
+  uint64_t o_free[NS];          // P(t) V(t) complete, by t % NS
   uint64_t drain, drain_pv;
   uint32_t tmem_slot;
   int abort;
@@ -172,6 +176,8 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
       mbar_init(&B->kempty[i], 1);
       mbar_init(&B->vfull[i], 1);
       mbar_init(&B->vempty[i], 1);
+    }
+    for (int i = 0; i < NS; ++i) {
       mbar_init(&B->s_full[i], 1);
       mbar_init(&B->p_full[i], 2 * QROWS);
       mbar_init(&B->o_free[i], 1);
@@ -276,29 +282,29 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
       constexpr uint32_t U_CH = CH / 16, U_KSLOT = KSLOT / 16, U_VSLOT = VSLOT / 16, U_KSTEP = 16 * 128 / 16;
       bool ok = true;
       if (warp == 5) {
-        // ---- S(t) = [q_nope | q_pe] K(t)^T into S buffer t % 2 ----
+        // ---- S(t) = [q_nope | q_pe] K(t)^T into S buffer t % NS ----
         const uint32_t id_s16 = idesc_f16(QROWS, KT, true), id_sbf = idesc_f16(QROWS, KT, false);
         const uint64_t dQ = smem_desc_sw128(smem + OFF_Q);
         const uint64_t dK0 = smem_desc_sw128(smem + OFF_KR);
         ok = wait_bar(B, &B->q_full, 0, P.status);
         tc_fence_after();
         for (int t = 0; t < nt && ok; ++t) {
-          const int s = t & 1;
-          // S buffer s holds P(t - 2): P(t - 2) V(t - 2) (the other thread) has
-          // completed reading it
-          if (t >= 2 && !(ok = wait_bar(B, &B->o_free[s], ((t - 2) >> 1) & 1, P.status))) break;
-          if (!(ok = wait_bar(B, &B->kfull[s], (t >> 1) & 1, P.status))) break;
+          const int s = t % NS, k = t & 1;
+          // S buffer s holds P(t - NS): P(t - NS) V(t - NS) (the other thread)
+          // has completed reading it
+          if (t >= NS && !(ok = wait_bar(B, &B->o_free[s], (t / NS - 1) & 1, P.status))) break;
+          if (!(ok = wait_bar(B, &B->kfull[k], (t >> 1) & 1, P.status))) break;
           tc_fence_after();
           const uint32_t tS = tmem + TM_S + 128 * s;
-          const uint64_t dK = dK0 + s * U_KSLOT;
+          const uint64_t dK = dK0 + k * U_KSLOT;
 #pragma unroll
           for (int ch = 0; ch < 3; ++ch) {
             const uint32_t id = ch < 2 ? id_s16 : id_sbf;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_f16(tS, dQ + ch * U_CH + 2 * k, dK + ch * U_CH + 2 * k, id, (ch | k) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16(tS, dQ + ch * U_CH + 2 * kk, dK + ch * U_CH + 2 * kk, id, (ch | kk) ? 1u : 0u);
           }
-          mma_commit(&B->kempty[s]);
+          mma_commit(&B->kempty[k]);
           mma_commit(&B->s_full[s]);
         }
       } else {
@@ -306,16 +312,16 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
         const uint32_t id_pv = idesc_f16_bmn(QROWS, 128, true);
         const uint64_t dV0 = smem_desc_sw128_mn(smem + OFF_VR, CH);
         for (int t = 0; t < nt && ok; ++t) {
-          const int s = t & 1;
-          if (!(ok = wait_bar(B, &B->p_full[s], (t >> 1) & 1, P.status))) break;
-          if (!(ok = wait_bar(B, &B->vfull[s], (t >> 1) & 1, P.status))) break;
+          const int s = t % NS, v = t & 1;
+          if (!(ok = wait_bar(B, &B->p_full[s], (t / NS) & 1, P.status))) break;
+          if (!(ok = wait_bar(B, &B->vfull[v], (t >> 1) & 1, P.status))) break;
           tc_fence_after();
           const uint32_t tP = tmem + TM_S + 128 * s;
-          const uint64_t dV = dV0 + s * U_VSLOT;
+          const uint64_t dV = dV0 + v * U_VSLOT;
 #pragma unroll
           for (int k = 0; k < KT / 16; ++k)   // 16 keys per MMA: 8 P columns, 16 V rows
             mma_f16_ts(tmem + TM_O, tP + 8 * k, dV + (uint64_t)U_KSTEP * k, id_pv, (t | k) ? 1u : 0u);
-          mma_commit(&B->vempty[s]);
+          mma_commit(&B->vempty[v]);
           mma_commit(&B->o_free[s]);
         }
       }
@@ -346,9 +352,15 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
     const int own_hi = sees ? bi * T + min(T, kvl - ctx_len) : 0;
     float mrun = -INFINITY, lsum = 0.f;
     for (int t = 0; t < nt; ++t) {
-      const int s = t & 1;
+      const int s = t % NS;
       float sv[KH];
-      wait_bar(B, &B->s_full[s], (t >> 1) & 1, P.status);
+      if (t == max(nt - 3, 0) && live && P.gate) {
+        // the epilogue's gate row half, into L2 while the last tiles run
+        const float* g = P.gate + m * P.ld_gate + (long)h * 128 + 64 * kh;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(g));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(g + 32));
+      }
+      wait_bar(B, &B->s_full[s], (t / NS) & 1, P.status);
       tc_fence_after();
 #pragma unroll
       for (int q = 0; q < KH; q += 32) tmem_ld32_nowait(tmem + TM_S + 128 * s + KH * kh + q + lane_base, sv + q);
@@ -377,10 +389,12 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
         }
       }
       const float hmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      xm[kh * QROWS + r] = hmax;
+      // half maxima exchanged in buffer t % 2: the barrier of tile t + 1
+      // orders this tile's reads before the writes of tile t + 2
+      float* xmt = xm + (t & 1) * 2 * QROWS;
+      xmt[kh * QROWS + r] = hmax;
       softmax_sync();
-      const float tmax = fmaxf(hmax, xm[(1 - kh) * QROWS + r]) * P.scale_log2;
-      softmax_sync();
+      const float tmax = fmaxf(hmax, xmt[(1 - kh) * QROWS + r]) * P.scale_log2;
       const bool grow = tmax > mrun + RESCALE_LOG2;
       const float m_new = grow ? tmax : mrun;
       const float mref = m_new == -INFINITY ? 0.f : m_new;
@@ -394,7 +408,7 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
       const float alpha = (grow && mrun != -INFINITY) ? exp2f(mrun - m_new) : 1.f;
       // P(t - 1) V(t - 1) may still run: a row that grew waits for it, then rescales
       if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        wait_bar(B, &B->o_free[(t - 1) & 1], ((t - 1) >> 1) & 1, P.status);
+        wait_bar(B, &B->o_free[(t - 1) % NS], ((t - 1) / NS) & 1, P.status);
         tc_fence_after();
 #pragma unroll 1
         for (int q = 64 * kh; q < 64 * kh + 64; q += 32) {
@@ -431,10 +445,11 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
       P.vis_stats[m * 3 + 2] = n ? hi - 1 : -1;
     }
     // ---- epilogue: O / l (times the gate) -> o[m, h, 64 kh .. 64 kh + 63] ----
-    xm[kh * QROWS + r] = lsum;
+    float* xmt = xm + (nt & 1) * 2 * QROWS;
+    xmt[kh * QROWS + r] = lsum;
     softmax_sync();
-    lsum += xm[(1 - kh) * QROWS + r];
-    wait_bar(B, &B->o_free[(nt - 1) & 1], ((nt - 1) >> 1) & 1, P.status);
+    lsum += xmt[(1 - kh) * QROWS + r];
+    wait_bar(B, &B->o_free[(nt - 1) % NS], ((nt - 1) / NS) & 1, P.status);
     tc_fence_after();
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
     __half* dst = P.o + (m * P.H + h) * 128 + 64 * kh;
