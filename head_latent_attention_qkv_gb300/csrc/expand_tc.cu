@@ -117,7 +117,34 @@ __device__ __forceinline__ float fast_exp2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
+// the two threads of a row sit in warps w and w + 8: each such pair of
+// warps synchronises on its own named barrier (4 + w % 4), so the four pairs
+// do not wait for one another
+__device__ __forceinline__ void pair_sync(int warp) {
+  asm volatile("bar.sync %0, 64;" ::"r"(4 + (warp & 3)) : "memory");
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// (x0, x1) = (x0 * a - b, x1 * a - b) and (s0, s1) += (x0, x1): paired fp32
+// operations, each rounded as its scalar form
+__device__ __forceinline__ void fms2(float& x0, float& x1, float a, float nb) {
+  uint64_t x, y, c;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(y) : "f"(a));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(c) : "f"(nb));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(x) : "l"(x), "l"(y), "l"(c));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x0), "=f"(x1) : "l"(x));
+}
+__device__ __forceinline__ void add2(float& s0, float& s1, float x0, float x1) {
+  uint64_t a, b;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(s0), "f"(s1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(b) : "f"(x0), "f"(x1));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(a) : "l"(a), "l"(b));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(a));
+}
 
 // Unit u: entries pstart .. pstart + nbu - 1 (at most bpu) of the block
 // order (perm, or the given order) of context c, whose keys start at row
@@ -377,32 +404,35 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
         hi = own_hi;
       }
       const int lo_h = lo - KH * kh, hi_h = hi - KH * kh;
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (__all_sync(0xffffffffu, lo_h <= 0 && hi_h >= KH)) {
+      if (!__all_sync(0xffffffffu, lo_h <= 0 && hi_h >= KH)) {
 #pragma unroll
-        for (int i = 0; i < KH; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], sv[i]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < KH; ++i) {
-          sv[i] = (i >= lo_h && i < hi_h) ? sv[i] : -INFINITY;
-          mx4[i & 3] = fmaxf(mx4[i & 3], sv[i]);
-        }
+        for (int i = 0; i < KH; ++i) sv[i] = (i >= lo_h && i < hi_h) ? sv[i] : -INFINITY;
       }
-      const float hmax = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int i = 0; i < KH; i += 8) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mx4[j] = max3(mx4[j], sv[i + 2 * j], sv[i + 2 * j + 1]);
+      }
+      const float hmax = max3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
       // half maxima exchanged in buffer t % 2: the barrier of tile t + 1
       // orders this tile's reads before the writes of tile t + 2
       float* xmt = xm + (t & 1) * 2 * QROWS;
       xmt[kh * QROWS + r] = hmax;
-      softmax_sync();
+      pair_sync(warp);
       const float tmax = fmaxf(hmax, xmt[(1 - kh) * QROWS + r]) * P.scale_log2;
       const bool grow = tmax > mrun + RESCALE_LOG2;
       const float m_new = grow ? tmax : mrun;
       const float mref = m_new == -INFINITY ? 0.f : m_new;
       float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < KH; ++i) {
-        sv[i] = fast_exp2(fmaf(sv[i], P.scale_log2, -mref));
-        ps4[i & 3] += sv[i];
+      for (int i = 0; i < KH; i += 4) {
+        fms2(sv[i], sv[i + 1], P.scale_log2, -mref);
+        fms2(sv[i + 2], sv[i + 3], P.scale_log2, -mref);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sv[i + j] = fast_exp2(sv[i + j]);
+        add2(ps4[0], ps4[1], sv[i], sv[i + 1]);
+        add2(ps4[2], ps4[3], sv[i + 2], sv[i + 3]);
       }
       const float psum = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
       const float alpha = (grow && mrun != -INFINITY) ? exp2f(mrun - m_new) : 1.f;
@@ -447,7 +477,7 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
     // ---- epilogue: O / l (times the gate) -> o[m, h, 64 kh .. 64 kh + 63] ----
     float* xmt = xm + (nt & 1) * 2 * QROWS;
     xmt[kh * QROWS + r] = lsum;
-    softmax_sync();
+    pair_sync(warp);
     lsum += xmt[(1 - kh) * QROWS + r];
     wait_bar(B, &B->o_free[(nt - 1) % NS], ((nt - 1) / NS) & 1, P.status);
     tc_fence_after();
