@@ -147,31 +147,56 @@ __device__ __forceinline__ void add2(float& s0, float& s1, float x0, float x1) {
 }
 
 // Unit u: entries pstart .. pstart + nbu - 1 (at most bpu) of the block
-// order (perm, or the given order) of context c, whose keys start at row
-// coff of the gathered rows.  With perm, a unit never mixes the context's
-// full-mask and windowed blocks.  False past the last unit.
-__device__ __forceinline__ bool unit_of(const ExpParams& P, int u, int& c, int& pstart, int& nbu, int& coff) {
-  int acc = 0;
-  coff = 0;
-  for (int cc = 0; cc < P.num_ctx; ++cc) {
-    const int s = P.ctx_start[cc], e = P.ctx_start[cc + 1];
-    const int n0 = P.perm ? P.ncls[2 * cc] : max(e - s, 0);
-    const int n1 = P.perm ? P.ncls[2 * cc + 1] : 0;
-    const int u0 = (n0 + P.bpu - 1) / P.bpu, u1 = (n1 + P.bpu - 1) / P.bpu;
-    if (u < acc + u0) {
-      c = cc;
-      pstart = s + (u - acc) * P.bpu;
-      nbu = min(P.bpu, n0 - (u - acc) * P.bpu);
+// order (perm, or the given order) of context c, whose ctx_len keys start at
+// row coff of the gathered rows.  With perm, a unit never mixes the
+// context's full-mask and windowed blocks.  False past the last unit.
+// Called by whole warps: lane l reads context base + l's counts, and the
+// unit and key offsets are scans over the lanes (one round of loads for up
+// to 32 contexts).
+__device__ __forceinline__ bool unit_of(const ExpParams& P, int u, int& c, int& pstart, int& nbu,
+                                        int& coff, int& ctx_len) {
+  const int lane = threadIdx.x & 31;
+  int acc = 0, kacc = 0;
+  for (int base = 0; base < P.num_ctx; base += 32) {
+    const int cc = base + lane;
+    int s = 0, n0 = 0, n1 = 0, len = 0;
+    if (cc < P.num_ctx) {
+      s = P.ctx_start[cc];
+      const int e = P.ctx_start[cc + 1];
+      n0 = P.perm ? P.ncls[2 * cc] : max(e - s, 0);
+      n1 = P.perm ? P.ncls[2 * cc + 1] : 0;
+      len = P.ctx_len[cc];
+    }
+    const int u0 = (n0 + P.bpu - 1) / P.bpu, nu = u0 + (n1 + P.bpu - 1) / P.bpu;
+    int x = nu, y = len;                          // inclusive scans over the lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int xs = __shfl_up_sync(0xffffffffu, x, o), ys = __shfl_up_sync(0xffffffffu, y, o);
+      if (lane >= o) {
+        x += xs;
+        y += ys;
+      }
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, cc < P.num_ctx && acc + x > u);
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      const int k = u - acc - __shfl_sync(0xffffffffu, x - nu, l);   // unit within the context
+      const int cs = __shfl_sync(0xffffffffu, s, l), cu0 = __shfl_sync(0xffffffffu, u0, l);
+      const int cn0 = __shfl_sync(0xffffffffu, n0, l), cn1 = __shfl_sync(0xffffffffu, n1, l);
+      c = base + l;
+      coff = kacc + __shfl_sync(0xffffffffu, y - len, l);
+      ctx_len = __shfl_sync(0xffffffffu, len, l);
+      if (k < cu0) {
+        pstart = cs + k * P.bpu;
+        nbu = min(P.bpu, cn0 - k * P.bpu);
+      } else {
+        pstart = cs + cn0 + (k - cu0) * P.bpu;
+        nbu = min(P.bpu, cn1 - (k - cu0) * P.bpu);
+      }
       return true;
     }
-    if (u < acc + u0 + u1) {
-      c = cc;
-      pstart = s + n0 + (u - acc - u0) * P.bpu;
-      nbu = min(P.bpu, n1 - (u - acc - u0) * P.bpu);
-      return true;
-    }
-    acc += u0 + u1;
-    coff += P.ctx_len[cc];
+    acc += __shfl_sync(0xffffffffu, x, 31);
+    kacc += __shfl_sync(0xffffffffu, y, 31);
   }
   return false;
 }
@@ -187,14 +212,14 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
   int* red = (int*)(smem + OFF_RED);
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int h = blockIdx.y;
-  int c, pstart, nbu, coff;
+  int c, pstart, nbu, coff, ctx_len;
   pdl_wait();                  // the block order comes from the kernel before this one
-  if (!unit_of(P, blockIdx.x, c, pstart, nbu, coff)) return;   // the grid is an upper bound
+  if (!unit_of(P, blockIdx.x, c, pstart, nbu, coff, ctx_len)) return;   // the grid is an upper bound
   const int T = P.T, nrows = nbu * T;
   const bool grouped = P.perm != nullptr;
   const long m0 = (long)pstart * T;                             // (contiguous units) first query row
-  const int ctx_len = P.ctx_len[c];
   const long own0 = (long)P.ctx_rows + m0;                      // (contiguous units) first own-key row
+  const int slots = QROWS / T;                                  // block_len-row groups of a tile (grouped)
 
   if (tid == 0) {
     mbar_init(&B->q_full, 1);
@@ -213,6 +238,26 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
     mbar_init(&B->drain_pv, 1);
     B->abort = 0;
     fence_mbar_init();
+    // the unit's queries, issued before anything else waits: block i's rows
+    // at rows i T of the tile (grouped units), the rest past the end (zeros)
+    mbar_arrive_expect_tx(&B->q_full, 3 * CH);
+    if (!grouped) {
+      tma_load_3d(smem + OFF_Q, &P.tmQn, &B->q_full, 0, (int)m0, 2 * h);
+      tma_load_3d(smem + OFF_Q + 2 * CH, &P.tmQp, &B->q_full, 0, (int)m0, 9 * h + 8);
+    } else {
+      int row[16];                                // slots <= 16 (block_len >= 8)
+#pragma unroll
+      for (int i = 0; i < 16; ++i) row[i] = i < nbu ? P.perm[pstart + i] * T : P.M;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (i < slots) {
+          uint8_t* dst = smem + OFF_Q + i * T * 128;
+          tma_load_3d(dst, &P.tmQnT, &B->q_full, 0, row[i], 2 * h);
+          tma_load_3d(dst + CH, &P.tmQnT, &B->q_full, 0, row[i], 2 * h + 1);
+          tma_load_3d(dst + 2 * CH, &P.tmQpT, &B->q_full, 0, row[i], 9 * h + 8);
+        }
+      }
+    }
   }
   if (warp == 5) tmem_alloc(&B->tmem_slot, TMEM_COLS);
   // first context key any row of the unit can see (whole tiles below it are
@@ -244,30 +289,8 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
     if (lane == 0) {
       // ---- warp 4: Q, then the key tiles; warp 6: the value tiles ----
       const bool keys = warp == 4;
-      if (keys) {
-        prefetch_tmap(&P.tmQn);
-        prefetch_tmap(&P.tmQp);
-        prefetch_tmap(&P.tmKp);
-      }
+      if (keys) prefetch_tmap(&P.tmKp);
       prefetch_tmap(&P.tmKV);
-      pdl_wait();
-      const int slots = QROWS / T;                // block_len-row groups of a 128-row tile (grouped)
-      if (keys) {
-        mbar_arrive_expect_tx(&B->q_full, 3 * CH);
-        if (!grouped) {
-          tma_load_3d(smem + OFF_Q, &P.tmQn, &B->q_full, 0, (int)m0, 2 * h);
-          tma_load_3d(smem + OFF_Q + 2 * CH, &P.tmQp, &B->q_full, 0, (int)m0, 9 * h + 8);
-        } else {
-          // block i's rows at rows i T of the tile; the rest past the end (zeros)
-          for (int i = 0; i < slots; ++i) {
-            const int row = i < nbu ? unit_block(P, pstart, i) * T : P.M;
-            uint8_t* dst = smem + OFF_Q + i * T * 128;
-            tma_load_3d(dst, &P.tmQnT, &B->q_full, 0, row, 2 * h);
-            tma_load_3d(dst + CH, &P.tmQnT, &B->q_full, 0, row, 2 * h + 1);
-            tma_load_3d(dst + 2 * CH, &P.tmQpT, &B->q_full, 0, row, 9 * h + 8);
-          }
-        }
-      }
       uint64_t* full = keys ? B->kfull : B->vfull;
       uint64_t* empty = keys ? B->kempty : B->vempty;
       bool ok = true;
