@@ -506,9 +506,25 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
     tc_fence_after();
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
     __half* dst = P.o + (m * P.H + h) * 128 + 64 * kh;
-    const float* g = P.gate ? P.gate + m * P.ld_gate + (long)h * 128 + 64 * kh : nullptr;
+    const float* g = P.gate && live ? P.gate + m * P.ld_gate + (long)h * 128 + 64 * kh : nullptr;
+    // the gate's row piece in 16-byte loads (one wavefront per lane and 16
+    // bytes, against one per 4 bytes) when its rows are 16-byte aligned
+    const bool g16 = (P.ld_gate & 3) == 0 && ((uintptr_t)P.gate & 15) == 0;
 #pragma unroll 1
     for (int q = 0; q < 64; q += 32) {
+      float gv[32];
+      if (g) {
+        if (g16) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 t4 = *reinterpret_cast<const float4*>(g + q + i);
+            gv[i] = t4.x; gv[i + 1] = t4.y; gv[i + 2] = t4.z; gv[i + 3] = t4.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) gv[i] = g[q + i];
+        }
+      }
       float o[32];
       tmem_ld32(tmem + TM_O + lane_base + 64 * kh + q, o);
       if (live) {
@@ -519,7 +535,7 @@ __global__ void __launch_bounds__(THREADS, 1) expand_attn_kernel(const __grid_co
           for (int u = 0; u < 8; ++u) v[u] = o[i + u] * inv;
           if (g) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] *= g[q + i + u];
+            for (int u = 0; u < 8; ++u) v[u] *= gv[i + u];
           }
           __half2 h2[4];
 #pragma unroll
