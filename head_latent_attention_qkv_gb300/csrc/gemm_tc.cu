@@ -394,7 +394,8 @@ __device__ __forceinline__ bool pwait(PBars* B, uint64_t* bar, uint32_t parity, 
 template <int BN, typename TC>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, bool tma_store,
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
+                   bool tma_store,
                    int M, int N, int K, TC* __restrict__ C, long ldc, long sC,
                    const float* __restrict__ G, long ldg, long sG, bool gate_act, int sig_from,
                    uint32_t idesc, int group_m, int tiles_n, int tiles_m, int batch, QSplit qs,
@@ -563,6 +564,62 @@ gemm_tc_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constan
           p = qs.positions[row];
           bad = p < 0 || p >= qs.max_pos;
           if (bad && n0 == 0) set_status(status, MLA_DEV_BAD_POSITION);
+        }
+        if (tma_store) {
+          // staged (dn a multiple of 64, dr 64): a 64-column group is half of
+          // one head's no-position dims or all of its RoPE dims, so it leaves
+          // as one 128-byte piece per row (fp16 to q_nope through tmC, bf16 to
+          // Q_abs's tail through tmR) by the warp's staging tile and one TMA
+          // store; rows past M are clipped by the store
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN; c0 += 64) {
+            const int n = n0 + c0, hh = n / dqk, d = n % dqk;
+            float v[64];
+            tmem_ld32(tmem + buf * ACC_COLS + lane_addr + c0, v);
+            tmem_ld32(tmem + buf * ACC_COLS + lane_addr + c0 + 32, v + 32);
+            if (n >= N) continue;                       // the same for the whole warp
+            const bool rope_dims = d >= qs.dn;
+            if (rope_dims) {
+              if (qs.interleaved) {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {          // pairs (2k, 2k + 1)
+                  const float2 cs = bad ? make_float2(0.f, 0.f) : qs.rope[(long)p * half + k];
+                  const float a = v[2 * k], bb = v[2 * k + 1];
+                  v[2 * k] = a * cs.x - bb * cs.y;
+                  v[2 * k + 1] = bb * cs.x + a * cs.y;
+                }
+              } else {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {          // pairs (k, k + 32)
+                  const float2 cs = bad ? make_float2(0.f, 0.f) : qs.rope[(long)p * half + k];
+                  const float a = v[k], bb = v[k + 32];
+                  v[k] = a * cs.x - bb * cs.y;
+                  v[k + 32] = bb * cs.x + a * cs.y;
+                }
+              }
+            }
+            uint8_t* stg = stg_warp + sbuf * PSmem<BN>::STG_TILE;
+            if (lane == 0) bulk_wait_read1();     // the store that last read this tile is done with it
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint4 pk = rope_dims ? pack16<__nv_bfloat16>(v + 8 * k) : pack16<__half>(v + 8 * k);
+              *reinterpret_cast<uint4*>(stg + lane * 128 + ((k ^ (lane & 7)) << 4)) = pk;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && ok) {
+              if (rope_dims)
+                tma_store_3d(&tmR, stg, 0, m0 + 32 * q, hh * (qs.L / 64) + qs.rkv / 64);
+              else
+                tma_store_3d(&tmC, stg, 0, m0 + 32 * q, hh * (qs.dn / 64) + d / 64);
+              bulk_commit();
+            }
+            sbuf ^= 1;
+          }
+          tc_fence_before();
+          mbar_arrive(&PB->acc_empty[buf]);
+          continue;
         }
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
@@ -783,14 +840,25 @@ mla_status_t launch(cudaStream_t st, const GemmArgs& a, int splitk, uint32_t* st
     std::call_once(once_p, [&] {
       cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, PSmem<BN>::BYTES);
     });
-    CUtensorMap tc{}, tpa, tpb;
-    const bool tma_store = !a.qsplit && make_store_map<TC>(&tc, a.C, a.M, a.N, a.ldc, a.sC, a.batch);
+    CUtensorMap tc{}, tr{}, tpa, tpb;
+    bool tma_store;
+    if (a.qsplit) {
+      // the q_b split: staged stores when every 64-column group is one piece
+      // of a head's no-position dims or its 64 RoPE dims
+      const QSplit& q = *a.qsplit;
+      tma_store = BN % 64 == 0 && q.dn % 64 == 0 && q.dr == 64 && q.rkv % 64 == 0 && q.L % 64 == 0 &&
+                  a.batch == 1 && a.N == q.H * (q.dn + q.dr) &&
+                  make_tmap_chunked(&tc, true, q.q_nope, a.M, (long)q.H * q.dn, (long)q.H * q.dn, 32, 1) &&
+                  make_tmap_chunked(&tr, false, q.q_abs, a.M, (long)q.H * q.L, (long)q.H * q.L, 32, 1);
+    } else {
+      tma_store = make_store_map<TC>(&tc, a.C, a.M, a.N, a.ldc, a.sC, a.batch);
+    }
     constexpr int PK = Smem<BN, PCfg<BN>>::KBS;
     if (!make_operand_map(&tpa, a.fp16, a.A, a.M, a.K, a.lda, a.sA, a.batch, BM, PK) ||
         !make_operand_map(&tpb, a.fp16, a.B, a.N, a.K, a.ldb, a.sB, a.batch, BN, PK))
       return fail(MLA_ERR_CUDA, "tcgen05 gemm: cuTensorMapEncodeTiled failed");
     Launch P(dim3((unsigned)num_sms_current()), dim3(THREADS), PSmem<BN>::BYTES, st, a.pdl);
-    const cudaError_t ep = cudaLaunchKernelEx(&P.cfg, pk, tpa, tpb, tc, tma_store, a.M, a.N, a.K, (TC*)a.C, a.ldc, a.sC,
+    const cudaError_t ep = cudaLaunchKernelEx(&P.cfg, pk, tpa, tpb, tc, tr, tma_store, a.M, a.N, a.K, (TC*)a.C, a.ldc, a.sC,
                                               a.G, a.ldg, a.sG, a.gate_act, a.sig_from,
                                               idesc_f16(BM, BN, a.fp16), group_m, tiles_n, tiles_m,
                                               a.batch, a.qsplit ? *a.qsplit : QSplit{}, status);

@@ -189,7 +189,7 @@ def test_few_row_blocks_match_oracle(case):
 
 
 @pytest.mark.parametrize("case", ["T7_ragged_windows_masked", "T16_gate_off", "T40_one_context",
-                                  "T32_grouped_masked"])
+                                  "T32_grouped_masked", "T16_neox_many_tiles"])
 def test_shared_context_blocks_match_oracle(case):
     """Blocks that share a context run the expanded form (the context's and
     the blocks' own latents expanded by kv_b_proj, one attention over
@@ -199,7 +199,9 @@ def test_shared_context_blocks_match_oracle(case):
     the block, masked query rows, with and without the output gate.  Block
     lengths that divide the 128-row tile into 8-row multiples (16, 32) take
     each context's full-mask blocks and windowed blocks in separate units, so
-    a unit's query and own-key rows come from blocks that are not adjacent."""
+    a unit's query and own-key rows come from blocks that are not adjacent.
+    With more q_b tiles than SMs (T16_neox_many_tiles) the query projection
+    takes the persistent GEMM's staged epilogue with NeoX RoPE."""
     import dataclasses
     from tests.parity import check_workload
     from head_latent_attention_qkv_gb300.runner import shared_contexts
@@ -223,6 +225,13 @@ def test_shared_context_blocks_match_oracle(case):
         qv = s.q_visible.copy()
         qv[[0, 31, 70, 300, 671]] = 0
         wl = dataclasses.replace(wl, steps=[dataclasses.replace(s, q_visible=qv)])
+    elif case == "T16_neox_many_tiles":
+        # 1280 query rows x 32 heads: q_b has more 128-row tiles than the GPU
+        # has SMs, so it runs persistent with its staged split epilogue
+        # (NeoX pairs (k, k + 32) inside one 64-column group)
+        wl = W.block_parallel_workload(case, d.replace(num_heads=32, rope_style="neox"), 35, batch=2,
+                                       ctx_len=256, blocks_per_seq=40, block_len=16, page_size=128,
+                                       windows=(0, 100))
     else:
         wl = W.block_parallel_workload(case, d, 33, batch=1, ctx_len=256, blocks_per_seq=4,
                                        block_len=40, page_size=128, windows=(0,))
