@@ -36,6 +36,14 @@ def shared_contexts(wl, step, min_blocks=2):
         return None
     if np.any(step.kv_len != ctx_len[seq] + wl.block_len):
         return None
+    # the context keys are read through each context's first block's page
+    # table: every block of the context must name the same pages for them
+    table = np.asarray(step.block_table)
+    for c in range(n_ctx):
+        pages = -(-int(ctx_len[c]) // wl.page_size)
+        rows = table[starts[c]:starts[c + 1], :pages]
+        if np.any(rows != rows[:1]):
+            return None
     return ctx_len, starts, int(ctx_len.sum())
 
 
