@@ -242,16 +242,20 @@ mla_status_t mla_draft_forward_after(mla_handle_t *h, const void *hidden,
                                      void *cache_ready);
 
 /* mla_draft_forward for blocks that share contexts (mla_shared_ctx_t), in
- * the expanded form when the layer allows it (bf16, qk_nope_head_dim and
- * v_head_dim 128, block_len <= 128): each context's latents and each block's
+ * the expanded form when the layer allows it (bf16, kv_lora_rank 512,
+ * qk_rope_head_dim 64, qk_nope_head_dim and v_head_dim 128, block_len <=
+ * 128): each context's latents and each block's
  * own latents are expanded once by kv_b_proj into per-head k_nope and v
  * (MLA blog, forward_mha: kv_b_proj on the prefill context), the queries
  * keep q_nope and q_pe (no W_UK / W_UV absorption), and one attention runs
  * per (head, up to 128 / block_len blocks of a context): the context keys,
  * then the blocks' own keys as one more key tile, masked to each block's
  * own.  Other layers run mla_draft_forward.  Same results and errors as
- * mla_draft_forward; the workspace is
- * mla_forward_shared_workspace_bytes(h, num_tokens, ctx_rows). */
+ * mla_draft_forward, plus MLA_ERR_INVALID_ARG for a NULL context list or one
+ * outside its contract (num_ctx not in 1 .. num_blocks, ctx_rows < 0); the
+ * workspace (256-byte aligned, caller-owned) is
+ * mla_forward_shared_workspace_bytes(h, num_tokens, ctx_rows) bytes, 0 for
+ * a NULL handle or negative counts. */
 size_t mla_forward_shared_workspace_bytes(const mla_handle_t *h, int32_t num_tokens,
                                           int32_t ctx_rows);
 mla_status_t mla_draft_forward_shared(mla_handle_t *h, const void *hidden,
@@ -278,7 +282,10 @@ mla_status_t mla_draft_forward_shared_after(mla_handle_t *h, const void *hidden,
  * list and token count): the queries' q_nope and q_pe, the gathered latent
  * rows and their kv_b_proj expansion, the gate.  It rewrites the workspace's
  * per-head output o (the input of o_proj) with the same values the forward
- * computed.  For timing and checking that step in isolation. */
+ * computed.  For timing and checking that step in isolation.
+ * MLA_ERR_UNSUPPORTED when the layer does not take the expanded form,
+ * MLA_ERR_INVALID_ARG for NULL pointers, a context list outside its contract
+ * or a workspace smaller than mla_forward_shared_workspace_bytes(). */
 mla_status_t mla_shared_attention(mla_handle_t *h, const int32_t *positions,
                                   const mla_attn_desc_t *desc, const mla_shared_ctx_t *ctx,
                                   void *workspace, size_t workspace_bytes, void *stream);

@@ -99,6 +99,15 @@ def test_null_handle_calls_return_invalid_arg():
                                        None, None) == _lib.MLA_ERR_INVALID_ARG
     assert lib.mla_get_device_status(None, None, None) == _lib.MLA_ERR_INVALID_ARG
     assert lib.mla_append_workspace_bytes(None, 4) == 0
+    ctx = _lib.mla_shared_ctx_t(num_ctx=1, ctx_rows=64)
+    assert lib.mla_draft_forward_shared(None, None, None, None, None, 1, C.byref(desc), C.byref(ctx),
+                                        None, None, 0, None) == _lib.MLA_ERR_INVALID_ARG
+    assert lib.mla_draft_forward_shared_after(None, None, None, None, None, 1, C.byref(desc),
+                                              C.byref(ctx), None, None, 0, None, None) \
+        == _lib.MLA_ERR_INVALID_ARG
+    assert lib.mla_shared_attention(None, None, C.byref(desc), C.byref(ctx), None, 0, None) \
+        == _lib.MLA_ERR_INVALID_ARG
+    assert lib.mla_forward_shared_workspace_bytes(None, 16, 64) == 0
     lib.mla_draft_destroy(None)
 
 
