@@ -544,8 +544,10 @@ mla_status_t forward_impl(mla_handle_t* h, const void* hidden, const int32_t* po
       s = proj<TI, TX>(h, st, pdl, M, l.D, l.H * l.dv, 1, o, (long)l.H * l.dv, 0, (const TI*)h->Wo,
                        (long)l.H * l.dv, 0, (TX*)out, l.D, 0);
       if (s != MLA_OK) return s;
-      // non-GEMM kernels: [kv finish], [q norm], [rope split], gather, attention
-      h->launches += (split_done ? 2 : 3) + (bslots ? 1 : 0) + (l.rq > 0 ? 1 : 0);
+      // non-GEMM kernels: [kv finish], [q norm], [rope split], gather, [unit
+      // order], attention
+      h->launches += (split_done ? 2 : 3) + (bslots ? 1 : 0) + (l.rq > 0 ? 1 : 0) +
+                     (tc::expand_grouped(d.block_len) ? 1 : 0);
       return MLA_OK;
     }
   }

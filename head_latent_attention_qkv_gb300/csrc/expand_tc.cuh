@@ -14,6 +14,11 @@ inline long expand_rows(const mla_shared_ctx_t& ctx, int num_blocks, int block_l
   return (long)ctx.ctx_rows + (long)num_blocks * block_len;
 }
 
+// True when the expanded attention takes each context's blocks in units of
+// one mask class (block_len a multiple of 8 dividing 128), which costs one
+// more kernel: the pre-pass that orders the blocks.
+inline bool expand_grouped(int block_len) { return block_len % 8 == 0 && 128 % block_len == 0; }
+
 // True when the expanded attention serves these blocks: bf16 layer,
 // kv_lora_rank 512, qk_rope 64, qk_nope 128, v_head 128, block_len <= 128.
 bool expand_applies(const mla_handle* h, int block_len);
