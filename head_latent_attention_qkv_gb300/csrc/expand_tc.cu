@@ -682,7 +682,7 @@ mla_status_t expanded_attention(cudaStream_t st, const mla_handle* h, const __ha
     return fail(MLA_ERR_CUDA, "expanded attention: cuTensorMapEncodeTiled failed");
   // units of one mask class when a block's rows fill whole 8-row groups of the tile
   const int T = d.block_len;
-  const bool grouped = expand_grouped(T);
+  const bool grouped = T % 8 == 0 && QROWS % T == 0;
   P.perm = nullptr;
   P.ncls = nullptr;
   if (grouped) {

@@ -15,8 +15,9 @@ inline long expand_rows(const mla_shared_ctx_t& ctx, int num_blocks, int block_l
 }
 
 // True when the expanded attention takes each context's blocks in units of
-// one mask class (block_len a multiple of 8 dividing 128), which costs one
-// more kernel: the pre-pass that orders the blocks.
+// one mask class (block_len a multiple of 8 dividing 128: the condition
+// expanded_attention tests), which costs one more kernel, the pre-pass
+// that orders the blocks.
 inline bool expand_grouped(int block_len) { return block_len % 8 == 0 && 128 % block_len == 0; }
 
 // True when the expanded attention serves these blocks: bf16 layer,
