@@ -40,7 +40,8 @@
 // P V.
 //   warps 0-3, 8-11: softmax, two threads per row (64 keys each), half
 //                    maxima exchanged through shared memory; epilogue
-//   warp 4         : Q and the key tiles (TMA)
+//                    (thread 0 also issues the unit's Q loads at start)
+//   warp 4         : the key tiles (TMA)
 //   warp 6         : the value tiles (TMA)
 //   warp 5         : tensor-memory allocation, S issue
 //   warp 7         : P V issue (two issuing threads: one thread's issue
